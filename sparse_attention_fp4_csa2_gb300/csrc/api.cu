@@ -1,0 +1,376 @@
+// C ABI of the CSA2 library: argument checks, workspace layout, TMA tensor
+// maps and the launch sequence of each call (declared in include/csa2.h).
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "kernels.cuh"
+
+namespace csa2 {
+
+__device__ unsigned int g_dev_error = 0;
+
+namespace {
+thread_local ProfileEvents g_profile[2];
+}
+
+ProfileEvents &profile_events(int kernel) { return g_profile[kernel & 1]; }
+
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, stream, cudaEventRecordExternal)
+                                             : cudaEventRecord(ev, stream);
+}
+
+namespace {
+
+thread_local int32_t g_last_launches = 0;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+  return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over rows of 128 elements, box {64, box_rows}, 128B swizzle.
+bool make_tmap_bf16_rows128(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {256};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool params_ok(const csa2_params *p) {
+  return p && p->index_topk >= 1 && p->index_topk <= 2048 && p->sliding_window >= 0 &&
+         p->sliding_window <= 1024 && p->candidate_block_size == BLOCK && p->candidate_topk_blocks >= 16 &&
+         p->candidate_topk_blocks <= TOPK_MAX_K && p->candidate_topk_blocks % 16 == 0 &&
+         (p->block_reduce == 0 || p->block_reduce == 1) && (p->hsi == 0 || p->hsi == 1);
+}
+
+// ------------------------------------------------------------ workspace
+struct IndexerLayout {
+  int64_t row_len;       // scores per row
+  size_t scores_off, topk_off, end;
+};
+
+IndexerLayout indexer_layout(int32_t batch, int64_t n_max, const csa2_params *p, bool pool) {
+  IndexerLayout L;
+  L.row_len = pool ? (int64_t)p->candidate_topk_blocks * BLOCK : round_up(n_max, SWEEP_TILE);
+  L.scores_off = 0;
+  L.topk_off = (size_t)round_up((int64_t)batch * L.row_len * 4, 256);
+  L.end = L.topk_off + topk_scratch_bytes(batch, L.row_len, p->index_topk);
+  return L;
+}
+
+size_t indexer_ws(int32_t batch, int64_t n_max, const csa2_params *p) {
+  const size_t a = indexer_layout(batch, n_max, p, false).end;
+  const size_t b = indexer_layout(batch, n_max, p, true).end;
+  return a > b ? a : b;
+}
+
+size_t pool_ws(int32_t batch, int64_t n_max, const csa2_params *p) {
+  const int64_t nblk = (n_max + BLOCK - 1) / BLOCK;
+  return topk_scratch_bytes(batch, nblk, p->candidate_topk_blocks);
+}
+
+size_t attn_ws(int32_t batch, const csa2_params *p) { return attn_scratch_bytes(batch, p->index_topk, p->sliding_window); }
+
+size_t decode_ws(int32_t batch, int64_t n_max, const csa2_params *p) {
+  const int64_t nblk = (n_max + BLOCK - 1) / BLOCK;
+  size_t bs = (size_t)round_up((int64_t)batch * nblk * 4, 256);
+  size_t a = indexer_ws(batch, n_max, p), b = pool_ws(batch, n_max, p), c = attn_ws(batch, p);
+  size_t m = a > b ? a : b;
+  m = m > c ? m : c;
+  return bs + m;
+}
+
+csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
+
+// ----------------------------------------------------------- operations
+csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, int32_t batch, int64_t cap,
+                        const int32_t *n_vis, int64_t n_max, const int32_t *pool_blocks, const csa2_params *p,
+                        int32_t *topk_idx, float *block_scores, void *ws, size_t ws_bytes, cudaStream_t stream,
+                        int *launches) {
+  if (!q_idx || !w || !k_idx || !n_vis || !topk_idx || !ws) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CSA2_ERR_INVALID_ARG;
+  if (batch < 1 || cap < 1 || n_max < 0 || n_max > cap) return CSA2_ERR_INVALID_ARG;
+  if ((int64_t)batch * cap >= (int64_t)1 << 31 || (int64_t)batch * HI >= (int64_t)1 << 31) return CSA2_ERR_UNSUPPORTED;
+  if (pool_blocks && block_scores) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < indexer_ws(batch, n_max, p)) return CSA2_ERR_WORKSPACE;
+  const bool pool = pool_blocks != nullptr;
+  const IndexerLayout L = indexer_layout(batch, n_max, p, pool);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  float *scores = reinterpret_cast<float *>(wsb + L.scores_off);
+
+  CUtensorMap tm_k, tm_q;
+  if (!make_tmap_bf16_rows128(&tm_k, k_idx, (int64_t)batch * cap, pool ? BLOCK : SWEEP_TILE)) return CSA2_ERR_CUDA;
+  if (!make_tmap_bf16_rows128(&tm_q, q_idx, (int64_t)batch * HI, HI)) return CSA2_ERR_CUDA;
+  SweepArgs a;
+  a.w = w;
+  a.n_vis = n_vis;
+  a.pool = pool_blocks;
+  a.scores = scores;
+  a.block_scores = block_scores;
+  a.cap = cap;
+  a.n_max = n_max;
+  a.row_len = L.row_len;
+  a.batch = batch;
+  a.tiles_per_seq = (int32_t)(L.row_len / SWEEP_TILE);
+  a.pool_nb = p->candidate_topk_blocks;
+  a.nblk_stride = (int32_t)((n_max + BLOCK - 1) / BLOCK);
+  a.block_reduce = p->block_reduce;
+  const int sms = num_sms();
+  cudaError_t e = launch_indexer_sweep(tm_k, tm_q, a, sms, stream, launches);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+
+  TopkRows r;
+  r.vals = scores;
+  r.row_len = L.row_len;
+  r.row_stride = L.row_len;
+  r.rows = batch;
+  r.k = p->index_topk;
+  r.force_nvis = nullptr;
+  r.force_block = BLOCK;
+  r.n_max = n_max;
+  r.pool = pool_blocks;
+  r.pool_stride = p->candidate_topk_blocks;
+  r.out = topk_idx;
+  const TopkScratch s = carve_topk_scratch(wsb + L.topk_off, batch, L.row_len, p->index_topk);
+  return cuda_status(launch_topk(r, s, sms, stream, launches));
+}
+
+csa2_status run_pool(const float *block_scores, const int32_t *n_vis, int32_t batch, int64_t n_max,
+                     const csa2_params *p, int32_t *pool_blocks, void *ws, size_t ws_bytes, cudaStream_t stream,
+                     int *launches) {
+  if (!block_scores || !n_vis || !pool_blocks || !ws) return CSA2_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u)) return CSA2_ERR_INVALID_ARG;
+  if (batch < 1 || n_max < 0) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < pool_ws(batch, n_max, p)) return CSA2_ERR_WORKSPACE;
+  const int64_t nblk = (n_max + BLOCK - 1) / BLOCK;
+  TopkRows r;
+  r.vals = block_scores;
+  r.row_len = nblk;
+  r.row_stride = nblk;
+  r.rows = batch;
+  r.k = p->candidate_topk_blocks;
+  r.force_nvis = n_vis;
+  r.force_block = BLOCK;
+  r.n_max = n_max;
+  r.pool = nullptr;
+  r.pool_stride = 0;
+  r.out = pool_blocks;
+  const TopkScratch s = carve_topk_scratch(ws, batch, nblk, r.k);
+  return cuda_status(launch_topk(r, s, num_sms(), stream, launches));
+}
+
+csa2_status run_attn(const csa2_params *p, int32_t batch, const void *q, const uint8_t *kv, int64_t cap,
+                     const int32_t *topk_idx, const uint8_t *swa, const float *swa_scale, const int32_t *swa_len,
+                     float *out, float *lse, void *ws, size_t ws_bytes, cudaStream_t stream, int *launches) {
+  if (!q || !kv || !topk_idx || !out || !ws) return CSA2_ERR_INVALID_ARG;
+  if (p->sliding_window > 0 && (!swa || !swa_scale || !swa_len)) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv) || (swa && !aligned16(swa)) || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return CSA2_ERR_INVALID_ARG;
+  if (batch < 1 || batch > 65535 || cap < 1) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < attn_ws(batch, p)) return CSA2_ERR_WORKSPACE;
+  AttnArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.kv = kv;
+  a.idx = topk_idx;
+  a.swa = swa;
+  a.swa_scale = swa_scale;
+  a.swa_len = swa_len;
+  a.out = out;
+  a.lse = lse;
+  a.cap = cap;
+  a.problems = batch;
+  a.K = p->index_topk;
+  a.W = p->sliding_window;
+  return cuda_status(launch_sparse_attn(a, ws, stream, launches));
+}
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" {
+
+csa2_params csa2_default_params(void) {
+  csa2_params p;
+  p.index_topk = 512;
+  p.sliding_window = 128;
+  p.candidate_block_size = 8;
+  p.candidate_topk_blocks = 2048;
+  p.block_reduce = 0;
+  p.hsi = 1;
+  return p;
+}
+
+int32_t csa2_entry_bytes(void) { return ENTRY_BYTES; }
+
+int32_t csa2_last_launch_count(void) { return g_last_launches; }
+
+csa2_status csa2_set_profile_events(csa2_kernel kernel, void *start, void *stop) {
+  if (kernel != CSA2_KERNEL_INDEXER_SWEEP && kernel != CSA2_KERNEL_SPARSE_ATTN) return CSA2_ERR_INVALID_ARG;
+  ProfileEvents &pe = profile_events(kernel);
+  pe.start = static_cast<cudaEvent_t>(start);
+  pe.stop = static_cast<cudaEvent_t>(stop);
+  return CSA2_OK;
+}
+
+const char *csa2_status_string(csa2_status s) {
+  switch (s) {
+    case CSA2_OK: return "ok";
+    case CSA2_ERR_INVALID_ARG: return "invalid argument";
+    case CSA2_ERR_UNSUPPORTED: return "unsupported parameter";
+    case CSA2_ERR_WORKSPACE: return "workspace too small";
+    case CSA2_ERR_CUDA: return "CUDA error";
+    case CSA2_ERR_DEVICE: return "device-side error";
+  }
+  return "unknown status";
+}
+
+size_t csa2_workspace_bytes(csa2_op op, int32_t batch, int64_t n_max, const csa2_params *params) {
+  if (!params_ok(params) || batch < 1 || n_max < 0) return 0;
+  switch (op) {
+    case CSA2_OP_INDEXER: return indexer_ws(batch, n_max, params);
+    case CSA2_OP_POOL: return pool_ws(batch, n_max, params);
+    case CSA2_OP_ATTN: return attn_ws(batch, params);
+    case CSA2_OP_DECODE: return decode_ws(batch, n_max, params);
+  }
+  return 0;
+}
+
+csa2_status csa2_get_device_status(csa2_stream_t stream, uint32_t *bits) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(v)) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (v && cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (bits) *bits = v;
+  return v ? CSA2_ERR_DEVICE : CSA2_OK;
+}
+
+csa2_status csa2_kv_quant_write(const void *latent, const void *z, int32_t m, int64_t n_entries,
+                                const int64_t *entry_pos, const int64_t *slot, uint8_t *kv, int64_t kv_rows,
+                                float rope_theta, csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (n_entries < 0 || kv_rows < 0 || (m != 1 && m != 2)) return CSA2_ERR_INVALID_ARG;
+  if (n_entries == 0) return CSA2_OK;
+  if (!latent || !entry_pos || !slot || !kv || (m == 2 && !z)) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(latent) || !aligned16(kv) || (z && !aligned16(z))) return CSA2_ERR_INVALID_ARG;
+  if (!(rope_theta > 1.0f)) return CSA2_ERR_INVALID_ARG;
+  if (n_entries > ((int64_t)1 << 34)) return CSA2_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_kv_quant_write(latent, m == 2 ? z : nullptr, m, n_entries, entry_pos, slot, kv,
+                                              kv_rows, rope_theta, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  g_last_launches = 1;
+  return CSA2_OK;
+}
+
+csa2_status csa2_indexer_score_topk(const void *q_idx, const float *w, const void *k_idx, int32_t batch, int64_t cap,
+                                    const int32_t *n_vis, int64_t n_max, const int32_t *pool_blocks,
+                                    const csa2_params *params, int32_t *topk_idx, float *block_scores, void *ws,
+                                    size_t ws_bytes, csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  int launches = 0;
+  const csa2_status s = run_indexer(q_idx, w, k_idx, batch, cap, n_vis, n_max, pool_blocks, params, topk_idx,
+                                    block_scores, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (s == CSA2_OK) g_last_launches = launches;
+  return s;
+}
+
+csa2_status csa2_hier_pool_select(const float *block_scores, const int32_t *n_vis, int32_t batch, int64_t n_max,
+                                  const csa2_params *params, int32_t *pool_blocks, void *ws, size_t ws_bytes,
+                                  csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  int launches = 0;
+  const csa2_status s = run_pool(block_scores, n_vis, batch, n_max, params, pool_blocks, ws, ws_bytes,
+                                 reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (s == CSA2_OK) g_last_launches = launches;
+  return s;
+}
+
+csa2_status csa2_sparse_attn(const csa2_params *params, int32_t batch, const void *q, const uint8_t *kv, int64_t cap,
+                             const int32_t *topk_idx, const uint8_t *swa, const float *swa_scale,
+                             const int32_t *swa_len, float *out, float *lse, void *ws, size_t ws_bytes,
+                             csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  int launches = 0;
+  const csa2_status s = run_attn(params, batch, q, kv, cap, topk_idx, swa, swa_scale, swa_len, out, lse, ws, ws_bytes,
+                                 reinterpret_cast<cudaStream_t>(stream), &launches);
+  if (s == CSA2_OK) g_last_launches = launches;
+  return s;
+}
+
+csa2_status csa2_sparse_decode(csa2_mode mode, const csa2_params *params, int32_t batch, const void *q,
+                               const void *q_idx, const float *w, const uint8_t *kv, const void *k_idx, int64_t cap,
+                               const int32_t *n_vis, int64_t n_max, const uint8_t *swa, const float *swa_scale,
+                               const int32_t *swa_len, int32_t *topk_idx, int32_t *pool_blocks, float *out,
+                               float *lse, void *ws, size_t ws_bytes, csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (mode != CSA2_MODE_FULL && mode != CSA2_MODE_REINDEX && mode != CSA2_MODE_REUSE) return CSA2_ERR_INVALID_ARG;
+  if (batch < 1 || n_max < 0 || !ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CSA2_ERR_INVALID_ARG;
+  if (ws_bytes < decode_ws(batch, n_max, params)) return CSA2_ERR_WORKSPACE;
+  if ((mode == CSA2_MODE_REINDEX || (mode == CSA2_MODE_FULL && params->hsi)) && !pool_blocks)
+    return CSA2_ERR_INVALID_ARG;
+  if (mode != CSA2_MODE_REUSE && (!q_idx || !w || !k_idx || !n_vis)) return CSA2_ERR_INVALID_ARG;
+  if (!q || !kv || !topk_idx || !out) return CSA2_ERR_INVALID_ARG;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  const int64_t nblk = (n_max + BLOCK - 1) / BLOCK;
+  const size_t bs_bytes = (size_t)round_up((int64_t)batch * nblk * 4, 256);
+  float *bscores = reinterpret_cast<float *>(wsb);
+  uint8_t *rest = wsb + bs_bytes;
+  const size_t rest_bytes = ws_bytes - bs_bytes;
+  int launches = 0;
+  csa2_status s = CSA2_OK;
+  if (mode == CSA2_MODE_FULL) {
+    s = run_indexer(q_idx, w, k_idx, batch, cap, n_vis, n_max, nullptr, params, topk_idx,
+                    params->hsi ? bscores : nullptr, rest, rest_bytes, st, &launches);
+    if (s == CSA2_OK && params->hsi)
+      s = run_pool(bscores, n_vis, batch, n_max, params, pool_blocks, rest, rest_bytes, st, &launches);
+  } else if (mode == CSA2_MODE_REINDEX) {
+    s = run_indexer(q_idx, w, k_idx, batch, cap, n_vis, n_max, pool_blocks, params, topk_idx, nullptr, rest,
+                    rest_bytes, st, &launches);
+  }
+  if (s == CSA2_OK)
+    s = run_attn(params, batch, q, kv, cap, topk_idx, swa, swa_scale, swa_len, out, lse, rest, rest_bytes, st,
+                 &launches);
+  if (s == CSA2_OK) g_last_launches = launches;
+  return s;
+}
+
+}  // extern "C"

@@ -1,0 +1,421 @@
+// Sparse-attention readout over gathered FP4 main-KV entries and the FP8 SWA
+// window, on the 5th-generation tensor cores.
+//
+// For one query token: one softmax over {top-K main-KV entries} U {SWA rows},
+// logits q_h . k_j / sqrt(512), key = value = the dequantised 512-d latent
+// ("DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression", sections
+// 3.3.1-3.3.2: key = value = content, a convex combination of the selected
+// entries; "DeepSeek-V4.1-Flash - Architecture", section 2: 64 heads x 512,
+// top-512 + SWA-128).  FP4 stores the cache; the values are dequantised before
+// the products (section 2.4.4: FP4 reduces storage, not matmul cost).
+//
+// Work split (flash-decoding): a CTA owns 128 keys of one query token -- one
+// chunk of the top-K list or of the SWA window -- and writes a partial (row
+// max, row sum, unnormalised output) per head; a combine kernel merges the
+// chunks.  Inside a CTA, with the keys as the MMA M dimension:
+//   gather   warp 0 issues one 288-byte bulk copy per selected entry into
+//            shared memory (cp.async.bulk, mbarrier tx-count);
+//   dequant  every thread turns its share of codes into fp16 (E2M1 x E4M3 is
+//            exact in fp16) in a 128B-swizzled K-major tile [128 keys x 512];
+//            SWA rows (E4M3) are converted straight from global memory;
+//   S^T      = K Q^T: 32 tcgen05 MMAs (M=128 keys, N=64 heads, K=16), fp32 in
+//            TMEM; Q (bf16 -> fp16) sits in shared memory K-major;
+//   softmax  each thread owns one key row of S^T for 32 heads; per-head max
+//            and sum over the 128 keys by warp butterfly transposes + shared
+//            memory; P = exp2(S - m) (times the SWA row scale) in fp16 written
+//            MN-major [128 keys x 64 heads];
+//   O^T      = V^T P: the same shared tile read MN-major as A (M = 512 dims in
+//            4 tiles of 128, K = 128 keys), P as B; fp32 in TMEM;
+//   store    per (head, dim) the unnormalised partial, coalesced along dims.
+// Shared memory: 128 KB tile (the FP4 staging area lives in its tail and is
+// consumed through registers before the tile is written), 64 KB Q (reused for
+// P), reductions; one CTA per SM.  TMEM: 256 columns (S^T uses 64 of them and
+// is dead before O^T is written).
+#include "kernels.cuh"
+
+namespace csa2 {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTileBytes = ATTN_CHUNK * D * 2;      // 128 KB fp16
+constexpr int kAtomCol = ATTN_CHUNK * 128;          // 16 KB per 64-dim column of the tile
+constexpr int kQBytes = H * D * 2;                  // 64 KB fp16
+constexpr int kQAtomCol = H * 128;                  // 8 KB
+constexpr int kStageOff = kTileBytes - ATTN_CHUNK * ENTRY_BYTES;   // FP4 staging at the tile's tail
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kIdescQK = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ H, /*M*/ ATTN_CHUNK);
+constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B MN-major*/ 1, /*N*/ H, /*M*/ 128);
+
+struct __align__(8) AttnSmem {
+  uint64_t bar_load;
+  uint64_t bar_mma;
+  uint32_t tmem_base;
+  uint32_t vmask[ATTN_CHUNK / 32];
+  float row_scale[ATTN_CHUNK];
+  float red[4][H];
+  float mfin[H];
+  float lfin[H];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)kTileBytes + kQBytes + sizeof(AttnSmem);
+
+// byte offset of 16-byte chunk `c` (0..63 along 512 fp16 channels) of row r in a
+// K-major SW128 tile made of 64-channel columns of `col_bytes` each
+__device__ __forceinline__ uint32_t swz_off(int r, int c, int col_bytes) {
+  return (uint32_t)((c >> 3) * col_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Butterfly transpose-reduction over the 32 lanes of a warp: on entry every
+// lane holds v[0..31] (one value per head column); on exit v[0] of lane l holds
+// the reduction over all lanes of column l.
+template <bool kMax>
+__device__ __forceinline__ void warp_transpose_reduce(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *tile = base;                  // [8 cols][128 keys][128 B] fp16, SW128
+  uint8_t *qs = base + kTileBytes;       // [8 cols][64 heads][128 B] fp16, SW128; later P
+  AttnSmem &S = *reinterpret_cast<AttnSmem *>(qs + kQBytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = blockIdx.x, p = blockIdx.y;
+  const bool is_swa = chunk >= a.n_kchunks;
+  const int64_t seq_row0 = (int64_t)p * a.cap;   // decode: problem p reads sequence p's cache
+
+  if (tid == 0) {
+    mbar_init(&S.bar_load, 1);
+    mbar_init(&S.bar_mma, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&S.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+  bool ok = true;
+
+  // ---------------------------------------------------------------- gather
+  if (!is_swa) {
+    if (warp == 0) {
+      int32_t ids[4];
+      uint32_t cnt = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = chunk * ATTN_CHUNK + i * 32 + lane;
+        int32_t id = (j < a.K) ? __ldg(a.idx + (int64_t)p * a.K + j) : -1;
+        if (id >= a.cap) {
+          set_error(CSA2_DEV_ERR_INDEX);
+          id = -1;
+        }
+        ids[i] = id;
+        const uint32_t m = __ballot_sync(0xffffffffu, id >= 0);
+        if (lane == 0) S.vmask[i] = m;
+        cnt += __popc(m);
+      }
+      if (lane == 0) mbar_arrive_expect_tx(&S.bar_load, cnt * ENTRY_BYTES);
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (ids[i] >= 0)
+          bulk_g2s(tile + kStageOff + (i * 32 + lane) * ENTRY_BYTES, a.kv + (seq_row0 + ids[i]) * ENTRY_BYTES,
+                   ENTRY_BYTES, &S.bar_load);
+    }
+    if (tid < ATTN_CHUNK) S.row_scale[tid] = 1.0f;
+  } else {
+    const int t0 = (chunk - a.n_kchunks) * ATTN_CHUNK;
+    const int len = min(__ldg(a.swa_len + p), a.W);
+    if (tid < ATTN_CHUNK) {
+      const int t = t0 + tid;
+      S.row_scale[tid] = (t < len) ? __ldg(a.swa_scale + (int64_t)p * a.W + t) : 0.0f;
+    }
+    if (warp == 0) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t m = __ballot_sync(0xffffffffu, t0 + i * 32 + lane < len);
+        if (lane == 0) S.vmask[i] = m;
+      }
+    }
+  }
+
+  // Q: bf16 -> fp16 into the K-major SW128 layout (|q| < 65504 assumed)
+  {
+    const uint4 *qg = reinterpret_cast<const uint4 *>(a.q + (int64_t)p * H * D);
+#pragma unroll 4
+    for (int i = tid; i < H * D / 8; i += kThreads) {
+      const int h = i >> 6, c = i & 63;
+      const uint4 v = __ldg(qg + i);
+      uint4 o;
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t r[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        r[k] = pack_half2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
+      o.x = r[0]; o.y = r[1]; o.z = r[2]; o.w = r[3];
+      *reinterpret_cast<uint4 *>(qs + swz_off(h, c, kQAtomCol)) = o;
+    }
+  }
+
+  // ---------------------------------------------------------------- dequant
+  const int row = tid >> 1, half = tid & 1;   // 2 threads per key, 256 channels each
+  if (!is_swa) {
+    ok = mbar_wait(&S.bar_load, 0);
+    const bool valid = (S.vmask[row >> 5] >> (row & 31)) & 1;
+    uint4 codes[8];
+    uint4 scl;
+    const uint8_t *src = tile + kStageOff + row * ENTRY_BYTES;
+    if (valid && ok) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) codes[k] = *reinterpret_cast<const uint4 *>(src + half * 128 + k * 16);
+      scl = *reinterpret_cast<const uint4 *>(src + 256 + half * 16);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) codes[k] = make_uint4(0, 0, 0, 0);
+      scl = make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();   // the staging area is read; the tile may now be written over it
+    const uint32_t sw[4] = {scl.x, scl.y, scl.z, scl.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      // 16 bytes of codes = 32 channels = scale groups 2k, 2k+1 of this half
+      const uint32_t cw[4] = {codes[k].x, codes[k].y, codes[k].z, codes[k].w};
+#pragma unroll
+      for (int g = 0; g < 2; ++g) {
+        const uint32_t sb = (sw[k >> 1] >> (8 * ((k & 1) * 2 + g))) & 0xFFu;
+        const uint32_t s2 = e4m3x2_to_half2((uint16_t)(sb | (sb << 8)));
+        uint32_t h0[4], h1[4];
+        e2m1x8_to_half2x4(cw[2 * g], h0);
+        e2m1x8_to_half2x4(cw[2 * g + 1], h1);
+        uint4 o0, o1;
+        o0.x = hmul2_u32(h0[0], s2); o0.y = hmul2_u32(h0[1], s2);
+        o0.z = hmul2_u32(h0[2], s2); o0.w = hmul2_u32(h0[3], s2);
+        o1.x = hmul2_u32(h1[0], s2); o1.y = hmul2_u32(h1[1], s2);
+        o1.z = hmul2_u32(h1[2], s2); o1.w = hmul2_u32(h1[3], s2);
+        const int ch16 = half * 32 + k * 4 + g * 2;   // 16-byte chunk index of the first 8 channels
+        *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16, kAtomCol)) = o0;
+        *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16 + 1, kAtomCol)) = o1;
+      }
+    }
+  } else {
+    const int t = (chunk - a.n_kchunks) * ATTN_CHUNK + row;
+    const bool valid = (S.vmask[row >> 5] >> (row & 31)) & 1;
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.swa + ((int64_t)p * a.W + t) * D + half * 256);
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+      const uint4 v = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint4 o0, o1;
+      o0.x = e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)); o0.y = e4m3x2_to_half2((uint16_t)(w[0] >> 16));
+      o0.z = e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)); o0.w = e4m3x2_to_half2((uint16_t)(w[1] >> 16));
+      o1.x = e4m3x2_to_half2((uint16_t)(w[2] & 0xFFFF)); o1.y = e4m3x2_to_half2((uint16_t)(w[2] >> 16));
+      o1.z = e4m3x2_to_half2((uint16_t)(w[3] & 0xFFFF)); o1.w = e4m3x2_to_half2((uint16_t)(w[3] >> 16));
+      const int ch16 = half * 32 + k * 2;
+      *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16, kAtomCol)) = o0;
+      *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16 + 1, kAtomCol)) = o1;
+    }
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+
+  // ------------------------------------------------------------- S^T = K Q^T
+  if (tid == 0 && ok) {
+    tc_fence_after();
+    const uint32_t ta = smem_u32(tile), qa = smem_u32(qs);
+#pragma unroll 4
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint64_t ad = smem_desc(ta + (kk >> 2) * kAtomCol + (kk & 3) * 32, 16, 1024);
+      const uint64_t bd = smem_desc(qa + (kk >> 2) * kQAtomCol + (kk & 3) * 32, 16, 1024);
+      mma_f16(tmem, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+    }
+    mma_commit(&S.bar_mma);
+  }
+  if (ok) ok = mbar_wait(&S.bar_mma, 0);
+  tc_fence_after();
+
+  // ---------------------------------------------------------------- softmax
+  const int quad = warp & 3, hh = warp >> 2;   // key rows 32*quad.., heads 32*hh..
+  const int key = quad * 32 + lane;
+  float s[32];
+  {
+    uint32_t v[32];
+    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(hh * 32), v);
+    tmem_ld_wait();
+    const bool valid = ok && ((S.vmask[key >> 5] >> (key & 31)) & 1);
+    // log2(e) / sqrt(512), times the SWA row scale (the key is code x scale)
+    const float f = 0.06375871295460785f * S.row_scale[key];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s[i] = valid ? __uint_as_float(v[i]) * f : -INFINITY;
+  }
+  {
+    float t[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) t[i] = s[i];
+    warp_transpose_reduce<true>(t, lane);
+    S.red[quad][hh * 32 + lane] = t[0];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (tid < H) S.mfin[tid] = fmaxf(fmaxf(S.red[0][tid], S.red[1][tid]), fmaxf(S.red[2][tid], S.red[3][tid]));
+  __syncthreads();
+  {
+    const float rs = S.row_scale[key];
+    uint8_t *prow = qs + key * 128;   // P tile: [128 keys][64 heads] fp16, MN-major SW128
+    float t[32];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i0 = c * 8 + 2 * k;
+        const float m0 = S.mfin[hh * 32 + i0], m1 = S.mfin[hh * 32 + i0 + 1];
+        const float p0 = (m0 == -INFINITY) ? 0.0f : exp2f(s[i0] - m0);
+        const float p1 = (m1 == -INFINITY) ? 0.0f : exp2f(s[i0 + 1] - m1);
+        t[i0] = p0;
+        t[i0 + 1] = p1;
+        w[k] = pack_half2(p0 * rs, p1 * rs);
+      }
+      *reinterpret_cast<uint4 *>(prow + (((hh * 4 + c) ^ (key & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    warp_transpose_reduce<false>(t, lane);
+    __syncthreads();   // every thread has read mfin/red before red is reused
+    S.red[quad][hh * 32 + lane] = t[0];
+  }
+  fence_proxy_async_smem();
+  __syncthreads();
+  if (tid < H) S.lfin[tid] = (S.red[0][tid] + S.red[1][tid]) + (S.red[2][tid] + S.red[3][tid]);
+
+  // ------------------------------------------------------------- O^T = V^T P
+  if (tid == 0 && ok) {
+    tc_fence_after();
+    const uint32_t ta = smem_u32(tile), pa = smem_u32(qs);
+#pragma unroll 1
+    for (int mt = 0; mt < D / 128; ++mt) {
+#pragma unroll
+      for (int kk = 0; kk < ATTN_CHUNK / 16; ++kk) {
+        const uint64_t ad = smem_desc(ta + (2 * mt) * kAtomCol + kk * 2048, kAtomCol, 1024);
+        const uint64_t bd = smem_desc(pa + kk * 2048, 8192, 1024);
+        mma_f16(tmem + mt * H, ad, bd, kIdescPV, kk > 0 ? 1u : 0u);
+      }
+    }
+    mma_commit(&S.bar_mma);
+  }
+  if (ok) ok = mbar_wait(&S.bar_mma, 1);
+  tc_fence_after();
+  __syncthreads();
+
+  // ---------------------------------------------------------------- store
+  {
+    const int64_t pc = (int64_t)p * a.n_chunks + chunk;
+    float *po = a.part_o + pc * H * D;
+#pragma unroll 1
+    for (int mt = 0; mt < D / 128; ++mt) {
+      uint32_t v[32];
+      tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * H + hh * 32), v);
+      tmem_ld_wait();
+      const int d = mt * 128 + quad * 32 + lane;
+#pragma unroll 8
+      for (int i = 0; i < 32; ++i) po[(int64_t)(hh * 32 + i) * D + d] = ok ? __uint_as_float(v[i]) : 0.0f;
+    }
+    if (tid < H) {
+      a.part_ml[pc * 2 * H + tid] = ok ? S.mfin[tid] : -INFINITY;
+      a.part_ml[pc * 2 * H + H + tid] = ok ? S.lfin[tid] : 0.0f;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Merge the chunk partials of each (token, head): m = max_c m_c,
+// l = sum_c l_c 2^(m_c - m), o = sum_c o_c 2^(m_c - m) / l; lse in natural log.
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+  const int p = blockIdx.y;
+  const int h = blockIdx.x;
+  const int n = a.n_chunks;
+  __shared__ float wgt[64];
+  __shared__ float inv_l;
+  if (threadIdx.x == 0) {
+    float m = -INFINITY;
+    for (int c = 0; c < n; ++c) m = fmaxf(m, a.part_ml[((int64_t)p * n + c) * 2 * H + h]);
+    float l = 0.0f;
+    for (int c = 0; c < n; ++c) {
+      const float mc = a.part_ml[((int64_t)p * n + c) * 2 * H + h];
+      const float w = (mc == -INFINITY) ? 0.0f : exp2f(mc - m);
+      wgt[c] = w;
+      l += w * a.part_ml[((int64_t)p * n + c) * 2 * H + H + h];
+    }
+    inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
+    if (a.lse) a.lse[(int64_t)p * H + h] = (l > 0.0f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+  }
+  __syncthreads();
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float acc = 0.0f;
+    for (int c = 0; c < n; ++c) acc += wgt[c] * a.part_o[(((int64_t)p * n + c) * H + h) * D + d];
+    a.out[((int64_t)p * H + h) * D + d] = acc * inv_l;
+  }
+}
+
+}  // namespace
+
+size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W) {
+  const int n_chunks = (K + ATTN_CHUNK - 1) / ATTN_CHUNK + (W + ATTN_CHUNK - 1) / ATTN_CHUNK;
+  size_t b = (size_t)problems * n_chunks * H * D * 4;
+  b = (b + 255) & ~size_t(255);
+  b += (size_t)problems * n_chunks * 2 * H * 4;
+  return (b + 255) & ~size_t(255);
+}
+
+cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches) {
+  if (a.problems <= 0) return cudaSuccess;
+  a.n_kchunks = (a.K + ATTN_CHUNK - 1) / ATTN_CHUNK;
+  a.n_chunks = a.n_kchunks + (a.W + ATTN_CHUNK - 1) / ATTN_CHUNK;
+  uint8_t *p = static_cast<uint8_t *>(scratch);
+  a.part_o = reinterpret_cast<float *>(p);
+  size_t off = ((size_t)a.problems * a.n_chunks * H * D * 4 + 255) & ~size_t(255);
+  a.part_ml = reinterpret_cast<float *>(p + off);
+  if (a.n_chunks == 0) {
+    // no key at all: out = 0, lse = -inf
+    cudaError_t e = cudaMemsetAsync(a.out, 0, (size_t)a.problems * H * D * 4, stream);
+    if (e != cudaSuccess || !a.lse) return e;
+    a.n_chunks = 0;
+    attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
+    ++*launches;
+    return cudaGetLastError();
+  }
+  cudaError_t err = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
+  const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
+  if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
+  sparse_attn_kernel<<<dim3(a.n_chunks, a.problems), kThreads, kSmemBytes, stream>>>(a);
+  if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
+  attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
+  *launches += 2;
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

@@ -1,0 +1,115 @@
+// Shared constants and launcher declarations of the CSA2 kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace csa2 {
+
+// Head geometry ("DeepSeek-V4.1-Flash - Architecture", section 2, main
+// attention settings): 512-d latent with a 64-channel RoPE tail, 64 query
+// heads, 32 indexer heads x 128.
+constexpr int D = 512;
+constexpr int ROPE_DIM = 64;
+constexpr int H = 64;
+constexpr int HI = 32;
+constexpr int DI = 128;
+constexpr int ENTRY_BYTES = 288;   // 256 B codes + 32 B E4M3 scales
+constexpr int BLOCK = 8;           // HSI candidate block width
+
+// Indexer sweep: 128 positions per tile (the MMA M dimension).
+constexpr int SWEEP_TILE = 128;
+// Attention: 128 keys per CTA (the MMA M dimension of S^T = K Q^T).
+constexpr int ATTN_CHUNK = 128;
+// Radix select: 11-bit first digit.
+constexpr int TOPK_BINS = 2048;
+constexpr int TOPK_MAX_K = 8192;
+
+// Per-row scratch of a top-K selection (kept in the caller's workspace).
+struct TopkScratch {
+  uint32_t *hist;      // [rows][TOPK_BINS]
+  uint32_t *counters;  // [rows][4]: selected, candidates, threshold bin + 1, above
+  int32_t *sel;        // [rows][k]
+  uint64_t *cand;      // [rows][row_len]
+};
+
+// Description of one batched top-K: rows of `row_len` fp32 values where -inf
+// marks an invalid slot.
+struct TopkRows {
+  const float *vals;       // [rows][row_stride]
+  int64_t row_len;
+  int64_t row_stride;
+  int32_t rows;
+  int32_t k;
+  // HSI: the block holding position n_vis[b]-1 is forced in (key of +inf)
+  const int32_t *force_nvis;  // NULL = no forcing
+  int32_t force_block;        // block width for the forced element
+  int64_t n_max;              // n_vis clamp
+  // output mapping: NULL -> index itself; else slot j -> pool[b][j/8]*8 + j%8
+  const int32_t *pool;
+  int32_t pool_stride;
+  int32_t *out;             // [rows][k] ascending, -1 padded
+};
+
+// Benchmark timing hook (csa2_set_profile_events): events recorded around a kernel.
+struct ProfileEvents {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+ProfileEvents &profile_events(int kernel);
+// Records `ev` on `stream`; inside a stream capture it becomes an event-record
+// node of the graph, so every replay records it.
+cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream);
+
+cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int64_t n_entries, const int64_t *pos,
+                                  const int64_t *slot, uint8_t *kv, int64_t kv_rows, float rope_theta,
+                                  cudaStream_t stream);
+
+struct SweepArgs {
+  const float *w;             // [B][32]
+  const int32_t *n_vis;       // [B]
+  const int32_t *pool;        // [B][pool_nb] (Reindex) or NULL (Full)
+  float *scores;              // [B][row_len]
+  float *block_scores;        // [B][nblk_stride] or NULL
+  int64_t cap;
+  int64_t n_max;
+  int64_t row_len;            // tiles_per_seq * 128
+  int32_t batch;
+  int32_t tiles_per_seq;
+  int32_t pool_nb;
+  int32_t nblk_stride;        // ceil(n_max / 8)
+  int32_t block_reduce;       // 0 max, 1 sum
+};
+
+cudaError_t launch_indexer_sweep(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
+                                 int num_sms, cudaStream_t stream, int *launches);
+
+size_t topk_scratch_bytes(int32_t rows, int64_t row_len, int32_t k);
+TopkScratch carve_topk_scratch(void *base, int32_t rows, int64_t row_len, int32_t k);
+cudaError_t launch_topk(const TopkRows &r, const TopkScratch &s, int num_sms, cudaStream_t stream, int *launches);
+
+struct AttnArgs {
+  const __nv_bfloat16 *q;     // [P][64][512]
+  const uint8_t *kv;          // [B][cap][288]
+  const int32_t *idx;         // [P][K]
+  const uint8_t *swa;         // [P][W][512] (E4M3)
+  const float *swa_scale;     // [P][W]
+  const int32_t *swa_len;     // [P]
+  float *part_o;              // [P][n_chunks][64][512]
+  float *part_ml;             // [P][n_chunks][2][64]
+  float *out;                 // [P][64][512]
+  float *lse;                 // [P][64] or NULL
+  int64_t cap;
+  int32_t problems;
+  int32_t K;
+  int32_t W;
+  int32_t n_kchunks;
+  int32_t n_chunks;
+};
+
+size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W);
+cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches);
+
+}  // namespace csa2

@@ -1,0 +1,114 @@
+// csa2_kv_quant_write kernel: compressor (m = 2) -> RoPE on the tail 64
+// channels -> FP4 (E2M1 codes, one E4M3 scale per 16 channels, no global
+// scale).  "DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression",
+// section 2.4.4 (quantisation after RoPE; E2M1 with an E4M3 scale per 16
+// channels, no second-level scale); "DeepSeek-V4.1-Flash - Architecture",
+// section 4.
+//
+// One warp writes one 288-byte entry; lane g owns channel group g (16
+// channels): it loads 32 bytes of bf16 per source position, produces its
+// scale byte and 8 bytes of codes, so the warp stores 256 contiguous code
+// bytes and 32 contiguous scale bytes.  Decode writes one entry per sequence,
+// so the kernel is latency-bound; the m = 2 chunked-prefill write streams
+// 4 KB of input per entry and is bandwidth-bound.
+#include "kernels.cuh"
+
+namespace csa2 {
+
+namespace {
+
+__device__ __forceinline__ void load_bf16x16(const __nv_bfloat16 *p, float (&x)[16]) {
+  const uint4 *v = reinterpret_cast<const uint4 *>(p);
+  uint4 a = __ldg(v), b = __ldg(v + 1);
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+__global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16 *__restrict__ latent,
+                                                             const __nv_bfloat16 *__restrict__ z, int m,
+                                                             int64_t n_entries, const int64_t *__restrict__ pos,
+                                                             const int64_t *__restrict__ slot,
+                                                             uint8_t *__restrict__ kv, int64_t kv_rows,
+                                                             float rope_theta) {
+  const int lane = threadIdx.x & 31;
+  const int64_t e = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e >= n_entries) return;
+  const int64_t row = slot[e];
+  if (row < 0 || row >= kv_rows) {
+    if (lane == 0) set_error(CSA2_DEV_ERR_INDEX);
+    return;
+  }
+  const int c0 = lane * 16;
+  float x[16];
+  if (m == 1) {
+    load_bf16x16(latent + e * D + c0, x);
+  } else {
+    // Channel-wise softmax over the m = 2 source positions, in double,
+    // rounded once to fp32.
+    float x0[16], x1[16], z0[16], z1[16];
+    load_bf16x16(latent + (e * 2 + 0) * D + c0, x0);
+    load_bf16x16(latent + (e * 2 + 1) * D + c0, x1);
+    load_bf16x16(z + (e * 2 + 0) * D + c0, z0);
+    load_bf16x16(z + (e * 2 + 1) * D + c0, z1);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      // explicit IEEE double ops: no contraction into fused multiply-adds
+      const double zm = fmax((double)z0[i], (double)z1[i]);
+      const double ea = exp(__dsub_rn((double)z0[i], zm)), eb = exp(__dsub_rn((double)z1[i], zm));
+      const double den = __dadd_rn(ea, eb);
+      const double wa = __ddiv_rn(ea, den), wb = __ddiv_rn(eb, den);
+      const double num = __dadd_rn(__dmul_rn(wa, (double)x0[i]), __dmul_rn(wb, (double)x1[i]));
+      x[i] = __double2float_rn(num);
+    }
+  }
+  if (c0 >= D - ROPE_DIM) {
+    // RoPE: interleaved pairs (448 + 2j, 449 + 2j), inverse frequency
+    // fl32(theta^(-2j/64)), angle exact in double, no fused multiply-add.
+    const double p = (double)pos[e];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int j = (c0 - (D - ROPE_DIM)) / 2 + i;
+      const float inv = (float)pow((double)rope_theta, -(2.0 * j) / (double)ROPE_DIM);
+      const double ang = p * (double)inv;
+      const float c = (float)cos(ang), s = (float)sin(ang);
+      const float a = x[2 * i], b = x[2 * i + 1];
+      x[2 * i] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+      x[2 * i + 1] = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
+    }
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
+  const uint32_t sbyte = cvt_e4m3(__fdiv_rn(amax, 6.0f));
+  const float sd = e4m3_to_f32(sbyte);
+  uint32_t lo = 0, hi = 0;
+  if (sd != 0.0f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lo |= cvt_e2m1x2(__fdiv_rn(x[2 * i + 1], sd), __fdiv_rn(x[2 * i], sd)) << (8 * i);
+      hi |= cvt_e2m1x2(__fdiv_rn(x[8 + 2 * i + 1], sd), __fdiv_rn(x[8 + 2 * i], sd)) << (8 * i);
+    }
+  }
+  uint8_t *dst = kv + row * ENTRY_BYTES;
+  reinterpret_cast<uint2 *>(dst)[lane] = make_uint2(lo, hi);
+  dst[256 + lane] = (uint8_t)sbyte;
+}
+
+}  // namespace
+
+cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int64_t n_entries, const int64_t *pos,
+                                  const int64_t *slot, uint8_t *kv, int64_t kv_rows, float rope_theta,
+                                  cudaStream_t stream) {
+  const int warps = 8;
+  const int64_t blocks = (n_entries + warps - 1) / warps;
+  kv_quant_write_kernel<<<(unsigned)blocks, warps * 32, 0, stream>>>(
+      static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
+      kv, kv_rows, rope_theta);
+  return cudaGetLastError();
+}
+
+}  // namespace csa2

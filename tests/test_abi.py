@@ -1,0 +1,98 @@
+"""CPU-side checks of the C ABI: the library builds for sm_103a, loads, exports
+every function include/csa2.h declares, and rejects bad arguments on the host
+without launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def c2():
+    import sparse_attention_fp4_csa2_gb300.build as b
+    b.build()
+    import sparse_attention_fp4_csa2_gb300 as c
+    return c
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "csa2.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(csa2_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(c2):
+    names = declared_functions()
+    assert len(names) >= 10
+    L = c2.lib()
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_defaults_and_sizes(c2):
+    p = c2.default_params()
+    assert (p.index_topk, p.sliding_window, p.candidate_block_size, p.candidate_topk_blocks, p.block_reduce,
+            p.hsi) == (512, 128, 8, 2048, 0, 1)
+    assert c2.entry_bytes() == 288
+    assert c2.lib().csa2_status_string(3) == b"workspace too small"
+
+
+def test_workspace_sizes(c2):
+    p = c2.Params.make()
+    for op in range(4):
+        assert c2.workspace_bytes(op, 32, 65536, p) > 0
+    # decode workspace covers every stage
+    d = c2.workspace_bytes(c2.OP_DECODE, 4, 1 << 20, p)
+    assert d >= c2.workspace_bytes(c2.OP_INDEXER, 4, 1 << 20, p)
+    assert d >= c2.workspace_bytes(c2.OP_ATTN, 4, 1 << 20, p)
+    bad = c2.Params.make(candidate_block_size=16)
+    assert c2.workspace_bytes(c2.OP_DECODE, 4, 1000, bad) == 0
+    assert c2.workspace_bytes(c2.OP_DECODE, 0, 1000, p) == 0
+
+
+def test_host_validation_rejects_without_launch(c2):
+    L = c2.lib()
+    P = ctypes.c_void_p
+    p = c2.Params.make()
+    fake = P(0x1000)          # never dereferenced: validation fails first
+    odd = P(0x1001)
+    # null pointers
+    assert L.csa2_kv_quant_write(None, None, 1, 4, fake, fake, fake, 4, 10000.0, None) == 1
+    # misaligned latent
+    assert L.csa2_kv_quant_write(odd, None, 1, 4, fake, fake, fake, 4, 10000.0, None) == 1
+    # m = 2 without logits
+    assert L.csa2_kv_quant_write(fake, None, 2, 4, fake, fake, fake, 4, 10000.0, None) == 1
+    # empty write is OK and launches nothing
+    assert L.csa2_kv_quant_write(None, None, 1, 0, None, None, None, 0, 10000.0, None) == 0
+    assert c2.last_launch_count() == 0
+    # unsupported block width
+    bad = c2.Params.make(candidate_block_size=4)
+    assert L.csa2_indexer_score_topk(fake, fake, fake, 1, 100, fake, 100, None, ctypes.byref(bad), fake, None,
+                                     P(0x1000), 1 << 30, None) == 2
+    # workspace too small
+    assert L.csa2_indexer_score_topk(fake, fake, fake, 1, 100, fake, 100, None, ctypes.byref(p), fake, None,
+                                     P(0x1000), 16, None) == 3
+    # n_max above the cache capacity
+    assert L.csa2_indexer_score_topk(fake, fake, fake, 1, 100, fake, 200, None, ctypes.byref(p), fake, None,
+                                     P(0x1000), 1 << 30, None) == 1
+    # REINDEX needs a pool
+    assert L.csa2_sparse_decode(1, ctypes.byref(p), 1, fake, fake, fake, fake, fake, 100, fake, 100, fake, fake,
+                                fake, fake, None, fake, None, P(0x1000), 1 << 30, None) == 1
+    # bad mode
+    assert L.csa2_sparse_decode(7, ctypes.byref(p), 1, fake, fake, fake, fake, fake, 100, fake, 100, fake, fake,
+                                fake, fake, fake, fake, None, P(0x1000), 1 << 30, None) == 1
+
+
+def test_schedule_host_logic():
+    from sparse_attention_fp4_csa2_gb300 import schedule as s
+    dec = s.decoder_modes()
+    assert [m.value for m in dec[:8]] == ["full", "reuse", "reuse", "reuse", "reindex", "reuse", "reuse", "reuse"]
+    assert len(dec) == 20 and sum(m == s.Mode.REINDEX for m in dec) == 4
+    enc = s.encoder_modes()
+    assert len(enc) == 20 and sum(m == s.Mode.FULL for m in enc) == 3
+    s.validate(dec)
+    with pytest.raises(ValueError):
+        s.validate(["reuse", "full"])
