@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--config", default="c1")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     return ap.parse_args()
 
 
@@ -157,6 +158,7 @@ class Workload:
         self.lse = torch.empty(len(cfg.schedule), B, 64, device=device)
         self.ws = c2.workspace(c2.OP_DECODE, B, N, self.params, device=device)
         torch.cuda.synchronize()
+        torch.cuda.empty_cache()
 
     def step(self):
         c2, L = self.c2, self.layers
@@ -192,6 +194,9 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     cfg = synth.CONFIGS[args.config]
+    if args.batch:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}[batch={args.batch}]")
     wl = Workload(cfg, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -203,6 +208,8 @@ def run_ours(args, rank, world, local_rank):
     assert c2.get_device_status(stream) == 0
     sweep_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     attn_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    for ev in sweep_ev + attn_ev:
+        ev.record(stream)          # marks the events recorded; the graph re-records them every replay
     c2.set_profile_events(c2.KERNEL_INDEXER_SWEEP, *sweep_ev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
