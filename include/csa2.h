@@ -189,6 +189,32 @@ csa2_status csa2_sparse_decode(csa2_mode mode, const csa2_params *params, int32_
                                int32_t *topk_idx, int32_t *pool_blocks, float *out, float *lse,
                                void *ws, size_t ws_bytes, csa2_stream_t stream);
 
+/*
+ * csa2_hier_pool_select_static -- csa2_hier_pool_select without a workspace.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory where they select the pool: a runtime that
+ * replays a fixed, pre-planned memory layout and forbids allocation while it
+ * executes, or host code that holds only raw pointers to its inputs and
+ * outputs and has no allocator to ask for scratch.
+ * Same arguments and result as csa2_hier_pool_select, minus ws / ws_bytes.
+ * The scratch is a static device array of CSA2_POOL_STATIC_SCRATCH_BYTES
+ * (16 MiB) inside this library, held by every GPU that loads it until the
+ * process exits.  The call never allocates or frees memory.  Its first call on
+ * a device looks up that array's device address (once per device, with the
+ * device current), so make that first call before any stream capture.  A
+ * request needing more scratch than the array holds (about batch *
+ * ceil(n_max/8) * 8 bytes of candidates plus 8 KB and 4 * candidate_topk_blocks
+ * bytes per sequence) returns CSA2_ERR_WORKSPACE without launching.  All calls
+ * on a device share the array and it keeps the last call's contents; each call
+ * clears the counters it needs first, and calls that overlap on the GPU
+ * (other streams or host threads) race on it and must be serialised by the
+ * caller.
+ */
+#define CSA2_POOL_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+csa2_status csa2_hier_pool_select_static(const float *block_scores, const int32_t *n_vis,
+                                         int32_t batch, int64_t n_max, const csa2_params *params,
+                                         int32_t *pool_blocks, csa2_stream_t stream);
+
 /* Operation selector for csa2_workspace_bytes. */
 typedef enum {
   CSA2_OP_INDEXER = 0,   /* csa2_indexer_score_topk        */
