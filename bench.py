@@ -8,7 +8,7 @@ in HBM.  The step is captured once in a CUDA graph and replayed; each step is
 timed with CUDA events on the launching stream and L2 is flushed (a 512 MB
 write) between steps, outside the timed events.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config c1|c2|c3] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config group_decode_32x64k|hsi_reindex_16x256k|decoder20_4x1m] [--impl ours|reference]
 
 N > 1 (torchrun): replicas -- every rank runs the same per-GPU workload on its
 own GPU; value = total tokens of all ranks / max-over-ranks time.
@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="c1")
+    ap.add_argument("--config", default="group_decode_32x64k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
@@ -160,7 +160,9 @@ class Workload:
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
-    def step(self):
+    def step(self, sweep_events=None):
+        """Enqueue one decode step; with sweep_events, the Full layer's indexer
+        sweep launch is bracketed by those events."""
         c2, L = self.c2, self.layers
         launches = 0
         c2.kv_quant_write(self.new_latent, None, 1, self.new_pos, self.new_slot, self.kv.view(-1, 288))
@@ -168,9 +170,13 @@ class Workload:
         for i, mode in enumerate(self.cfg.schedule):
             li = L[i]
             idx_args = {} if mode == "reuse" else dict(q_idx=li.q_idx, w=li.w, k_idx=self.k_idx)
+            if sweep_events and mode == "full":
+                c2.set_profile_events(c2.KERNEL_INDEXER_SWEEP, *sweep_events)
             c2.sparse_decode(mode, self.params, li.q, self.kv, self.n_vis, self.N, li.swa, li.swa_scale,
                              li.swa_len, self.topk, self.out[i], self.ws, pool_blocks=self.pool,
                              lse=self.lse[i], **idx_args)
+            if sweep_events and mode == "full":
+                c2.set_profile_events(c2.KERNEL_INDEXER_SWEEP, None, None)
             launches += c2.last_launch_count()
         return launches
 
@@ -200,6 +206,7 @@ def run_ours(args, rank, world, local_rank):
     wl = Workload(cfg, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    flush2 = torch.ones(128 << 20, dtype=torch.float32, device=dev)
 
     # eager warm-up (also counts our launches per step), then capture the step
     with torch.cuda.stream(stream):
@@ -210,14 +217,19 @@ def run_ours(args, rank, world, local_rank):
     attn_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     for ev in sweep_ev + attn_ev:
         ev.record(stream)          # marks the events recorded; the graph re-records them every replay
-    c2.set_profile_events(c2.KERNEL_INDEXER_SWEEP, *sweep_ev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
-        wl.step()
-    c2.set_profile_events(c2.KERNEL_INDEXER_SWEEP, None, None)
+        wl.step(sweep_events=sweep_ev)
+
+    def flush_l2():
+        # write a buffer larger than L2, then read another one so the written
+        # lines are evicted (written back) before the timed region starts
+        flush.zero_()
+        flush2.sum()
+
     for _ in range(max(3, args.warmup)):
         with torch.cuda.stream(stream):
-            flush.zero_()
+            flush_l2()
             g.replay()
     stream.synchronize()
 
@@ -226,7 +238,7 @@ def run_ours(args, rank, world, local_rank):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for _ in range(n):
             with torch.cuda.stream(stream):
-                flush.zero_()
+                flush_l2()
                 e0.record(stream)
                 if with_io:
                     for h, d in with_io[0]:
@@ -280,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": cfg.name, "batch": B, "context": cfg.n_ctx, "layers": "+".join(cfg.schedule),
-                   "hsi": bool(wl.hsi), "l2": "flushed between steps (512 MB write)",
+                   "hsi": bool(wl.hsi), "l2": "flushed between steps (512 MB write, then 512 MB read), outside the timed events",
                    "storage": "FP4 E2M1+E4M3/16 main KV, bf16 indexer K, E4M3 SWA",
                    "step_alg_bytes": step_bytes,
                    "step_hbm_gbs": round(step_bytes / (ms / 1e3) / 1e9, 1)},

@@ -216,7 +216,7 @@ void csa2o_kv_entries(const uint16_t *latent, const uint16_t *z, int m, int64_t 
 
 /* Lightning-indexer score of each key row: s_n = sum_h w_h * ReLU(q_h . k_n)
  * over 32 heads x 128 dims ([N] sec.2 main attention settings; the score form
- * is the one the benchmark spec fixes, no extra scale).  fp64. */
+ * is the plain weighted ReLU sum of head dot products, no extra scale).  fp64. */
 void csa2o_index_scores(const uint16_t *q, const float *w, const uint16_t *k, int64_t n,
                         double *s) {
     double qd[O_HI * O_DI];

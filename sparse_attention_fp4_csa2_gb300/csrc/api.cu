@@ -54,18 +54,26 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over rows of 128 elements, box {64, box_rows}, 128B swizzle.
-bool make_tmap_bf16_rows128(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows) {
+}  // namespace
+
+// 2-D bf16 tensor map over rows of `inner` elements, box {64, box_rows}, 128B swizzle.
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t inner, int64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {256};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)inner * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+bool make_tmap_bf16_rows128(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows) {
+  return make_tmap_bf16(m, ptr, 128, rows, box_rows);
 }
 
 bool params_ok(const csa2_params *p) {
@@ -86,7 +94,7 @@ IndexerLayout indexer_layout(int32_t batch, int64_t n_max, const csa2_params *p,
   L.row_len = pool ? (int64_t)p->candidate_topk_blocks * BLOCK : round_up(n_max, SWEEP_TILE);
   L.scores_off = 0;
   L.topk_off = (size_t)round_up((int64_t)batch * L.row_len * 4, 256);
-  L.end = L.topk_off + topk_scratch_bytes(batch, L.row_len, p->index_topk);
+  L.end = L.topk_off;   // the cluster top-K needs no scratch beyond the scores
   return L;
 }
 
@@ -163,8 +171,7 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   r.pool = pool_blocks;
   r.pool_stride = p->candidate_topk_blocks;
   r.out = topk_idx;
-  const TopkScratch s = carve_topk_scratch(wsb + L.topk_off, batch, L.row_len, p->index_topk);
-  return cuda_status(launch_topk(r, s, sms, stream, launches));
+  return cuda_status(launch_topk_cluster(r, stream, launches));
 }
 
 csa2_status run_pool(const float *block_scores, const int32_t *n_vis, int32_t batch, int64_t n_max,

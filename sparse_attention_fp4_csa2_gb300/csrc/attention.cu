@@ -43,6 +43,7 @@ constexpr int kAtomCol = ATTN_CHUNK * 128;          // 16 KB per 64-dim column o
 constexpr int kQBytes = H * D * 2;                  // 64 KB fp16
 constexpr int kQAtomCol = H * 128;                  // 8 KB
 constexpr int kStageOff = kTileBytes - ATTN_CHUNK * ENTRY_BYTES;   // FP4 staging at the tile's tail
+constexpr int kSwaStageOff = kTileBytes - ATTN_CHUNK * D;          // E4M3 SWA staging: the tile's upper half
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kIdescQK = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ H, /*M*/ ATTN_CHUNK);
 constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B MN-major*/ 1, /*N*/ H, /*M*/ 128);
@@ -89,7 +90,8 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[32], int lane) 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *tile = base;                  // [8 cols][128 keys][128 B] fp16, SW128
@@ -116,71 +118,82 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
   const uint32_t tmem = S.tmem_base;
   bool ok = true;
 
-  // ---------------------------------------------------------------- gather
-  if (!is_swa) {
-    if (warp == 0) {
-      int32_t ids[4];
-      uint32_t cnt = 0;
+  // ------------------------------------------------------------------ loads
+  // One mbarrier counts every byte: Q (8 TMA boxes of [64 heads x 64 dims]
+  // bf16 into the SW128 K-major layout) and either the selected FP4 entries
+  // (one 288-byte bulk copy each, into the staging area at the tile's tail) or
+  // the chunk's SWA rows (one contiguous bulk copy into the tile's upper half).
+  const int t0 = (chunk - a.n_kchunks) * ATTN_CHUNK;   // first SWA row of this chunk
+  int swa_rows = 0;
+  if (is_swa) {
+    const int len = min(__ldg(a.swa_len + p), a.W);
+    swa_rows = max(0, min(ATTN_CHUNK, len - t0));
+    if (tid < ATTN_CHUNK) S.row_scale[tid] = (tid < swa_rows) ? __ldg(a.swa_scale + (int64_t)p * a.W + t0 + tid) : 0.0f;
+  } else if (tid < ATTN_CHUNK) {
+    S.row_scale[tid] = 1.0f;
+  }
+  if (warp == 0) {
+    int32_t ids[4];
+    uint32_t cnt = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = chunk * ATTN_CHUNK + i * 32 + lane;
+    for (int i = 0; i < 4; ++i) {
+      const int r = i * 32 + lane;
+      bool v;
+      if (!is_swa) {
+        const int j = chunk * ATTN_CHUNK + r;
         int32_t id = (j < a.K) ? __ldg(a.idx + (int64_t)p * a.K + j) : -1;
         if (id >= a.cap) {
           set_error(CSA2_DEV_ERR_INDEX);
           id = -1;
         }
         ids[i] = id;
-        const uint32_t m = __ballot_sync(0xffffffffu, id >= 0);
-        if (lane == 0) S.vmask[i] = m;
-        cnt += __popc(m);
+        v = id >= 0;
+      } else {
+        ids[i] = -1;
+        v = r < swa_rows;
       }
-      if (lane == 0) mbar_arrive_expect_tx(&S.bar_load, cnt * ENTRY_BYTES);
-      __syncwarp();
+      const uint32_t m = __ballot_sync(0xffffffffu, v);
+      if (lane == 0) S.vmask[i] = m;
+      cnt += __popc(m);
+    }
+    if (lane == 0) {
+      const uint32_t bytes = (uint32_t)kQBytes +
+                             (is_swa ? (uint32_t)swa_rows * D : cnt * ENTRY_BYTES);
+      mbar_arrive_expect_tx(&S.bar_load, bytes);
+#pragma unroll
+      for (int j = 0; j < D / 64; ++j) tma_load_2d(qs + j * kQAtomCol, &tm_q, j * 64, p * H, &S.bar_load);
+      if (is_swa && swa_rows > 0)
+        bulk_g2s(tile + kSwaStageOff, a.swa + ((int64_t)p * a.W + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
+    }
+    __syncwarp();
+    if (!is_swa) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         if (ids[i] >= 0)
           bulk_g2s(tile + kStageOff + (i * 32 + lane) * ENTRY_BYTES, a.kv + (seq_row0 + ids[i]) * ENTRY_BYTES,
                    ENTRY_BYTES, &S.bar_load);
     }
-    if (tid < ATTN_CHUNK) S.row_scale[tid] = 1.0f;
-  } else {
-    const int t0 = (chunk - a.n_kchunks) * ATTN_CHUNK;
-    const int len = min(__ldg(a.swa_len + p), a.W);
-    if (tid < ATTN_CHUNK) {
-      const int t = t0 + tid;
-      S.row_scale[tid] = (t < len) ? __ldg(a.swa_scale + (int64_t)p * a.W + t) : 0.0f;
-    }
-    if (warp == 0) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t m = __ballot_sync(0xffffffffu, t0 + i * 32 + lane < len);
-        if (lane == 0) S.vmask[i] = m;
-      }
-    }
   }
+  ok = mbar_wait(&S.bar_load, 0);
 
-  // Q: bf16 -> fp16 into the K-major SW128 layout (|q| < 65504 assumed)
-  {
-    const uint4 *qg = reinterpret_cast<const uint4 *>(a.q + (int64_t)p * H * D);
+  // Q: bf16 -> fp16 in place (same 2-byte slots of the swizzled layout;
+  // |q| < 65504 assumed)
 #pragma unroll 4
-    for (int i = tid; i < H * D / 8; i += kThreads) {
-      const int h = i >> 6, c = i & 63;
-      const uint4 v = __ldg(qg + i);
-      uint4 o;
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t r[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        r[k] = pack_half2(__uint_as_float(w[k] << 16), __uint_as_float(w[k] & 0xFFFF0000u));
-      o.x = r[0]; o.y = r[1]; o.z = r[2]; o.w = r[3];
-      *reinterpret_cast<uint4 *>(qs + swz_off(h, c, kQAtomCol)) = o;
-    }
+  for (int i = tid; i < kQBytes / 16; i += kThreads) {
+    uint4 *ptr = reinterpret_cast<uint4 *>(qs) + i;
+    const uint4 v = *ptr;
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint4 o;
+    o.x = pack_half2(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u));
+    o.y = pack_half2(__uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
+    o.z = pack_half2(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u));
+    o.w = pack_half2(__uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
+    *ptr = o;
   }
 
   // ---------------------------------------------------------------- dequant
   const int row = tid >> 1, half = tid & 1;   // 2 threads per key, 256 channels each
   if (!is_swa) {
-    ok = mbar_wait(&S.bar_load, 0);
     const bool valid = (S.vmask[row >> 5] >> (row & 31)) & 1;
     uint4 codes[8];
     uint4 scl;
@@ -218,13 +231,17 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       }
     }
   } else {
-    const int t = (chunk - a.n_kchunks) * ATTN_CHUNK + row;
-    const bool valid = (S.vmask[row >> 5] >> (row & 31)) & 1;
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.swa + ((int64_t)p * a.W + t) * D + half * 256);
-#pragma unroll 4
+    // SWA rows (E4M3) staged in the tile's upper half: through registers, then
+    // converted to fp16 (exact) into the tile
+    const bool valid = row < swa_rows && ok;
+    uint4 raw[16];
+    const uint4 *src = reinterpret_cast<const uint4 *>(tile + kSwaStageOff + row * D + half * 256);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) raw[k] = valid ? src[k] : make_uint4(0, 0, 0, 0);
+    __syncthreads();   // the staging area is read; the tile may now be written over it
+#pragma unroll
     for (int k = 0; k < 16; ++k) {
-      const uint4 v = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
       uint4 o0, o1;
       o0.x = e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)); o0.y = e4m3x2_to_half2((uint16_t)(w[0] >> 16));
       o0.z = e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)); o0.w = e4m3x2_to_half2((uint16_t)(w[1] >> 16));
@@ -334,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_attn_kernel(const AttnArgs
       tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * H + hh * 32), v);
       tmem_ld_wait();
       const int d = mt * 128 + quad * 32 + lane;
-#pragma unroll 8
+#pragma unroll
       for (int i = 0; i < 32; ++i) po[(int64_t)(hh * 32 + i) * D + d] = ok ? __uint_as_float(v[i]) : 0.0f;
     }
     if (tid < H) {
@@ -409,9 +426,11 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
   cudaError_t err = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
+  CUtensorMap tm_q;
+  if (!make_tmap_bf16(&tm_q, a.q, D, (int64_t)a.problems * H, H)) return cudaErrorInvalidValue;
   const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-  sparse_attn_kernel<<<dim3(a.n_chunks, a.problems), kThreads, kSmemBytes, stream>>>(a);
+  sparse_attn_kernel<<<dim3(a.n_chunks, a.problems), kThreads, kSmemBytes, stream>>>(tm_q, a);
   if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
   attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
   *launches += 2;

@@ -63,6 +63,9 @@ ProfileEvents &profile_events(int kernel);
 // node of the graph, so every replay records it.
 cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream);
 
+// 2-D bf16 tensor map over rows of `inner` elements, box {64, box_rows}, 128B swizzle.
+bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t inner, int64_t rows, uint32_t box_rows);
+
 cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int64_t n_entries, const int64_t *pos,
                                   const int64_t *slot, uint8_t *kv, int64_t kv_rows, float rope_theta,
                                   cudaStream_t stream);
@@ -85,6 +88,11 @@ struct SweepArgs {
 
 cudaError_t launch_indexer_sweep(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
                                  int num_sms, cudaStream_t stream, int *launches);
+
+// Single-kernel top-K with one thread-block cluster per row (no scratch);
+// for k <= 2048.
+bool topk_cluster_supported(const TopkRows &r);
+cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches);
 
 size_t topk_scratch_bytes(int32_t rows, int64_t row_len, int32_t k);
 TopkScratch carve_topk_scratch(void *base, int32_t rows, int64_t row_len, int32_t k);

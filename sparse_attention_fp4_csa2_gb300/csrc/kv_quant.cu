@@ -11,11 +11,20 @@
 // bytes and 32 contiguous scale bytes.  Decode writes one entry per sequence,
 // so the kernel is latency-bound; the m = 2 chunked-prefill write streams
 // 4 KB of input per entry and is bandwidth-bound.
+#include <cmath>
+
 #include "kernels.cuh"
 
 namespace csa2 {
 
 namespace {
+
+struct RopeFreqs {
+  float inv[ROPE_DIM / 2];
+};
+
+// Positions must stay below 2^22 so that the 2*pi reduction stays exact.
+constexpr int64_t kMaxRopePos = int64_t(1) << 22;
 
 __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16 *p, float (&x)[16]) {
   const uint4 *v = reinterpret_cast<const uint4 *>(p);
@@ -28,19 +37,43 @@ __device__ __forceinline__ void load_bf16x16(const __nv_bfloat16 *p, float (&x)[
   }
 }
 
+// Cody-Waite split of 2*pi: C1 and C2 carry 33 significant bits each, so
+// k * C1 and k * C2 are exact for k < 2^20; C1 + C2 + C3 = 2*pi to about
+// 2^-120 (the three parts were derived with 300-bit arithmetic).
+constexpr double kTwoPi1 = 0x1.921fb544p+2;
+constexpr double kTwoPi2 = 0x1.0b4611a6p-32;
+constexpr double kTwoPi3 = 0x1.3198a2e037073p-67;
+constexpr double kInvTwoPi = 0.15915494309189535;
+
 __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16 *__restrict__ latent,
                                                              const __nv_bfloat16 *__restrict__ z, int m,
                                                              int64_t n_entries, const int64_t *__restrict__ pos,
                                                              const int64_t *__restrict__ slot,
                                                              uint8_t *__restrict__ kv, int64_t kv_rows,
-                                                             float rope_theta) {
+                                                             const RopeFreqs freqs) {
   const int lane = threadIdx.x & 31;
   const int64_t e = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (e >= n_entries) return;
+  if (e >= n_entries) return;   // warp-uniform
   const int64_t row = slot[e];
-  if (row < 0 || row >= kv_rows) {
+  const int64_t p = pos[e];
+  if (row < 0 || row >= kv_rows || p < 0 || p >= kMaxRopePos) {
     if (lane == 0) set_error(CSA2_DEV_ERR_INDEX);
     return;
+  }
+  // Lane j evaluates the rotation of pair j: angle = pos * inv_freq_j (exact
+  // in double), reduced modulo 2*pi (Cody-Waite, k < 2^20), cos / sin in
+  // double, rounded to fp32.
+  float cj, sj;
+  {
+    const double ang = (double)p * (double)freqs.inv[lane];
+    const double k = rint(ang * kInvTwoPi);
+    double r = fma(-k, kTwoPi1, ang);
+    r = fma(-k, kTwoPi2, r);
+    r = fma(-k, kTwoPi3, r);
+    double sd, cd;
+    sincos(r, &sd, &cd);
+    cj = __double2float_rn(cd);
+    sj = __double2float_rn(sd);
   }
   const int c0 = lane * 16;
   float x[16];
@@ -65,16 +98,16 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
       x[i] = __double2float_rn(num);
     }
   }
-  if (c0 >= D - ROPE_DIM) {
-    // RoPE: interleaved pairs (448 + 2j, 449 + 2j), inverse frequency
-    // fl32(theta^(-2j/64)), angle exact in double, no fused multiply-add.
-    const double p = (double)pos[e];
+  // RoPE: interleaved pairs (448 + 2j, 449 + 2j); lanes 28..31 own channels
+  // 448..511 and take the 8 rotations they need from the lanes that computed
+  // them; products and sums rounded separately (no fused multiply-add).
+  const int jbase = (lane - (D - ROPE_DIM) / 16) * 8;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int j = (c0 - (D - ROPE_DIM)) / 2 + i;
-      const float inv = (float)pow((double)rope_theta, -(2.0 * j) / (double)ROPE_DIM);
-      const double ang = p * (double)inv;
-      const float c = (float)cos(ang), s = (float)sin(ang);
+  for (int i = 0; i < 8; ++i) {
+    const int src = (jbase + i) & 31;
+    const float c = __shfl_sync(0xffffffffu, cj, src);
+    const float s = __shfl_sync(0xffffffffu, sj, src);
+    if (c0 >= D - ROPE_DIM) {
       const float a = x[2 * i], b = x[2 * i + 1];
       x[2 * i] = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
       x[2 * i + 1] = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
@@ -103,11 +136,15 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
 cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int64_t n_entries, const int64_t *pos,
                                   const int64_t *slot, uint8_t *kv, int64_t kv_rows, float rope_theta,
                                   cudaStream_t stream) {
+  // inverse frequencies fl32(theta^(-2j/64)), j = 0..31, evaluated on the host
+  RopeFreqs freqs;
+  for (int j = 0; j < ROPE_DIM / 2; ++j)
+    freqs.inv[j] = (float)std::pow((double)rope_theta, -(2.0 * j) / (double)ROPE_DIM);
   const int warps = 8;
   const int64_t blocks = (n_entries + warps - 1) / warps;
   kv_quant_write_kernel<<<(unsigned)blocks, warps * 32, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
-      kv, kv_rows, rope_theta);
+      kv, kv_rows, freqs);
   return cudaGetLastError();
 }
 

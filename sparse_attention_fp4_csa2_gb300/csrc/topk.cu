@@ -30,6 +30,7 @@ constexpr int kPerThread = 16;
 constexpr int kChunk = kHistThreads * kPerThread;   // 4096 values per CTA
 constexpr int kFinThreads = 1024;
 constexpr int kCandSmem = 12288;                    // candidates kept in shared memory
+constexpr int kRankMax = 2048;                      // rank-by-counting below this many
 
 __device__ __forceinline__ uint32_t row_force_index(const TopkRows &r, int row) {
   if (!r.force_nvis) return 0xFFFFFFFFu;
@@ -39,11 +40,21 @@ __device__ __forceinline__ uint32_t row_force_index(const TopkRows &r, int row) 
   return (uint32_t)((nv - 1) / r.force_block);
 }
 
-// key of value i of a row; 0 = invalid (below every valid key)
-__device__ __forceinline__ uint32_t value_key(const TopkRows &r, const float *row, int64_t i, uint32_t force) {
-  if ((uint32_t)i == force) return f32_key(INFINITY);
-  const float v = row[i];
-  return (v == -INFINITY || v != v) ? 0u : f32_key(v);
+// All kPerThread keys of this thread's share of a chunk, loads issued together.
+__device__ __forceinline__ void load_keys(const TopkRows &r, const float *row, int64_t c0, uint32_t force,
+                                          uint32_t (&keys)[kPerThread]) {
+  float v[kPerThread];
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int64_t i = c0 + j * kHistThreads + threadIdx.x;
+    v[j] = (i < r.row_len) ? row[i] : -INFINITY;
+  }
+#pragma unroll
+  for (int j = 0; j < kPerThread; ++j) {
+    const int64_t i = c0 + j * kHistThreads + threadIdx.x;
+    keys[j] = ((uint32_t)i == force && i < r.row_len) ? f32_key(INFINITY)
+              : (v[j] == -INFINITY || v[j] != v[j]) ? 0u : f32_key(v[j]);
+  }
 }
 
 __global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const TopkRows r, TopkScratch s) {
@@ -55,14 +66,11 @@ __global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const TopkRows 
   const uint32_t force = row_force_index(r, row);
   const int64_t c0 = (int64_t)blockIdx.x * kChunk;
   const int lane = threadIdx.x & 31;
-#pragma unroll 4
+  uint32_t keys[kPerThread];
+  load_keys(r, vals, c0, force, keys);
+#pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
-    const int64_t i = c0 + j * kHistThreads + threadIdx.x;
-    uint32_t bin = TOPK_BINS;  // sentinel: nothing to count
-    if (i < r.row_len) {
-      const uint32_t key = value_key(r, vals, i, force);
-      if (key) bin = key >> 21;
-    }
+    const uint32_t bin = keys[j] ? (keys[j] >> 21) : (uint32_t)TOPK_BINS;  // sentinel: nothing to count
     const uint32_t peers = __match_any_sync(0xffffffffu, bin);
     if (bin < TOPK_BINS && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
   }
@@ -136,10 +144,12 @@ __global__ void __launch_bounds__(kHistThreads) topk_select_kernel(const TopkRow
   uint64_t *cand = s.cand + (int64_t)row * r.row_len;
   const int64_t c0 = (int64_t)blockIdx.x * kChunk;
   const int lane = threadIdx.x & 31;
+  uint32_t keys[kPerThread];
+  load_keys(r, vals, c0, force, keys);
+#pragma unroll
   for (int j = 0; j < kPerThread; ++j) {
     const int64_t i = c0 + j * kHistThreads + threadIdx.x;
-    uint32_t key = 0;
-    if (i < r.row_len) key = value_key(r, vals, i, force);
+    const uint32_t key = keys[j];
     const int bin = key ? (int)(key >> 21) : -2;
     const bool take = key && bin > T;
     const bool maybe = key && bin == T;
@@ -200,6 +210,17 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(const TopkRows
   const uint64_t *c = in_smem ? cs : gc;
   __syncthreads();
 
+  if (in_smem && n_cand <= (uint32_t)kRankMax && need > 0) {
+    // few candidates: rank each by counting larger composites (all distinct)
+    for (uint32_t i = threadIdx.x; i < n_cand; i += kFinThreads) {
+      const uint64_t v = c[i];
+      uint32_t rank = 0;
+      for (uint32_t j = 0; j < n_cand; ++j) rank += c[j] > v;
+      if (rank < need) list[n_sel + rank] = (int32_t)(0xFFFFFFFFu - (uint32_t)(v & 0xFFFFFFFFull));
+    }
+    if (threadIdx.x == 0) n_list = n_sel + min(need, n_cand);
+    need = 0;
+  }
   // radix select of `need` largest among the candidates on bits 55..0
   // (the top 11 key bits are equal for all of them)
   uint64_t prefix = 0;
@@ -262,8 +283,28 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(const TopkRows
     __syncthreads();
   }
   __syncthreads();
-  // map to output positions, then bitonic sort ascending (padding = INT_MAX)
+  // map to output positions, then sort ascending (padding = INT_MAX)
   const uint32_t n_final = min(n_list, (uint32_t)r.k);
+  int32_t *out = r.out + (int64_t)row * r.k;
+  if (n_final <= (uint32_t)kRankMax) {
+    // rank sort: distinct positions, each placed by counting the smaller ones
+    int32_t mine[kRankMax / kFinThreads];
+    int cnt = 0;
+    for (uint32_t i = threadIdx.x; i < n_final; i += kFinThreads) mine[cnt++] = map_out(r, row, list[i]);
+    __syncthreads();
+    cnt = 0;
+    for (uint32_t i = threadIdx.x; i < n_final; i += kFinThreads) list[i] = mine[cnt++];
+    __syncthreads();
+    cnt = 0;
+    for (uint32_t i = threadIdx.x; i < n_final; i += kFinThreads) {
+      const int32_t v = list[i];
+      uint32_t rank = 0;
+      for (uint32_t j = 0; j < n_final; ++j) rank += list[j] < v;
+      out[rank] = v;
+    }
+    for (int i = (int)n_final + threadIdx.x; i < r.k; i += kFinThreads) out[i] = -1;
+    return;
+  }
   for (int i = threadIdx.x; i < P; i += kFinThreads)
     list[i] = (i < (int)n_final) ? map_out(r, row, list[i]) : 0x7FFFFFFF;
   __syncthreads();
@@ -283,7 +324,6 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(const TopkRows
       __syncthreads();
     }
   }
-  int32_t *out = r.out + (int64_t)row * r.k;
   for (int i = threadIdx.x; i < r.k; i += kFinThreads) out[i] = (i < (int)n_final) ? list[i] : -1;
 }
 

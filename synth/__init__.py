@@ -163,17 +163,17 @@ def decoder_layer_modes(groups: int = 5, per_group: int = 4, first: str = "full"
 
 CONFIGS = {
     # tiny single-layer Full decode, seed 0
-    "c0": Config("c0_full_decode_1x4k", 1, 4096, ["full"], layer_seeds=[0]),
+    "decode_1x4k": Config("decode_1x4k", 1, 4096, ["full"], layer_seeds=[0]),
     # decoder group decode: Full + 3 Reuse, seeds 1..4
-    "c1": Config("c1_group_decode_32x64k", 32, 65536, ["full", "reuse", "reuse", "reuse"],
+    "group_decode_32x64k": Config("group_decode_32x64k", 32, 65536, ["full", "reuse", "reuse", "reuse"],
                  layer_seeds=[1, 2, 3, 4]),
     # hierarchical indexer: Full (HSI) + 4 Reindex, planted blocks
-    "c2": Config("c2_hsi_reindex_16x256k", 16, 262144, ["full", "reindex", "reindex", "reindex", "reindex"],
+    "hsi_reindex_16x256k": Config("hsi_reindex_16x256k", 16, 262144, ["full", "reindex", "reindex", "reindex", "reindex"],
                  hsi=True, planted_blocks=16, layer_seeds=[2000 + i for i in range(5)]),
     # long-context full 20-layer decoder step
-    "c3": Config("c3_decoder20_4x1m", 4, 1048576, decoder_layer_modes(), hsi=True,
+    "decoder20_4x1m": Config("decoder20_4x1m", 4, 1048576, decoder_layer_modes(), hsi=True,
                  layer_seeds=[3000 + i for i in range(20)]),
     # chunked prefill at m=2: 131072-token context + 16384-token chunk
-    "c4": Config("c4_prefill_m2_2x128k+16k", 2, 131072, ["full"], m=2, chunk=16384,
+    "prefill_m2_2x128k": Config("prefill_m2_2x128k+16k", 2, 131072, ["full"], m=2, chunk=16384,
                  layer_seeds=[4000]),
 }

@@ -1,6 +1,6 @@
 """Helpers shared by the GPU parity tests: comparison rules and seeded setups.
 
-Matching rules (benchmark spec of the workload): FP4 codes and scales
+Matching rules of the workload: FP4 codes and scales
 bit-exact; top-K sets exact except for positions whose oracle score lies within
 1e-4 relative of the K-th score; attention outputs within 2e-3 relative
 (per (sequence, head) row: max|o - r| / max|r|)."""

@@ -199,7 +199,7 @@ def test_sparse_attn_no_keys(c2):
 def test_full_decode_chain_c0(c2, orc):
     """Config 0: 1 sequence, N = 4096, Full layer with HSI, then Reuse with the
     same query and SWA reproduces the Full output exactly."""
-    cfg = synth.CONFIGS["c0"]
+    cfg = synth.CONFIGS["decode_1x4k"]
     B, N = cfg.batch, cfg.n_ctx
     lat = synth.context_latent(0, B, N)
     k = synth.indexer_keys(0, B, N)
@@ -240,3 +240,39 @@ def test_full_decode_chain_c0(c2, orc):
                      pool_blocks=allb)
     assert torch.equal(topk, topk_r)
     assert torch.equal(out, out_r)
+
+
+def test_topk_many_ties_across_cluster(c2, orc):
+    """Scores drawn from four values over a long row: the selection must take
+    the lowest indices of the tied value, across the CTAs of the cluster."""
+    B, cap, K = 2, 200_000, 512
+    q_idx = torch.zeros(B, 32, 128, dtype=torch.bfloat16)
+    q_idx[:, :, 0] = 1.0
+    w = synth.uniform((B, 32), 5, 4)
+    g = torch.Generator().manual_seed(9)
+    k = torch.zeros(B, cap, 128, dtype=torch.bfloat16)
+    k[:, :, 0] = torch.randint(0, 4, (B, cap), generator=g).to(torch.bfloat16)
+    k[0, :, 0] = torch.where(torch.arange(cap) % 1000 == 0, 3.0, 1.0).to(torch.bfloat16)   # 200 threes
+    nv = torch.tensor([cap, 150_001], dtype=torch.int32)
+    p = _params(c2, index_topk=K)
+    ws = c2.workspace(c2.OP_INDEXER, B, cap, p)
+    topk = torch.empty(B, K, dtype=torch.int32, device="cuda")
+    c2.indexer_score_topk(q_idx.cuda(), w.cuda(), k.cuda(), nv.cuda(), cap, p, topk, ws)
+    assert c2.get_device_status() == 0
+    topk = topk.cpu().numpy()
+    for b in range(B):
+        s = orc.index_scores(q_idx[b], w[b], k[b, :int(nv[b])])
+        assert np.array_equal(topk[b], orc.topk(s, K))
+
+
+def test_topk_long_row_1m(c2, orc):
+    """One 1M-position row (the longest context): the cluster spans 16 CTAs."""
+    B, cap, K = 1, 1 << 20, 512
+    q_idx, w, k, nv = _index_case(77, B, cap, [cap - 3])
+    p = _params(c2, index_topk=K)
+    ws = c2.workspace(c2.OP_INDEXER, B, cap, p)
+    topk = torch.empty(B, K, dtype=torch.int32, device="cuda")
+    c2.indexer_score_topk(q_idx.cuda(), w.cuda(), k.cuda(), nv.cuda(), cap, p, topk, ws)
+    assert c2.get_device_status() == 0
+    s = orc.index_scores(q_idx[0], w[0], k[0, :cap - 3])
+    check_topk(topk[0].cpu().numpy(), orc.topk(s, K), s, n_valid=cap - 3)

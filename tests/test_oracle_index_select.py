@@ -116,7 +116,7 @@ def test_pool_positions_truncate_to_width(orc):
 
 def test_pool_covering_all_blocks_equals_flat_indexer(orc):
     """A hierarchical pool that covers every block leaves the flat indexer's
-    top-K unchanged (the invariant the benchmark spec names)."""
+    top-K unchanged."""
     rng = np.random.default_rng(6)
     n_vis = 8 * 40 + 5
     q = _bf16(rng.standard_normal((32, 128)) / math.sqrt(128))
