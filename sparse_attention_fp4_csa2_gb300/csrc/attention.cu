@@ -10,14 +10,18 @@
 // the products (section 2.4.4: FP4 reduces storage, not matmul cost).
 //
 // Work split (flash-decoding): a CTA owns 128 keys of one query token -- one
-// chunk of the top-K list or of the SWA window -- and writes a partial (row
-// max, row sum, unnormalised output) per head; a combine kernel merges the
-// chunks.  Inside a CTA, with the keys as the MMA M dimension:
-//   gather   warp 0 issues one 288-byte bulk copy per selected entry into
-//            shared memory (cp.async.bulk, mbarrier tx-count);
+// chunk of the top-K list or of the SWA window -- and writes its partial (row
+// max, row sum, unnormalised output) to the workspace.  With up to 8 chunks
+// (the pages' 512 + 128 keys make 5) the chunks of a token form one
+// thread-block cluster and merge after one cluster barrier, each CTA a slice
+// of the dims, from the partials in L2; with more chunks a separate combine
+// kernel merges them.  Inside a CTA, with the keys as the MMA M dimension:
+//   gather   Q arrives by TMA and the SWA rows by one bulk copy (mbarrier);
+//            every thread issues 16-byte cp.async copies of the selected FP4
+//            entries (18 per 288-byte entry) into a shared staging area;
 //   dequant  every thread turns its share of codes into fp16 (E2M1 x E4M3 is
 //            exact in fp16) in a 128B-swizzled K-major tile [128 keys x 512];
-//            SWA rows (E4M3) are converted straight from global memory;
+//            SWA rows (E4M3) likewise from their staging area;
 //   S^T      = K Q^T: 32 tcgen05 MMAs (M=128 keys, N=64 heads, K=16), fp32 in
 //            TMEM; Q (bf16 -> fp16) sits in shared memory K-major;
 //   softmax  each thread owns one key row of S^T for 32 heads; per-head max
@@ -48,15 +52,19 @@ constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kIdescQK = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ H, /*M*/ ATTN_CHUNK);
 constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B MN-major*/ 1, /*N*/ H, /*M*/ 128);
 
+constexpr int kMaxClusterChunks = 8;   // portable cluster size
+
 struct __align__(8) AttnSmem {
   uint64_t bar_load;
   uint64_t bar_mma;
   uint32_t tmem_base;
   uint32_t vmask[ATTN_CHUNK / 32];
+  int32_t ids[ATTN_CHUNK];
   float row_scale[ATTN_CHUNK];
   float red[4][H];
   float mfin[H];
   float lfin[H];
+  float rm[kMaxClusterChunks][H];   // cluster merge: every chunk's per-head weight
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kTileBytes + kQBytes + sizeof(AttnSmem);
@@ -132,47 +140,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (tid < ATTN_CHUNK) {
     S.row_scale[tid] = 1.0f;
   }
-  if (warp == 0) {
-    int32_t ids[4];
-    uint32_t cnt = 0;
+  if (tid == 0) {
+    // Q and the SWA rows first: their latency overlaps the index loads below
+    const uint32_t bytes = (uint32_t)kQBytes + (is_swa ? (uint32_t)swa_rows * D : 0u);
+    mbar_arrive_expect_tx(&S.bar_load, bytes);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = i * 32 + lane;
-      bool v;
-      if (!is_swa) {
-        const int j = chunk * ATTN_CHUNK + r;
-        int32_t id = (j < a.K) ? __ldg(a.idx + (int64_t)p * a.K + j) : -1;
-        if (id >= a.cap) {
-          set_error(CSA2_DEV_ERR_INDEX);
-          id = -1;
-        }
-        ids[i] = id;
-        v = id >= 0;
-      } else {
-        ids[i] = -1;
-        v = r < swa_rows;
-      }
-      const uint32_t m = __ballot_sync(0xffffffffu, v);
-      if (lane == 0) S.vmask[i] = m;
-      cnt += __popc(m);
-    }
-    if (lane == 0) {
-      const uint32_t bytes = (uint32_t)kQBytes +
-                             (is_swa ? (uint32_t)swa_rows * D : cnt * ENTRY_BYTES);
-      mbar_arrive_expect_tx(&S.bar_load, bytes);
-#pragma unroll
-      for (int j = 0; j < D / 64; ++j) tma_load_2d(qs + j * kQAtomCol, &tm_q, j * 64, p * H, &S.bar_load);
-      if (is_swa && swa_rows > 0)
-        bulk_g2s(tile + kSwaStageOff, a.swa + ((int64_t)p * a.W + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
-    }
-    __syncwarp();
+    for (int j = 0; j < D / 64; ++j) tma_load_2d(qs + j * kQAtomCol, &tm_q, j * 64, p * H, &S.bar_load);
+    if (is_swa && swa_rows > 0)
+      bulk_g2s(tile + kSwaStageOff, a.swa + ((int64_t)p * a.W + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
+  }
+  if (tid < ATTN_CHUNK) {
+    bool v;
     if (!is_swa) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (ids[i] >= 0)
-          bulk_g2s(tile + kStageOff + (i * 32 + lane) * ENTRY_BYTES, a.kv + (seq_row0 + ids[i]) * ENTRY_BYTES,
-                   ENTRY_BYTES, &S.bar_load);
+      const int j = chunk * ATTN_CHUNK + tid;
+      int32_t id = (j < a.K) ? __ldg(a.idx + (int64_t)p * a.K + j) : -1;
+      if (id >= a.cap) {
+        set_error(CSA2_DEV_ERR_INDEX);
+        id = -1;
+      }
+      S.ids[tid] = id;
+      v = id >= 0;
+    } else {
+      v = tid < swa_rows;
     }
+    const uint32_t m = __ballot_sync(0xffffffffu, v);
+    if (lane == 0) S.vmask[warp] = m;
+  }
+  if (!is_swa) {
+    // gather: the selected entries' 288 bytes as 18 16-byte pieces each, all
+    // threads issuing their cp.async copies at once
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < (ATTN_CHUNK * ENTRY_BYTES / 16) / kThreads; ++j) {
+      const int c = tid + j * kThreads;
+      const int e = c / (ENTRY_BYTES / 16), piece = c % (ENTRY_BYTES / 16);
+      const int32_t id = S.ids[e];
+      if (id >= 0)
+        cp_async16(tile + kStageOff + e * ENTRY_BYTES + piece * 16,
+                   a.kv + (seq_row0 + id) * ENTRY_BYTES + piece * 16);
+    }
+    cp_async_commit();
   }
   ok = mbar_wait(&S.bar_load, 0);
 
@@ -194,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------------------------------------------------------- dequant
   const int row = tid >> 1, half = tid & 1;   // 2 threads per key, 256 channels each
   if (!is_swa) {
+    cp_async_wait_all();
+    __syncthreads();   // every thread's gathered pieces have landed
     const bool valid = (S.vmask[row >> 5] >> (row & 31)) & 1;
     uint4 codes[8];
     uint4 scl;
@@ -341,9 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   __syncthreads();
 
-  // ---------------------------------------------------------------- store
+  // ---------------------------------------------------------------- merge
+  const int64_t pc = (int64_t)p * a.n_chunks + chunk;
   {
-    const int64_t pc = (int64_t)p * a.n_chunks + chunk;
+    // unnormalised partial O of this chunk, with its per-head (max, sum), to
+    // the workspace (coalesced along dims; it stays in L2)
     float *po = a.part_o + pc * H * D;
 #pragma unroll 1
     for (int mt = 0; mt < D / 128; ++mt) {
@@ -357,6 +368,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < H) {
       a.part_ml[pc * 2 * H + tid] = ok ? S.mfin[tid] : -INFINITY;
       a.part_ml[pc * 2 * H + H + tid] = ok ? S.lfin[tid] : 0.0f;
+    }
+  }
+  if (a.cluster) {
+    // The token's chunks are the CTAs of one cluster: after one cluster
+    // barrier (release / acquire orders the partial stores above) CTA c
+    // merges its slice of the 512 dims from every chunk's partial:
+    // M = max m_c, L = sum l_c 2^(m_c - M), out = sum_c 2^(m_c - M) O_c / L.
+    const uint32_t crank = cluster_ctarank(), nct = cluster_nctarank();
+    __threadfence();
+    cluster_sync();
+    const float *pbase = a.part_o + (int64_t)p * a.n_chunks * H * D;
+    const float *mlbase = a.part_ml + (int64_t)p * a.n_chunks * 2 * H;
+    if (tid < H) {
+      float M = -INFINITY;
+      for (uint32_t c = 0; c < nct; ++c) M = fmaxf(M, mlbase[c * 2 * H + tid]);
+      float L = 0.0f;
+      for (uint32_t c = 0; c < nct; ++c) {
+        const float mc = mlbase[c * 2 * H + tid];
+        const float w = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
+        S.rm[c][tid] = w;   // merge weight of chunk c for this head
+        L += w * mlbase[c * 2 * H + H + tid];
+      }
+      S.red[0][tid] = (L > 0.0f) ? 1.0f / L : 0.0f;
+      if (crank == 0 && a.lse)
+        a.lse[(int64_t)p * H + tid] = (L > 0.0f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    }
+    __syncthreads();
+    const int q0 = (int)(crank * (D / 4) / nct), q1 = (int)((crank + 1) * (D / 4) / nct);
+    const int nq = q1 - q0;
+    float *outp = a.out + (int64_t)p * H * D;
+    for (int e = tid; e < H * nq; e += kThreads) {
+      const int h = e / nq, q = q0 + e % nq;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+      for (uint32_t c = 0; c < nct; ++c) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(pbase + ((size_t)c * H + h) * D) + q);
+        const float w = S.rm[c][h];
+        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+      }
+      const float il = S.red[0][h];
+      acc.x *= il; acc.y *= il; acc.z *= il; acc.w *= il;
+      *reinterpret_cast<float4 *>(outp + h * D + 4 * q) = acc;
     }
   }
   tc_fence_before();
@@ -430,6 +483,27 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
   if (!make_tmap_bf16(&tm_q, a.q, D, (int64_t)a.problems * H, H)) return cudaErrorInvalidValue;
   const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
+  a.cluster = a.n_chunks <= kMaxClusterChunks ? 1 : 0;
+  if (a.cluster) {
+    // one cluster per token: its chunks merge over distributed shared memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.n_chunks, (unsigned)a.problems, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)a.n_chunks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, tm_q, a);
+    if (err != cudaSuccess) return err;
+    if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
+    *launches += 1;
+    return cudaSuccess;
+  }
   sparse_attn_kernel<<<dim3(a.n_chunks, a.problems), kThreads, kSmemBytes, stream>>>(tm_q, a);
   if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
   attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);

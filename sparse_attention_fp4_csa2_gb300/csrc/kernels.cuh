@@ -115,6 +115,7 @@ struct AttnArgs {
   int32_t W;
   int32_t n_kchunks;
   int32_t n_chunks;
+  int32_t cluster;            // 1: the chunks of a token form a cluster and merge over DSMEM
 };
 
 size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W);

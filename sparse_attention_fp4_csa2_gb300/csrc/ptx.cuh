@@ -91,6 +91,16 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), completed by
+// cp_async_wait_all() of the issuing thread.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // 2-D tiled tensor copy global -> shared (box and swizzle from the tensor map).
 // x is the innermost coordinate in elements; x * elem_size must be a multiple
 // of 16 bytes.

@@ -196,6 +196,9 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
         const uint32_t key = score_key(v[j]);
         const bool m = level_match(key, level, prefix);
         const int d = m ? (int)level_digit(key, level) : -1;
+        // most keys are below the threshold bin: skip the warp unless a lane
+        // has work (selection, next-level histogram or tie count)
+        if (!__any_sync(0xffffffffu, m && d >= thr)) continue;
         append_sel(m && (d > thr || (take_thr && d == thr)), (int32_t)i, nsel0, sel0, lane);
         if (!last) {
           const uint32_t nbin = (m && d == thr) ? level_digit(key, level + 1) : (uint32_t)kBins;

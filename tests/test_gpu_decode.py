@@ -160,6 +160,7 @@ def _kv_cache(c2, lat):
     (1, 100, 0, [0], [100]),                   # top-K only, K not a multiple of 128
     (1, 512, 128, [128], [0]),                 # SWA only
     (1, 256, 200, [200], [256]),               # two SWA chunks
+    (2, 1024, 128, [128, 5], [1024, 700]),     # 9 chunks: merged by the separate combine kernel
 ])
 def test_sparse_attn_reuse(c2, orc, B, K, W, swa_len, n_valid):
     cap = 3000
