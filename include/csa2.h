@@ -190,6 +190,41 @@ csa2_status csa2_sparse_decode(csa2_mode mode, const csa2_params *params, int32_
                                void *ws, size_t ws_bytes, csa2_stream_t stream);
 
 /*
+ * csa2_prefill_chunk -- the indexer, top-K and sparse readout of every token
+ * of a prefill chunk ([N] section 1-2: the encoder's CSA2 layers at m = 2;
+ * [A] 2.3.1-2.3.3).  Token i (0 <= i < n_tokens) of sequence b sits at position
+ * pos = first_pos + i and sees the compressed entries j with m*j + m-1 <= pos
+ * (an entry is visible once all its m source tokens are).  For each token:
+ * score(j) = sum_h w_h ReLU(q_idx_h . k_j) over its visible entries (bf16
+ * tensor-core products, fp32), the index_topk best (ties toward the lower
+ * entry, ascending, -1 padded), then one softmax over those entries together
+ * with the token's own causal SWA window -- the rows of positions
+ * max(pos - sliding_window + 1, 0) .. pos -- as in csa2_sparse_attn.  The
+ * chunk's own entries must already be in the caches (csa2_kv_quant_write with
+ * m = 2 for the chunk's complete pairs).
+ *   q         bf16 [batch][n_tokens][64][512], 16-byte aligned
+ *   q_idx     bf16 [batch][n_tokens][32][128], 16-byte aligned
+ *   w         fp32 [batch][n_tokens][32], 16-byte aligned
+ *   kv        uint8 [batch][cap][288]; k_idx bf16 [batch][cap][128]
+ *   n_tokens  a multiple of 8; (first_pos + n_tokens) / m <= cap
+ *   m         1 or 2
+ *   swa       uint8 E4M3 [batch][swa_rows][512]; swa_scale fp32 [batch][swa_rows];
+ *             row r of a sequence holds position swa_first_pos + r, and must
+ *             cover every window (swa_first_pos <= max(first_pos - W + 1, 0),
+ *             first_pos + n_tokens - 1 < swa_first_pos + swa_rows)
+ *   topk_idx  int32 [batch][n_tokens][index_topk] (out)
+ *   out       fp32 [batch][n_tokens][64][512] (out); lse fp32 [batch][n_tokens][64] or NULL
+ *   ws        at least csa2_workspace_bytes(CSA2_OP_PREFILL, batch, cap, params)
+ * The chunk is processed in blocks of 1024 tokens (indexer, top-K, readout per block).
+ */
+csa2_status csa2_prefill_chunk(const csa2_params *params, int32_t batch, int32_t n_tokens, int64_t first_pos,
+                               int32_t m, const void *q, const void *q_idx, const float *w,
+                               const uint8_t *kv, const void *k_idx, int64_t cap, const uint8_t *swa,
+                               const float *swa_scale, int64_t swa_rows, int64_t swa_first_pos,
+                               int32_t *topk_idx, float *out, float *lse, void *ws, size_t ws_bytes,
+                               csa2_stream_t stream);
+
+/*
  * csa2_hier_pool_select_static -- csa2_hier_pool_select without a workspace.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory where they select the pool: a runtime that
@@ -220,7 +255,8 @@ typedef enum {
   CSA2_OP_INDEXER = 0,   /* csa2_indexer_score_topk        */
   CSA2_OP_POOL = 1,      /* csa2_hier_pool_select          */
   CSA2_OP_ATTN = 2,      /* csa2_sparse_attn               */
-  CSA2_OP_DECODE = 3     /* csa2_sparse_decode (any mode)  */
+  CSA2_OP_DECODE = 3,    /* csa2_sparse_decode (any mode)  */
+  CSA2_OP_PREFILL = 4    /* csa2_prefill_chunk (n_max = cap) */
 } csa2_op;
 
 /* Scratch bytes an operation needs for `batch` sequences and visible

@@ -71,6 +71,8 @@ def lib():
         L.csa2_sparse_attn.argtypes = [PP, i32, P, P, i64, P, P, P, P, P, P, P, sz, P]
         L.csa2_sparse_decode.argtypes = [ctypes.c_int, PP, i32, P, P, P, P, P, i64, P, i64, P, P, P, P, P, P, P, P,
                                          sz, P]
+        L.csa2_prefill_chunk.argtypes = [PP, i32, i32, i64, i32, P, P, P, P, P, i64, P, P, i64, i64, P, P, P, P, sz, P]
+        L.csa2_prefill_chunk.restype = ctypes.c_int
         L.csa2_set_profile_events.argtypes, L.csa2_set_profile_events.restype = [ctypes.c_int, P, P], ctypes.c_int
         for f in ("csa2_kv_quant_write", "csa2_indexer_score_topk", "csa2_hier_pool_select", "csa2_sparse_attn",
                   "csa2_sparse_decode"):
@@ -202,3 +204,24 @@ def set_profile_events(kernel: int, start=None, stop=None):
     sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
     ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
     _check(lib().csa2_set_profile_events(kernel, sp, ep), "csa2_set_profile_events")
+
+
+OP_PREFILL = 4
+
+
+def prefill_chunk(params, q, q_idx, w, kv, k_idx, first_pos, m, swa, swa_scale, swa_first_pos, topk_idx, out,
+                  ws, lse=None, stream=None):
+    """Every token of a prefill chunk: indexer over its visible entries, top-K,
+    readout with its causal SWA window.  q bf16 [B,T,64,512]; q_idx bf16
+    [B,T,32,128]; w fp32 [B,T,32]; kv uint8 [B,cap,288]; k_idx bf16 [B,cap,128];
+    swa uint8 [B,rows,512] + swa_scale fp32 [B,rows] (row r = position
+    swa_first_pos + r); topk_idx int32 [B,T,K]; out fp32 [B,T,64,512]."""
+    B, T = q.shape[0], q.shape[1]
+    cap = kv.shape[1]
+    _check(lib().csa2_prefill_chunk(
+        ctypes.byref(params), B, T, int(first_pos), int(m), _ptr(q, torch.bfloat16, "q"),
+        _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w, torch.float32, "w"), _ptr(kv, torch.uint8, "kv"),
+        _ptr(k_idx, torch.bfloat16, "k_idx"), cap, _ptr(swa, torch.uint8, "swa"),
+        _ptr(swa_scale, torch.float32, "swa_scale"), swa.shape[1], int(swa_first_pos),
+        _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)), "csa2_prefill_chunk")

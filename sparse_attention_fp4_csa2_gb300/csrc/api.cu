@@ -120,6 +120,16 @@ size_t decode_ws(int32_t batch, int64_t n_max, const csa2_params *p) {
   return bs + m;
 }
 
+constexpr int64_t kPrefillBlock = 1024;   // query tokens per indexer / top-K / attention block
+
+size_t prefill_ws(int32_t batch, int64_t cap, const csa2_params *p) {
+  const int64_t qb = kPrefillBlock;
+  size_t b = (size_t)round_up(qb * round_up(cap, SWEEP_TILE) * 4, 256);
+  b += attn_scratch_bytes((int32_t)qb, p->index_topk, p->sliding_window);
+  (void)batch;
+  return b;
+}
+
 csa2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
 // ----------------------------------------------------------- operations
@@ -221,6 +231,9 @@ csa2_status run_attn(const csa2_params *p, int32_t batch, const void *q, const u
   a.problems = batch;
   a.K = p->index_topk;
   a.W = p->sliding_window;
+  a.p0 = 0;
+  a.tokens = 1;
+  a.causal_swa = 0;
   return cuda_status(launch_sparse_attn(a, ws, stream, launches));
 }
 
@@ -273,6 +286,7 @@ size_t csa2_workspace_bytes(csa2_op op, int32_t batch, int64_t n_max, const csa2
     case CSA2_OP_POOL: return pool_ws(batch, n_max, params);
     case CSA2_OP_ATTN: return attn_ws(batch, params);
     case CSA2_OP_DECODE: return decode_ws(batch, n_max, params);
+    case CSA2_OP_PREFILL: return prefill_ws(batch, n_max, params);
   }
   return 0;
 }
@@ -381,3 +395,106 @@ csa2_status csa2_sparse_decode(csa2_mode mode, const csa2_params *params, int32_
 }
 
 }  // extern "C"
+
+extern "C" csa2_status csa2_prefill_chunk(const csa2_params *params, int32_t batch, int32_t n_tokens, int64_t first_pos,
+                                          int32_t m, const void *q, const void *q_idx, const float *w,
+                                          const uint8_t *kv, const void *k_idx, int64_t cap, const uint8_t *swa,
+                                          const float *swa_scale, int64_t swa_rows, int64_t swa_first_pos,
+                                          int32_t *topk_idx, float *out, float *lse, void *ws, size_t ws_bytes,
+                                          csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  const csa2_params *p = params;
+  if (batch < 1 || n_tokens < 8 || n_tokens % 8 != 0 || (m != 1 && m != 2) || first_pos < 0 || cap < 1)
+    return CSA2_ERR_INVALID_ARG;
+  if (!q || !q_idx || !w || !kv || !k_idx || !topk_idx || !out || !ws) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(q_idx) || !aligned16(w) || !aligned16(kv) || !aligned16(k_idx) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return CSA2_ERR_INVALID_ARG;
+  const int64_t last_pos = first_pos + n_tokens - 1;
+  if ((last_pos + 1) / m > cap) return CSA2_ERR_INVALID_ARG;   // the chunk's entries must be in the cache
+  const int W = p->sliding_window;
+  if (W > 0) {
+    if (!swa || !swa_scale || !aligned16(swa) || swa_first_pos < 0) return CSA2_ERR_INVALID_ARG;
+    const int64_t first_start = first_pos - W + 1 > 0 ? first_pos - W + 1 : 0;
+    if (first_start < swa_first_pos || last_pos - swa_first_pos >= swa_rows) return CSA2_ERR_INVALID_ARG;
+  }
+  const int64_t total = (int64_t)batch * n_tokens;
+  if (total * HI >= ((int64_t)1 << 31) || (int64_t)batch * cap >= ((int64_t)1 << 31)) return CSA2_ERR_UNSUPPORTED;
+  if (ws_bytes < prefill_ws(batch, cap, p)) return CSA2_ERR_WORKSPACE;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  const size_t scores_bytes = (size_t)round_up(kPrefillBlock * round_up(cap, SWEEP_TILE) * 4, 256);
+  float *scores = reinterpret_cast<float *>(wsb);
+  void *attn_ws = wsb + scores_bytes;
+  CUtensorMap tm_k, tm_q;
+  if (!make_tmap_bf16_rows128(&tm_k, k_idx, (int64_t)batch * cap, SWEEP_TILE)) return CSA2_ERR_CUDA;
+  if (!make_tmap_bf16_rows128(&tm_q, q_idx, total * HI, 256)) return CSA2_ERR_CUDA;
+  auto visible = [&](int64_t i) {
+    const int64_t n = (first_pos + i + 1) / m;
+    return n < cap ? n : cap;
+  };
+  const int sms = num_sms();
+  int launches = 0;
+  for (int64_t q0 = 0; q0 < total; q0 += kPrefillBlock) {
+    const int64_t nq = total - q0 < kPrefillBlock ? total - q0 : kPrefillBlock;
+    // the most entries any token of the block sees: the last token of a sequence
+    // if the block holds one, else the block's last token
+    const bool holds_end = (q0 / n_tokens) != ((q0 + nq - 1) / n_tokens) || (q0 + nq) % n_tokens == 0;
+    const int64_t nv_max = holds_end ? visible(n_tokens - 1) : visible((q0 + nq - 1) % n_tokens);
+    const int32_t tiles = (int32_t)((nv_max + SWEEP_TILE - 1) / SWEEP_TILE);
+    PrefillIdxArgs ia;
+    ia.w = w;
+    ia.scores = scores;
+    ia.cap = cap;
+    ia.row_len = (int64_t)tiles * SWEEP_TILE;
+    ia.first_pos = first_pos;
+    ia.tokens = n_tokens;
+    ia.q0 = q0;
+    ia.groups = nq / 8;
+    int64_t rt = (tiles * ia.groups + 4 * sms - 1) / (4 * sms);   // about 4 items per SM
+    if (rt < 16) rt = 16;
+    if (rt > tiles) rt = tiles > 0 ? tiles : 1;
+    ia.range_tiles = (int32_t)rt;
+    ia.ranges = (int32_t)((tiles + rt - 1) / rt);
+    ia.tiles = tiles;
+    ia.m = m;
+    if (launch_prefill_indexer(tm_k, tm_q, ia, sms, st, &launches) != cudaSuccess) return CSA2_ERR_CUDA;
+    TopkRows r;
+    r.vals = scores;
+    r.row_len = ia.row_len;
+    r.row_stride = ia.row_len;
+    r.rows = (int32_t)nq;
+    r.k = p->index_topk;
+    r.force_nvis = nullptr;
+    r.force_block = BLOCK;
+    r.n_max = cap;
+    r.pool = nullptr;
+    r.pool_stride = 0;
+    r.out = topk_idx + q0 * p->index_topk;
+    if (launch_topk_cluster(r, st, &launches) != cudaSuccess) return CSA2_ERR_CUDA;
+    AttnArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.kv = kv;
+    a.idx = topk_idx;
+    a.swa = swa;
+    a.swa_scale = swa_scale;
+    a.swa_len = nullptr;
+    a.out = out;
+    a.lse = lse;
+    a.cap = cap;
+    a.problems = (int32_t)nq;
+    a.K = p->index_topk;
+    a.W = W;
+    a.p0 = q0;
+    a.tokens = n_tokens;
+    a.causal_swa = 1;
+    a.first_pos = first_pos;
+    a.swa_first_pos = swa_first_pos;
+    a.swa_seq_rows = swa_rows;
+    if (launch_sparse_attn(a, attn_ws, st, &launches) != cudaSuccess) return CSA2_ERR_CUDA;
+  }
+  g_last_launches = launches;
+  return CSA2_OK;
+}

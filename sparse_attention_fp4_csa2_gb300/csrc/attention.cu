@@ -107,9 +107,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   AttnSmem &S = *reinterpret_cast<AttnSmem *>(qs + kQBytes);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk = blockIdx.x, p = blockIdx.y;
+  const int chunk = blockIdx.x, p = blockIdx.y;   // p: this launch's problem (block-local)
+  const int64_t gp = a.p0 + p;                     // the query token it serves
   const bool is_swa = chunk >= a.n_kchunks;
-  const int64_t seq_row0 = (int64_t)p * a.cap;   // decode: problem p reads sequence p's cache
+  const int64_t seq = gp / a.tokens;
+  const int64_t seq_row0 = seq * a.cap;           // the token's sequence in the main-KV cache
 
   if (tid == 0) {
     mbar_init(&S.bar_load, 1);
@@ -133,10 +135,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the chunk's SWA rows (one contiguous bulk copy into the tile's upper half).
   const int t0 = (chunk - a.n_kchunks) * ATTN_CHUNK;   // first SWA row of this chunk
   int swa_rows = 0;
+  int64_t swa_row0 = 0;                              // first SWA row of the token's window
   if (is_swa) {
-    const int len = min(__ldg(a.swa_len + p), a.W);
+    int len;
+    if (a.causal_swa) {
+      const int64_t pos = a.first_pos + gp % a.tokens;
+      const int64_t start = pos - a.W + 1 > 0 ? pos - a.W + 1 : 0;
+      swa_row0 = seq * a.swa_seq_rows + (start - a.swa_first_pos);
+      len = (int)(pos - start + 1);
+    } else {
+      swa_row0 = gp * a.W;
+      len = min(__ldg(a.swa_len + gp), a.W);
+    }
     swa_rows = max(0, min(ATTN_CHUNK, len - t0));
-    if (tid < ATTN_CHUNK) S.row_scale[tid] = (tid < swa_rows) ? __ldg(a.swa_scale + (int64_t)p * a.W + t0 + tid) : 0.0f;
+    if (tid < ATTN_CHUNK) S.row_scale[tid] = (tid < swa_rows) ? __ldg(a.swa_scale + swa_row0 + t0 + tid) : 0.0f;
   } else if (tid < ATTN_CHUNK) {
     S.row_scale[tid] = 1.0f;
   }
@@ -145,15 +157,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bytes = (uint32_t)kQBytes + (is_swa ? (uint32_t)swa_rows * D : 0u);
     mbar_arrive_expect_tx(&S.bar_load, bytes);
 #pragma unroll
-    for (int j = 0; j < D / 64; ++j) tma_load_2d(qs + j * kQAtomCol, &tm_q, j * 64, p * H, &S.bar_load);
+    for (int j = 0; j < D / 64; ++j) tma_load_2d(qs + j * kQAtomCol, &tm_q, j * 64, (int32_t)(gp * H), &S.bar_load);
     if (is_swa && swa_rows > 0)
-      bulk_g2s(tile + kSwaStageOff, a.swa + ((int64_t)p * a.W + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
+      bulk_g2s(tile + kSwaStageOff, a.swa + (swa_row0 + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
   }
   if (tid < ATTN_CHUNK) {
     bool v;
     if (!is_swa) {
       const int j = chunk * ATTN_CHUNK + tid;
-      int32_t id = (j < a.K) ? __ldg(a.idx + (int64_t)p * a.K + j) : -1;
+      int32_t id = (j < a.K) ? __ldg(a.idx + gp * a.K + j) : -1;
       if (id >= a.cap) {
         set_error(CSA2_DEV_ERR_INDEX);
         id = -1;
@@ -392,12 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       S.red[0][tid] = (L > 0.0f) ? 1.0f / L : 0.0f;
       if (crank == 0 && a.lse)
-        a.lse[(int64_t)p * H + tid] = (L > 0.0f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+        a.lse[gp * H + tid] = (L > 0.0f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
     const int q0 = (int)(crank * (D / 4) / nct), q1 = (int)((crank + 1) * (D / 4) / nct);
     const int nq = q1 - q0;
-    float *outp = a.out + (int64_t)p * H * D;
+    float *outp = a.out + gp * H * D;
     for (int e = tid; e < H * nq; e += kThreads) {
       const int h = e / nq, q = q0 + e % nq;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -439,13 +451,13 @@ __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
       l += w * a.part_ml[((int64_t)p * n + c) * 2 * H + H + h];
     }
     inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-    if (a.lse) a.lse[(int64_t)p * H + h] = (l > 0.0f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    if (a.lse) a.lse[(a.p0 + p) * H + h] = (l > 0.0f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
   __syncthreads();
   for (int d = threadIdx.x; d < D; d += blockDim.x) {
     float acc = 0.0f;
     for (int c = 0; c < n; ++c) acc += wgt[c] * a.part_o[(((int64_t)p * n + c) * H + h) * D + d];
-    a.out[((int64_t)p * H + h) * D + d] = acc * inv_l;
+    a.out[((a.p0 + p) * H + h) * D + d] = acc * inv_l;
   }
 }
 
@@ -469,7 +481,7 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
   a.part_ml = reinterpret_cast<float *>(p + off);
   if (a.n_chunks == 0) {
     // no key at all: out = 0, lse = -inf
-    cudaError_t e = cudaMemsetAsync(a.out, 0, (size_t)a.problems * H * D * 4, stream);
+    cudaError_t e = cudaMemsetAsync(a.out + a.p0 * H * D, 0, (size_t)a.problems * H * D * 4, stream);
     if (e != cudaSuccess || !a.lse) return e;
     a.n_chunks = 0;
     attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
@@ -480,7 +492,7 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
                                          (int)kSmemBytes);
   if (err != cudaSuccess) return err;
   CUtensorMap tm_q;
-  if (!make_tmap_bf16(&tm_q, a.q, D, (int64_t)a.problems * H, H)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tm_q, a.q, D, (a.p0 + a.problems) * H, H)) return cudaErrorInvalidValue;
   const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
   a.cluster = a.n_chunks <= kMaxClusterChunks ? 1 : 0;

@@ -94,6 +94,25 @@ cudaError_t launch_indexer_sweep(const CUtensorMap &tm_k, const CUtensorMap &tm_
 bool topk_cluster_supported(const TopkRows &r);
 cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches);
 
+// Chunked prefill: multi-query indexer over the causally visible entries.
+struct PrefillIdxArgs {
+  const float *w;             // [B*T][32] head weights of every chunk token
+  float *scores;              // [groups*8][row_len] (block-local query rows)
+  int64_t cap;                // entries per sequence in the caches
+  int64_t row_len;            // tiles * 128
+  int64_t first_pos;          // position of chunk token 0
+  int64_t tokens;             // chunk tokens per sequence (multiple of 8)
+  int64_t q0;                 // first flattened query token (b*tokens + i) of this block
+  int64_t groups;             // groups of 8 tokens in this block
+  int32_t ranges;             // key-tile ranges per group
+  int32_t range_tiles;        // tiles per range
+  int32_t tiles;              // key tiles every group covers (block maximum)
+  int32_t m;                  // compression ratio
+};
+
+cudaError_t launch_prefill_indexer(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const PrefillIdxArgs &a,
+                                   int num_sms, cudaStream_t stream, int *launches);
+
 size_t topk_scratch_bytes(int32_t rows, int64_t row_len, int32_t k);
 TopkScratch carve_topk_scratch(void *base, int32_t rows, int64_t row_len, int32_t k);
 cudaError_t launch_topk(const TopkRows &r, const TopkScratch &s, int num_sms, cudaStream_t stream, int *launches);
@@ -115,7 +134,18 @@ struct AttnArgs {
   int32_t W;
   int32_t n_kchunks;
   int32_t n_chunks;
-  int32_t cluster;            // 1: the chunks of a token form a cluster and merge over DSMEM
+  int32_t cluster;            // 1: the chunks of a token form a cluster and merge after one barrier
+  // Problem p of this launch is token gp = p0 + p; it reads the caches of
+  // sequence gp / tokens.  Decode: tokens = 1, SWA rows [gp*W, gp*W + swa_len[gp]).
+  // Prefill (causal_swa): token i of its sequence sits at position
+  // first_pos + i and reads the SWA rows of positions max(pos - W + 1, 0) .. pos,
+  // row r of a sequence holding position swa_first_pos + r.
+  int64_t p0;
+  int64_t tokens;
+  int32_t causal_swa;
+  int64_t first_pos;
+  int64_t swa_first_pos;
+  int64_t swa_seq_rows;
 };
 
 size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W);
