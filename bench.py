@@ -37,11 +37,13 @@ KVW_BYTES = 1024 + 288 + 16                 # new entry per sequence
 
 
 def peaks():
+    """Roofline denominators: measured on this GPU pool when available."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return {"hbm": (float(d["hbm_gbs"]), "measured"),
+                "bf16_sustained": (float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured sustained")}
+    return {"hbm": (6800.0, "fallback"), "bf16_sustained": (1700.0, "fallback sustained")}
 
 
 def parse():
@@ -160,6 +162,28 @@ class Workload:
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
+    kind = "decode"
+
+    def tokens(self):
+        return self.B
+
+    def roofline(self, launch_ms, peaks_):
+        """HBM roofline of the Full layer's indexer sweep (one launch)."""
+        if not launch_ms or "full" not in self.cfg.schedule:
+            return None
+        hbm, kind = peaks_["hbm"]
+        alg = self.B * (256 * self.N + SWEEP_FIXED)
+        ach = alg / (launch_ms / 1e3) / 1e9
+        return {"kernel": "indexer_sweep_kernel", "bound": "hbm", "achieved": round(ach, 1), "peak": hbm,
+                "peak_kind": kind, "unit": "GB/s", "frac": round(ach / hbm, 4), "traffic": None,
+                "launch_ms": round(launch_ms, 4), "alg_bytes_per_launch": alg}
+
+    def config(self, ms):
+        step_bytes = algorithmic_bytes(self.cfg, self.hsi)
+        return {"workload": self.cfg.name, "batch": self.B, "context": self.N, "layers": "+".join(self.cfg.schedule),
+                "hsi": bool(self.hsi), "storage": "FP4 E2M1+E4M3/16 main KV, bf16 indexer K, E4M3 SWA",
+                "step_alg_bytes": step_bytes, "step_hbm_gbs": round(step_bytes / (ms / 1e3) / 1e9, 1)}
+
     def step(self, sweep_events=None):
         """Enqueue one decode step; with sweep_events, the Full layer's indexer
         sweep launch is bracketed by those events."""
@@ -190,6 +214,102 @@ class Workload:
         return hin, hout
 
 
+class PrefillWorkload:
+    """Chunked prefill at m = 2: every step writes the chunk's compressed
+    entries (csa2_kv_quant_write, m = 2) and runs csa2_prefill_chunk for all
+    chunk tokens of every sequence."""
+    kind = "prefill"
+
+    def __init__(self, cfg, device):
+        import torch
+
+        import synth
+        import sparse_attention_fp4_csa2_gb300 as c2
+        self.c2, self.cfg, self.dev = c2, cfg, device
+        B, m, T = cfg.batch, cfg.m, cfg.chunk
+        self.B, self.m, self.T = B, m, T
+        self.first_pos = cfg.n_ctx
+        E_ctx, E_new = cfg.n_ctx // m, T // m
+        self.E = E_ctx + E_new
+        self.params = c2.Params.make()
+        seed = cfg.layer_seeds[0]
+        self.kv = torch.empty(B, self.E, 288, dtype=torch.uint8, device=device)
+        for b in range(B):   # context entries (setup)
+            lat = synth.context_latent(seed * 977 + b, 1, E_ctx, device=device, m=m)[0]
+            z = synth.compression_logits(seed * 991 + b, 1, E_ctx, device=device, m=m)[0]
+            pos = torch.arange(E_ctx, dtype=torch.int64, device=device) * m + m - 1
+            slot = torch.arange(E_ctx, dtype=torch.int64, device=device) + b * self.E
+            c2.kv_quant_write(lat, z, m, pos, slot, self.kv.view(-1, 288))
+            del lat, z
+        self.k_idx = synth.indexer_keys(seed, B, self.E, device=device)
+        # per-step inputs: the chunk's latent pairs and logits, queries, SWA rows
+        self.new_lat = synth.context_latent(seed + 11, B, E_new, device=device, m=m)
+        self.new_z = synth.compression_logits(seed + 13, B, E_new, device=device, m=m)
+        self.new_pos = ((torch.arange(E_new, dtype=torch.int64, device=device) + E_ctx) * m + m - 1).repeat(B)
+        self.new_slot = (torch.arange(E_new, dtype=torch.int64, device=device) + E_ctx).repeat(B) + \
+            torch.arange(B, dtype=torch.int64, device=device).repeat_interleave(E_new) * self.E
+        self.q = synth.normal((B, T, 64, 512), seed, 2, device)
+        self.q_idx = synth.normal((B, T, 32, 128), seed, 3, device, std=1 / math.sqrt(128))
+        self.w = synth.uniform((B, T, 32), seed, 4, device)
+        W = self.params.sliding_window
+        self.swa_first = max(self.first_pos - W + 1, 0)
+        rows = self.first_pos + T - self.swa_first
+        self.swa, self.swa_scale = synth.fp8_rows(synth.normal((B, rows, 512), seed, 5, device, dtype=torch.float32))
+        self.topk = torch.empty(B, T, 512, dtype=torch.int32, device=device)
+        self.out = torch.empty(B, T, 64, 512, device=device)
+        self.lse = torch.empty(B, T, 64, device=device)
+        self.ws = c2.workspace(c2.OP_PREFILL, B, self.E, self.params, device=device)
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+    def tokens(self):
+        return self.B * self.T
+
+    def step(self, sweep_events=None):
+        c2 = self.c2
+        c2.kv_quant_write(self.new_lat.reshape(-1, self.m, 512), self.new_z.reshape(-1, self.m, 512), self.m,
+                          self.new_pos, self.new_slot, self.kv.view(-1, 288))
+        launches = c2.last_launch_count()
+        if sweep_events:
+            c2.set_profile_events(c2.KERNEL_PREFILL_INDEXER, *sweep_events)
+        c2.prefill_chunk(self.params, self.q, self.q_idx, self.w, self.kv, self.k_idx, self.first_pos, self.m,
+                         self.swa, self.swa_scale, self.swa_first, self.topk, self.out, self.ws, lse=self.lse)
+        if sweep_events:
+            c2.set_profile_events(c2.KERNEL_PREFILL_INDEXER, None, None)
+        return launches + c2.last_launch_count()
+
+    def _visible(self, i):
+        return min((self.first_pos + i + 1) // self.m, self.E)
+
+    def index_flops(self):
+        return sum(self._visible(i) for i in range(self.T)) * 32 * 128 * 2 * self.B
+
+    def roofline(self, launch_ms, peaks_):
+        """Tensor roofline of the prefill indexer; the timed launch is the last
+        1024-token block of the step (the last sequence's last tokens)."""
+        if not launch_ms:
+            return None
+        tf, kind = peaks_["bf16_sustained"]
+        flops = sum(self._visible(i) for i in range(self.T - 1024, self.T)) * 32 * 128 * 2
+        ach = flops / (launch_ms / 1e3) / 1e12
+        return {"kernel": "prefill_indexer_kernel", "bound": "tensor", "achieved": round(ach, 1), "peak": tf,
+                "peak_kind": kind, "unit": "TFLOP/s", "frac": round(ach / tf, 4), "traffic": None,
+                "launch_ms": round(launch_ms, 4), "alg_flops_per_launch": flops}
+
+    def config(self, ms):
+        flops = self.index_flops() + self.B * self.T * 2 * 2 * 64 * 512 * (512 + 128)
+        return {"workload": self.cfg.name, "batch": self.B, "context_tokens": self.first_pos, "chunk_tokens": self.T,
+                "m": self.m, "storage": "FP4 E2M1+E4M3/16 main KV, bf16 indexer K, E4M3 SWA",
+                "step_alg_flops": flops, "step_tflops": round(flops / (ms / 1e3) / 1e12, 1)}
+
+    def host_io(self):
+        import torch
+        ins = [self.new_lat, self.new_z, self.q, self.q_idx, self.w, self.swa, self.swa_scale]
+        hin = [(t.cpu().pin_memory(), t) for t in ins]
+        hout = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in (self.out, self.lse, self.topk)]
+        return hin, hout
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -203,7 +323,7 @@ def run_ours(args, rank, world, local_rank):
     if args.batch:
         import dataclasses
         cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}[batch={args.batch}]")
-    wl = Workload(cfg, dev)
+    wl = PrefillWorkload(cfg, dev) if cfg.chunk else Workload(cfg, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     flush2 = torch.ones(128 << 20, dtype=torch.float32, device=dev)
@@ -214,8 +334,7 @@ def run_ours(args, rank, world, local_rank):
     stream.synchronize()
     assert c2.get_device_status(stream) == 0
     sweep_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    attn_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-    for ev in sweep_ev + attn_ev:
+    for ev in sweep_ev:
         ev.record(stream)          # marks the events recorded; the graph re-records them every replay
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -274,36 +393,25 @@ def run_ours(args, rank, world, local_rank):
     d2h = sum(h.numel() * h.element_size() for h, _ in hout)
     assert c2.get_device_status(stream) == 0
 
-    B = cfg.batch
     ms = total_ms / args.steps
-    tokens_per_s = world * B / (ms / 1e3)
-    hbm, kind = peaks()
-    sweep_avg = statistics.mean(sweep_ms) if sweep_ms and "full" in cfg.schedule else None
-    roof = None
-    if sweep_avg:
-        alg = B * (256 * cfg.n_ctx + SWEEP_FIXED)
-        ach = alg / (sweep_avg / 1e3) / 1e9
-        roof = {"kernel": "indexer_sweep_kernel", "bound": "hbm", "achieved": round(ach, 1),
-                "peak": hbm, "peak_kind": kind, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                "traffic": None, "launch_ms": round(sweep_avg, 4), "alg_bytes_per_launch": alg}
-    step_bytes = algorithmic_bytes(cfg, wl.hsi)
+    tokens_per_s = world * wl.tokens() / (ms / 1e3)
+    launch_ms = statistics.mean(sweep_ms) if sweep_ms else None
+    roof = wl.roofline(launch_ms, peaks())
+    conf = wl.config(ms)
+    conf["l2"] = "flushed between steps (512 MB write, then 512 MB read), outside the timed events"
     line = {
         "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": cfg.name, "batch": B, "context": cfg.n_ctx, "layers": "+".join(cfg.schedule),
-                   "hsi": bool(wl.hsi), "l2": "flushed between steps (512 MB write, then 512 MB read), outside the timed events",
-                   "storage": "FP4 E2M1+E4M3/16 main KV, bf16 indexer K, E4M3 SWA",
-                   "step_alg_bytes": step_bytes,
-                   "step_hbm_gbs": round(step_bytes / (ms / 1e3) / 1e9, 1)},
+        "config": conf,
         "roofline": roof,
-        "e2e": {"value": round(world * B / (e2e_ms / e2e_steps / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(world * wl.tokens() / (e2e_ms / e2e_steps / 1e3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(local_rank),
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(args, cfg, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = (cpu_baseline_prefill if cfg.chunk else cpu_baseline)(args, cfg, seconds=args.cpu_seconds)
         print(json.dumps(line), flush=True)
 
 
@@ -345,21 +453,58 @@ def cpu_baseline(args, cfg, seconds=12.0):
                                         f"FP4 entries of the selected rows written inside the timed region"}
 
 
+def cpu_baseline_prefill(args, cfg, seconds=12.0):
+    """The oracle on the host cores for chunk tokens of the prefill workload:
+    per token the index scores over its visible entries, top-K, the FP4 entries
+    of the selection and the readout with its causal SWA window; tokens are
+    taken across the chunk until ~`seconds` elapse."""
+    import numpy as np
+
+    import oracle
+    import synth
+    oracle.build()
+    m, T = cfg.m, cfg.chunk
+    first = cfg.n_ctx
+    E = (first + T) // m
+    seed = cfg.layer_seeds[0]
+    k = synth.indexer_keys(seed * 31, 1, E)[0]
+    lat = synth.context_latent(seed * 37, 1, E, m=m)[0]
+    z = synth.compression_logits(seed * 41, 1, E, m=m)[0]
+    li = synth.layer_inputs(seed, 1)
+    rng = np.random.default_rng(0)
+    done, t_total = 0, 0.0
+    while t_total < seconds or done == 0:
+        i = int(rng.integers(0, T))
+        pos = first + i
+        nvis = min((pos + 1) // m, E)
+        t0 = time.perf_counter()
+        s = oracle.index_scores(li.q_idx[0], li.w[0], k[:nvis])
+        sel = oracle.topk(s, 512)
+        valid = sel[sel >= 0]
+        rows = oracle.kv_entries(lat[valid], z[valid], m, valid * m + m - 1)
+        oracle.sparse_attn(li.q[0], rows, np.arange(len(valid)), li.swa[0], li.swa_scale[0], 128)
+        t_total += time.perf_counter() - t0
+        done += 1
+    return {"value": round(done / t_total, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{done} chunk tokens drawn uniformly from the {T}-token chunk ({cfg.name})"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
     import synth
     cfg = synth.CONFIGS[args.config]
     per_step = []
+    base = cpu_baseline_prefill if cfg.chunk else cpu_baseline
     for _ in range(args.steps):
-        r = cpu_baseline(args, cfg, seconds=max(1.0, args.cpu_seconds / max(1, args.steps)))
+        r = base(args, cfg, seconds=max(1.0, args.cpu_seconds / max(1, args.steps)))
         per_step.append(r)
     v = statistics.mean(r["value"] for r in per_step)
     line = {"metric": METRIC, "value": round(v, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(cfg.batch / v * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "batch": cfg.batch, "context": cfg.n_ctx,
-                       "layers": "+".join(cfg.schedule)},
+                       "layers": "+".join(cfg.schedule), "chunk_tokens": cfg.chunk},
             "impl": "reference",
             "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": per_step[0]["cores"],
                              "kind": "oracle", "sample": per_step[0]["sample"]},

@@ -239,9 +239,13 @@ cudaError_t launch_prefill_indexer(const CUtensorMap &tm_k, const CUtensorMap &t
       cudaFuncSetAttribute(prefill_indexer_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (err != cudaSuccess) return err;
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
+  const ProfileEvents &pe = profile_events(CSA2_KERNEL_PREFILL_INDEXER);
+  if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
   prefill_indexer_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
   ++*launches;
-  return cudaGetLastError();
+  err = cudaGetLastError();
+  if (err == cudaSuccess && pe.stop) err = record_profile_event(pe.stop, stream);
+  return err;
 }
 
 }  // namespace csa2
