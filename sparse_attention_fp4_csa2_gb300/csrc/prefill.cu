@@ -12,7 +12,8 @@
 // Warp 0 issues TMA loads (the group's 8 x 32 x 128 indexer queries once per
 // item, key tiles into a 4-stage ring, the group's head weights into a double
 // buffer), warp 1 issues the MMAs into two 256-column TMEM accumulators,
-// warps 2-5 reduce each row to score(token, position) = sum_h w_h *
+// warps 2-9 (two per TMEM lane quadrant, four tokens each) reduce each row to
+// score(token, position) = sum_h w_h *
 // ReLU(q_h . k) and write it, -inf where the position is not yet visible to
 // the token (entry j is visible to the token at position g iff m*j + m-1 <= g).
 #include "kernels.cuh"
@@ -27,7 +28,8 @@ constexpr int kN = kGroup * HI;                   // 256
 constexpr int kTileBytes = SWEEP_TILE * DI * 2;   // 32 KB
 constexpr int kQBytes = kN * DI * 2;              // 64 KB: two K-atoms of [256 rows][128 B]
 constexpr int kWBytes = kN * 4;                   // 1 KB of head weights per group
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                      // two warps per TMEM lane quadrant
+constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr uint32_t kIdesc = idesc_f16(/*bf16*/ 1, 0, 0, /*N*/ kN, /*M*/ SWEEP_TILE);
 
 struct __align__(8) PrefillSmem {
@@ -90,9 +92,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&S.qempty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.wfull[i], 1);
-      mbar_init(&S.wempty[i], 4 * 32);
+      mbar_init(&S.wempty[i], kEpiWarps * 32);
       mbar_init(&S.accfull[i], 1);
-      mbar_init(&S.accempty[i], 4 * 32);
+      mbar_init(&S.accempty[i], kEpiWarps * 32);
     }
     mbar_init(&S.mma_done, 1);
     abort_flag(S) = 0;
@@ -182,7 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int quad = warp & 3;
+    // warps 2..9: lane quadrant (warp & 3) of the tile, tokens 4*half .. 4*half+3
+    const int quad = warp & 3, half = (warp - 2) >> 2;
     const int r = quad * 32 + lane;
     int64_t step = 0, j = 0;
     for (int64_t it = blockIdx.x; it < n_items; it += gridDim.x, ++j) {
@@ -190,28 +193,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int wb = (int)(j & 1);
       if (!mbar_wait(&S.wfull[wb], (uint32_t)((j >> 1) & 1))) { abort_flag(S) = 1; break; }
       const float *wv = wbuf + wb * kN;
-      int32_t nv[kGroup];
+      int32_t nv[4];
 #pragma unroll
-      for (int q = 0; q < kGroup; ++q) nv[q] = (int32_t)visible(a, I.qg + q);
-      float *srow = a.scores + (I.qg - a.q0) * a.row_len;
+      for (int q = 0; q < 4; ++q) nv[q] = (int32_t)visible(a, I.qg + 4 * half + q);
+      float *srow = a.scores + (I.qg - a.q0 + 4 * half) * a.row_len;
       bool stop = false;
       for (int32_t t = I.t0; t < I.t1; ++t, ++step) {
         const int acc = (int)(step & 1);
         if (!mbar_wait(&S.accfull[acc], (uint32_t)((step >> 1) & 1))) { stop = true; break; }
         tc_fence_after();
         const int64_t pos = (int64_t)t * SWEEP_TILE + r;
-#pragma unroll 1
-        for (int q = 0; q < kGroup; ++q) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int qq = 4 * half + q;
           uint32_t v[32];
-          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kN + q * HI), v);
+          tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kN + qq * HI), v);
           tmem_ld_wait();
-          float s = 0.0f;
+          // four independent partial sums of w_h * ReLU(q_h . k)
+          const float4 *w4 = reinterpret_cast<const float4 *>(wv + qq * HI);
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-          for (int h = 0; h < HI; ++h) s = fmaf(wv[q * HI + h], fmaxf(__uint_as_float(v[h]), 0.0f), s);
-          int32_t nvq = nv[0];
-#pragma unroll
-          for (int u = 1; u < kGroup; ++u) nvq = (q == u) ? nv[u] : nvq;
-          srow[(int64_t)q * a.row_len + pos] = pos < nvq ? s : -INFINITY;
+          for (int h4 = 0; h4 < HI / 4; ++h4) {
+            const float4 ww = w4[h4];
+            s0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f), s0);
+            s1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), s1);
+            s2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), s2);
+            s3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), s3);
+          }
+          const float sc = (s0 + s1) + (s2 + s3);
+          srow[(int64_t)q * a.row_len + pos] = pos < nv[q] ? sc : -INFINITY;
         }
         tc_fence_before();
         mbar_arrive(&S.accempty[acc]);

@@ -1,54 +1,72 @@
 // Exact top-K of each indexer score row in one kernel: one thread-block
 // cluster per row, radix select across the cluster through distributed
 // shared memory, no global scratch.  Used for the index_topk = 512 selection
-// of the Full and Reindex layers ("DeepSeek-V4.1-Flash - Architecture",
-// sections 2 and 3).
+// of the Full and Reindex layers and of every chunk token in prefill
+// ("DeepSeek-V4.1-Flash - Architecture", sections 2 and 3).
 //
 // Scores become order-preserving 32-bit keys (-inf marks an invalid slot).
-// The CTAs of the cluster split the row into contiguous slices.  Level 0
-// histograms the top 11 key bits; every CTA sums the cluster's histograms
-// over DSMEM and finds the same threshold bin; keys above it are selected,
-// keys in it go on to level 1 (next 11 bits) and level 2 (last 10 bits).  A
-// level stops early when its threshold bin holds exactly the count still
-// needed.  Keys equal on all 32 bits are resolved toward the lower index: each
-// CTA takes its quota of them in index order after a cluster prefix of the
-// per-CTA counts.  Selected indices are appended to CTA 0's list; CTA 0 maps
-// them to positions (through the HSI pool for Reindex rows), sorts them
-// ascending and writes them, -1 padded.  Each level re-reads the slice (from
-// L2: the sweep has just written it); no CTA waits on another except at
-// cluster barriers, which the hardware co-schedules.
+// The CTAs of the cluster split the row into contiguous slices (float4
+// loads, 32 values in flight per thread).
+//   1. sample: 1/8 of each slice, level-0 histogram of the top 11 key bits;
+//      a low threshold t_low is the bin holding about twice the sample's share
+//      of k;
+//   2. filter: every key >= t_low is compacted into the CTA's candidate list
+//      in shared memory;
+//   3. exact radix select -- 11, 11 and 10 key bits -- on the candidate lists
+//      when together they hold >= k keys and none overflowed, else on the
+//      whole slices; a level stops early when its threshold bin holds exactly
+//      the count still needed; keys equal on all 32 bits are taken toward the
+//      lower index (each CTA its quota, in index order, after a cluster prefix
+//      of the per-CTA tie counts);
+//   4. each CTA sorts the indices it selected and writes them at its cluster
+//      prefix offset (slices are in index order), mapped through the HSI pool
+//      for Reindex rows; the last CTA pads with -1.
+// Histograms are exchanged by pushing each CTA's non-zero bins into every
+// CTA's cluster total with remote atomic adds; all waiting is at cluster
+// barriers, which the hardware co-schedules.
 #include "kernels.cuh"
 
 namespace csa2 {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 256;
 constexpr int kBins = 2048;
-constexpr int kSelMax = 2048;     // index_topk limit
-constexpr int kPer = 8;           // values per thread per sweep of a slice segment
+constexpr int kBinsPerThread = kBins / kThreads;
+constexpr int kSelMax = 2048;          // index_topk limit
+constexpr int kVec = 8;                // float4 loads per thread per round (32 values)
+constexpr int kRound = kThreads * kVec * 4;   // values per CTA per round
+constexpr int kCand = 4096;            // per-CTA candidate list
+constexpr int kSampleEvery = 8;        // the sample: one round's worth out of every 8
+constexpr int kMaxCluster = 16;        // CTAs per row (non-portable cluster size)
 
 struct __align__(16) TopkClusterSmem {
-  uint32_t hist[2][kBins];
-  uint32_t tot[kBins];
-  int32_t sel[kSelMax];
-  uint32_t n_sel;
-  uint32_t tie_cnt;
-  uint32_t warp_cnt[kThreads / 32];
+  uint32_t hist[kBins];                // this CTA's histogram of the current level
+  uint32_t tot[2][kBins];              // cluster totals, pushed by every CTA
+  uint32_t ckey[kCand];
+  int32_t cidx[kCand];
+  int32_t sel[kSelMax];                // this CTA's selected indices
+  uint32_t cand_cnt[kMaxCluster];      // per-CTA counts, pushed by the CTAs
+  uint32_t tie_cnt[kMaxCluster];
+  uint32_t sel_cnt[kMaxCluster];
+  uint32_t ccount, n_sel, n_tie;
   uint32_t scan[kThreads / 32];
+  uint32_t warp_cnt[kThreads / 32];
   int thr;
-  uint32_t above;
-  uint32_t total;
-  uint32_t in_thr;
+  uint32_t above, total, in_thr;
 };
 
 __device__ __forceinline__ uint32_t score_key(float v) {
   return (v == -INFINITY || v != v) ? 0u : f32_key(v);
 }
 
-// Matching predicate and digit of a level.  Level 0: every valid key, digit =
-// bits 31..21.  Level 1: keys whose bits 31..21 equal the prefix, digit =
-// bits 20..10.  Level 2: bits 31..10 equal the prefix, digit = bits 9..0.
+__device__ __forceinline__ void red_add_remote(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Level-L predicate and digit.  Level 0: every valid key, bits 31..21.
+// Level 1: bits 31..21 equal the prefix, digit 20..10.  Level 2: bits 31..10
+// equal the prefix, digit 9..0.
 __device__ __forceinline__ bool level_match(uint32_t key, int level, uint32_t prefix) {
   if (!key) return false;
   if (level == 0) return true;
@@ -60,41 +78,46 @@ __device__ __forceinline__ uint32_t level_digit(uint32_t key, int level) {
   return level == 0 ? (key >> 21) : level == 1 ? ((key >> 10) & 2047u) : (key & 1023u);
 }
 
-// Appends the flagged indices of this warp to CTA 0's selection list.
-__device__ __forceinline__ void append_sel(bool flag, int32_t idx, uint32_t nsel_addr0, uint32_t sel_addr0,
-                                           int lane) {
+__device__ __forceinline__ void hist_add(TopkClusterSmem &S, uint32_t bin, int lane) {
+  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
+  if (bin < kBins && lane == __ffs(peers) - 1) atomicAdd(&S.hist[bin], (uint32_t)__popc(peers));
+}
+
+// Appends the flagged indices of this warp to the CTA's selection list.
+__device__ __forceinline__ void append_sel(TopkClusterSmem &S, bool flag, int32_t idx, int lane) {
   const uint32_t m = __ballot_sync(0xffffffffu, flag);
   if (!m) return;
   uint32_t base = 0;
-  if (lane == 0) base = dsmem_atom_add(nsel_addr0, (uint32_t)__popc(m));
+  if (lane == 0) base = atomicAdd(&S.n_sel, (uint32_t)__popc(m));
   base = __shfl_sync(0xffffffffu, base, 0);
   if (flag) {
     const uint32_t pos = base + __popc(m & ((1u << lane) - 1));
-    if (pos < kSelMax) dsmem_st_u32(sel_addr0 + 4 * pos, (uint32_t)idx);
+    if (pos < kSelMax) S.sel[pos] = idx;
   }
 }
 
-// Sums the cluster's level histograms into tot (every CTA does it), then
-// finds the threshold bin for `need`: thr = -1 when everything matching fits.
-__device__ void cluster_threshold(TopkClusterSmem &S, int buf, uint32_t nctas, uint32_t need, int bins) {
-  const int tid = threadIdx.x;
-  for (int b4 = tid; b4 < kBins / 4; b4 += kThreads) {
-    uint4 acc = make_uint4(0, 0, 0, 0);
-    for (uint32_t c = 0; c < nctas; ++c) {
-      const uint4 v = dsmem_ld_v4(dsmem_addr(&S.hist[buf][4 * b4], c));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+// Adds this CTA's histogram into tot[buf] of every CTA of the cluster (non-zero
+// bins only) and clears it.  Visible everywhere after the next cluster barrier.
+__device__ __forceinline__ void push_hist(TopkClusterSmem &S, int buf, uint32_t nctas) {
+  for (int b = threadIdx.x; b < kBins; b += kThreads) {
+    const uint32_t v = S.hist[b];
+    if (v) {
+      for (uint32_t c = 0; c < nctas; ++c) red_add_remote(dsmem_addr(&S.tot[buf][b], c), v);
+      S.hist[b] = 0;
     }
-    *reinterpret_cast<uint4 *>(&S.tot[4 * b4]) = acc;
   }
-  __syncthreads();
-  // descending scan: thread t owns bins [bins-1-4t, bins-4-4t]
-  const int lane = tid & 31, wid = tid >> 5;
-  uint32_t c4[4], loc = 0;
+}
+
+// Threshold of the cluster totals tot[buf] for `need` (bins of the level):
+// thr = -1 when everything matching fits.  Clears tot[buf] for its next use.
+__device__ void local_threshold(TopkClusterSmem &S, int buf, uint32_t need, int bins) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  uint32_t c[kBinsPerThread], loc = 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int b = bins - 1 - (4 * tid + j);
-    c4[j] = (b >= 0) ? S.tot[b] : 0u;
-    loc += c4[j];
+  for (int j = 0; j < kBinsPerThread; ++j) {
+    const int b = bins - 1 - (kBinsPerThread * tid + j);
+    c[j] = (b >= 0) ? S.tot[buf][b] : 0u;
+    loc += c[j];
   }
   uint32_t incl = loc;
 #pragma unroll
@@ -119,56 +142,61 @@ __device__ void cluster_threshold(TopkClusterSmem &S, int buf, uint32_t nctas, u
   __syncthreads();
   if (total > need) {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int b = bins - 1 - (4 * tid + j);
-      if (b >= 0 && before < need && before + c4[j] >= need) {
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      const int b = bins - 1 - (kBinsPerThread * tid + j);
+      if (b >= 0 && before < need && before + c[j] >= need) {
         S.thr = b;
         S.above = before;
-        S.in_thr = c4[j];
+        S.in_thr = c[j];
       }
-      before += c4[j];
+      before += c[j];
     }
   }
+  for (int b = tid; b < kBins; b += kThreads) S.tot[buf][b] = 0;
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r) {
-  extern __shared__ uint8_t smem_raw[];
-  TopkClusterSmem &S = *reinterpret_cast<TopkClusterSmem *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const uint32_t crank = cluster_ctarank(), nctas = cluster_nctarank();
-  const int row = blockIdx.y;
-  const float *vals = r.vals + (int64_t)row * r.row_stride;
-  const int64_t lo = r.row_len * crank / nctas, hi = r.row_len * (crank + 1) / nctas;
-  const uint32_t nsel0 = dsmem_addr(&S.n_sel, 0), sel0 = dsmem_addr(&S.sel[0], 0);
-
-  for (int i = tid; i < kBins; i += kThreads) S.hist[0][i] = 0;
-  if (tid == 0) {
-    S.n_sel = 0;
-    S.tie_cnt = 0;
-  }
-  __syncthreads();
-
-  // level-0 histogram of this slice
-  for (int64_t base = lo; base < hi; base += (int64_t)kThreads * kPer) {
-    float v[kPer];
+// Calls f(key, index) for the keys of this CTA's slice [lo, hi) (multiples of
+// 4), 32 per thread per round, taking one round of every step_rounds.
+template <typename F>
+__device__ __forceinline__ void for_slice(const float *vals, int64_t lo, int64_t hi, int64_t step_rounds, F &&f) {
+  const int tid = threadIdx.x;
+  for (int64_t base = lo; base < hi; base += (int64_t)kRound * step_rounds) {
+    float4 v[kVec];
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int64_t i = base + j * kThreads + tid;
-      v[j] = (i < hi) ? vals[i] : -INFINITY;
+    for (int j = 0; j < kVec; ++j) {
+      const int64_t i = base + ((int64_t)j * kThreads + tid) * 4;
+      v[j] = (i < hi) ? __ldcg(reinterpret_cast<const float4 *>(vals + i))
+                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
     }
 #pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const uint32_t key = score_key(v[j]);
-      const uint32_t bin = key ? (key >> 21) : (uint32_t)kBins;
-      const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-      if (bin < kBins && lane == __ffs(peers) - 1) atomicAdd(&S.hist[0][bin], (uint32_t)__popc(peers));
+    for (int j = 0; j < kVec; ++j) {
+      const int32_t i = (int32_t)(base + ((int64_t)j * kThreads + tid) * 4);
+      f(score_key(v[j].x), i);
+      f(score_key(v[j].y), i + 1);
+      f(score_key(v[j].z), i + 2);
+      f(score_key(v[j].w), i + 3);
     }
   }
-  cluster_sync();
+}
 
-  cluster_threshold(S, 0, nctas, (uint32_t)r.k, kBins);
+// Calls f(key, index) for the CTA's candidate list; uniform trip count.
+template <typename F>
+__device__ __forceinline__ void for_cands(TopkClusterSmem &S, F &&f) {
+  const int n = (int)min(S.ccount, (uint32_t)kCand);
+  for (int b0 = 0; b0 < n; b0 += kThreads) {
+    const int i = b0 + threadIdx.x;
+    f(i < n ? S.ckey[i] : 0u, i < n ? S.cidx[i] : -1);
+  }
+}
+
+// The radix levels; tot[0] holds the cluster's level-0 histogram on entry.
+// Returns the count still needed (full-key ties) and the tie key in *full.
+template <bool kCands>
+__device__ uint32_t run_levels(TopkClusterSmem &S, const TopkRows &r, const float *vals, int64_t lo, int64_t hi,
+                               uint32_t nctas, uint32_t *full) {
+  const int lane = threadIdx.x & 31;
+  local_threshold(S, 0, (uint32_t)r.k, kBins);
   uint32_t need = S.total < (uint32_t)r.k ? S.total : (uint32_t)r.k;
   int level = 0, buf = 0;
   uint32_t prefix = 0;
@@ -179,38 +207,16 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
     // needed (or when everything matching fits: thr = -1)
     const bool take_thr = thr < 0 || above + in_thr == need;
     const bool last = take_thr || level == 2;
-    const int nbuf = buf ^ 1;
-    if (!last)
-      for (int i = tid; i < kBins; i += kThreads) S.hist[nbuf][i] = 0;
-    __syncthreads();
-    for (int64_t base = lo; base < hi; base += (int64_t)kThreads * kPer) {
-      float v[kPer];
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int64_t i = base + j * kThreads + tid;
-        v[j] = (i < hi) ? vals[i] : -INFINITY;
-      }
-#pragma unroll
-      for (int j = 0; j < kPer; ++j) {
-        const int64_t i = base + j * kThreads + tid;
-        const uint32_t key = score_key(v[j]);
-        const bool m = level_match(key, level, prefix);
-        const int d = m ? (int)level_digit(key, level) : -1;
-        // most keys are below the threshold bin: skip the warp unless a lane
-        // has work (selection, next-level histogram or tie count)
-        if (!__any_sync(0xffffffffu, m && d >= thr)) continue;
-        append_sel(m && (d > thr || (take_thr && d == thr)), (int32_t)i, nsel0, sel0, lane);
-        if (!last) {
-          const uint32_t nbin = (m && d == thr) ? level_digit(key, level + 1) : (uint32_t)kBins;
-          const uint32_t peers = __match_any_sync(0xffffffffu, nbin);
-          if (nbin < kBins && lane == __ffs(peers) - 1) atomicAdd(&S.hist[nbuf][nbin], (uint32_t)__popc(peers));
-        } else if (level == 2 && !take_thr) {
-          // keys equal on all 32 bits: counted here, resolved by index below
-          const uint32_t tm = __ballot_sync(0xffffffffu, m && d == thr);
-          if (lane == 0 && tm) atomicAdd(&S.tie_cnt, (uint32_t)__popc(tm));
-        }
-      }
-    }
+    auto body = [&](uint32_t key, int32_t idx) {
+      const bool m = level_match(key, level, prefix);
+      const int d = m ? (int)level_digit(key, level) : -1;
+      // most keys are below the threshold bin: skip the warp unless a lane has work
+      if (!__any_sync(0xffffffffu, m && d >= thr)) return;
+      append_sel(S, m && (d > thr || (take_thr && d == thr)), idx, lane);
+      if (!last) hist_add(S, (m && d == thr) ? level_digit(key, level + 1) : (uint32_t)kBins, lane);
+    };
+    if (kCands) for_cands(S, body);
+    else for_slice(vals, lo, hi, 1, body);
     if (last) {
       if (take_thr) {
         need = 0;
@@ -220,26 +226,119 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
       }
       break;
     }
-    cluster_sync();   // every CTA's next-level histogram is complete
+    __syncthreads();
+    push_hist(S, buf ^ 1, nctas);
+    cluster_sync();   // every CTA's next-level histogram has been added everywhere
     need -= above;
     prefix = (level == 0) ? (uint32_t)thr : ((prefix << 11) | (uint32_t)thr);
     ++level;
-    buf = nbuf;
-    cluster_threshold(S, buf, nctas, need, level == 2 ? 1024 : kBins);
+    buf ^= 1;
+    local_threshold(S, buf, need, level == 2 ? 1024 : kBins);
   }
+  *full = prefix;
+  return need;
+}
+
+__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r) {
+  extern __shared__ uint8_t smem_raw[];
+  TopkClusterSmem &S = *reinterpret_cast<TopkClusterSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const uint32_t crank = cluster_ctarank(), nctas = cluster_nctarank();
+  const int row = blockIdx.y;
+  const float *vals = r.vals + (int64_t)row * r.row_stride;
+  const int64_t n4 = r.row_len / 4;
+  const int64_t lo = 4 * (n4 * crank / nctas), hi = 4 * (n4 * (crank + 1) / nctas);
+
+  for (int i = tid; i < kBins; i += kThreads) {
+    S.hist[i] = 0;
+    S.tot[0][i] = 0;
+    S.tot[1][i] = 0;
+  }
+  if (tid < kMaxCluster) {
+    S.cand_cnt[tid] = 0;
+    S.tie_cnt[tid] = 0;
+    S.sel_cnt[tid] = 0;
+  }
+  if (tid == 0) {
+    S.ccount = 0;
+    S.n_sel = 0;
+    S.n_tie = 0;
+  }
+  cluster_sync();   // every CTA's totals are cleared before anyone pushes
+
+  // 1. sample: one round of every kSampleEvery
+  for_slice(vals, lo, hi, kSampleEvery,
+            [&](uint32_t key, int32_t) { hist_add(S, key ? (key >> 21) : (uint32_t)kBins, lane); });
+  __syncthreads();
+  push_hist(S, 0, nctas);
+  cluster_sync();
+  {
+    // the sample's share of the row (the same in every CTA: CTA 0's slice)
+    const int64_t slice = 4 * (n4 / nctas) > 0 ? 4 * (n4 / nctas) : 1;
+    const int64_t rounds = (slice + kRound - 1) / kRound;
+    const int64_t sampled = ((rounds + kSampleEvery - 1) / kSampleEvery) * kRound;
+    const double frac = sampled >= slice ? 1.0 : (double)sampled / (double)slice;
+    local_threshold(S, 0, (uint32_t)(2.0 * r.k * frac) + 16, kBins);
+  }
+  const uint32_t t_low = S.thr < 0 ? 1u : ((uint32_t)S.thr << 21);
+
+  // 2. filter into the candidate list
+  for_slice(vals, lo, hi, 1, [&](uint32_t key, int32_t idx) {
+    const bool f = key >= t_low;
+    const uint32_t m = __ballot_sync(0xffffffffu, f);
+    if (!m) return;
+    uint32_t base = 0;
+    if (lane == 0) base = atomicAdd(&S.ccount, (uint32_t)__popc(m));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    if (f) {
+      const uint32_t pos = base + __popc(m & ((1u << lane) - 1));
+      if (pos < kCand) {
+        S.ckey[pos] = key;
+        S.cidx[pos] = idx;
+      }
+    }
+  });
+  __syncthreads();
+  if (tid < (int)nctas) dsmem_st_u32(dsmem_addr(&S.cand_cnt[crank], (uint32_t)tid), S.ccount);
+  cluster_sync();
+  uint32_t total_cand = 0;
+  bool overflow = false;
+  for (uint32_t c = 0; c < nctas; ++c) {
+    total_cand += S.cand_cnt[c];
+    overflow |= S.cand_cnt[c] > (uint32_t)kCand;
+  }
+
+  // 3. exact select, on the candidate lists when they are complete
+  uint32_t need, full = 0;
+  const bool fast = !overflow && total_cand >= (uint32_t)r.k;
+  if (fast)
+    for_cands(S, [&](uint32_t key, int32_t) { hist_add(S, key ? (key >> 21) : (uint32_t)kBins, lane); });
+  else
+    for_slice(vals, lo, hi, 1,
+              [&](uint32_t key, int32_t) { hist_add(S, key ? (key >> 21) : (uint32_t)kBins, lane); });
+  __syncthreads();
+  push_hist(S, 0, nctas);
+  cluster_sync();
+  need = fast ? run_levels<true>(S, r, vals, lo, hi, nctas, &full)
+              : run_levels<false>(S, r, vals, lo, hi, nctas, &full);
 
   if (need > 0) {
     // ties on the full key: the `need` lowest indices, CTA slices in order
-    const uint32_t full = prefix;   // 32-bit key
+    for_slice(vals, lo, hi, 1, [&](uint32_t key, int32_t) {
+      const uint32_t tm = __ballot_sync(0xffffffffu, key == full);
+      if (lane == 0 && tm) atomicAdd(&S.n_tie, (uint32_t)__popc(tm));
+    });
     __syncthreads();
+    if (tid < (int)nctas) dsmem_st_u32(dsmem_addr(&S.tie_cnt[crank], (uint32_t)tid), S.n_tie);
     cluster_sync();
     uint32_t before = 0;
-    for (uint32_t c = 0; c < crank; ++c) before += dsmem_ld_u32(dsmem_addr(&S.tie_cnt, c));
-    const uint32_t quota = need > before ? min(need - before, S.tie_cnt) : 0u;
+    for (uint32_t c = 0; c < crank; ++c) before += S.tie_cnt[c];
+    const uint32_t quota = need > before ? min(need - before, S.n_tie) : 0u;
     uint32_t running = 0;
     for (int64_t base = lo; base < hi && running < quota; base += kThreads) {
       const int64_t i = base + tid;
-      const bool f = i < hi && score_key(vals[i]) == full;
+      const bool f = i < hi && score_key(__ldcg(vals + i)) == full;
       const uint32_t m = __ballot_sync(0xffffffffu, f);
       if (lane == 0) S.warp_cnt[wid] = __popc(m);
       __syncthreads();
@@ -249,48 +348,54 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
         tot += S.warp_cnt[w];
       }
       const uint32_t rank = running + wb + __popc(m & ((1u << lane) - 1));
-      append_sel(f && rank < quota, (int32_t)i, nsel0, sel0, lane);
+      append_sel(S, f && rank < quota, (int32_t)i, lane);
       running += tot;
       __syncthreads();
     }
   }
-  cluster_sync();
 
-  if (crank != 0) return;
-  // CTA 0: map to positions, sort ascending, write (-1 padded)
-  const uint32_t n = min(S.n_sel, (uint32_t)r.k);
-  int32_t *out = r.out + (int64_t)row * r.k;
-  for (uint32_t i = tid; i < n; i += kThreads) {
-    const int32_t s = S.sel[i];
-    int32_t pos = s;
-    if (r.pool) {
-      const int32_t blk = __ldg(r.pool + (int64_t)row * r.pool_stride + s / BLOCK);
-      pos = blk * BLOCK + (s & (BLOCK - 1));
-    }
-    S.sel[i] = pos;
-  }
+  // 4. every CTA writes its sorted selections at its cluster prefix offset
   __syncthreads();
-  for (uint32_t i = tid; i < n; i += kThreads) {
+  const uint32_t mine = min(S.n_sel, (uint32_t)kSelMax);
+  if (tid < (int)nctas) dsmem_st_u32(dsmem_addr(&S.sel_cnt[crank], (uint32_t)tid), mine);
+  cluster_sync();   // the last remote access: afterwards every CTA works on its own memory
+  uint32_t off = 0, all = 0;
+  for (uint32_t c = 0; c < nctas; ++c) {
+    if (c < crank) off += S.sel_cnt[c];
+    all += S.sel_cnt[c];
+  }
+  int32_t *out = r.out + (int64_t)row * r.k;
+  for (uint32_t i = tid; i < mine; i += kThreads) {
     const int32_t v = S.sel[i];
     uint32_t rank = 0;
-    for (uint32_t j = 0; j < n; ++j) rank += S.sel[j] < v;
-    out[rank] = v;
+    for (uint32_t j = 0; j < mine; ++j) rank += S.sel[j] < v;
+    int32_t pos = v;
+    if (r.pool) {
+      const int32_t blk = __ldg(r.pool + (int64_t)row * r.pool_stride + v / BLOCK);
+      pos = blk * BLOCK + (v & (BLOCK - 1));
+    }
+    if (off + rank < (uint32_t)r.k) out[off + rank] = pos;
   }
-  for (int i = (int)n + tid; i < r.k; i += kThreads) out[i] = -1;
+  if (crank == nctas - 1)
+    for (int i = (int)min(all, (uint32_t)r.k) + tid; i < r.k; i += kThreads) out[i] = -1;
 }
 
 }  // namespace
 
-bool topk_cluster_supported(const TopkRows &r) { return r.k <= kSelMax; }
+bool topk_cluster_supported(const TopkRows &r) {
+  return r.k <= kSelMax && r.row_len % 4 == 0 && r.row_stride % 4 == 0 &&
+         (reinterpret_cast<uintptr_t>(r.vals) & 15u) == 0;
+}
 
 cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches) {
   if (r.rows <= 0) return cudaSuccess;
+  if (!topk_cluster_supported(r)) return cudaErrorInvalidValue;
   static int max_cluster = 0;
   if (!max_cluster) {
     max_cluster = 8;
     if (cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
         cudaSuccess)
-      max_cluster = 16;
+      max_cluster = kMaxCluster;
     else
       (void)cudaGetLastError();
   }
