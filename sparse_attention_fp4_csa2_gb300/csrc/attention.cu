@@ -10,12 +10,13 @@
 // the products (section 2.4.4: FP4 reduces storage, not matmul cost).
 //
 // Work split (flash-decoding): a CTA owns 128 keys of one query token -- one
-// chunk of the top-K list or of the SWA window -- and writes its partial (row
-// max, row sum, unnormalised output) to the workspace.  With up to 8 chunks
-// (the pages' 512 + 128 keys make 5) the chunks of a token form one
-// thread-block cluster and merge after one cluster barrier, each CTA a slice
-// of the dims, from the partials in L2; with more chunks a separate combine
-// kernel merges them.  Inside a CTA, with the keys as the MMA M dimension:
+// chunk of the top-K list or of the SWA window -- and produces a partial (row
+// max, row sum, output).  With up to 8 chunks (the pages' 512 + 128 keys make
+// 5) the chunks of a token form one thread-block cluster and merge in shared
+// memory: each CTA pushes to every other one, by bulk shared-to-shared copies,
+// the slice of its normalised fp16 partial that CTA owns, and sums its own
+// slice into the output; with more chunks the partials go to the workspace
+// and a separate combine kernel merges them.  Inside a CTA:
 //   gather   Q arrives by TMA and the SWA rows by one bulk copy (mbarrier);
 //            every thread issues 16-byte cp.async copies of the selected FP4
 //            entries (18 per 288-byte entry) into a shared staging area;
@@ -28,13 +29,15 @@
 //            and sum over the 128 keys by warp butterfly transposes + shared
 //            memory; P = exp2(S - m) (times the SWA row scale) in fp16 written
 //            MN-major [128 keys x 64 heads];
-//   O^T      = V^T P: the same shared tile read MN-major as A (M = 512 dims in
-//            4 tiles of 128, K = 128 keys), P as B; fp32 in TMEM;
-//   store    per (head, dim) the unnormalised partial, coalesced along dims.
+//   O        = P V: P as A (heads as M), the same shared tile read MN-major as
+//            B (N = 2 x 256 dims, K = 128 keys); fp32 in TMEM with the heads
+//            as lanes, so a thread reads 32 consecutive dims of one head;
+//   merge    as above.
 // Shared memory: 128 KB tile (the FP4 staging area lives in its tail and is
-// consumed through registers before the tile is written), 64 KB Q (reused for
-// P), reductions; one CTA per SM.  TMEM: 256 columns (S^T uses 64 of them and
-// is dead before O^T is written).
+// consumed through registers before the tile is written; later the fp16
+// partial), 64 KB Q (reused for P, then as the merge's receive area),
+// reductions; one CTA per SM.  TMEM: 512 columns (S^T uses 64 of them and is
+// dead before O is written).
 #include "kernels.cuh"
 
 namespace csa2 {
@@ -48,23 +51,31 @@ constexpr int kQBytes = H * D * 2;                  // 64 KB fp16
 constexpr int kQAtomCol = H * 128;                  // 8 KB
 constexpr int kStageOff = kTileBytes - ATTN_CHUNK * ENTRY_BYTES;   // FP4 staging at the tile's tail
 constexpr int kSwaStageOff = kTileBytes - ATTN_CHUNK * D;          // E4M3 SWA staging: the tile's upper half
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ H, /*M*/ ATTN_CHUNK);
-constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B MN-major*/ 1, /*N*/ H, /*M*/ 128);
+// O = P V: A = P (M = 128 rows: the 64 heads, then 64 rows nobody reads), B = V
+// read MN-major from the tile, N = 256 dims per instruction
+constexpr uint32_t kPVN = 256;
+constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B MN-major*/ 1, /*N*/ kPVN, /*M*/ 128);
 
 constexpr int kMaxClusterChunks = 8;   // portable cluster size
+// cluster merge: the [64 heads x 512 dims] fp16 partial is 512 groups of 128 B
+constexpr int kRowBytes = D * 2;
+constexpr int kGroups = H * kRowBytes / 128;
 
-struct __align__(8) AttnSmem {
+struct __align__(16) AttnSmem {
+  float mfin[H];   // mfin, lfin adjacent: one 512-byte (m, l) record per chunk
+  float lfin[H];
+  float ml_in[kMaxClusterChunks][2][H];   // cluster merge: every chunk's (m, l)
+  float wgt[kMaxClusterChunks][H];        // cluster merge: every chunk's per-head weight
   uint64_t bar_load;
   uint64_t bar_mma;
+  uint64_t bar_merge;
   uint32_t tmem_base;
   uint32_t vmask[ATTN_CHUNK / 32];
   int32_t ids[ATTN_CHUNK];
   float row_scale[ATTN_CHUNK];
   float red[4][H];
-  float mfin[H];
-  float lfin[H];
-  float rm[kMaxClusterChunks][H];   // cluster merge: every chunk's per-head weight
 };
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kTileBytes + kQBytes + sizeof(AttnSmem);
@@ -116,6 +127,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&S.bar_load, 1);
     mbar_init(&S.bar_mma, 1);
+    mbar_init(&S.bar_merge, 1);
+    if (a.cluster) {
+      // armed before the first cluster barrier, so before any peer's copy
+      // into this CTA can start: every other chunk sends its (m, l) record
+      // and this CTA's slice of its partial
+      const uint32_t crank = cluster_ctarank(), nct = cluster_nctarank();
+      const uint32_t slice = ((crank + 1) * kGroups / nct - crank * kGroups / nct) * 128;
+      mbar_arrive_expect_tx(&S.bar_merge, (nct - 1) * (slice + 2 * H * 4));
+    }
     fence_barrier_init();
   }
   if (warp == 0) {
@@ -343,85 +363,158 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (tid < H) S.lfin[tid] = (S.red[0][tid] + S.red[1][tid]) + (S.red[2][tid] + S.red[3][tid]);
 
-  // ------------------------------------------------------------- O^T = V^T P
+  // --------------------------------------------------------------- O = P V
+  // P as A, MN-major (heads contiguous): rows 0-63 are the heads; the second
+  // 64-row atom points at the next 16 KB of the Q region, so D rows 64-127 are
+  // computed from stale values and never read.  V as B, MN-major: 4 of the
+  // tile's 64-dim columns per instruction.  D overwrites S in TMEM (S has been
+  // read into registers): lane = head, column = dim.
   if (tid == 0 && ok) {
     tc_fence_after();
     const uint32_t ta = smem_u32(tile), pa = smem_u32(qs);
-#pragma unroll 1
-    for (int mt = 0; mt < D / 128; ++mt) {
 #pragma unroll
-      for (int kk = 0; kk < ATTN_CHUNK / 16; ++kk) {
-        const uint64_t ad = smem_desc(ta + (2 * mt) * kAtomCol + kk * 2048, kAtomCol, 1024);
-        const uint64_t bd = smem_desc(pa + kk * 2048, 8192, 1024);
-        mma_f16(tmem + mt * H, ad, bd, kIdescPV, kk > 0 ? 1u : 0u);
+    for (int kk = 0; kk < ATTN_CHUNK / 16; ++kk) {
+      const uint64_t ad = smem_desc(pa + kk * 2048, 16384, 1024);
+#pragma unroll
+      for (int nh = 0; nh < D / (int)kPVN; ++nh) {
+        const uint64_t bd = smem_desc(ta + (nh * (kPVN / 64)) * kAtomCol + kk * 2048, kAtomCol, 1024);
+        mma_f16(tmem + nh * kPVN, ad, bd, kIdescPV, kk > 0 ? 1u : 0u);
       }
     }
     mma_commit(&S.bar_mma);
   }
   if (ok) ok = mbar_wait(&S.bar_mma, 1);
   tc_fence_after();
-  __syncthreads();
+  const bool all_ok = __syncthreads_and(ok) != 0;
+
+  // TMEM lanes 0-63 (the heads) are reachable from warps 0, 1, 4, 5; warps
+  // w and w+4 take the lower and upper 256 dims of the same 32 heads.
+  const bool epi = (warp & 3) < 2;
+  const int eh = (warp & 3) * 32 + lane;   // head of this thread's TMEM lane
+  const int ec0 = (warp >> 2) * 256;       // first dim of its half
+  const uint32_t etm = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)ec0;
 
   // ---------------------------------------------------------------- merge
-  const int64_t pc = (int64_t)p * a.n_chunks + chunk;
-  {
-    // unnormalised partial O of this chunk, with its per-head (max, sum), to
-    // the workspace (coalesced along dims; it stays in L2)
-    float *po = a.part_o + pc * H * D;
-#pragma unroll 1
-    for (int mt = 0; mt < D / 128; ++mt) {
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(mt * H + hh * 32), v);
-      tmem_ld_wait();
-      const int d = mt * 128 + quad * 32 + lane;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) po[(int64_t)(hh * 32 + i) * D + d] = ok ? __uint_as_float(v[i]) : 0.0f;
-    }
-    if (tid < H) {
-      a.part_ml[pc * 2 * H + tid] = ok ? S.mfin[tid] : -INFINITY;
-      a.part_ml[pc * 2 * H + H + tid] = ok ? S.lfin[tid] : 0.0f;
-    }
-  }
   if (a.cluster) {
-    // The token's chunks are the CTAs of one cluster: after one cluster
-    // barrier (release / acquire orders the partial stores above) CTA c
-    // merges its slice of the 512 dims from every chunk's partial:
-    // M = max m_c, L = sum l_c 2^(m_c - M), out = sum_c 2^(m_c - M) O_c / L.
+    // The token's chunks are the CTAs of one cluster.  Each CTA normalises
+    // its partial (O / l) into fp16 (a convex combination of values: |.| <=
+    // 6 x 448), then pushes to every other CTA, by bulk shared-to-shared
+    // copies, its (m, l) record and the slice of the [head][dim] partial that
+    // CTA owns.  Each CTA then sums its slice over the chunks with weights
+    // l_c 2^(m_c - M) / L straight into the output.
     const uint32_t crank = cluster_ctarank(), nct = cluster_nctarank();
-    __threadfence();
-    cluster_sync();
-    const float *pbase = a.part_o + (int64_t)p * a.n_chunks * H * D;
-    const float *mlbase = a.part_ml + (int64_t)p * a.n_chunks * 2 * H;
-    if (tid < H) {
-      float M = -INFINITY;
-      for (uint32_t c = 0; c < nct; ++c) M = fmaxf(M, mlbase[c * 2 * H + tid]);
-      float L = 0.0f;
-      for (uint32_t c = 0; c < nct; ++c) {
-        const float mc = mlbase[c * 2 * H + tid];
-        const float w = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
-        S.rm[c][tid] = w;   // merge weight of chunk c for this head
-        L += w * mlbase[c * 2 * H + H + tid];
+    cluster_arrive();   // this CTA's Q/P region is free to receive
+    if (tid < H && !all_ok) {
+      S.mfin[tid] = -INFINITY;
+      S.lfin[tid] = 0.0f;
+    }
+    uint8_t *sendb = tile;   // [64 heads][1024 B] fp16, 16-byte chunks XOR-swizzled by (head & 7)
+    if (epi) {
+      const float l = S.lfin[eh];
+      const float inv = (all_ok && l > 0.0f) ? 1.0f / l : 0.0f;
+#pragma unroll 1
+      for (int j = 0; j < 8; ++j) {
+        uint32_t v[32];
+        tmem_ld32(etm + (uint32_t)(j * 32), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          uint4 o;
+          o.x = pack_half2(__uint_as_float(v[8 * t + 0]) * inv, __uint_as_float(v[8 * t + 1]) * inv);
+          o.y = pack_half2(__uint_as_float(v[8 * t + 2]) * inv, __uint_as_float(v[8 * t + 3]) * inv);
+          o.z = pack_half2(__uint_as_float(v[8 * t + 4]) * inv, __uint_as_float(v[8 * t + 5]) * inv);
+          o.w = pack_half2(__uint_as_float(v[8 * t + 6]) * inv, __uint_as_float(v[8 * t + 7]) * inv);
+          const int cr = (ec0 + j * 32) / 8 + t;   // 16-byte chunk of the head's row
+          *reinterpret_cast<uint4 *>(sendb + eh * kRowBytes + (((cr & ~7) | ((cr & 7) ^ (eh & 7))) << 4)) = o;
+        }
       }
-      S.red[0][tid] = (L > 0.0f) ? 1.0f / L : 0.0f;
+    }
+    fence_proxy_async_smem();   // the bulk copies read what the threads wrote
+    __syncthreads();
+    cluster_wait();             // every CTA of the cluster may now receive
+    if (tid < (int)nct && tid != (int)crank) {
+      const uint32_t s = (uint32_t)tid;
+      const uint32_t g0 = s * kGroups / nct, bytes = ((s + 1) * kGroups / nct - g0) * 128;
+      const uint32_t slot = crank < s ? crank : crank - 1;
+      const uint32_t bar = dsmem_addr(&S.bar_merge, s);
+      bulk_s2s_cluster(dsmem_addr(&S.ml_in[crank][0][0], s), S.mfin, 2 * H * 4, bar);
+      bulk_s2s_cluster(dsmem_addr(qs + slot * bytes, s), sendb + g0 * 128, bytes, bar);
+    }
+    mbar_wait(&S.bar_merge, 0);
+    cluster_arrive();   // everything this CTA needs has arrived: its peers' buffers are free
+    if (tid < H) {
+      float mc[kMaxClusterChunks], lc[kMaxClusterChunks];
+      float M = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c)
+        if (c < (int)nct) {
+          mc[c] = c == (int)crank ? S.mfin[tid] : S.ml_in[c][0][tid];
+          lc[c] = c == (int)crank ? S.lfin[tid] : S.ml_in[c][1][tid];
+          M = fmaxf(M, mc[c]);
+        }
+      float L = 0.0f;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c)
+        if (c < (int)nct && mc[c] != -INFINITY) L += lc[c] * exp2f(mc[c] - M);
+      const float invL = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c)
+        if (c < (int)nct) S.wgt[c][tid] = mc[c] == -INFINITY ? 0.0f : lc[c] * exp2f(mc[c] - M) * invL;
       if (crank == 0 && a.lse)
         a.lse[gp * H + tid] = (L > 0.0f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
-    const int q0 = (int)(crank * (D / 4) / nct), q1 = (int)((crank + 1) * (D / 4) / nct);
-    const int nq = q1 - q0;
+    const uint32_t g0 = crank * kGroups / nct, g1 = (crank + 1) * kGroups / nct;
+    const uint32_t bytes = (g1 - g0) * 128;
     float *outp = a.out + gp * H * D;
-    for (int e = tid; e < H * nq; e += kThreads) {
-      const int h = e / nq, q = q0 + e % nq;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-      for (uint32_t c = 0; c < nct; ++c) {
-        const float4 v = __ldcg(reinterpret_cast<const float4 *>(pbase + ((size_t)c * H + h) * D) + q);
-        const float w = S.rm[c][h];
-        acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+    for (int k = (int)g0 * 8 + tid; k < (int)g1 * 8; k += kThreads) {
+      const int h = k >> 6, cr = k & 63;   // head, 16-byte chunk (8 dims) of its row
+      const uint32_t off = (uint32_t)(h * kRowBytes + (((cr & ~7) | ((cr & 7) ^ (h & 7))) << 4));
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+#pragma unroll
+      for (int c = 0; c < kMaxClusterChunks; ++c)
+        if (c < (int)nct) {
+          const uint8_t *src = c == (int)crank ? sendb + off
+                                               : qs + (uint32_t)(c < (int)crank ? c : c - 1) * bytes + off - g0 * 128;
+          const uint4 v = *reinterpret_cast<const uint4 *>(src);
+          const float w = S.wgt[c][h];
+          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[i]));
+            acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+          }
+        }
+      float4 *dst = reinterpret_cast<float4 *>(outp + h * D + cr * 8);
+      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+    cluster_wait();   // no CTA leaves while a peer's copy may still read its buffer
+  } else {
+    // unnormalised partial O of this chunk, with its per-head (max, sum), to
+    // the workspace for the combine kernel
+    const int64_t pc = (int64_t)p * a.n_chunks + chunk;
+    if (epi) {
+      float *po = a.part_o + (pc * H + eh) * D + ec0;
+#pragma unroll 1
+      for (int j = 0; j < 8; ++j) {
+        uint32_t v[32];
+        tmem_ld32(etm + (uint32_t)(j * 32), v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int t = 0; t < 8; ++t)
+          reinterpret_cast<float4 *>(po + j * 32)[t] =
+              all_ok ? make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
+                                   __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3]))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      const float il = S.red[0][h];
-      acc.x *= il; acc.y *= il; acc.z *= il; acc.w *= il;
-      *reinterpret_cast<float4 *>(outp + h * D + 4 * q) = acc;
+    }
+    if (tid < H) {
+      a.part_ml[pc * 2 * H + tid] = all_ok ? S.mfin[tid] : -INFINITY;
+      a.part_ml[pc * 2 * H + H + tid] = all_ok ? S.lfin[tid] : 0.0f;
     }
   }
   tc_fence_before();

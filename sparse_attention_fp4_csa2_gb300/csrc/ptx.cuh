@@ -211,6 +211,27 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split cluster barrier: arrive (release) now, wait (acquire) later, so that
+// independent work can run between the two halves.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// 1-D bulk copy from this CTA's shared memory into another CTA's shared memory
+// in the cluster; completion counted in bytes on that CTA's mbarrier.  `dst`
+// and `bar` are shared::cluster addresses (dsmem_addr), `src` a local shared
+// pointer; both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2s_cluster(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(smem_u32(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // Address of the same shared-memory variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t dsmem_addr(const void *local, uint32_t rank) {
   uint32_t r;
