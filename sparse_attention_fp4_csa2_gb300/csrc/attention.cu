@@ -36,8 +36,8 @@
 // Shared memory: 128 KB tile (the FP4 staging area lives in its tail and is
 // consumed through registers before the tile is written; later the fp16
 // partial), 64 KB Q (reused for P, then as the merge's receive area),
-// reductions; one CTA per SM.  TMEM: 512 columns (S^T uses 64 of them and is
-// dead before O is written).
+// reductions; one CTA per SM.  TMEM: 512 columns (S^T uses 128 of them, two
+// accumulation chains, and is dead before O is written).
 #include "kernels.cuh"
 
 namespace csa2 {
@@ -70,6 +70,7 @@ struct __align__(16) AttnSmem {
   float wgt[kMaxClusterChunks][H];        // cluster merge: every chunk's per-head weight
   uint64_t bar_load;
   uint64_t bar_mma;
+  uint64_t bar_ml;
   uint64_t bar_merge;
   uint32_t tmem_base;
   uint32_t vmask[ATTN_CHUNK / 32];
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(&S.bar_load, 1);
     mbar_init(&S.bar_mma, 1);
+    mbar_init(&S.bar_ml, 1);
     mbar_init(&S.bar_merge, 1);
     if (a.cluster) {
       // armed before the first cluster barrier, so before any peer's copy
@@ -134,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // and this CTA's slice of its partial
       const uint32_t crank = cluster_ctarank(), nct = cluster_nctarank();
       const uint32_t slice = ((crank + 1) * kGroups / nct - crank * kGroups / nct) * 128;
-      mbar_arrive_expect_tx(&S.bar_merge, (nct - 1) * (slice + 2 * H * 4));
+      mbar_arrive_expect_tx(&S.bar_ml, (nct - 1) * (2 * H * 4));
+      mbar_arrive_expect_tx(&S.bar_merge, (nct - 1) * slice);
     }
     fence_barrier_init();
   }
@@ -300,11 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0 && ok) {
     tc_fence_after();
     const uint32_t ta = smem_u32(tile), qa = smem_u32(qs);
+    // even and odd K steps accumulate into two column blocks, two
+    // independent chains that the softmax adds
 #pragma unroll 4
     for (int kk = 0; kk < D / 16; ++kk) {
       const uint64_t ad = smem_desc(ta + (kk >> 2) * kAtomCol + (kk & 3) * 32, 16, 1024);
       const uint64_t bd = smem_desc(qa + (kk >> 2) * kQAtomCol + (kk & 3) * 32, 16, 1024);
-      mma_f16(tmem, ad, bd, kIdescQK, kk > 0 ? 1u : 0u);
+      mma_f16(tmem + (uint32_t)((kk & 1) * H), ad, bd, kIdescQK, kk > 1 ? 1u : 0u);
     }
     mma_commit(&S.bar_mma);
   }
@@ -316,14 +321,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int key = quad * 32 + lane;
   float s[32];
   {
-    uint32_t v[32];
+    uint32_t v[32], v2[32];
     tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(hh * 32), v);
+    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(H + hh * 32), v2);
     tmem_ld_wait();
     const bool valid = ok && ((S.vmask[key >> 5] >> (key & 31)) & 1);
     // log2(e) / sqrt(512), times the SWA row scale (the key is code x scale)
     const float f = 0.06375871295460785f * S.row_scale[key];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) s[i] = valid ? __uint_as_float(v[i]) * f : -INFINITY;
+    for (int i = 0; i < 32; ++i) s[i] = valid ? (__uint_as_float(v[i]) + __uint_as_float(v2[i])) * f : -INFINITY;
   }
   {
     float t[32];
@@ -364,17 +370,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid < H) S.lfin[tid] = (S.red[0][tid] + S.red[1][tid]) + (S.red[2][tid] + S.red[3][tid]);
 
   // --------------------------------------------------------------- O = P V
-  // P as A, MN-major (heads contiguous): rows 0-63 are the heads; the second
-  // 64-row atom points at the next 16 KB of the Q region, so D rows 64-127 are
-  // computed from stale values and never read.  V as B, MN-major: 4 of the
-  // tile's 64-dim columns per instruction.  D overwrites S in TMEM (S has been
-  // read into registers): lane = head, column = dim.
+  // P as A, MN-major (heads contiguous): rows 0-63 are the heads, and the
+  // second 64-row atom is the same P (leading offset 0), so D lanes 64-127
+  // repeat lanes 0-63 and all four TMEM lane quadrants hold heads.  V as B,
+  // MN-major: 4 of the tile's 64-dim columns per instruction.  D overwrites S
+  // in TMEM (S has been read into registers): lane = head, column = dim.
   if (tid == 0 && ok) {
     tc_fence_after();
     const uint32_t ta = smem_u32(tile), pa = smem_u32(qs);
 #pragma unroll
     for (int kk = 0; kk < ATTN_CHUNK / 16; ++kk) {
-      const uint64_t ad = smem_desc(pa + kk * 2048, 16384, 1024);
+      const uint64_t ad = smem_desc(pa + kk * 2048, 0, 1024);
 #pragma unroll
       for (int nh = 0; nh < D / (int)kPVN; ++nh) {
         const uint64_t bd = smem_desc(ta + (nh * (kPVN / 64)) * kAtomCol + kk * 2048, kAtomCol, 1024);
@@ -387,11 +393,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const bool all_ok = __syncthreads_and(ok) != 0;
 
-  // TMEM lanes 0-63 (the heads) are reachable from warps 0, 1, 4, 5; warps
-  // w and w+4 take the lower and upper 256 dims of the same 32 heads.
-  const bool epi = (warp & 3) < 2;
-  const int eh = (warp & 3) * 32 + lane;   // head of this thread's TMEM lane
-  const int ec0 = (warp >> 2) * 256;       // first dim of its half
+  // Warp w reads TMEM lane quadrant w % 4, i.e. heads 32 (w & 1) + lane; the
+  // four warps on the same heads take one quarter of the 512 dims each.
+  const int eh = (warp & 1) * 32 + lane;                       // head of this thread's TMEM lane
+  const int ec0 = (((warp >> 1) & 1) * 2 + (warp >> 2)) * 128;  // first dim of its quarter
   const uint32_t etm = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)ec0;
 
   // ---------------------------------------------------------------- merge
@@ -409,24 +414,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       S.lfin[tid] = 0.0f;
     }
     uint8_t *sendb = tile;   // [64 heads][1024 B] fp16, 16-byte chunks XOR-swizzled by (head & 7)
-    if (epi) {
+    {
       const float l = S.lfin[eh];
       const float inv = (all_ok && l > 0.0f) ? 1.0f / l : 0.0f;
 #pragma unroll 1
-      for (int j = 0; j < 8; ++j) {
-        uint32_t v[32];
-        tmem_ld32(etm + (uint32_t)(j * 32), v);
+      for (int j = 0; j < 4; j += 2) {
+        uint32_t v[2][32];
+        tmem_ld32(etm + (uint32_t)(j * 32), v[0]);
+        tmem_ld32(etm + (uint32_t)(j * 32 + 32), v[1]);
         tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          uint4 o;
-          o.x = pack_half2(__uint_as_float(v[8 * t + 0]) * inv, __uint_as_float(v[8 * t + 1]) * inv);
-          o.y = pack_half2(__uint_as_float(v[8 * t + 2]) * inv, __uint_as_float(v[8 * t + 3]) * inv);
-          o.z = pack_half2(__uint_as_float(v[8 * t + 4]) * inv, __uint_as_float(v[8 * t + 5]) * inv);
-          o.w = pack_half2(__uint_as_float(v[8 * t + 6]) * inv, __uint_as_float(v[8 * t + 7]) * inv);
-          const int cr = (ec0 + j * 32) / 8 + t;   // 16-byte chunk of the head's row
-          *reinterpret_cast<uint4 *>(sendb + eh * kRowBytes + (((cr & ~7) | ((cr & 7) ^ (eh & 7))) << 4)) = o;
-        }
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint4 o;
+            o.x = pack_half2(__uint_as_float(v[u][8 * t + 0]) * inv, __uint_as_float(v[u][8 * t + 1]) * inv);
+            o.y = pack_half2(__uint_as_float(v[u][8 * t + 2]) * inv, __uint_as_float(v[u][8 * t + 3]) * inv);
+            o.z = pack_half2(__uint_as_float(v[u][8 * t + 4]) * inv, __uint_as_float(v[u][8 * t + 5]) * inv);
+            o.w = pack_half2(__uint_as_float(v[u][8 * t + 6]) * inv, __uint_as_float(v[u][8 * t + 7]) * inv);
+            const int cr = (ec0 + (j + u) * 32) / 8 + t;   // 16-byte chunk of the head's row
+            *reinterpret_cast<uint4 *>(sendb + eh * kRowBytes + (((cr & ~7) | ((cr & 7) ^ (eh & 7))) << 4)) = o;
+          }
       }
     }
     fence_proxy_async_smem();   // the bulk copies read what the threads wrote
@@ -436,13 +444,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s = (uint32_t)tid;
       const uint32_t g0 = s * kGroups / nct, bytes = ((s + 1) * kGroups / nct - g0) * 128;
       const uint32_t slot = crank < s ? crank : crank - 1;
-      const uint32_t bar = dsmem_addr(&S.bar_merge, s);
-      bulk_s2s_cluster(dsmem_addr(&S.ml_in[crank][0][0], s), S.mfin, 2 * H * 4, bar);
-      bulk_s2s_cluster(dsmem_addr(qs + slot * bytes, s), sendb + g0 * 128, bytes, bar);
+      bulk_s2s_cluster(dsmem_addr(&S.ml_in[crank][0][0], s), S.mfin, 2 * H * 4, dsmem_addr(&S.bar_ml, s));
+      bulk_s2s_cluster(dsmem_addr(qs + slot * bytes, s), sendb + g0 * 128, bytes, dsmem_addr(&S.bar_merge, s));
     }
-    mbar_wait(&S.bar_merge, 0);
-    cluster_arrive();   // everything this CTA needs has arrived: its peers' buffers are free
+    // warps 0-1 wait for the (m, l) records and compute the weights while
+    // warp 2 waits for the partial slices
+    if (warp == 2) mbar_wait(&S.bar_merge, 0);
     if (tid < H) {
+      mbar_wait(&S.bar_ml, 0);
       float mc[kMaxClusterChunks], lc[kMaxClusterChunks];
       float M = -INFINITY;
 #pragma unroll
@@ -464,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.lse[gp * H + tid] = (L > 0.0f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
     __syncthreads();
+    cluster_arrive();   // everything this CTA needs has arrived: its peers' buffers are free
     const uint32_t g0 = crank * kGroups / nct, g1 = (crank + 1) * kGroups / nct;
     const uint32_t bytes = (g1 - g0) * 128;
     float *outp = a.out + gp * H * D;
@@ -497,10 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // unnormalised partial O of this chunk, with its per-head (max, sum), to
     // the workspace for the combine kernel
     const int64_t pc = (int64_t)p * a.n_chunks + chunk;
-    if (epi) {
+    {
       float *po = a.part_o + (pc * H + eh) * D + ec0;
 #pragma unroll 1
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < 4; ++j) {
         uint32_t v[32];
         tmem_ld32(etm + (uint32_t)(j * 32), v);
         tmem_ld_wait();

@@ -140,7 +140,10 @@ cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int6
   RopeFreqs freqs;
   for (int j = 0; j < ROPE_DIM / 2; ++j)
     freqs.inv[j] = (float)std::pow((double)rope_theta, -(2.0 * j) / (double)ROPE_DIM);
-  const int warps = 8;
+  // Few entries (decode): one warp per block, so that the double-precision
+  // rotations of different entries run on different SMs (FP64 throughput per
+  // SM is low); many entries: 8 warps per block.
+  const int warps = n_entries <= 1024 ? 1 : 8;
   const int64_t blocks = (n_entries + warps - 1) / warps;
   kv_quant_write_kernel<<<(unsigned)blocks, warps * 32, 0, stream>>>(
       static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
