@@ -45,12 +45,23 @@ namespace csa2 {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileBytes = ATTN_CHUNK * D * 2;      // 128 KB fp16
-constexpr int kAtomCol = ATTN_CHUNK * 128;          // 16 KB per 64-dim column of the tile
 constexpr int kQBytes = H * D * 2;                  // 64 KB fp16
 constexpr int kQAtomCol = H * 128;                  // 8 KB
-constexpr int kStageOff = kTileBytes - ATTN_CHUNK * ENTRY_BYTES;   // FP4 staging at the tile's tail
-constexpr int kSwaStageOff = kTileBytes - ATTN_CHUNK * D;          // E4M3 SWA staging: the tile's upper half
+constexpr int kMixSwa = 32;                         // SWA rows per chunk of the mixed layout
+constexpr int kRedOff = 32768;                      // softmax reductions: in the Q region, past P
+
+// Chunk layouts.  Split (kSwa = 0): a chunk is 128 top-K entries or 128 SWA
+// rows.  Mixed (kSwa = 32): a chunk is 128 top-K entries and 32 SWA rows, so
+// the pages' 512 + 128 keys make 4 chunks instead of 5 -- chosen when the
+// chunks outnumber the SMs.  The tile is [8 columns of 64 dims][rows][128 B].
+template <int kSwa>
+struct Layout {
+  static constexpr int kRows = ATTN_CHUNK + kSwa;
+  static constexpr int kTileBytes = kRows * D * 2;                          // fp16 tile
+  static constexpr int kAtomCol = kRows * 128;                             // one 64-dim column
+  static constexpr int kStageOff = kTileBytes - ATTN_CHUNK * ENTRY_BYTES;  // FP4 staging at the tile's tail
+  static constexpr int kSwaStageOff = kTileBytes - ATTN_CHUNK * D;         // split: SWA staging, upper half
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescQK = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ H, /*M*/ ATTN_CHUNK);
 // O = P V: A = P (M = 128 rows: the 64 heads, then 64 rows nobody reads), B = V
@@ -66,20 +77,28 @@ constexpr int kGroups = H * kRowBytes / 128;
 struct __align__(16) AttnSmem {
   float mfin[H];   // mfin, lfin adjacent: one 512-byte (m, l) record per chunk
   float lfin[H];
-  float ml_in[kMaxClusterChunks][2][H];   // cluster merge: every chunk's (m, l)
-  float wgt[kMaxClusterChunks][H];        // cluster merge: every chunk's per-head weight
   uint64_t bar_load;
   uint64_t bar_mma;
   uint64_t bar_ml;
   uint64_t bar_merge;
   uint32_t tmem_base;
-  uint32_t vmask[ATTN_CHUNK / 32];
+  uint32_t vmask[(ATTN_CHUNK + kMixSwa) / 32];
   int32_t ids[ATTN_CHUNK];
-  float row_scale[ATTN_CHUNK];
-  float red[4][H];
+  float row_scale[ATTN_CHUNK + kMixSwa];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)kTileBytes + kQBytes + sizeof(AttnSmem);
+// cluster merge scratch, in the tile region behind the 64 KB fp16 partial
+struct MergeSmem {
+  float ml_in[kMaxClusterChunks][2][H];   // every chunk's (m, l)
+  float wgt[kMaxClusterChunks][H];        // every chunk's per-head weight
+};
+
+template <int kSwa>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Layout<kSwa>::kTileBytes + kQBytes + sizeof(AttnSmem);
+}
+static_assert(smem_bytes<kMixSwa>() <= 232448, "mixed layout exceeds the shared-memory limit");
+static_assert(kRedOff >= (ATTN_CHUNK + kMixSwa) * 128 && kRedOff + 4 * H * 4 <= kQBytes, "reductions overlap P");
 
 // byte offset of 16-byte chunk `c` (0..63 along 512 fp16 channels) of row r in a
 // K-major SW128 tile made of 64-channel columns of `col_bytes` each
@@ -110,18 +129,24 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[32], int lane) 
   }
 }
 
+template <int kSwa>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a) {
+  using Lay = Layout<kSwa>;
+  constexpr bool kMixed = kSwa > 0;
+  constexpr int kAtomCol = Lay::kAtomCol;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *tile = base;                  // [8 cols][128 keys][128 B] fp16, SW128
-  uint8_t *qs = base + kTileBytes;       // [8 cols][64 heads][128 B] fp16, SW128; later P
+  uint8_t *tile = base;                  // [8 cols][rows][128 B] fp16, SW128
+  uint8_t *qs = base + Lay::kTileBytes;  // [8 cols][64 heads][128 B] fp16, SW128; later P
   AttnSmem &S = *reinterpret_cast<AttnSmem *>(qs + kQBytes);
+  MergeSmem &MS = *reinterpret_cast<MergeSmem *>(tile + H * D * 2);
+  float(*red)[H] = reinterpret_cast<float(*)[H]>(qs + kRedOff);   // [4][64]: live only in the softmax
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x, p = blockIdx.y;   // p: this launch's problem (block-local)
   const int64_t gp = a.p0 + p;                     // the query token it serves
-  const bool is_swa = chunk >= a.n_kchunks;
+  const bool is_swa = !kMixed && chunk >= a.n_kchunks;   // split layout: a chunk of SWA rows
   const int64_t seq = gp / a.tokens;
   const int64_t seq_row0 = seq * a.cap;           // the token's sequence in the main-KV cache
 
@@ -152,14 +177,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool ok = true;
 
   // ------------------------------------------------------------------ loads
-  // One mbarrier counts every byte: Q (8 TMA boxes of [64 heads x 64 dims]
-  // bf16 into the SW128 K-major layout) and either the selected FP4 entries
-  // (one 288-byte bulk copy each, into the staging area at the tile's tail) or
-  // the chunk's SWA rows (one contiguous bulk copy into the tile's upper half).
-  const int t0 = (chunk - a.n_kchunks) * ATTN_CHUNK;   // first SWA row of this chunk
+  // One mbarrier counts the bulk bytes: Q (8 TMA boxes of [64 heads x 64
+  // dims] bf16 into the SW128 K-major layout) and the chunk's SWA rows (split:
+  // one contiguous copy into the tile's upper half; mixed: 8-row pieces into
+  // the SWA-row areas of tile columns 0-3, which the top-K rows never touch).
+  // The selected FP4 entries arrive by cp.async into the tile's tail.
+  constexpr int kSwaPer = kMixed ? kSwa : ATTN_CHUNK;   // SWA rows per chunk
+  constexpr int kSwaRow = kMixed ? ATTN_CHUNK : 0;      // their first tile row
+  const int t0 = kMixed ? chunk * kSwa : (chunk - a.n_kchunks) * ATTN_CHUNK;   // first SWA row of this chunk
   int swa_rows = 0;
   int64_t swa_row0 = 0;                              // first SWA row of the token's window
-  if (is_swa) {
+  if (kMixed || is_swa) {
     int len;
     if (a.causal_swa) {
       const int64_t pos = a.first_pos + gp % a.tokens;
@@ -170,19 +198,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       swa_row0 = gp * a.W;
       len = min(__ldg(a.swa_len + gp), a.W);
     }
-    swa_rows = max(0, min(ATTN_CHUNK, len - t0));
-    if (tid < ATTN_CHUNK) S.row_scale[tid] = (tid < swa_rows) ? __ldg(a.swa_scale + swa_row0 + t0 + tid) : 0.0f;
-  } else if (tid < ATTN_CHUNK) {
-    S.row_scale[tid] = 1.0f;
+    swa_rows = max(0, min(kSwaPer, len - t0));
+    if (tid < kSwaPer)
+      S.row_scale[kSwaRow + tid] = (tid < swa_rows) ? __ldg(a.swa_scale + swa_row0 + t0 + tid) : 0.0f;
   }
+  if (!is_swa && tid < ATTN_CHUNK) S.row_scale[tid] = 1.0f;
   if (tid == 0) {
     // Q and the SWA rows first: their latency overlaps the index loads below
-    const uint32_t bytes = (uint32_t)kQBytes + (is_swa ? (uint32_t)swa_rows * D : 0u);
+    const uint32_t bytes = (uint32_t)kQBytes + (uint32_t)swa_rows * D;
     mbar_arrive_expect_tx(&S.bar_load, bytes);
 #pragma unroll
     for (int j = 0; j < D / 64; ++j) tma_load_2d(qs + j * kQAtomCol, &tm_q, j * 64, (int32_t)(gp * H), &S.bar_load);
-    if (is_swa && swa_rows > 0)
-      bulk_g2s(tile + kSwaStageOff, a.swa + (swa_row0 + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
+    if (kMixed) {
+      for (int i = 0; i * 8 < swa_rows; ++i)
+        bulk_g2s(tile + i * kAtomCol + ATTN_CHUNK * 128, a.swa + (swa_row0 + t0 + 8 * i) * D,
+                 (uint32_t)min(8, swa_rows - 8 * i) * D, &S.bar_load);
+    } else if (is_swa && swa_rows > 0) {
+      bulk_g2s(tile + Lay::kSwaStageOff, a.swa + (swa_row0 + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
+    }
   }
   if (tid < ATTN_CHUNK) {
     bool v;
@@ -200,6 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t m = __ballot_sync(0xffffffffu, v);
     if (lane == 0) S.vmask[warp] = m;
+  } else if (kMixed && warp == ATTN_CHUNK / 32) {
+    const uint32_t m = __ballot_sync(0xffffffffu, lane < swa_rows);
+    if (lane == 0) S.vmask[warp] = m;
   }
   if (!is_swa) {
     // gather: the selected entries' 288 bytes as 18 16-byte pieces each, all
@@ -211,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int e = c / (ENTRY_BYTES / 16), piece = c % (ENTRY_BYTES / 16);
       const int32_t id = S.ids[e];
       if (id >= 0)
-        cp_async16(tile + kStageOff + e * ENTRY_BYTES + piece * 16,
+        cp_async16(tile + Lay::kStageOff + e * ENTRY_BYTES + piece * 16,
                    a.kv + (seq_row0 + id) * ENTRY_BYTES + piece * 16);
     }
     cp_async_commit();
@@ -241,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool valid = (S.vmask[row >> 5] >> (row & 31)) & 1;
     uint4 codes[8];
     uint4 scl;
-    const uint8_t *src = tile + kStageOff + row * ENTRY_BYTES;
+    const uint8_t *src = tile + Lay::kStageOff + row * ENTRY_BYTES;
     if (valid && ok) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) codes[k] = *reinterpret_cast<const uint4 *>(src + half * 128 + k * 16);
@@ -279,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // converted to fp16 (exact) into the tile
     const bool valid = row < swa_rows && ok;
     uint4 raw[16];
-    const uint4 *src = reinterpret_cast<const uint4 *>(tile + kSwaStageOff + row * D + half * 256);
+    const uint4 *src = reinterpret_cast<const uint4 *>(tile + Lay::kSwaStageOff + row * D + half * 256);
 #pragma unroll
     for (int k = 0; k < 16; ++k) raw[k] = valid ? src[k] : make_uint4(0, 0, 0, 0);
     __syncthreads();   // the staging area is read; the tile may now be written over it
@@ -296,6 +332,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16 + 1, kAtomCol)) = o1;
     }
   }
+  if (kMixed) {
+    // the 32 SWA rows: thread (r, j) converts dims 64j..64j+63 of row r from
+    // its staging piece (column r / 8, slot r % 8) into tile row 128 + r
+    const int r = tid >> 3, j = tid & 7;
+    const bool valid = r < swa_rows && ok;
+    const uint4 *src =
+        reinterpret_cast<const uint4 *>(tile + (r >> 3) * kAtomCol + ATTN_CHUNK * 128 + (r & 7) * D + j * 64);
+    uint4 raw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) raw[k] = valid ? src[k] : make_uint4(0, 0, 0, 0);
+    __syncthreads();   // every staging piece is read before any SWA row is written
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+      uint4 o0, o1;
+      o0.x = e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)); o0.y = e4m3x2_to_half2((uint16_t)(w[0] >> 16));
+      o0.z = e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)); o0.w = e4m3x2_to_half2((uint16_t)(w[1] >> 16));
+      o1.x = e4m3x2_to_half2((uint16_t)(w[2] & 0xFFFF)); o1.y = e4m3x2_to_half2((uint16_t)(w[2] >> 16));
+      o1.z = e4m3x2_to_half2((uint16_t)(w[3] & 0xFFFF)); o1.w = e4m3x2_to_half2((uint16_t)(w[3] >> 16));
+      const int ch16 = j * 8 + k * 2;
+      *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + r, ch16, kAtomCol)) = o0;
+      *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + r, ch16 + 1, kAtomCol)) = o1;
+    }
+  }
   fence_proxy_async_smem();
   __syncthreads();
 
@@ -307,9 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // independent chains that the softmax adds
 #pragma unroll 4
     for (int kk = 0; kk < D / 16; ++kk) {
-      const uint64_t ad = smem_desc(ta + (kk >> 2) * kAtomCol + (kk & 3) * 32, 16, 1024);
+      const uint32_t aa = ta + (kk >> 2) * kAtomCol + (kk & 3) * 32;
       const uint64_t bd = smem_desc(qa + (kk >> 2) * kQAtomCol + (kk & 3) * 32, 16, 1024);
-      mma_f16(tmem + (uint32_t)((kk & 1) * H), ad, bd, kIdescQK, kk > 1 ? 1u : 0u);
+      mma_f16(tmem + (uint32_t)((kk & 1) * H), smem_desc(aa, 16, 1024), bd, kIdescQK, kk > 1 ? 1u : 0u);
+      // mixed: the same over tile rows 32..159, whose D lanes 96..127 are the SWA rows
+      if (kMixed)
+        mma_f16(tmem + (uint32_t)((2 + (kk & 1)) * H), smem_desc(aa + 32 * 128, 16, 1024), bd, kIdescQK,
+                kk > 1 ? 1u : 0u);
     }
     mma_commit(&S.bar_mma);
   }
@@ -317,57 +381,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
 
   // ---------------------------------------------------------------- softmax
-  const int quad = warp & 3, hh = warp >> 2;   // key rows 32*quad.., heads 32*hh..
+  // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quadrant) for heads
+  // 32 (w / 4) .. + 31; in the mixed layout warps 3 and 7 also own the SWA
+  // rows 128..159 (lanes 96..127 of the second accumulator).
+  const int quad = warp & 3, hh = warp >> 2;
   const int key = quad * 32 + lane;
-  float s[32];
+  const bool extra = kMixed && quad == 3;
+  const int key2 = ATTN_CHUNK + lane;
+  // log2(e) / sqrt(512), times the SWA row scale (the key is code x scale)
+  constexpr float kLogit = 0.06375871295460785f;
+  float s[32], s2[32];
   {
     uint32_t v[32], v2[32];
     tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(hh * 32), v);
     tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(H + hh * 32), v2);
     tmem_ld_wait();
     const bool valid = ok && ((S.vmask[key >> 5] >> (key & 31)) & 1);
-    // log2(e) / sqrt(512), times the SWA row scale (the key is code x scale)
-    const float f = 0.06375871295460785f * S.row_scale[key];
+    const float f = kLogit * S.row_scale[key];
 #pragma unroll
     for (int i = 0; i < 32; ++i) s[i] = valid ? (__uint_as_float(v[i]) + __uint_as_float(v2[i])) * f : -INFINITY;
   }
+  if (extra) {
+    uint32_t v[32], v2[32];
+    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(2 * H + hh * 32), v);
+    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(3 * H + hh * 32), v2);
+    tmem_ld_wait();
+    const bool valid = ok && ((S.vmask[key2 >> 5] >> (key2 & 31)) & 1);
+    const float f = kLogit * S.row_scale[key2];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) s2[i] = valid ? (__uint_as_float(v[i]) + __uint_as_float(v2[i])) * f : -INFINITY;
+  }
   {
     float t[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) t[i] = s[i];
+    for (int i = 0; i < 32; ++i) t[i] = extra ? fmaxf(s[i], s2[i]) : s[i];
     warp_transpose_reduce<true>(t, lane);
-    S.red[quad][hh * 32 + lane] = t[0];
+    red[quad][hh * 32 + lane] = t[0];
   }
   tc_fence_before();
   __syncthreads();
-  if (tid < H) S.mfin[tid] = fmaxf(fmaxf(S.red[0][tid], S.red[1][tid]), fmaxf(S.red[2][tid], S.red[3][tid]));
+  if (tid < H) S.mfin[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
   __syncthreads();
   {
-    const float rs = S.row_scale[key];
-    uint8_t *prow = qs + key * 128;   // P tile: [128 keys][64 heads] fp16, MN-major SW128
+    // P = 2^(s - m) per head, times the row scale, as fp16 [rows][64 heads],
+    // MN-major SW128 (row r at byte 128 r, 16-byte chunks XOR r % 8)
     float t[32];
+    auto write_p = [&](const float(&sv)[32], int k, bool acc) {
+      const float rs = S.row_scale[k];
+      uint8_t *prow = qs + k * 128;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint32_t w[4];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t w[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i0 = c * 8 + 2 * k;
-        const float m0 = S.mfin[hh * 32 + i0], m1 = S.mfin[hh * 32 + i0 + 1];
-        const float p0 = (m0 == -INFINITY) ? 0.0f : exp2f(s[i0] - m0);
-        const float p1 = (m1 == -INFINITY) ? 0.0f : exp2f(s[i0 + 1] - m1);
-        t[i0] = p0;
-        t[i0 + 1] = p1;
-        w[k] = pack_half2(p0 * rs, p1 * rs);
+        for (int q = 0; q < 4; ++q) {
+          const int i0 = c * 8 + 2 * q;
+          const float m0 = S.mfin[hh * 32 + i0], m1 = S.mfin[hh * 32 + i0 + 1];
+          const float p0 = (m0 == -INFINITY) ? 0.0f : exp2f(sv[i0] - m0);
+          const float p1 = (m1 == -INFINITY) ? 0.0f : exp2f(sv[i0 + 1] - m1);
+          t[i0] = acc ? t[i0] + p0 : p0;
+          t[i0 + 1] = acc ? t[i0 + 1] + p1 : p1;
+          w[q] = pack_half2(p0 * rs, p1 * rs);
+        }
+        *reinterpret_cast<uint4 *>(prow + (((hh * 4 + c) ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      *reinterpret_cast<uint4 *>(prow + (((hh * 4 + c) ^ (key & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    };
+    write_p(s, key, false);
+    if (extra) write_p(s2, key2, true);
     warp_transpose_reduce<false>(t, lane);
     __syncthreads();   // every thread has read mfin/red before red is reused
-    S.red[quad][hh * 32 + lane] = t[0];
+    red[quad][hh * 32 + lane] = t[0];
   }
   fence_proxy_async_smem();
   __syncthreads();
-  if (tid < H) S.lfin[tid] = (S.red[0][tid] + S.red[1][tid]) + (S.red[2][tid] + S.red[3][tid]);
+  if (tid < H) S.lfin[tid] = (red[0][tid] + red[1][tid]) + (red[2][tid] + red[3][tid]);
 
   // --------------------------------------------------------------- O = P V
   // P as A, MN-major (heads contiguous): rows 0-63 are the heads, and the
@@ -379,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t ta = smem_u32(tile), pa = smem_u32(qs);
 #pragma unroll
-    for (int kk = 0; kk < ATTN_CHUNK / 16; ++kk) {
+    for (int kk = 0; kk < Lay::kRows / 16; ++kk) {
       const uint64_t ad = smem_desc(pa + kk * 2048, 0, 1024);
 #pragma unroll
       for (int nh = 0; nh < D / (int)kPVN; ++nh) {
@@ -444,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s = (uint32_t)tid;
       const uint32_t g0 = s * kGroups / nct, bytes = ((s + 1) * kGroups / nct - g0) * 128;
       const uint32_t slot = crank < s ? crank : crank - 1;
-      bulk_s2s_cluster(dsmem_addr(&S.ml_in[crank][0][0], s), S.mfin, 2 * H * 4, dsmem_addr(&S.bar_ml, s));
+      bulk_s2s_cluster(dsmem_addr(&MS.ml_in[crank][0][0], s), S.mfin, 2 * H * 4, dsmem_addr(&S.bar_ml, s));
       bulk_s2s_cluster(dsmem_addr(qs + slot * bytes, s), sendb + g0 * 128, bytes, dsmem_addr(&S.bar_merge, s));
     }
     // warps 0-1 wait for the (m, l) records and compute the weights while
@@ -457,8 +543,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kMaxClusterChunks; ++c)
         if (c < (int)nct) {
-          mc[c] = c == (int)crank ? S.mfin[tid] : S.ml_in[c][0][tid];
-          lc[c] = c == (int)crank ? S.lfin[tid] : S.ml_in[c][1][tid];
+          mc[c] = c == (int)crank ? S.mfin[tid] : MS.ml_in[c][0][tid];
+          lc[c] = c == (int)crank ? S.lfin[tid] : MS.ml_in[c][1][tid];
           M = fmaxf(M, mc[c]);
         }
       float L = 0.0f;
@@ -468,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float invL = L > 0.0f ? 1.0f / L : 0.0f;
 #pragma unroll
       for (int c = 0; c < kMaxClusterChunks; ++c)
-        if (c < (int)nct) S.wgt[c][tid] = mc[c] == -INFINITY ? 0.0f : lc[c] * exp2f(mc[c] - M) * invL;
+        if (c < (int)nct) MS.wgt[c][tid] = mc[c] == -INFINITY ? 0.0f : lc[c] * exp2f(mc[c] - M) * invL;
       if (crank == 0 && a.lse)
         a.lse[gp * H + tid] = (L > 0.0f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
     }
@@ -489,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint8_t *src = c == (int)crank ? sendb + off
                                                : qs + (uint32_t)(c < (int)crank ? c : c - 1) * bytes + off - g0 * 128;
           const uint4 v = *reinterpret_cast<const uint4 *>(src);
-          const float w = S.wgt[c][h];
+          const float w = MS.wgt[c][h];
           const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
@@ -574,37 +660,20 @@ size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W) {
   return (b + 255) & ~size_t(255);
 }
 
-cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches) {
-  if (a.problems <= 0) return cudaSuccess;
-  a.n_kchunks = (a.K + ATTN_CHUNK - 1) / ATTN_CHUNK;
-  a.n_chunks = a.n_kchunks + (a.W + ATTN_CHUNK - 1) / ATTN_CHUNK;
-  uint8_t *p = static_cast<uint8_t *>(scratch);
-  a.part_o = reinterpret_cast<float *>(p);
-  size_t off = ((size_t)a.problems * a.n_chunks * H * D * 4 + 255) & ~size_t(255);
-  a.part_ml = reinterpret_cast<float *>(p + off);
-  if (a.n_chunks == 0) {
-    // no key at all: out = 0, lse = -inf
-    cudaError_t e = cudaMemsetAsync(a.out + a.p0 * H * D, 0, (size_t)a.problems * H * D * 4, stream);
-    if (e != cudaSuccess || !a.lse) return e;
-    a.n_chunks = 0;
-    attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
-    ++*launches;
-    return cudaGetLastError();
-  }
-  cudaError_t err = cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
+namespace {
+
+template <int kSwa>
+cudaError_t launch_layout(const AttnArgs &a, const CUtensorMap &tm_q, cudaStream_t stream, int *launches) {
+  constexpr size_t smem = smem_bytes<kSwa>();
+  cudaError_t err =
+      cudaFuncSetAttribute(sparse_attn_kernel<kSwa>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  CUtensorMap tm_q;
-  if (!make_tmap_bf16(&tm_q, a.q, D, (a.p0 + a.problems) * H, H)) return cudaErrorInvalidValue;
-  const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
-  if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-  a.cluster = a.n_chunks <= kMaxClusterChunks ? 1 : 0;
   if (a.cluster) {
-    // one cluster per token: its chunks merge over distributed shared memory
+    // one cluster per token: its chunks merge in shared memory
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)a.n_chunks, (unsigned)a.problems, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -613,17 +682,60 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel, tm_q, a);
-    if (err != cudaSuccess) return err;
-    if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
+    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel<kSwa>, tm_q, a);
     *launches += 1;
-    return cudaSuccess;
+    return err;
   }
-  sparse_attn_kernel<<<dim3(a.n_chunks, a.problems), kThreads, kSmemBytes, stream>>>(tm_q, a);
-  if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
-  attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
-  *launches += 2;
+  sparse_attn_kernel<kSwa><<<dim3(a.n_chunks, a.problems), kThreads, smem, stream>>>(tm_q, a);
+  *launches += 1;
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches) {
+  if (a.problems <= 0) return cudaSuccess;
+  const int n_top = (a.K + ATTN_CHUNK - 1) / ATTN_CHUNK;
+  const int n_split = n_top + (a.W + ATTN_CHUNK - 1) / ATTN_CHUNK;
+  const int n_mixed = max(n_top, (a.W + kMixSwa - 1) / kMixSwa);
+  uint8_t *p = static_cast<uint8_t *>(scratch);
+  a.part_o = reinterpret_cast<float *>(p);
+  size_t off = ((size_t)a.problems * n_split * H * D * 4 + 255) & ~size_t(255);
+  a.part_ml = reinterpret_cast<float *>(p + off);
+  if (n_split == 0) {
+    // no key at all: out = 0, lse = -inf
+    cudaError_t e = cudaMemsetAsync(a.out + a.p0 * H * D, 0, (size_t)a.problems * H * D * 4, stream);
+    if (e != cudaSuccess || !a.lse) return e;
+    a.n_chunks = 0;
+    attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
+    ++*launches;
+    return cudaGetLastError();
+  }
+  // The mixed layout (4 chunks for 512 + 128 keys) when the split layout's
+  // chunks would not fit in one wave of CTAs (one per SM); the split layout
+  // (5 chunks, each less work) otherwise.
+  int dev = 0, sms = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  const bool mixed = a.W > 0 && n_mixed < n_split && n_mixed <= kMaxClusterChunks &&
+                     (int64_t)a.problems * n_split > (int64_t)sms;
+  a.n_chunks = mixed ? n_mixed : n_split;
+  a.n_kchunks = mixed ? n_mixed : n_top;
+  a.cluster = a.n_chunks <= kMaxClusterChunks ? 1 : 0;
+  CUtensorMap tm_q;
+  if (!make_tmap_bf16(&tm_q, a.q, D, (a.p0 + a.problems) * H, H)) return cudaErrorInvalidValue;
+  const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
+  if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
+  err = mixed ? launch_layout<kMixSwa>(a, tm_q, stream, launches) : launch_layout<0>(a, tm_q, stream, launches);
+  if (err != cudaSuccess) return err;
+  if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
+  if (!a.cluster) {
+    attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
+    ++*launches;
+    err = cudaGetLastError();
+  }
+  return err;
 }
 
 }  // namespace csa2

@@ -181,6 +181,40 @@ def test_sparse_attn_reuse(c2, orc, B, K, W, swa_len, n_valid):
         check_lse(lse[b].cpu().numpy(), l)
 
 
+@pytest.mark.parametrize("K,W", [(512, 128), (384, 96)])
+def test_sparse_attn_mixed_layout(c2, orc, K, W):
+    """Enough tokens that the split layout's chunks outnumber the SMs: the
+    kernel takes 128 top-K entries + 32 SWA rows per chunk.  Ragged SWA
+    lengths (0 .. W) and top-K fills, every token checked."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    n_split = -(-K // 128) + -(-W // 128)
+    B = sms // n_split + 1
+    cap = 1024
+    rng = np.random.default_rng(K + W)
+    swa_len = [int(x) for x in rng.integers(0, W + 1, B)]
+    swa_len[0], swa_len[1] = W, 0
+    n_valid = [int(x) for x in rng.integers(0, K + 1, B)]
+    n_valid[0], n_valid[2] = K, 0
+    lat, li, idx, sl = _attn_inputs(97 + K, B, cap, K, W, swa_len, n_valid)
+    p = _params(c2, index_topk=K, sliding_window=W)
+    ws = c2.workspace(c2.OP_ATTN, B, cap, p)
+    kv = _kv_cache(c2, lat)
+    out = torch.empty(B, 64, 512, dtype=torch.float32, device="cuda")
+    lse = torch.empty(B, 64, dtype=torch.float32, device="cuda")
+    swa = li.swa[:, :W].contiguous()
+    sc = li.swa_scale[:, :W].contiguous()
+    c2.sparse_attn(p, li.q.cuda(), kv, idx.cuda(), swa.cuda(), sc.cuda(), sl.cuda(), out, ws, lse=lse)
+    assert c2.get_device_status() == 0
+    kvh = orc.kv_entries(lat.reshape(-1, 512), None, 1, np.tile(np.arange(cap), B)).reshape(B, cap, 288)
+    for b in range(B):
+        o, l = orc.sparse_attn(li.q[b], kvh[b], idx[b].numpy(), swa[b], sc[b], int(sl[b]))
+        if swa_len[b] == 0 and n_valid[b] == 0:
+            assert torch.all(out[b] == 0) and torch.all(torch.isneginf(lse[b]))
+            continue
+        check_attn(out[b].cpu().numpy(), o)
+        check_lse(lse[b].cpu().numpy(), l)
+
+
 def test_sparse_attn_no_keys(c2):
     B, cap, K = 1, 64, 128
     p = _params(c2, index_topk=K, sliding_window=128)
