@@ -104,6 +104,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // K rows are read once: evict them first, so that the scores this
+      // kernel writes stay in L2 for the top-K that reads them next
+      const uint64_t pol = l2_policy_evict_first();
       int prev_b = -1, qi = -1;
       int32_t nv = 0;
       int64_t n_issued = 0;
@@ -130,8 +133,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!kPool) {
           if ((int64_t)t * SWEEP_TILE < nv) {
             mbar_arrive_expect_tx(&S.full[s], kTileBytes);
-            tma_load_2d(dst, &tm_k, 0, (int32_t)(row0 + (int64_t)t * SWEEP_TILE), &S.full[s]);
-            tma_load_2d(dst + kTileBytes / 2, &tm_k, 64, (int32_t)(row0 + (int64_t)t * SWEEP_TILE), &S.full[s]);
+            tma_load_2d_hint(dst, &tm_k, 0, (int32_t)(row0 + (int64_t)t * SWEEP_TILE), &S.full[s], pol);
+            tma_load_2d_hint(dst + kTileBytes / 2, &tm_k, 64, (int32_t)(row0 + (int64_t)t * SWEEP_TILE), &S.full[s],
+                             pol);
           } else {
             mbar_arrive(&S.full[s]);
           }
@@ -151,8 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < SWEEP_TILE / BLOCK; ++j) {
               if (!(valid >> j & 1)) continue;
               const int32_t y = (int32_t)(row0 + (int64_t)__ldg(pb + j) * BLOCK);
-              tma_load_2d(dst + j * 1024, &tm_k, 0, y, &S.full[s]);
-              tma_load_2d(dst + kTileBytes / 2 + j * 1024, &tm_k, 64, y, &S.full[s]);
+              tma_load_2d_hint(dst + j * 1024, &tm_k, 0, y, &S.full[s], pol);
+              tma_load_2d_hint(dst + kTileBytes / 2 + j * 1024, &tm_k, 64, y, &S.full[s], pol);
             }
           } else {
             mbar_arrive(&S.full[s]);

@@ -112,6 +112,24 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int32_t
       : "memory");
 }
 
+// The same with an L2 cache policy (createpolicy below) for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const void *tmap, int32_t x, int32_t y, uint64_t *bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, "
+      "{%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// L2 policy: lines loaded under it are the first to be evicted (data read
+// once, streamed past what should stay resident).
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -5,13 +5,15 @@
 // ("DeepSeek-V4.1-Flash - Architecture", sections 2 and 3).
 //
 // Scores become order-preserving 32-bit keys (-inf marks an invalid slot).
-// The CTAs of the cluster split the row into contiguous slices (float4
-// loads, 32 values in flight per thread).
-//   1. sample: 1/8 of each slice, level-0 histogram of the top 11 key bits;
-//      a low threshold t_low is the bin holding about twice the sample's share
-//      of k;
-//   2. filter: every key >= t_low is compacted into the CTA's candidate list
-//      in shared memory;
+// The CTAs of the cluster split the row into contiguous slices; in a round
+// each warp covers 1024 consecutive values with 8 coalesced float4 loads in
+// flight per thread.
+//   1. sample: the first of every warp's 8 loads (1/8 of the values),
+//      level-0 histogram of the top 11 key bits; a low threshold t_low is the
+//      bin holding about twice the sample's share of k;
+//   2. filter: every key >= t_low goes to the CTA's candidate list in shared
+//      memory, in index order (warp and CTA prefix sums of per-thread counts
+//      give every thread its output slots: no per-key atomics);
 //   3. exact radix select -- 11, 11 and 10 key bits -- on the candidate lists
 //      when together they hold >= k keys and none overflowed, else on the
 //      whole slices; a level stops early when its threshold bin holds exactly
@@ -37,7 +39,7 @@ constexpr int kSelMax = 2048;          // index_topk limit
 constexpr int kVec = 8;                // float4 loads per thread per round (32 values)
 constexpr int kRound = kThreads * kVec * 4;   // values per CTA per round
 constexpr int kCand = 4096;            // per-CTA candidate list
-constexpr int kSampleEvery = 8;        // the sample: one round's worth out of every 8
+constexpr int kSampleEvery = 8;        // the sample: 1 of every warp's 8 loads
 constexpr int kMaxCluster = 16;        // CTAs per row (non-portable cluster size)
 
 struct __align__(16) TopkClusterSmem {
@@ -78,9 +80,9 @@ __device__ __forceinline__ uint32_t level_digit(uint32_t key, int level) {
   return level == 0 ? (key >> 21) : level == 1 ? ((key >> 10) & 2047u) : (key & 1023u);
 }
 
-__device__ __forceinline__ void hist_add(TopkClusterSmem &S, uint32_t bin, int lane) {
+__device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, int lane) {
   const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-  if (bin < kBins && lane == __ffs(peers) - 1) atomicAdd(&S.hist[bin], (uint32_t)__popc(peers));
+  if (bin < kBins && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
 }
 
 // Appends the flagged indices of this warp to the CTA's selection list.
@@ -156,28 +158,62 @@ __device__ void local_threshold(TopkClusterSmem &S, int buf, uint32_t need, int 
   __syncthreads();
 }
 
+// One round of a CTA's slice: warp w covers the 1024 consecutive values
+// base + 1024 w ..; its load j (coalesced) the 128 values from
+// base + 1024 w + 128 j, 4 per lane.  Values past `hi` read as -inf.
+__device__ __forceinline__ int64_t round_index(int64_t base, int j) {
+  return base + (int64_t)(threadIdx.x >> 5) * (32 * 4 * kVec) + j * 128 + (threadIdx.x & 31) * 4;
+}
+
+__device__ __forceinline__ void load_round(const float *vals, int64_t base, int64_t hi, float4 (&v)[kVec]) {
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const int64_t i = round_index(base, j);
+    v[j] = (i < hi) ? __ldcg(reinterpret_cast<const float4 *>(vals + i))
+                    : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+  }
+}
+
 // Calls f(key, index) for the keys of this CTA's slice [lo, hi) (multiples of
-// 4), 32 per thread per round, taking one round of every step_rounds.
+// 4), 32 per thread per round.
 template <typename F>
-__device__ __forceinline__ void for_slice(const float *vals, int64_t lo, int64_t hi, int64_t step_rounds, F &&f) {
-  const int tid = threadIdx.x;
-  for (int64_t base = lo; base < hi; base += (int64_t)kRound * step_rounds) {
+__device__ __forceinline__ void for_slice(const float *vals, int64_t lo, int64_t hi, F &&f) {
+  for (int64_t base = lo; base < hi; base += kRound) {
     float4 v[kVec];
+    load_round(vals, base, hi, v);
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
-      const int64_t i = base + ((int64_t)j * kThreads + tid) * 4;
-      v[j] = (i < hi) ? __ldcg(reinterpret_cast<const float4 *>(vals + i))
-                      : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    }
-#pragma unroll
-    for (int j = 0; j < kVec; ++j) {
-      const int32_t i = (int32_t)(base + ((int64_t)j * kThreads + tid) * 4);
-      f(score_key(v[j].x), i);
-      f(score_key(v[j].y), i + 1);
-      f(score_key(v[j].z), i + 2);
-      f(score_key(v[j].w), i + 3);
+      const int32_t i0 = (int32_t)round_index(base, j);
+      f(score_key(v[j].x), i0);
+      f(score_key(v[j].y), i0 + 1);
+      f(score_key(v[j].z), i0 + 2);
+      f(score_key(v[j].w), i0 + 3);
     }
   }
+}
+
+// Exclusive prefix sum of one value per thread over the CTA; *total gets the
+// sum.  Uses S.scan; ends with the CTA synchronised.
+__device__ __forceinline__ uint32_t block_excl_scan(TopkClusterSmem &S, uint32_t v, uint32_t *total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) S.scan[wid] = incl;
+  __syncthreads();
+  uint32_t before = 0, tot = 0;
+#pragma unroll
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const uint32_t x = S.scan[w];
+    before += w < wid ? x : 0u;
+    tot += x;
+  }
+  __syncthreads();   // S.scan may be reused
+  *total = tot;
+  return before + incl - v;
 }
 
 // Calls f(key, index) for the CTA's candidate list; uniform trip count.
@@ -213,10 +249,10 @@ __device__ uint32_t run_levels(TopkClusterSmem &S, const TopkRows &r, const floa
       // most keys are below the threshold bin: skip the warp unless a lane has work
       if (!__any_sync(0xffffffffu, m && d >= thr)) return;
       append_sel(S, m && (d > thr || (take_thr && d == thr)), idx, lane);
-      if (!last) hist_add(S, (m && d == thr) ? level_digit(key, level + 1) : (uint32_t)kBins, lane);
+      if (!last) hist_add(S.hist, (m && d == thr) ? level_digit(key, level + 1) : (uint32_t)kBins, lane);
     };
     if (kCands) for_cands(S, body);
-    else for_slice(vals, lo, hi, 1, body);
+    else for_slice(vals, lo, hi, body);
     if (last) {
       if (take_thr) {
         need = 0;
@@ -267,38 +303,81 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
   }
   cluster_sync();   // every CTA's totals are cleared before anyone pushes
 
-  // 1. sample: one round of every kSampleEvery
-  for_slice(vals, lo, hi, kSampleEvery,
-            [&](uint32_t key, int32_t) { hist_add(S, key ? (key >> 21) : (uint32_t)kBins, lane); });
+  // 1. sample: load 0 of every warp of every round, 1/8 of the values
+  for (int64_t base = lo; base < hi; base += kRound) {
+    const int64_t i = round_index(base, 0);
+    const float4 v = (i < hi) ? __ldca(reinterpret_cast<const float4 *>(vals + i))
+                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t key = score_key(x[e]);
+      hist_add(S.hist, key ? (key >> 21) : (uint32_t)kBins, lane);
+    }
+  }
   __syncthreads();
   push_hist(S, 0, nctas);
   cluster_sync();
-  {
-    // the sample's share of the row (the same in every CTA: CTA 0's slice)
-    const int64_t slice = 4 * (n4 / nctas) > 0 ? 4 * (n4 / nctas) : 1;
-    const int64_t rounds = (slice + kRound - 1) / kRound;
-    const int64_t sampled = ((rounds + kSampleEvery - 1) / kSampleEvery) * kRound;
-    const double frac = sampled >= slice ? 1.0 : (double)sampled / (double)slice;
-    local_threshold(S, 0, (uint32_t)(2.0 * r.k * frac) + 16, kBins);
-  }
+  // about twice the sample's share of k above the low threshold
+  local_threshold(S, 0, (uint32_t)(2 * r.k / kSampleEvery) + 16, kBins);
   const uint32_t t_low = S.thr < 0 ? 1u : ((uint32_t)S.thr << 21);
 
-  // 2. filter into the candidate list
-  for_slice(vals, lo, hi, 1, [&](uint32_t key, int32_t idx) {
-    const bool f = key >= t_low;
-    const uint32_t m = __ballot_sync(0xffffffffu, f);
-    if (!m) return;
-    uint32_t base = 0;
-    if (lane == 0) base = atomicAdd(&S.ccount, (uint32_t)__popc(m));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    if (f) {
-      const uint32_t pos = base + __popc(m & ((1u << lane) - 1));
-      if (pos < kCand) {
-        S.ckey[pos] = key;
-        S.cidx[pos] = idx;
+  // 2. filter into the candidate list, in index order.  Within a warp the
+  // order is (load j, lane, component): the per-lane counts of the 8 loads
+  // are packed into two words of 8-bit fields (a field sums to at most 128)
+  // and prefix-summed across the warp at once; warps are in index order, and
+  // a CTA prefix sum of the warp totals places them.
+  uint32_t n_cand = 0;
+  for (int64_t base = lo; base < hi; base += kRound) {
+    float4 v[kVec];
+    load_round(vals, base, hi, v);
+    uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const uint32_t c = (score_key(v[j].x) >= t_low) + (score_key(v[j].y) >= t_low) +
+                         (score_key(v[j].z) >= t_low) + (score_key(v[j].w) >= t_low);
+      pk[j >> 2] |= c << (8 * (j & 3));
+    }
+    uint32_t inc[2] = {pk[0], pk[1]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n0 = __shfl_up_sync(0xffffffffu, inc[0], o), n1 = __shfl_up_sync(0xffffffffu, inc[1], o);
+      if (lane >= o) {
+        inc[0] += n0;
+        inc[1] += n1;
       }
     }
-  });
+    const uint32_t tw0 = __shfl_sync(0xffffffffu, inc[0], 31), tw1 = __shfl_sync(0xffffffffu, inc[1], 31);
+    uint32_t wtot = 0, jbase[kVec];   // warp-local start of load j's candidates
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      jbase[j] = wtot;
+      wtot += ((j < 4 ? tw0 : tw1) >> (8 * (j & 3))) & 0xFFu;
+    }
+    uint32_t tot;
+    const uint32_t wbase = n_cand + block_excl_scan(S, lane == 0 ? wtot : 0u, &tot);
+    const uint32_t wb = __shfl_sync(0xffffffffu, wbase, 0);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const uint32_t ex = (((j < 4 ? inc[0] - pk[0] : inc[1] - pk[1]) >> (8 * (j & 3))) & 0xFFu);
+      uint32_t pos = wb + jbase[j] + ex;
+      const int32_t i0 = (int32_t)round_index(base, j);
+      const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t key = score_key(x[e]);
+        if (key >= t_low) {
+          if (pos < kCand) {
+            S.ckey[pos] = key;
+            S.cidx[pos] = i0 + e;
+          }
+          ++pos;
+        }
+      }
+    }
+    n_cand += tot;
+  }
+  if (tid == 0) S.ccount = n_cand;
   __syncthreads();
   if (tid < (int)nctas) dsmem_st_u32(dsmem_addr(&S.cand_cnt[crank], (uint32_t)tid), S.ccount);
   cluster_sync();
@@ -313,10 +392,10 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
   uint32_t need, full = 0;
   const bool fast = !overflow && total_cand >= (uint32_t)r.k;
   if (fast)
-    for_cands(S, [&](uint32_t key, int32_t) { hist_add(S, key ? (key >> 21) : (uint32_t)kBins, lane); });
+    for_cands(S, [&](uint32_t key, int32_t) { hist_add(S.hist, key ? (key >> 21) : (uint32_t)kBins, lane); });
   else
-    for_slice(vals, lo, hi, 1,
-              [&](uint32_t key, int32_t) { hist_add(S, key ? (key >> 21) : (uint32_t)kBins, lane); });
+    for_slice(vals, lo, hi,
+              [&](uint32_t key, int32_t) { hist_add(S.hist, key ? (key >> 21) : (uint32_t)kBins, lane); });
   __syncthreads();
   push_hist(S, 0, nctas);
   cluster_sync();
@@ -325,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
 
   if (need > 0) {
     // ties on the full key: the `need` lowest indices, CTA slices in order
-    for_slice(vals, lo, hi, 1, [&](uint32_t key, int32_t) {
+    for_slice(vals, lo, hi, [&](uint32_t key, int32_t) {
       const uint32_t tm = __ballot_sync(0xffffffffu, key == full);
       if (lane == 0 && tm) atomicAdd(&S.n_tie, (uint32_t)__popc(tm));
     });
