@@ -279,13 +279,14 @@ int32_t csa2_last_launch_count(void);
  * are non-NULL, later calls on this thread record `start` on their stream
  * right before every launch of the chosen kernel and `stop` right after it
  * (kernel 0 = the indexer sweep, 1 = the sparse-attention kernel, 2 = the
- * chunked-prefill indexer).  NULL
+ * chunked-prefill indexer, 3 = the top-K selection).  NULL
  * handles switch the hook off.  Events recorded during stream capture become
  * part of the captured graph. */
 typedef enum {
   CSA2_KERNEL_INDEXER_SWEEP = 0,
   CSA2_KERNEL_SPARSE_ATTN = 1,
-  CSA2_KERNEL_PREFILL_INDEXER = 2
+  CSA2_KERNEL_PREFILL_INDEXER = 2,
+  CSA2_KERNEL_TOPK = 3
 } csa2_kernel;
 csa2_status csa2_set_profile_events(csa2_kernel kernel, void *start, void *stop);
 

@@ -195,7 +195,7 @@ def sparse_decode(mode, params, q, kv, n_vis, n_max, swa, swa_scale, swa_len, to
         ws.numel() * ws.element_size(), _stream(stream)), "csa2_sparse_decode")
 
 
-KERNEL_INDEXER_SWEEP, KERNEL_SPARSE_ATTN, KERNEL_PREFILL_INDEXER = 0, 1, 2
+KERNEL_INDEXER_SWEEP, KERNEL_SPARSE_ATTN, KERNEL_PREFILL_INDEXER, KERNEL_TOPK = 0, 1, 2, 3
 
 
 def set_profile_events(kernel: int, start=None, stop=None):

@@ -12,10 +12,10 @@ namespace csa2 {
 __device__ unsigned int g_dev_error = 0;
 
 namespace {
-thread_local ProfileEvents g_profile[3];
+thread_local ProfileEvents g_profile[4];
 }
 
-ProfileEvents &profile_events(int kernel) { return g_profile[kernel >= 0 && kernel < 3 ? kernel : 0]; }
+ProfileEvents &profile_events(int kernel) { return g_profile[kernel >= 0 && kernel < 4 ? kernel : 0]; }
 
 cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
@@ -261,7 +261,7 @@ int32_t csa2_last_launch_count(void) { return g_last_launches; }
 
 csa2_status csa2_set_profile_events(csa2_kernel kernel, void *start, void *stop) {
   if (kernel != CSA2_KERNEL_INDEXER_SWEEP && kernel != CSA2_KERNEL_SPARSE_ATTN &&
-      kernel != CSA2_KERNEL_PREFILL_INDEXER)
+      kernel != CSA2_KERNEL_PREFILL_INDEXER && kernel != CSA2_KERNEL_TOPK)
     return CSA2_ERR_INVALID_ARG;
   ProfileEvents &pe = profile_events(kernel);
   pe.start = static_cast<cudaEvent_t>(start);

@@ -8,9 +8,10 @@
 // The CTAs of the cluster split the row into contiguous slices; in a round
 // each warp covers 1024 consecutive values with 8 coalesced float4 loads in
 // flight per thread.
-//   1. sample: the first of every warp's 8 loads (1/8 of the values),
-//      level-0 histogram of the top 11 key bits; a low threshold t_low is the
-//      bin holding about twice the sample's share of k;
+//   1. sample: the first of every warp's 8 loads (1/8 of the values); a low
+//      threshold t_low with about twice the sample's share of k above it,
+//      located to 22 key bits by two histogram levels (the top 11 bits, then
+//      the next 11 inside the threshold bin);
 //   2. filter: every key >= t_low goes to the CTA's candidate list in shared
 //      memory, in index order (warp and CTA prefix sums of per-thread counts
 //      give every thread its output slots: no per-key atomics);
@@ -303,24 +304,40 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
   }
   cluster_sync();   // every CTA's totals are cleared before anyone pushes
 
-  // 1. sample: load 0 of every warp of every round, 1/8 of the values
-  for (int64_t base = lo; base < hi; base += kRound) {
-    const int64_t i = round_index(base, 0);
-    const float4 v = (i < hi) ? __ldca(reinterpret_cast<const float4 *>(vals + i))
-                              : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-    const float x[4] = {v.x, v.y, v.z, v.w};
+  // 1. sample: load 0 of every warp of every round, 1/8 of the values; the
+  // histogram of level `lvl` (0: key bits 31..21; 1: bits 20..10 of the keys
+  // whose top bits are b0) goes into tot[lvl] of every CTA
+  auto sample_hist = [&](int lvl, uint32_t b0) {
+    for (int64_t base = lo; base < hi; base += kRound) {
+      const int64_t i = round_index(base, 0);
+      const float4 v = (i < hi) ? __ldca(reinterpret_cast<const float4 *>(vals + i))
+                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      const float x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t key = score_key(x[e]);
-      hist_add(S.hist, key ? (key >> 21) : (uint32_t)kBins, lane);
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t key = score_key(x[e]);
+        const uint32_t bin = !key ? (uint32_t)kBins
+                             : lvl == 0 ? (key >> 21)
+                             : (key >> 21) == b0 ? ((key >> 10) & 2047u) : (uint32_t)kBins;
+        hist_add(S.hist, bin, lane);
+      }
     }
+    __syncthreads();
+    push_hist(S, lvl, nctas);
+    cluster_sync();
+  };
+  // about twice the sample's share of k above the low threshold, located to
+  // 22 key bits: the level-0 bin, then the level-1 bin inside it
+  const uint32_t need_s = (uint32_t)(2 * r.k / kSampleEvery) + 16;
+  sample_hist(0, 0);
+  local_threshold(S, 0, need_s, kBins);
+  uint32_t t_low = 1u;
+  if (S.thr >= 0) {
+    const uint32_t b0 = (uint32_t)S.thr, above0 = S.above;
+    sample_hist(1, b0);
+    local_threshold(S, 1, need_s - above0, kBins);
+    t_low = S.thr < 0 ? (b0 << 21) : ((b0 << 21) | ((uint32_t)S.thr << 10));
   }
-  __syncthreads();
-  push_hist(S, 0, nctas);
-  cluster_sync();
-  // about twice the sample's share of k above the low threshold
-  local_threshold(S, 0, (uint32_t)(2 * r.k / kSampleEvery) + 16, kBins);
-  const uint32_t t_low = S.thr < 0 ? 1u : ((uint32_t)S.thr << 21);
 
   // 2. filter into the candidate list, in index order.  Within a warp the
   // order is (load j, lane, component): the per-lane counts of the 8 loads
@@ -481,9 +498,18 @@ cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *lau
   const size_t smem = sizeof(TopkClusterSmem) + 16;
   cudaError_t err = cudaFuncSetAttribute(topk_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
+  // CTAs per row: one per 8192 scores (a single round each) when there are
+  // few rows -- latency; fewer when the rows alone fill the GPU (3 CTAs fit
+  // on an SM) -- throughput.
+  int dev = 0, sms = 0;
+  err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
   int64_t c = (r.row_len + 8191) / 8192;
-  if (c < 1) c = 1;
   if (c > max_cluster) c = max_cluster;
+  const int64_t fill = 3 * (int64_t)sms / r.rows;
+  if (c > fill) c = fill;
+  if (c < 1) c = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)c, (unsigned)r.rows, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
@@ -496,8 +522,12 @@ cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *lau
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  const ProfileEvents &pe = profile_events(CSA2_KERNEL_TOPK);
+  if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
   err = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, r);
-  if (err == cudaSuccess) ++*launches;
+  if (err != cudaSuccess) return err;
+  ++*launches;
+  if (pe.stop) err = record_profile_event(pe.stop, stream);
   return err;
 }
 

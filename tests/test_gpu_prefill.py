@@ -104,3 +104,12 @@ def test_prefill_first_chunk_of_sequence(c2, orc):
     d = _prefill_case(c2, 402, 1, 0, 1024 + 256)
     _check_all_valid(d)
     _check_tokens(orc, d, [(0, i) for i in (0, 1, 2, 7, 126, 127, 128, 1023, 1024, 1279)])
+
+
+def test_prefill_full_context_block(c2, orc):
+    """A 131,072-token context and one 1,024-token block: the per-block launch
+    configuration of the 2 x 131,072 + 16,384 workload (1,024 top-K rows of
+    ~65.5K entries -- one CTA per row, several rounds per slice)."""
+    d = _prefill_case(c2, 403, 1, 131072, 1024)
+    _check_all_valid(d)
+    _check_tokens(orc, d, [(0, i) for i in (0, 1, 333, 512, 1022, 1023)])
