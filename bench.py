@@ -40,7 +40,6 @@ SWEEP_FIXED = 32 * 128 * 2 + 32 * 4        # q_idx + w per sequence
 # kernel code on that workload (profiles/<kernel>_<workload>.md); absent: null
 TRAFFIC = {
     ("indexer_sweep_kernel", "group_decode_32x64k"): 537180160 + 6373888,
-    ("topk_cluster_kernel", "group_decode_32x64k"): 8462848,
     ("sparse_attn_kernel", "group_decode_32x64k"): 10633984,
 }
 REINDEX_BYTES = 16384 * 256 + 18560         # per (seq, layer)
@@ -55,6 +54,22 @@ def peaks():
         return {"hbm": (float(d["hbm_gbs"]), "measured"),
                 "bf16_sustained": (float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured sustained")}
     return {"hbm": (6800.0, "fallback"), "bf16_sustained": (1700.0, "fallback sustained")}
+
+
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over the ranks of the process
+    group (the slowest rank's time); the values themselves with one rank."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_rate(world, units_per_rank, ms_per_step):
+    """Units of every rank per second of the (max-over-ranks) step time."""
+    return world * units_per_rank / (ms_per_step / 1e3)
 
 
 def roof_entry(kernel, workload, bound, work, launch_ms, count, peaks_):
@@ -479,6 +494,7 @@ def run_ours(args, rank, world, local_rank):
         stream.synchronize()
         per = probe_ms / 3 + fl0.elapsed_time(fl1)
         args.steps = int(min(5000, max(20, math.ceil(1500.0 / per))))
+        args.steps = int(max_over_ranks([args.steps], dev)[0])   # every rank times the same count
 
     if world > 1:
         torch.distributed.barrier()
@@ -487,11 +503,7 @@ def run_ours(args, rank, world, local_rank):
             os.path.join(ROOT, "gpurun_out")) else f"/tmp/csa2_clocks_r{rank}.csv") as clk:
         total_ms, live_ms = timed(args.steps, g, live)
     torch.cuda.synchronize()
-    t = torch.tensor([total_ms], device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.barrier()
-    total_ms = float(t.item())
+    total_ms = max_over_ranks([total_ms], dev)[0]
 
     # end to end: every step's inputs copied from pinned host memory and its
     # outputs read back, inside the timed region (overlapped per layer)
@@ -507,12 +519,15 @@ def run_ours(args, rank, world, local_rank):
             g_io.replay()
     stream.synchronize()
     e2e_steps = max(3, min(args.steps, 20))
+    if world > 1:
+        torch.distributed.barrier()
     e2e_ms, _ = timed(e2e_steps, g_io)
+    e2e_ms = max_over_ranks([e2e_ms], dev)[0]
     h2d, d2h = io.h2d, io.d2h
     assert c2.get_device_status(stream) == 0
 
     ms = total_ms / args.steps
-    tokens_per_s = world * wl.tokens() / (ms / 1e3)
+    tokens_per_s = whole_job_rate(world, wl.tokens(), ms)
     # the dominant kernel (largest estimated share of the step), its launch
     # time measured live over the timed region; every profiled kernel from
     # the profiling replays
@@ -532,7 +547,7 @@ def run_ours(args, rank, world, local_rank):
         "config": conf,
         "roofline": roof,
         "roofline_kernels": roofs,
-        "e2e": {"value": round(world * wl.tokens() / (e2e_ms / e2e_steps / 1e3), 1), "unit": "tokens/s",
+        "e2e": {"value": round(whole_job_rate(world, wl.tokens(), e2e_ms / e2e_steps), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(local_rank),
@@ -669,6 +684,8 @@ def run_reference(args, rank, world):
     cfg = synth.CONFIGS[args.config]
     per_step = []
     base = cpu_baseline_prefill if cfg.chunk else cpu_baseline
+    if args.steps <= 0:
+        args.steps = 3
     for _ in range(args.steps):
         r = base(args, cfg, seconds=max(1.0, args.cpu_seconds / max(1, args.steps)))
         per_step.append(r)
