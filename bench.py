@@ -97,6 +97,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--attn-kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="readout kernel: 0 automatic, 1 chunk-parallel, 2 streaming")
     return ap.parse_args()
 
 
@@ -175,7 +177,7 @@ class Workload:
         B, N = cfg.batch, cfg.n_ctx
         self.B, self.N = B, N
         self.hsi = 1 if cfg.hsi else 0
-        self.params = c2.Params.make(hsi=self.hsi)
+        self.params = c2.Params.make(hsi=self.hsi, attn_kernel=ATTN_KERNEL)
         seed = cfg.layer_seeds[0]
         # context: latents -> FP4 main KV with this library's writer; indexer K bf16
         self.kv = torch.empty(B, N, 288, dtype=torch.uint8, device=device)
@@ -307,7 +309,7 @@ class PrefillWorkload:
         self.first_pos = cfg.n_ctx
         E_ctx, E_new = cfg.n_ctx // m, T // m
         self.E = E_ctx + E_new
-        self.params = c2.Params.make()
+        self.params = c2.Params.make(attn_kernel=ATTN_KERNEL)
         seed = cfg.layer_seeds[0]
         self.kv = torch.empty(B, self.E, 288, dtype=torch.uint8, device=device)
         for b in range(B):   # context entries (setup)
@@ -401,7 +403,12 @@ class PrefillWorkload:
                 [[self.out, self.lse, self.topk]])
 
 
+ATTN_KERNEL = 0   # csa2_params.attn_kernel of the workloads (--attn-kernel)
+
+
 def run_ours(args, rank, world, local_rank):
+    global ATTN_KERNEL
+    ATTN_KERNEL = args.attn_kernel
     import torch
 
     import synth

@@ -70,6 +70,10 @@ typedef struct {
   int32_t candidate_topk_blocks; /* HSI pool blocks, 16..8192, multiple of 16; 2048 */
   int32_t block_reduce;          /* 0 = max over the block (pages), 1 = sum      */
   int32_t hsi;                   /* FULL: also build the candidate pool (1/0)    */
+  int32_t attn_kernel;           /* readout kernel: 0 automatic, 1 chunk-parallel
+                                    (a token's chunks on a cluster of CTAs),
+                                    2 streaming (a CTA pipelines a token's chunks);
+                                    the result is the same up to rounding      */
 } csa2_params;
 
 /* Defaults of the pages: K=512, W=128, blocks of 8, 2048 blocks, max, hsi=1. */

@@ -34,15 +34,17 @@ class Csa2Error(RuntimeError):
 
 class Params(ctypes.Structure):
     """csa2_params: index_topk, sliding_window, candidate_block_size,
-    candidate_topk_blocks, block_reduce (0 max, 1 sum), hsi."""
+    candidate_topk_blocks, block_reduce (0 max, 1 sum), hsi, attn_kernel (0
+    automatic, 1 chunk-parallel, 2 streaming)."""
     _fields_ = [("index_topk", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
                 ("candidate_block_size", ctypes.c_int32), ("candidate_topk_blocks", ctypes.c_int32),
-                ("block_reduce", ctypes.c_int32), ("hsi", ctypes.c_int32)]
+                ("block_reduce", ctypes.c_int32), ("hsi", ctypes.c_int32), ("attn_kernel", ctypes.c_int32)]
 
     @classmethod
     def make(cls, index_topk=512, sliding_window=128, candidate_block_size=8, candidate_topk_blocks=2048,
-             block_reduce=0, hsi=1):
-        return cls(index_topk, sliding_window, candidate_block_size, candidate_topk_blocks, block_reduce, hsi)
+             block_reduce=0, hsi=1, attn_kernel=0):
+        return cls(index_topk, sliding_window, candidate_block_size, candidate_topk_blocks, block_reduce, hsi,
+                   attn_kernel)
 
 
 _lib = None

@@ -80,7 +80,8 @@ bool params_ok(const csa2_params *p) {
   return p && p->index_topk >= 1 && p->index_topk <= 2048 && p->sliding_window >= 0 &&
          p->sliding_window <= 1024 && p->candidate_block_size == BLOCK && p->candidate_topk_blocks >= 16 &&
          p->candidate_topk_blocks <= TOPK_MAX_K && p->candidate_topk_blocks % 16 == 0 &&
-         (p->block_reduce == 0 || p->block_reduce == 1) && (p->hsi == 0 || p->hsi == 1);
+         (p->block_reduce == 0 || p->block_reduce == 1) && (p->hsi == 0 || p->hsi == 1) &&
+         p->attn_kernel >= 0 && p->attn_kernel <= 2;
 }
 
 // ------------------------------------------------------------ workspace
@@ -234,6 +235,7 @@ csa2_status run_attn(const csa2_params *p, int32_t batch, const void *q, const u
   a.p0 = 0;
   a.tokens = 1;
   a.causal_swa = 0;
+  a.kernel = p->attn_kernel;
   return cuda_status(launch_sparse_attn(a, ws, stream, launches));
 }
 
@@ -252,6 +254,7 @@ csa2_params csa2_default_params(void) {
   p.candidate_topk_blocks = 2048;
   p.block_reduce = 0;
   p.hsi = 1;
+  p.attn_kernel = 0;
   return p;
 }
 
@@ -489,6 +492,7 @@ extern "C" csa2_status csa2_prefill_chunk(const csa2_params *params, int32_t bat
     a.problems = (int32_t)nq;
     a.K = p->index_topk;
     a.W = W;
+    a.kernel = p->attn_kernel;
     a.p0 = q0;
     a.tokens = n_tokens;
     a.causal_swa = 1;

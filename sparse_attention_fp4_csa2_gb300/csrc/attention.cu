@@ -287,7 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; k < 8; ++k) codes[k] = make_uint4(0, 0, 0, 0);
       scl = make_uint4(0, 0, 0, 0);
     }
-    __syncthreads();   // the staging area is read; the tile may now be written over it
+    // mixed: the 32 SWA rows -- thread (r, j) takes dims 64j..64j+63 of row r
+    // from its staging piece (column r / 8, slot r % 8); read now, so that
+    // one barrier covers both staging areas
+    const int sr = tid >> 3, sj = tid & 7;
+    uint4 sraw[4];
+    if (kMixed) {
+      const bool sv = sr < swa_rows && ok;
+      const uint4 *ssrc =
+          reinterpret_cast<const uint4 *>(tile + (sr >> 3) * kAtomCol + ATTN_CHUNK * 128 + (sr & 7) * D + sj * 64);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sraw[k] = sv ? ssrc[k] : make_uint4(0, 0, 0, 0);
+    }
+    __syncthreads();   // the staging areas are read; the tile may now be written over them
     const uint32_t sw[4] = {scl.x, scl.y, scl.z, scl.w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -310,6 +322,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16 + 1, kAtomCol)) = o1;
       }
     }
+    if (kMixed) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t w[4] = {sraw[k].x, sraw[k].y, sraw[k].z, sraw[k].w};
+        uint4 o0, o1;
+        o0.x = e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)); o0.y = e4m3x2_to_half2((uint16_t)(w[0] >> 16));
+        o0.z = e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)); o0.w = e4m3x2_to_half2((uint16_t)(w[1] >> 16));
+        o1.x = e4m3x2_to_half2((uint16_t)(w[2] & 0xFFFF)); o1.y = e4m3x2_to_half2((uint16_t)(w[2] >> 16));
+        o1.z = e4m3x2_to_half2((uint16_t)(w[3] & 0xFFFF)); o1.w = e4m3x2_to_half2((uint16_t)(w[3] >> 16));
+        const int ch16 = sj * 8 + k * 2;
+        *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + sr, ch16, kAtomCol)) = o0;
+        *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + sr, ch16 + 1, kAtomCol)) = o1;
+      }
+    }
   } else {
     // SWA rows (E4M3) staged in the tile's upper half: through registers, then
     // converted to fp16 (exact) into the tile
@@ -330,30 +356,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ch16 = half * 32 + k * 2;
       *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16, kAtomCol)) = o0;
       *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16 + 1, kAtomCol)) = o1;
-    }
-  }
-  if (kMixed) {
-    // the 32 SWA rows: thread (r, j) converts dims 64j..64j+63 of row r from
-    // its staging piece (column r / 8, slot r % 8) into tile row 128 + r
-    const int r = tid >> 3, j = tid & 7;
-    const bool valid = r < swa_rows && ok;
-    const uint4 *src =
-        reinterpret_cast<const uint4 *>(tile + (r >> 3) * kAtomCol + ATTN_CHUNK * 128 + (r & 7) * D + j * 64);
-    uint4 raw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) raw[k] = valid ? src[k] : make_uint4(0, 0, 0, 0);
-    __syncthreads();   // every staging piece is read before any SWA row is written
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-      uint4 o0, o1;
-      o0.x = e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)); o0.y = e4m3x2_to_half2((uint16_t)(w[0] >> 16));
-      o0.z = e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)); o0.w = e4m3x2_to_half2((uint16_t)(w[1] >> 16));
-      o1.x = e4m3x2_to_half2((uint16_t)(w[2] & 0xFFFF)); o1.y = e4m3x2_to_half2((uint16_t)(w[2] >> 16));
-      o1.z = e4m3x2_to_half2((uint16_t)(w[3] & 0xFFFF)); o1.w = e4m3x2_to_half2((uint16_t)(w[3] >> 16));
-      const int ch16 = j * 8 + k * 2;
-      *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + r, ch16, kAtomCol)) = o0;
-      *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + r, ch16 + 1, kAtomCol)) = o1;
     }
   }
   fence_proxy_async_smem();
@@ -711,13 +713,23 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
     ++*launches;
     return cudaGetLastError();
   }
-  // The mixed layout (4 chunks for 512 + 128 keys) when the split layout's
-  // chunks would not fit in one wave of CTAs (one per SM); the split layout
-  // (5 chunks, each less work) otherwise.
   int dev = 0, sms = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (err != cudaSuccess) return err;
+  // Streaming (a CTA pipelines whole tokens) once the tokens alone fill the
+  // SMs -- it keeps every SM's tensor cores busy without a merge; below that,
+  // chunk-parallel (a token's chunks on a cluster of CTAs) for latency.
+  if (a.kernel == 2 || (a.kernel == 0 && a.problems >= sms)) {
+    const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
+    if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
+    err = launch_sparse_attn_stream(a, sms, stream, launches);
+    if (err == cudaSuccess && pe.stop) err = record_profile_event(pe.stop, stream);
+    return err;
+  }
+  // The mixed layout (4 chunks for 512 + 128 keys) when the split layout's
+  // chunks would not fit in one wave of CTAs (one per SM); the split layout
+  // (5 chunks, each less work) otherwise.
   const bool mixed = a.W > 0 && n_mixed < n_split && n_mixed <= kMaxClusterChunks &&
                      (int64_t)a.problems * n_split > (int64_t)sms;
   a.n_chunks = mixed ? n_mixed : n_split;

@@ -146,9 +146,11 @@ struct AttnArgs {
   int64_t first_pos;
   int64_t swa_first_pos;
   int64_t swa_seq_rows;
+  int32_t kernel;             // 0 automatic, 1 chunk-parallel, 2 streaming
 };
 
 size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W);
 cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches);
+cudaError_t launch_sparse_attn_stream(const AttnArgs &a, int num_sms, cudaStream_t stream, int *launches);
 
 }  // namespace csa2

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(c2):
 def test_defaults_and_sizes(c2):
     p = c2.default_params()
     assert (p.index_topk, p.sliding_window, p.candidate_block_size, p.candidate_topk_blocks, p.block_reduce,
-            p.hsi) == (512, 128, 8, 2048, 0, 1)
+            p.hsi, p.attn_kernel) == (512, 128, 8, 2048, 0, 1, 0)
     assert c2.entry_bytes() == 288
     assert c2.lib().csa2_status_string(3) == b"workspace too small"
 
@@ -50,6 +50,8 @@ def test_workspace_sizes(c2):
     assert d >= c2.workspace_bytes(c2.OP_ATTN, 4, 1 << 20, p)
     bad = c2.Params.make(candidate_block_size=16)
     assert c2.workspace_bytes(c2.OP_DECODE, 4, 1000, bad) == 0
+    assert c2.workspace_bytes(c2.OP_ATTN, 4, 1000, c2.Params.make(attn_kernel=3)) == 0
+    assert c2.workspace_bytes(c2.OP_ATTN, 4, 1000, c2.Params.make(attn_kernel=2)) > 0
     assert c2.workspace_bytes(c2.OP_DECODE, 0, 1000, p) == 0
 
 

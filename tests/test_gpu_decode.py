@@ -162,10 +162,11 @@ def _kv_cache(c2, lat):
     (1, 256, 200, [200], [256]),               # two SWA chunks
     (2, 1024, 128, [128, 5], [1024, 700]),     # 9 chunks: merged by the separate combine kernel
 ])
-def test_sparse_attn_reuse(c2, orc, B, K, W, swa_len, n_valid):
+@pytest.mark.parametrize("ak", [1, 2])            # chunk-parallel, streaming
+def test_sparse_attn_reuse(c2, orc, B, K, W, swa_len, n_valid, ak):
     cap = 3000
     lat, li, idx, sl = _attn_inputs(41 + K, B, cap, K, W, swa_len, n_valid)
-    p = _params(c2, index_topk=K, sliding_window=W)
+    p = _params(c2, index_topk=K, sliding_window=W, attn_kernel=ak)
     ws = c2.workspace(c2.OP_ATTN, B, cap, p)
     kv = _kv_cache(c2, lat)
     out = torch.empty(B, 64, 512, dtype=torch.float32, device="cuda")
@@ -181,8 +182,8 @@ def test_sparse_attn_reuse(c2, orc, B, K, W, swa_len, n_valid):
         check_lse(lse[b].cpu().numpy(), l)
 
 
-@pytest.mark.parametrize("K,W", [(512, 128), (384, 96)])
-def test_sparse_attn_mixed_layout(c2, orc, K, W):
+@pytest.mark.parametrize("K,W,ak", [(512, 128, 0), (384, 96, 0), (512, 128, 2)])
+def test_sparse_attn_mixed_layout(c2, orc, K, W, ak):
     """Enough tokens that the split layout's chunks outnumber the SMs: the
     kernel takes 128 top-K entries + 32 SWA rows per chunk.  Ragged SWA
     lengths (0 .. W) and top-K fills, every token checked."""
@@ -196,7 +197,7 @@ def test_sparse_attn_mixed_layout(c2, orc, K, W):
     n_valid = [int(x) for x in rng.integers(0, K + 1, B)]
     n_valid[0], n_valid[2] = K, 0
     lat, li, idx, sl = _attn_inputs(97 + K, B, cap, K, W, swa_len, n_valid)
-    p = _params(c2, index_topk=K, sliding_window=W)
+    p = _params(c2, index_topk=K, sliding_window=W, attn_kernel=ak)
     ws = c2.workspace(c2.OP_ATTN, B, cap, p)
     kv = _kv_cache(c2, lat)
     out = torch.empty(B, 64, 512, dtype=torch.float32, device="cuda")
@@ -215,9 +216,10 @@ def test_sparse_attn_mixed_layout(c2, orc, K, W):
         check_lse(lse[b].cpu().numpy(), l)
 
 
-def test_sparse_attn_no_keys(c2):
+@pytest.mark.parametrize("ak", [1, 2])
+def test_sparse_attn_no_keys(c2, ak):
     B, cap, K = 1, 64, 128
-    p = _params(c2, index_topk=K, sliding_window=128)
+    p = _params(c2, index_topk=K, sliding_window=128, attn_kernel=ak)
     ws = c2.workspace(c2.OP_ATTN, B, cap, p)
     kv = torch.zeros(B, cap, 288, dtype=torch.uint8, device="cuda")
     idx = torch.full((B, K), -1, dtype=torch.int32, device="cuda")
