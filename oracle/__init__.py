@@ -63,6 +63,10 @@ def lib():
         L.csa2o_kv_entry.argtypes, L.csa2o_kv_entry.restype = [P, P, i32, i64, f64, P], None
         L.csa2o_kv_entries.argtypes, L.csa2o_kv_entries.restype = [P, P, i32, i64, P, f64, P], None
         L.csa2o_index_scores.argtypes, L.csa2o_index_scores.restype = [P, P, P, i64, P], None
+        L.csa2o_mxfp4_quantise.argtypes, L.csa2o_mxfp4_quantise.restype = [P, P, P], None
+        L.csa2o_mxfp4_quantise_rows.argtypes, L.csa2o_mxfp4_quantise_rows.restype = [P, i64, P, P], None
+        L.csa2o_mxfp4_dequant.argtypes, L.csa2o_mxfp4_dequant.restype = [P, P, P], None
+        L.csa2o_index_scores_mxfp4.argtypes, L.csa2o_index_scores_mxfp4.restype = [P, P, P, P, i64, P], None
         L.csa2o_topk.argtypes, L.csa2o_topk.restype = [P, P, i64, i64, P], i64
         L.csa2o_block_scores.argtypes, L.csa2o_block_scores.restype = [P, i64, i32, i32, P], None
         L.csa2o_hsi_pool.argtypes, L.csa2o_hsi_pool.restype = [P, i64, i32, i64, i32, P], i64
@@ -161,6 +165,49 @@ def index_scores(q_idx, w, k_rows) -> np.ndarray:
     kk = _u16(k_rows).reshape(-1, DI)
     s = np.empty(kk.shape[0], np.float64)
     lib().csa2o_index_scores(_p(q), _p(ww), _p(kk), int(kk.shape[0]), _p(s))
+    return s
+
+
+# ------------------------------------------------------------------ MXFP4
+def mxfp4_quantise(x):
+    """Rows [n, 128] (bf16 tensor or float array) -> (codes uint8 [n, 64],
+    scales uint8 [n, 4]) by the OCP MX rule (see csa2o_mxfp4_quantise)."""
+    if hasattr(x, "dtype") and "bfloat16" in str(x.dtype):
+        xx = _u16(x).reshape(-1, DI)
+        n = xx.shape[0]
+        codes = np.empty((n, DI // 2), np.uint8)
+        scales = np.empty((n, DI // 32), np.uint8)
+        lib().csa2o_mxfp4_quantise_rows(_p(xx), int(n), _p(codes), _p(scales))
+        return codes, scales
+    xf = _np(x, np.float32).reshape(-1, DI)
+    n = xf.shape[0]
+    codes = np.empty((n, DI // 2), np.uint8)
+    scales = np.empty((n, DI // 32), np.uint8)
+    for r in range(n):
+        row = np.ascontiguousarray(xf[r])
+        lib().csa2o_mxfp4_quantise(_p(row), _p(codes[r]), _p(scales[r]))
+    return codes, scales
+
+
+def mxfp4_dequant(codes, scales) -> np.ndarray:
+    """codes [n, 64], scales [n, 4] -> fp64 [n, 128]."""
+    cc = _np(codes, np.uint8).reshape(-1, DI // 2)
+    ss = _np(scales, np.uint8).reshape(-1, DI // 32)
+    out = np.empty((cc.shape[0], DI), np.float64)
+    for r in range(cc.shape[0]):
+        lib().csa2o_mxfp4_dequant(_p(np.ascontiguousarray(cc[r])), _p(np.ascontiguousarray(ss[r])), _p(out[r]))
+    return out
+
+
+def index_scores_mxfp4(q_idx, w, k_codes, k_scales) -> np.ndarray:
+    """q_idx bf16 [32,128] (quantised to MXFP4 inside), w fp32 [32], MXFP4 keys
+    (codes [n,64], scales [n,4]) -> fp64 [n]."""
+    q = _u16(q_idx).reshape(HI * DI)
+    ww = _np(w, np.float32).reshape(HI)
+    cc = _np(k_codes, np.uint8).reshape(-1, DI // 2)
+    ss = _np(k_scales, np.uint8).reshape(-1, DI // 32)
+    s = np.empty(cc.shape[0], np.float64)
+    lib().csa2o_index_scores_mxfp4(_p(q), _p(ww), _p(cc), _p(ss), int(cc.shape[0]), _p(s))
     return s
 
 

@@ -235,6 +235,82 @@ void csa2o_index_scores(const uint16_t *q, const float *w, const uint16_t *k, in
     }
 }
 
+/* --------------------------------------------------- MXFP4 indexer cache */
+
+/* MXFP4 (OCP Microscaling v1.0): a block of 32 elements shares one UE8M0
+ * scale 2^E; elements are E2M1.  The indexer Q and K are FP4 ([A] 2.4.4: QAT
+ * "for the FP4 Indexer Q and K"; [A] 3.1: a 128-dimensional MXFP4 indexer-K
+ * entry is 68 B = 64 B of codes + 4 scale bytes).
+ * READING (the OCP conversion rule): E = floor(log2(max |x|)) - 2 (2 = the
+ * largest E2M1 exponent), clamped to [-127, 127]; an all-zero block takes
+ * E = -127; code_i = E2M1_RNE_satfinite(x_i / 2^E) (the quotient is exact).
+ * Scale byte = E + 127.  READING (layout): element 2j in the low nibble of
+ * code byte j; the 4 scale bytes cover dims 0-31, 32-63, 64-95, 96-127. */
+void csa2o_mxfp4_quantise(const float *x, uint8_t *codes, uint8_t *scales) {
+    for (int b = 0; b < O_DI / 32; ++b) {
+        double amax = 0.0;
+        for (int i = 0; i < 32; ++i) {
+            double a = fabs((double)x[b * 32 + i]);
+            if (a > amax) amax = a;
+        }
+        int E = -127;
+        if (amax > 0.0) {
+            int e;
+            frexp(amax, &e);          /* amax = f 2^e, f in [0.5, 1): floor(log2 amax) = e - 1 */
+            E = e - 1 - 2;
+            if (E < -127) E = -127;
+            if (E > 127) E = 127;
+        }
+        scales[b] = (uint8_t)(E + 127);
+        for (int i = 0; i < 32; i += 2) {
+            uint8_t lo = csa2o_e2m1_encode((float)ldexp((double)x[b * 32 + i], -E));
+            uint8_t hi = csa2o_e2m1_encode((float)ldexp((double)x[b * 32 + i + 1], -E));
+            codes[(b * 32 + i) / 2] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+/* Rows of bf16 -> MXFP4 (codes [n][64], scales [n][4]). */
+void csa2o_mxfp4_quantise_rows(const uint16_t *x, int64_t n, uint8_t *codes, uint8_t *scales) {
+    for (int64_t r = 0; r < n; ++r) {
+        float xf[O_DI];
+        for (int d = 0; d < O_DI; ++d) xf[d] = bf16_to_f32(x[r * O_DI + d]);
+        csa2o_mxfp4_quantise(xf, codes + r * (O_DI / 2), scales + r * (O_DI / 32));
+    }
+}
+
+/* code x 2^E, exact in double */
+void csa2o_mxfp4_dequant(const uint8_t *codes, const uint8_t *scales, double *out) {
+    for (int d = 0; d < O_DI; ++d) {
+        uint8_t c = (uint8_t)((codes[d / 2] >> (4 * (d & 1))) & 15);
+        out[d] = ldexp(csa2o_e2m1_decode(c), (int)scales[d / 32] - 127);
+    }
+}
+
+/* The indexer score with FP4 operands: the query rows (bf16) are quantised
+ * to MXFP4 like the keys; s_n = sum_h w_h ReLU(dq(q_h) . dq(k_n)) in fp64. */
+void csa2o_index_scores_mxfp4(const uint16_t *q, const float *w, const uint8_t *k_codes,
+                              const uint8_t *k_scales, int64_t n, double *s) {
+    double qd[O_HI * O_DI];
+    for (int h = 0; h < O_HI; ++h) {
+        uint8_t qc[O_DI / 2], qs[O_DI / 32];
+        csa2o_mxfp4_quantise_rows(q + h * O_DI, 1, qc, qs);
+        csa2o_mxfp4_dequant(qc, qs, qd + h * O_DI);
+    }
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < n; ++r) {
+        double kd[O_DI];
+        csa2o_mxfp4_dequant(k_codes + r * (O_DI / 2), k_scales + r * (O_DI / 32), kd);
+        double acc = 0.0;
+        for (int h = 0; h < O_HI; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < O_DI; ++d) dot += qd[h * O_DI + d] * kd[d];
+            acc += (double)w[h] * (dot > 0.0 ? dot : 0.0);
+        }
+        s[r] = acc;
+    }
+}
+
 /* ---------------------------------------------------------------- top-K */
 
 typedef struct { double s; int64_t i; } scored;
