@@ -43,6 +43,7 @@ TRAFFIC = {
     ("sparse_attn_kernel", "group_decode_32x64k"): 10633984,
 }
 REINDEX_BYTES = 16384 * 256 + 18560         # per (seq, layer)
+K_BYTES = {False: 256, True: 68}            # indexer-K bytes per position: bf16, MXFP4 (codes + scales)
 KVW_BYTES = 1024 + 288 + 16                 # new entry per sequence
 
 
@@ -99,18 +100,20 @@ def parse():
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--attn-kernel", type=int, default=0, choices=[0, 1, 2],
                     help="readout kernel: 0 automatic, 1 chunk-parallel, 2 streaming")
+    ap.add_argument("--indexer-fp4", action="store_true",
+                    help="MXFP4 indexer K cache and query (decode workloads)")
     return ap.parse_args()
 
 
-def algorithmic_bytes(cfg, hsi):
-    B, N = cfg.batch, cfg.n_ctx
-    total = B * KVW_BYTES
+def algorithmic_bytes(cfg, hsi, fp4=False):
+    B, N, kb = cfg.batch, cfg.n_ctx, K_BYTES[fp4]
+    total = B * KVW_BYTES + (B * (256 + 68) if fp4 else 0)    # + the new indexer-K entry
     for m in cfg.schedule:
         total += B * ATTN_BYTES
         if m == "full":
-            total += B * (256 * N + SWEEP_FIXED + 512 * 4)
+            total += B * (kb * N + SWEEP_FIXED + 512 * 4)
         elif m == "reindex":
-            total += B * REINDEX_BYTES
+            total += B * (REINDEX_BYTES - 16384 * (256 - kb))
     return total
 
 
@@ -177,7 +180,8 @@ class Workload:
         B, N = cfg.batch, cfg.n_ctx
         self.B, self.N = B, N
         self.hsi = 1 if cfg.hsi else 0
-        self.params = c2.Params.make(hsi=self.hsi, attn_kernel=ATTN_KERNEL)
+        self.fp4 = INDEXER_FP4
+        self.params = c2.Params.make(hsi=self.hsi, attn_kernel=ATTN_KERNEL, indexer_fp4=int(self.fp4))
         seed = cfg.layer_seeds[0]
         # context: latents -> FP4 main KV with this library's writer; indexer K bf16
         self.kv = torch.empty(B, N, 288, dtype=torch.uint8, device=device)
@@ -193,6 +197,14 @@ class Workload:
         if cfg.planted_blocks:
             li0 = synth.layer_inputs(cfg.layer_seeds[0], B, device=device)
             synth.plant_blocks(self.k_idx, li0.q_idx, li0.w, N, cfg.planted_blocks, seed)
+        if self.fp4:
+            # the same keys through this library's MXFP4 writer; every step
+            # also writes the new token's entry
+            self.k_fp4 = c2.indexer_k_fp4_cache(B * N, device=device)
+            c2.indexer_k_quant(self.k_idx.view(B * N, 128), torch.arange(B * N, device=device), self.k_fp4)
+            self.k_idx = self.k_fp4
+            self.new_k = synth.normal((B, 128), seed + 11, 0, device)
+            self.PROFILED = ((0, "indexer_sweep_fp4_kernel"), (3, "topk_cluster_kernel"), (1, "sparse_attn_kernel"))
         self.layers = [synth.layer_inputs(s, B, device=device) for s in cfg.layer_seeds]
         self.new_latent = synth.normal((B, 512), seed + 7, 0, device)
         self.new_pos = torch.full((B,), N - 1, dtype=torch.int64, device=device)
@@ -220,9 +232,10 @@ class Workload:
         sch, B, N, wl = self.cfg.schedule, self.B, self.N, self.cfg.name
         n_full = sum(m == "full" for m in sch)
         out = []
-        if launch_ms.get("indexer_sweep_kernel") and n_full:
-            out.append(roof_entry("indexer_sweep_kernel", wl, "hbm", B * (256 * N + SWEEP_FIXED),
-                                  launch_ms["indexer_sweep_kernel"], n_full, peaks_))
+        sweep = self.PROFILED[0][1]
+        if launch_ms.get(sweep) and n_full:
+            out.append(roof_entry(sweep, wl, "hbm", B * (K_BYTES[self.fp4] * N + SWEEP_FIXED),
+                                  launch_ms[sweep], n_full, peaks_))
         if launch_ms.get("topk_cluster_kernel") and n_full:
             out.append(roof_entry("topk_cluster_kernel", wl, "hbm", B * (4 * N + 4 * 512),
                                   launch_ms["topk_cluster_kernel"], n_full, peaks_))
@@ -232,9 +245,10 @@ class Workload:
         return out
 
     def config(self, ms):
-        step_bytes = algorithmic_bytes(self.cfg, self.hsi)
+        step_bytes = algorithmic_bytes(self.cfg, self.hsi, self.fp4)
+        ik = "MXFP4 indexer K and Q" if self.fp4 else "bf16 indexer K"
         return {"workload": self.cfg.name, "batch": self.B, "context": self.N, "layers": "+".join(self.cfg.schedule),
-                "hsi": bool(self.hsi), "storage": "FP4 E2M1+E4M3/16 main KV, bf16 indexer K, E4M3 SWA",
+                "hsi": bool(self.hsi), "storage": f"FP4 E2M1+E4M3/16 main KV, {ik}, E4M3 SWA",
                 "step_alg_bytes": step_bytes, "step_hbm_gbs": round(step_bytes / (ms / 1e3) / 1e9, 1)}
 
     def step(self, prof=None, io=None):
@@ -251,6 +265,9 @@ class Workload:
             io.wait_in(0)
         c2.kv_quant_write(self.new_latent, None, 1, self.new_pos, self.new_slot, self.kv.view(-1, 288))
         launches += c2.last_launch_count()
+        if self.fp4:
+            c2.indexer_k_quant(self.new_k, self.new_slot, self.k_fp4)
+            launches += c2.last_launch_count()
         for i, mode in enumerate(self.cfg.schedule):
             if io:
                 io.wait_in(i)
@@ -284,7 +301,8 @@ class Workload:
         (the new token's latent goes with layer 0), and the ones it returns."""
         ins, outs = [], []
         for i, (li, m) in enumerate(zip(self.layers, self.cfg.schedule)):
-            g = ([self.new_latent] if i == 0 else []) + [li.q, li.swa, li.swa_scale]
+            g = ([self.new_latent] + ([self.new_k] if self.fp4 else []) if i == 0 else []) + [li.q, li.swa,
+                                                                                            li.swa_scale]
             if m != "reuse":
                 g += [li.q_idx, li.w]
             ins.append(g)
@@ -403,12 +421,14 @@ class PrefillWorkload:
                 [[self.out, self.lse, self.topk]])
 
 
-ATTN_KERNEL = 0   # csa2_params.attn_kernel of the workloads (--attn-kernel)
+ATTN_KERNEL = 0       # csa2_params.attn_kernel of the workloads (--attn-kernel)
+INDEXER_FP4 = False   # csa2_params.indexer_fp4 of the decode workloads (--indexer-fp4)
 
 
 def run_ours(args, rank, world, local_rank):
-    global ATTN_KERNEL
+    global ATTN_KERNEL, INDEXER_FP4
     ATTN_KERNEL = args.attn_kernel
+    INDEXER_FP4 = args.indexer_fp4
     import torch
 
     import synth
@@ -421,6 +441,8 @@ def run_ours(args, rank, world, local_rank):
     if args.batch:
         import dataclasses
         cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}[batch={args.batch}]")
+    if cfg.chunk and INDEXER_FP4:
+        raise SystemExit("--indexer-fp4: the MXFP4 indexer is decode-only")
     wl = PrefillWorkload(cfg, dev) if cfg.chunk else Workload(cfg, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -621,20 +643,27 @@ def cpu_baseline(args, cfg, seconds=12.0):
     oracle.build()
     B, N = cfg.batch, cfg.n_ctx
     seed = cfg.layer_seeds[0]
+    fp4 = getattr(args, "indexer_fp4", False)
     layers = [synth.layer_inputs(s, 1) for s in cfg.layer_seeds]
     done, t_total, b = 0, 0.0, 0
     while b < B and (t_total < seconds or done == 0):
         k = synth.indexer_keys(seed * 31 + b, 1, N)[0]
         lat = synth.context_latent(seed * 37 + b, 1, N)[0]
+        kq = oracle.mxfp4_quantise(k) if fp4 else None      # the cached MXFP4 entries
         t0 = time.perf_counter()
         sel = pool = None
         for i, mode in enumerate(cfg.schedule):
             li = layers[i]
             if mode == "full":
-                s = oracle.index_scores(li.q_idx[0], li.w[0], k)
+                s = (oracle.index_scores_mxfp4(li.q_idx[0], li.w[0], *kq) if fp4
+                     else oracle.index_scores(li.q_idx[0], li.w[0], k))
                 sel = oracle.topk(s, 512)
                 if cfg.hsi:
                     pool = oracle.hsi_pool(s, N, 8, 2048)
+            elif mode == "reindex" and fp4:
+                pos = oracle.pool_positions(pool, N)
+                sp = oracle.topk(oracle.index_scores_mxfp4(li.q_idx[0], li.w[0], kq[0][pos], kq[1][pos]), 512)
+                sel = np.where(sp >= 0, pos[np.clip(sp, 0, None)], -1)
             elif mode == "reindex":
                 sel = oracle.reindex_topk(li.q_idx[0], li.w[0], k, pool, N, 512)
             valid = sel[sel >= 0]
@@ -701,7 +730,8 @@ def run_reference(args, rank, world):
             "warmup": args.warmup, "ms_per_step": round(cfg.batch / v * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": cfg.name, "batch": cfg.batch, "context": cfg.n_ctx,
-                       "layers": "+".join(cfg.schedule), "chunk_tokens": cfg.chunk},
+                       "layers": "+".join(cfg.schedule), "chunk_tokens": cfg.chunk,
+                       "indexer": "mxfp4" if getattr(args, "indexer_fp4", False) else "bf16"},
             "impl": "reference",
             "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "cores": per_step[0]["cores"],
                              "kind": "oracle", "sample": per_step[0]["sample"]},

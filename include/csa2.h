@@ -74,6 +74,11 @@ typedef struct {
                                     (a token's chunks on a cluster of CTAs),
                                     2 streaming (a CTA pipelines a token's chunks);
                                     the result is the same up to rounding      */
+  int32_t indexer_fp4;           /* 0: indexer K cache bf16 [.][128]; 1: MXFP4
+                                    (csa2_indexer_k_quant) and the indexer
+                                    query quantised to MXFP4 as well ([A] 2.4.4:
+                                    "FP4 Indexer Q and K"; [A] 3.1: 68 B per
+                                    entry).  Decode only.                      */
 } csa2_params;
 
 /* Defaults of the pages: K=512, W=128, blocks of 8, 2048 blocks, max, hsi=1. */
@@ -107,6 +112,23 @@ csa2_status csa2_kv_quant_write(const void *latent, const void *z, int32_t m, in
                                 int64_t kv_rows, float rope_theta, csa2_stream_t stream);
 
 /*
+ * csa2_indexer_k_quant -- write MXFP4 indexer-K entries (OCP Microscaling:
+ * blocks of 32 dims share one UE8M0 scale 2^E, E = floor(log2(max |x|)) - 2
+ * clamped to [-127, 127] (-127 for an all-zero block); codes =
+ * E2M1_rne_satfinite(x / 2^E)).  The cache holds two planes: codes
+ * [rows][64] (dim 2j in the low nibble of byte j) at k_fp4, then scales
+ * [rows][4] (byte E + 127 for dims 32i..32i+31) at k_fp4 + rows * 64: 68 B per
+ * entry ([A] 3.1).
+ *   k      bf16 [n][128], 16-byte aligned
+ *   slot   int64 [n] destination rows, 0 <= slot < rows (others are skipped
+ *          and set CSA2_DEV_ERR_INDEX)
+ *   k_fp4  uint8 [rows * 68], 16-byte aligned; rows a multiple of 4
+ * n == 0 is a no-op.
+ */
+csa2_status csa2_indexer_k_quant(const void *k, int64_t n, const int64_t *slot, uint8_t *k_fp4, int64_t rows,
+                                 csa2_stream_t stream);
+
+/*
  * csa2_indexer_score_topk -- lightning indexer + top-K ([N] sections 2-3,
  * [A] 2.3.4).  For sequence b: score(n) = sum_h w[b][h] * ReLU(q_idx[b][h] .
  * k_idx[b][n]) in fp32 over 32 heads x 128 dims (bf16 tensor-core products,
@@ -118,7 +140,13 @@ csa2_status csa2_kv_quant_write(const void *latent, const void *z, int32_t m, in
  * the lower position), ascending, -1 padded when fewer are visible.
  *   q_idx  bf16 [batch][32][128], 16-byte aligned
  *   w      fp32 [batch][32]
- *   k_idx  bf16 [batch][cap][128], 16-byte aligned (indexer K cache)
+ *   k_idx  bf16 [batch][cap][128], 16-byte aligned (indexer K cache); with
+ *          params.indexer_fp4 the MXFP4 planes of csa2_indexer_k_quant with
+ *          rows = batch * cap (cap a multiple of 4), and q_idx is quantised to
+ *          MXFP4 the same way; the products are those of the dequantised
+ *          values, taken on fp16 tensor cores as code x 2^(E - Emax) with
+ *          2^Emax (the row's largest block scale) applied in fp32 after the
+ *          dot product: exact for every block within 2^23 of its row's largest
  *   n_vis  int32 [batch], 0 <= n_vis[b] <= n_max <= cap (checked on device)
  *   n_max  host-side bound on n_vis, sizes the launch and the workspace
  *   pool_blocks int32 [batch][candidate_topk_blocks] ascending, -1 padded

@@ -35,16 +35,18 @@ class Csa2Error(RuntimeError):
 class Params(ctypes.Structure):
     """csa2_params: index_topk, sliding_window, candidate_block_size,
     candidate_topk_blocks, block_reduce (0 max, 1 sum), hsi, attn_kernel (0
-    automatic, 1 chunk-parallel, 2 streaming)."""
+    automatic, 1 chunk-parallel, 2 streaming), indexer_fp4 (0 bf16 indexer K
+    cache, 1 MXFP4 planes written by ``indexer_k_quant``)."""
     _fields_ = [("index_topk", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
                 ("candidate_block_size", ctypes.c_int32), ("candidate_topk_blocks", ctypes.c_int32),
-                ("block_reduce", ctypes.c_int32), ("hsi", ctypes.c_int32), ("attn_kernel", ctypes.c_int32)]
+                ("block_reduce", ctypes.c_int32), ("hsi", ctypes.c_int32), ("attn_kernel", ctypes.c_int32),
+                ("indexer_fp4", ctypes.c_int32)]
 
     @classmethod
     def make(cls, index_topk=512, sliding_window=128, candidate_block_size=8, candidate_topk_blocks=2048,
-             block_reduce=0, hsi=1, attn_kernel=0):
+             block_reduce=0, hsi=1, attn_kernel=0, indexer_fp4=0):
         return cls(index_topk, sliding_window, candidate_block_size, candidate_topk_blocks, block_reduce, hsi,
-                   attn_kernel)
+                   attn_kernel, indexer_fp4)
 
 
 _lib = None
@@ -68,6 +70,7 @@ def lib():
         L.csa2_get_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         L.csa2_get_device_status.restype = ctypes.c_int
         L.csa2_kv_quant_write.argtypes = [P, P, i32, i64, P, P, P, i64, f32, P]
+        L.csa2_indexer_k_quant.argtypes = [P, i64, P, P, i64, P]
         L.csa2_indexer_score_topk.argtypes = [P, P, P, i32, i64, P, i64, P, PP, P, P, P, sz, P]
         L.csa2_hier_pool_select.argtypes = [P, P, i32, i64, PP, P, P, sz, P]
         L.csa2_sparse_attn.argtypes = [PP, i32, P, P, i64, P, P, P, P, P, P, P, sz, P]
@@ -76,8 +79,8 @@ def lib():
         L.csa2_prefill_chunk.argtypes = [PP, i32, i32, i64, i32, P, P, P, P, P, i64, P, P, i64, i64, P, P, P, P, sz, P]
         L.csa2_prefill_chunk.restype = ctypes.c_int
         L.csa2_set_profile_events.argtypes, L.csa2_set_profile_events.restype = [ctypes.c_int, P, P], ctypes.c_int
-        for f in ("csa2_kv_quant_write", "csa2_indexer_score_topk", "csa2_hier_pool_select", "csa2_sparse_attn",
-                  "csa2_sparse_decode"):
+        for f in ("csa2_kv_quant_write", "csa2_indexer_k_quant", "csa2_indexer_score_topk", "csa2_hier_pool_select",
+                  "csa2_sparse_attn", "csa2_sparse_decode"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -148,13 +151,50 @@ def kv_quant_write(latent, z, m, entry_pos, slot, kv, rope_theta=10000.0, stream
                                      _stream(stream)), "csa2_kv_quant_write")
 
 
+FP4_ENTRY_BYTES = 68
+
+
+def indexer_k_fp4_cache(rows: int, device=None) -> torch.Tensor:
+    """An MXFP4 indexer-K cache of `rows` entries (rows a multiple of 4): the
+    codes plane [rows][64] followed by the scales plane [rows][4]."""
+    if rows % 4:
+        raise Csa2Error("MXFP4 indexer cache rows must be a multiple of 4")
+    return torch.zeros(rows * FP4_ENTRY_BYTES, dtype=torch.uint8, device=device or "cuda")
+
+
+def indexer_k_fp4_planes(k_fp4: torch.Tensor):
+    """Views (codes [rows, 64], scales [rows, 4]) of an MXFP4 indexer-K cache."""
+    rows = k_fp4.numel() // FP4_ENTRY_BYTES
+    return k_fp4[:rows * 64].view(rows, 64), k_fp4[rows * 64:rows * FP4_ENTRY_BYTES].view(rows, 4)
+
+
+def indexer_k_quant(k, slot, k_fp4, stream=None):
+    """k bf16 [n, 128]; slot int64 [n]; k_fp4 uint8 cache of ``indexer_k_fp4_cache``."""
+    n = slot.numel()
+    _check(lib().csa2_indexer_k_quant(_ptr(k, torch.bfloat16, "k"), n, _ptr(slot, torch.int64, "slot"),
+                                      _ptr(k_fp4, torch.uint8, "k_fp4"), k_fp4.numel() // FP4_ENTRY_BYTES,
+                                      _stream(stream)), "csa2_indexer_k_quant")
+
+
+def _k_idx(k_idx, params, cap):
+    """Pointer to the indexer K cache: bf16 [B, cap, 128], or with
+    params.indexer_fp4 the uint8 MXFP4 cache of B * cap rows."""
+    if k_idx is None:
+        return None
+    if params.indexer_fp4:
+        return _ptr(k_idx, torch.uint8, "k_idx")
+    return _ptr(k_idx, torch.bfloat16, "k_idx")
+
+
 def indexer_score_topk(q_idx, w, k_idx, n_vis, n_max, params, topk_idx, ws, pool_blocks=None, block_scores=None,
                        stream=None):
-    """q_idx bf16 [B,32,128]; w fp32 [B,32]; k_idx bf16 [B,cap,128]; n_vis int32 [B];
-    topk_idx int32 [B,K] (out); block_scores fp32 [B, ceil(n_max/8)] (out, Full) or None."""
-    B, cap = k_idx.shape[0], k_idx.shape[1]
+    """q_idx bf16 [B,32,128]; w fp32 [B,32]; k_idx bf16 [B,cap,128] (with params.indexer_fp4 the
+    uint8 MXFP4 cache of B*cap rows); n_vis int32 [B]; topk_idx int32 [B,K] (out);
+    block_scores fp32 [B, ceil(n_max/8)] (out, Full) or None."""
+    B = q_idx.shape[0]
+    cap = k_idx.numel() // (B * FP4_ENTRY_BYTES) if params.indexer_fp4 else k_idx.shape[1]
     _check(lib().csa2_indexer_score_topk(
-        _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w, torch.float32, "w"), _ptr(k_idx, torch.bfloat16, "k_idx"),
+        _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w, torch.float32, "w"), _k_idx(k_idx, params, cap),
         B, cap, _ptr(n_vis, torch.int32, "n_vis"), int(n_max), _ptr(pool_blocks, torch.int32, "pool_blocks"),
         ctypes.byref(params), _ptr(topk_idx, torch.int32, "topk_idx"),
         _ptr(block_scores, torch.float32, "block_scores"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
@@ -189,7 +229,7 @@ def sparse_decode(mode, params, q, kv, n_vis, n_max, swa, swa_scale, swa_len, to
     _check(lib().csa2_sparse_decode(
         MODE[mode] if isinstance(mode, str) else int(mode), ctypes.byref(params), B,
         _ptr(q, torch.bfloat16, "q"), _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w, torch.float32, "w"),
-        _ptr(kv, torch.uint8, "kv"), _ptr(k_idx, torch.bfloat16, "k_idx"), cap,
+        _ptr(kv, torch.uint8, "kv"), _k_idx(k_idx, params, cap), cap,
         _ptr(n_vis, torch.int32, "n_vis"), int(n_max), _ptr(swa, torch.uint8, "swa"),
         _ptr(swa_scale, torch.float32, "swa_scale"), _ptr(swa_len, torch.int32, "swa_len"),
         _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(pool_blocks, torch.int32, "pool_blocks"),

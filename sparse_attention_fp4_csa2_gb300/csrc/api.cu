@@ -76,26 +76,44 @@ bool make_tmap_bf16_rows128(CUtensorMap *m, const void *ptr, int64_t rows, uint3
   return make_tmap_bf16(m, ptr, 128, rows, box_rows);
 }
 
+// 2-D byte tensor map over rows of 128 B, box {128, box_rows}, 128B swizzle.
+bool make_tmap_u8_rows128(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {128, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool params_ok(const csa2_params *p) {
   return p && p->index_topk >= 1 && p->index_topk <= 2048 && p->sliding_window >= 0 &&
          p->sliding_window <= 1024 && p->candidate_block_size == BLOCK && p->candidate_topk_blocks >= 16 &&
          p->candidate_topk_blocks <= TOPK_MAX_K && p->candidate_topk_blocks % 16 == 0 &&
          (p->block_reduce == 0 || p->block_reduce == 1) && (p->hsi == 0 || p->hsi == 1) &&
-         p->attn_kernel >= 0 && p->attn_kernel <= 2;
+         p->attn_kernel >= 0 && p->attn_kernel <= 2 && (p->indexer_fp4 == 0 || p->indexer_fp4 == 1);
 }
 
 // ------------------------------------------------------------ workspace
 struct IndexerLayout {
   int64_t row_len;       // scores per row
-  size_t scores_off, topk_off, end;
+  size_t scores_off, q8_off, wq_off, end;
 };
 
 IndexerLayout indexer_layout(int32_t batch, int64_t n_max, const csa2_params *p, bool pool) {
   IndexerLayout L;
-  L.row_len = pool ? (int64_t)p->candidate_topk_blocks * BLOCK : round_up(n_max, SWEEP_TILE);
+  const bool fp4 = p->indexer_fp4 != 0;
+  L.row_len = pool ? (int64_t)p->candidate_topk_blocks * BLOCK : round_up(n_max, fp4 ? FP4_SWEEP_TILE : SWEEP_TILE);
   L.scores_off = 0;
-  L.topk_off = (size_t)round_up((int64_t)batch * L.row_len * 4, 256);
-  L.end = L.topk_off;   // the cluster top-K needs no scratch beyond the scores
+  L.q8_off = (size_t)round_up((int64_t)batch * L.row_len * 4, 256);
+  // MXFP4 indexer: the queries' E5M2 rows and the head weights with their
+  // row exponents folded in; the cluster top-K needs no scratch beyond the scores
+  L.wq_off = L.q8_off + (fp4 ? (size_t)round_up((int64_t)batch * HI * DI, 256) : 0);
+  L.end = L.wq_off + (fp4 ? (size_t)round_up((int64_t)batch * HI * 4, 256) : 0);
   return L;
 }
 
@@ -149,11 +167,23 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   float *scores = reinterpret_cast<float *>(wsb + L.scores_off);
 
+  const bool fp4 = p->indexer_fp4 != 0;
+  if (fp4 && cap % 4 != 0) return CSA2_ERR_INVALID_ARG;
   CUtensorMap tm_k, tm_q;
-  if (!make_tmap_bf16_rows128(&tm_k, k_idx, (int64_t)batch * cap, pool ? BLOCK : SWEEP_TILE)) return CSA2_ERR_CUDA;
-  if (!make_tmap_bf16_rows128(&tm_q, q_idx, (int64_t)batch * HI, HI)) return CSA2_ERR_CUDA;
+  float *wq = nullptr;
+  if (fp4) {
+    // the queries in MXFP4 (as E5M2 bytes), then the sweep over the planes
+    void *q8 = wsb + L.q8_off;
+    wq = reinterpret_cast<float *>(wsb + L.wq_off);
+    if (launch_indexer_q_fp4(q_idx, w, (int64_t)batch * HI, q8, wq, stream) != cudaSuccess) return CSA2_ERR_CUDA;
+    ++*launches;
+    if (!make_tmap_u8_rows128(&tm_q, q8, (int64_t)batch * HI, HI)) return CSA2_ERR_CUDA;
+  } else {
+    if (!make_tmap_bf16_rows128(&tm_k, k_idx, (int64_t)batch * cap, pool ? BLOCK : SWEEP_TILE)) return CSA2_ERR_CUDA;
+    if (!make_tmap_bf16_rows128(&tm_q, q_idx, (int64_t)batch * HI, HI)) return CSA2_ERR_CUDA;
+  }
   SweepArgs a;
-  a.w = w;
+  a.w = fp4 ? wq : w;
   a.n_vis = n_vis;
   a.pool = pool_blocks;
   a.scores = scores;
@@ -162,12 +192,17 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   a.n_max = n_max;
   a.row_len = L.row_len;
   a.batch = batch;
-  a.tiles_per_seq = (int32_t)(L.row_len / SWEEP_TILE);
+  a.tiles_per_seq = fp4 ? (int32_t)((L.row_len + FP4_SWEEP_TILE - 1) / FP4_SWEEP_TILE)
+                        : (int32_t)(L.row_len / SWEEP_TILE);
   a.pool_nb = p->candidate_topk_blocks;
   a.nblk_stride = (int32_t)((n_max + BLOCK - 1) / BLOCK);
   a.block_reduce = p->block_reduce;
+  a.k_codes = fp4 ? static_cast<const uint8_t *>(k_idx) : nullptr;
+  a.k_scales = fp4 ? static_cast<const uint8_t *>(k_idx) + (int64_t)batch * cap * (DI / 2) : nullptr;
+  a.k_rows = (int64_t)batch * cap;
   const int sms = num_sms();
-  cudaError_t e = launch_indexer_sweep(tm_k, tm_q, a, sms, stream, launches);
+  cudaError_t e = fp4 ? launch_indexer_sweep_fp4(tm_q, a, sms, stream, launches)
+                      : launch_indexer_sweep(tm_k, tm_q, a, sms, stream, launches);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
 
   TopkRows r;
@@ -255,6 +290,7 @@ csa2_params csa2_default_params(void) {
   p.block_reduce = 0;
   p.hsi = 1;
   p.attn_kernel = 0;
+  p.indexer_fp4 = 0;
   return p;
 }
 
@@ -318,6 +354,19 @@ csa2_status csa2_kv_quant_write(const void *latent, const void *z, int32_t m, in
   const cudaError_t e = launch_kv_quant_write(latent, m == 2 ? z : nullptr, m, n_entries, entry_pos, slot, kv,
                                               kv_rows, rope_theta, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  g_last_launches = 1;
+  return CSA2_OK;
+}
+
+csa2_status csa2_indexer_k_quant(const void *k, int64_t n, const int64_t *slot, uint8_t *k_fp4, int64_t rows,
+                                 csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (n < 0 || rows < 0 || rows % 4 != 0) return CSA2_ERR_INVALID_ARG;
+  if (n == 0) return CSA2_OK;
+  if (!k || !slot || !k_fp4 || !aligned16(k) || !aligned16(k_fp4)) return CSA2_ERR_INVALID_ARG;
+  if (n > ((int64_t)1 << 34)) return CSA2_ERR_UNSUPPORTED;
+  if (launch_indexer_k_quant(k, n, slot, k_fp4, rows, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return CSA2_ERR_CUDA;
   g_last_launches = 1;
   return CSA2_OK;
 }
@@ -409,6 +458,7 @@ extern "C" csa2_status csa2_prefill_chunk(const csa2_params *params, int32_t bat
                                           csa2_stream_t stream) {
   g_last_launches = 0;
   if (!params_ok(params)) return CSA2_ERR_UNSUPPORTED;
+  if (params->indexer_fp4) return CSA2_ERR_UNSUPPORTED;   // the MXFP4 indexer is decode-only
   const csa2_params *p = params;
   if (batch < 1 || n_tokens < 8 || n_tokens % 8 != 0 || (m != 1 && m != 2) || first_pos < 0 || cap < 1)
     return CSA2_ERR_INVALID_ARG;

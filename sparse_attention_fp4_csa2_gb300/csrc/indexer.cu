@@ -21,7 +21,7 @@
 // the K tiles into a ring of shared-memory stages, warp 1 issues the MMAs into
 // two TMEM accumulators, warps 2-5 drain the accumulators.  Every CTA owns a
 // contiguous run of (sequence, tile) work items.
-#include "kernels.cuh"
+#include "sweep_epilogue.cuh"
 
 namespace csa2 {
 
@@ -236,39 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&S.accempty[acc]);
-      float sc = 0.0f;
-#pragma unroll
-      for (int h = 0; h < HI; ++h) sc = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.0f), sc);
-      float *srow = a.scores + (int64_t)b * a.row_len;
-      if (!kPool) {
-        const int64_t pos = (int64_t)t * SWEEP_TILE + r;
-        const bool valid = pos < nv;
-        srow[pos] = valid ? sc : -INFINITY;
-        if (a.block_scores) {
-          float bv;
-          if (a.block_reduce == 0) {
-            bv = valid ? sc : -INFINITY;
-            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 1));
-            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 2));
-            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 4));
-          } else {
-            bv = valid ? sc : 0.0f;
-            bv += __shfl_xor_sync(0xffffffffu, bv, 1);
-            bv += __shfl_xor_sync(0xffffffffu, bv, 2);
-            bv += __shfl_xor_sync(0xffffffffu, bv, 4);
-            if ((pos & ~int64_t(BLOCK - 1)) >= nv) bv = -INFINITY;
-          }
-          const int64_t blk = pos / BLOCK;
-          if ((lane & (BLOCK - 1)) == 0 && blk < a.nblk_stride)
-            a.block_scores[(int64_t)b * a.nblk_stride + blk] = bv;
-        }
-      } else {
-        const int64_t slot = (int64_t)t * SWEEP_TILE + r;
-        const int32_t blk = __ldg(a.pool + (int64_t)b * a.pool_nb + slot / BLOCK);
-        const int64_t pos = (int64_t)blk * BLOCK + (r & (BLOCK - 1));
-        const bool valid = blk >= 0 && pos < nv;
-        srow[slot] = valid ? sc : -INFINITY;
-      }
+      sweep_store_row<kPool>(a, b, t, r, lane, nv, wv, v);
     }
   }
 

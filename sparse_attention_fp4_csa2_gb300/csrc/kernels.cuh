@@ -22,6 +22,7 @@ constexpr int BLOCK = 8;           // HSI candidate block width
 
 // Indexer sweep: 128 positions per tile (the MMA M dimension).
 constexpr int SWEEP_TILE = 128;
+constexpr int FP4_SWEEP_TILE = 256;   // keys per tile of the MXFP4 sweep
 // Attention: 128 keys per CTA (the MMA M dimension of S^T = K Q^T).
 constexpr int ATTN_CHUNK = 128;
 // Radix select: 11-bit first digit.
@@ -65,6 +66,7 @@ cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream);
 
 // 2-D bf16 tensor map over rows of `inner` elements, box {64, box_rows}, 128B swizzle.
 bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t inner, int64_t rows, uint32_t box_rows);
+// 2-D byte tensor map over rows of 64 bytes, box {64, box_rows}, no swizzle.
 
 cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int64_t n_entries, const int64_t *pos,
                                   const int64_t *slot, uint8_t *kv, int64_t kv_rows, float rope_theta,
@@ -84,10 +86,23 @@ struct SweepArgs {
   int32_t pool_nb;
   int32_t nblk_stride;        // ceil(n_max / 8)
   int32_t block_reduce;       // 0 max, 1 sum
+  const uint8_t *k_codes;     // MXFP4 sweep: the code plane [k_rows][64]
+  const uint8_t *k_scales;    // MXFP4 sweep: the scale plane [k_rows][4]
+  int64_t k_rows;             // MXFP4 sweep: rows of the planes (batch * cap)
 };
 
 cudaError_t launch_indexer_sweep(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
                                  int num_sms, cudaStream_t stream, int *launches);
+// MXFP4 indexer: the planes through a.k_codes / a.k_scales, tm_q over the
+// queries' E5M2 rows (bytes [batch * 32][128], 128B swizzle, boxes of 32 rows).
+cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_q, const SweepArgs &a, int num_sms, cudaStream_t stream,
+                                     int *launches);
+cudaError_t launch_indexer_k_quant(const void *k, int64_t n, const int64_t *slot, uint8_t *k_fp4, int64_t rows,
+                                   cudaStream_t stream);
+// The queries' MXFP4 values as E5M2 bytes [rows][128] (code x 2^(E - Emax) per
+// row) and wq = w x 2^Emax.
+cudaError_t launch_indexer_q_fp4(const void *q, const float *w, int64_t rows, void *q_e5m2, float *wq,
+                                 cudaStream_t stream);
 
 // Single-kernel top-K with one thread-block cluster per row (no scratch);
 // for k <= 2048.

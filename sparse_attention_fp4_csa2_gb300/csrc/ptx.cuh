@@ -135,6 +135,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const void *tmap, in
       : "memory");
 }
 
+// bulk_g2s under an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // L2 policy: lines loaded under it are the first to be evicted (data read
 // once, streamed past what should stay resident).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
@@ -182,6 +192,18 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] x B[smem desc]^T, kind::f8f6f4 (8-bit operands,
+// K = 32 per instruction, fp32 accumulator).
+__device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -221,6 +243,15 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t ab_bf16, uint32_t a_mn
                                                  uint32_t m) {
   return (1u << 4) | (ab_bf16 << 7) | (ab_bf16 << 10) | (a_mn << 15) | (b_mn << 16) | ((n >> 3) << 17) |
          ((m >> 4) << 24);
+}
+
+// Operand formats of kind::f8f6f4 in the instruction descriptor.
+constexpr uint32_t kFmtE4M3 = 0, kFmtE5M2 = 1;
+
+// Instruction descriptor for kind::f8f6f4: fp32 accumulator, A/B formats,
+// both K-major, N, M (the same fields as kind::f16).
+__host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t a_fmt, uint32_t b_fmt, uint32_t n, uint32_t m) {
+  return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
 // ------------------------------------------------------ thread-block clusters

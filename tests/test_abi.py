@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(c2):
 def test_defaults_and_sizes(c2):
     p = c2.default_params()
     assert (p.index_topk, p.sliding_window, p.candidate_block_size, p.candidate_topk_blocks, p.block_reduce,
-            p.hsi, p.attn_kernel) == (512, 128, 8, 2048, 0, 1, 0)
+            p.hsi, p.attn_kernel, p.indexer_fp4) == (512, 128, 8, 2048, 0, 1, 0, 0)
     assert c2.entry_bytes() == 288
     assert c2.lib().csa2_status_string(3) == b"workspace too small"
 
@@ -53,6 +53,10 @@ def test_workspace_sizes(c2):
     assert c2.workspace_bytes(c2.OP_ATTN, 4, 1000, c2.Params.make(attn_kernel=3)) == 0
     assert c2.workspace_bytes(c2.OP_ATTN, 4, 1000, c2.Params.make(attn_kernel=2)) > 0
     assert c2.workspace_bytes(c2.OP_DECODE, 0, 1000, p) == 0
+    # the MXFP4 indexer adds its E5M2 query rows (128 B) and folded weights (4 B)
+    f4 = c2.Params.make(indexer_fp4=1)
+    assert c2.workspace_bytes(c2.OP_INDEXER, 4, 4096, f4) >= c2.workspace_bytes(c2.OP_INDEXER, 4, 4096, p) + 4 * 32 * (128 + 4)
+    assert c2.workspace_bytes(c2.OP_INDEXER, 4, 4096, c2.Params.make(indexer_fp4=2)) == 0
 
 
 def test_host_validation_rejects_without_launch(c2):
@@ -80,6 +84,19 @@ def test_host_validation_rejects_without_launch(c2):
     # n_max above the cache capacity
     assert L.csa2_indexer_score_topk(fake, fake, fake, 1, 100, fake, 200, None, ctypes.byref(p), fake, None,
                                      P(0x1000), 1 << 30, None) == 1
+    # MXFP4 indexer-K write: rows must be a multiple of 4, pointers aligned; n = 0 is a no-op
+    assert L.csa2_indexer_k_quant(fake, 4, fake, fake, 6, None) == 1
+    assert L.csa2_indexer_k_quant(odd, 4, fake, fake, 8, None) == 1
+    assert L.csa2_indexer_k_quant(fake, 4, fake, odd, 8, None) == 1
+    assert L.csa2_indexer_k_quant(None, 4, fake, fake, 8, None) == 1
+    assert L.csa2_indexer_k_quant(None, 0, None, None, 0, None) == 0
+    assert c2.last_launch_count() == 0
+    # MXFP4 cache capacity must be a multiple of 4; the prefill has no MXFP4 indexer
+    f4 = c2.Params.make(indexer_fp4=1)
+    assert L.csa2_indexer_score_topk(fake, fake, fake, 1, 102, fake, 100, None, ctypes.byref(f4), fake, None,
+                                     P(0x1000), 1 << 30, None) == 1
+    assert L.csa2_prefill_chunk(ctypes.byref(f4), 1, 64, 0, 1, fake, fake, fake, fake, fake, 128, fake, fake, 0, 0,
+                                fake, fake, None, P(0x1000), 1 << 30, None) == 2
     # REINDEX needs a pool
     assert L.csa2_sparse_decode(1, ctypes.byref(p), 1, fake, fake, fake, fake, fake, 100, fake, 100, fake, fake,
                                 fake, fake, None, fake, None, P(0x1000), 1 << 30, None) == 1
