@@ -76,6 +76,20 @@ bool make_tmap_bf16_rows128(CUtensorMap *m, const void *ptr, int64_t rows, uint3
   return make_tmap_bf16(m, ptr, 128, rows, box_rows);
 }
 
+// 2-D byte tensor map over rows of 64 B, box {64, box_rows}, 64B swizzle.
+bool make_tmap_u8_rows64(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {64, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {64};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // 2-D byte tensor map over rows of 128 B, box {128, box_rows}, 128B swizzle.
 bool make_tmap_u8_rows128(CUtensorMap *m, const void *ptr, int64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
@@ -178,6 +192,7 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
     if (launch_indexer_q_fp4(q_idx, w, (int64_t)batch * HI, q8, wq, stream) != cudaSuccess) return CSA2_ERR_CUDA;
     ++*launches;
     if (!make_tmap_u8_rows128(&tm_q, q8, (int64_t)batch * HI, HI)) return CSA2_ERR_CUDA;
+    if (!make_tmap_u8_rows64(&tm_k, k_idx, (int64_t)batch * cap, pool ? BLOCK : FP4_SWEEP_TILE)) return CSA2_ERR_CUDA;
   } else {
     if (!make_tmap_bf16_rows128(&tm_k, k_idx, (int64_t)batch * cap, pool ? BLOCK : SWEEP_TILE)) return CSA2_ERR_CUDA;
     if (!make_tmap_bf16_rows128(&tm_q, q_idx, (int64_t)batch * HI, HI)) return CSA2_ERR_CUDA;
@@ -197,11 +212,10 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   a.pool_nb = p->candidate_topk_blocks;
   a.nblk_stride = (int32_t)((n_max + BLOCK - 1) / BLOCK);
   a.block_reduce = p->block_reduce;
-  a.k_codes = fp4 ? static_cast<const uint8_t *>(k_idx) : nullptr;
   a.k_scales = fp4 ? static_cast<const uint8_t *>(k_idx) + (int64_t)batch * cap * (DI / 2) : nullptr;
   a.k_rows = (int64_t)batch * cap;
   const int sms = num_sms();
-  cudaError_t e = fp4 ? launch_indexer_sweep_fp4(tm_q, a, sms, stream, launches)
+  cudaError_t e = fp4 ? launch_indexer_sweep_fp4(tm_k, tm_q, a, sms, stream, launches)
                       : launch_indexer_sweep(tm_k, tm_q, a, sms, stream, launches);
   if (e != cudaSuccess) return CSA2_ERR_CUDA;
 
@@ -240,8 +254,7 @@ csa2_status run_pool(const float *block_scores, const int32_t *n_vis, int32_t ba
   r.pool = nullptr;
   r.pool_stride = 0;
   r.out = pool_blocks;
-  const TopkScratch s = carve_topk_scratch(ws, batch, nblk, r.k);
-  return cuda_status(launch_topk(r, s, num_sms(), stream, launches));
+  return cuda_status(launch_pool_topk(r, ws, num_sms(), stream, launches));
 }
 
 csa2_status run_attn(const csa2_params *p, int32_t batch, const void *q, const uint8_t *kv, int64_t cap,

@@ -10,49 +10,52 @@
 // (byte E + 127), so that both stay 16-byte aligned for bulk copies.
 //
 // The sweep reads 68 B per position instead of 256 B.  Tiles are 256 keys:
-// a producer brings a tile's code and scale bytes by bulk copies into a ring
-// of raw stages; eight dequant warps (a thread per key) turn each key row into
+// a producer brings a tile's codes (a tensor copy with 64-byte swizzle, so
+// that the dequant threads' row reads hit distinct banks) and its scales (a
+// bulk copy) into a ring of raw stages; eight dequant warps (a thread per key) turn each key row into
 // 128 E5M2 bytes code x 2^(E - Emax), Emax the largest of the row's four
-// block exponents, in a 128B-swizzled ring; one thread issues four
-// kind::f8f6f4 MMAs per tile, D[128 x 256] = Q4 . K^T, where Q4 holds the
-// query's 32 head rows four times over (so that each TMEM lane quarter has
-// every head), and four epilogue warps each reduce 64 keys over the 32 heads
-// of their lanes: score = 2^Emax_key sum_h wq_h ReLU(D[h][key]).  The query is
-// quantised the same way (E5M2 code x 2^(E - Emax_h)) with 2^Emax_h folded
-// into wq_h = w_h 2^Emax_h (ReLU commutes with a positive factor).
+// block exponents, in a 128B-swizzled ring; one thread issues eight
+// kind::f8f6f4 MMAs per tile (two halves of 128 keys x K = 4 x 32), D[key][h]
+// = K . Q^T with the keys on TMEM lanes and the 32 heads on columns, and four
+// epilogue warps take a key per thread: score = 2^Emax_key sum_h wq_h
+// ReLU(D[key][h]).  The query is quantised the same way (E5M2 code x
+// 2^(E - Emax_h)) with 2^Emax_h folded into wq_h = w_h 2^Emax_h (ReLU commutes
+// with a positive factor).
 //
 // Exactness: E2M1 values have two significant bits, so code x 2^k is an E5M2
 // number for k >= -15: every operand is the exact dequantised value while a
 // block lies within 2^15 of its row's largest block (rows further apart lose
 // their smallest elements); the products and their fp32 sums are those of the
 // dequantised MXFP4 values.
-#include "sweep_epilogue.cuh"
+#include "pipeline.cuh"
 
 namespace csa2 {
 
 namespace {
 
-constexpr int kKeys = FP4_SWEEP_TILE;                    // keys per tile (MMA N)
+constexpr int kKeys = FP4_SWEEP_TILE;                    // keys per tile: two MMA halves of M = 128
 constexpr int kRaw = 5;                                  // raw stages
 constexpr int kRawCodes = kKeys * DI / 2;                // 16 KB of codes
 constexpr int kRawBytes = kRawCodes + kKeys * 4;         // + 1 KB of scales
 constexpr int kTiles = 3;                                // E5M2 key tiles
 constexpr int kTileBytes = kKeys * DI;                   // 32 KB: [256 rows][128 B], one K-atom wide
-constexpr int kQRows = 128;                              // MMA M: 4 copies of the 32 heads
-constexpr int kQBytes = kQRows * DI;                     // 16 KB
-constexpr int kAcc = 2;                                  // TMEM accumulators of 256 columns
-constexpr int kTmemCols = kAcc * kKeys;                  // 512: all of TMEM (one CTA per SM)
+constexpr int kHalfKeys = 128;                           // MMA M
+constexpr int kQBytes = HI * DI;                         // 4 KB: the 32 head rows (MMA N)
+constexpr int kAcc = 2;                                  // TMEM accumulators of 2 x 32 columns
+constexpr int kTmemCols = kAcc * 2 * HI;                 // 128
+constexpr int kEpiWarps = 4;                             // one per TMEM lane quarter
 constexpr int kDeqWarps = 8;                             // a thread per key
 constexpr int kDeqThreads = kDeqWarps * 32;
-constexpr int kThreads = (6 + kDeqWarps) * 32;           // producer, MMA, 4 epilogue, dequant warps
+constexpr int kDeqWarp0 = 2 + kEpiWarps;
+constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;   // producer, MMA, epilogue, dequant warps
 // Row exponents handed from the dequant warps to the epilogue.  Slot
 // li % kExpSlots is rewritten only after the epilogue has read it: dequant
 // (li + kTiles + kAcc) waits for MMA(li + kAcc) to free its tile, and
 // MMA(li + kAcc) waits for the epilogue of li to free their accumulator.
 constexpr int kExpSlots = kTiles + kAcc;
-constexpr uint32_t kIdesc = idesc_f8f6f4(kFmtE5M2, kFmtE5M2, /*N*/ kKeys, /*M*/ kQRows);
+constexpr uint32_t kIdesc = idesc_f8f6f4(kFmtE5M2, kFmtE5M2, /*N*/ HI, /*M*/ kHalfKeys);
 static_assert(kDeqThreads == kKeys, "one dequant thread per key");
-static_assert(kTmemCols <= 512, "TMEM holds 512 columns");
+static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM allocation");
 
 struct __align__(8) Fp4Smem {
   uint64_t raw_full[kRaw];
@@ -73,33 +76,6 @@ struct __align__(8) Fp4Smem {
 __device__ __forceinline__ volatile uint32_t &abort_of(Fp4Smem &S) {
   return *reinterpret_cast<volatile uint32_t *>(&S.abort);
 }
-
-// Slot and phase of a ring of N mbarrier-guarded buffers, advanced per tile
-// (no division in the per-tile loops: they run on one thread each).
-template <int N>
-struct Ring {
-  int slot = 0;
-  uint32_t phase = 0;
-  __device__ __forceinline__ void next() {
-    if (++slot == N) {
-      slot = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
-// (sequence, tile) of the tiles a CTA sweeps, advanced per tile.
-struct TileCursor {
-  int b, t, per_seq;
-  __device__ __forceinline__ TileCursor(int64_t it, int tiles_per_seq)
-      : b((int)(it / tiles_per_seq)), t((int)(it % tiles_per_seq)), per_seq(tiles_per_seq) {}
-  __device__ __forceinline__ void next() {
-    if (++t == per_seq) {
-      t = 0;
-      ++b;
-    }
-  }
-};
 
 constexpr size_t kSmemBytes = 1024 + (size_t)kTiles * kTileBytes + 2 * (size_t)kQBytes + (size_t)kRaw * kRawBytes +
                               sizeof(Fp4Smem);
@@ -214,39 +190,14 @@ __device__ __forceinline__ int row_emax(uint32_t sc) {
   return (int)max(m & 0xFFu, (m >> 8) & 0xFFu) - 127;
 }
 
-// One halving step of the transposed reduction: lanes with bit `half` set
-// keep the upper n of their 2n columns and take the partner's, the others the
-// lower n.
-template <int N, int HALF>
-__device__ __forceinline__ void reduce_step(float (&x)[64], int lane) {
-  const bool up = lane & HALF;
-#pragma unroll
-  for (int i = 0; i < N; ++i) {
-    const float send = up ? x[i] : x[i + N];
-    const float keep = up ? x[i + N] : x[i];
-    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, HALF);
-  }
-}
-
-// Sum over the 32 lanes of each of 64 columns (x[c] on every lane): after
-// the exchange lane l holds the sums of columns 2l and 2l + 1.
-__device__ __forceinline__ void transpose_reduce64(float (&x)[64], int lane, float &s0, float &s1) {
-  reduce_step<32, 16>(x, lane);
-  reduce_step<16, 8>(x, lane);
-  reduce_step<8, 4>(x, lane);
-  reduce_step<4, 2>(x, lane);
-  reduce_step<2, 1>(x, lane);
-  s0 = x[0];
-  s1 = x[1];
-}
-
 template <bool kPool>
 __global__ void __launch_bounds__(kThreads, 1)
-    indexer_sweep_fp4_kernel(const __grid_constant__ CUtensorMap tm_q, const SweepArgs a) {
+    indexer_sweep_fp4_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_q,
+                             const SweepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *tiles = base;                                    // kTiles x 32 KB, 1024-aligned
-  uint8_t *qbuf = tiles + (size_t)kTiles * kTileBytes;      // 2 x 16 KB
+  uint8_t *qbuf = tiles + (size_t)kTiles * kTileBytes;      // 2 x 4 KB
   uint8_t *raw = qbuf + 2 * kQBytes;                        // kRaw x 17 KB
   Fp4Smem &S = *reinterpret_cast<Fp4Smem *>(raw + (size_t)kRaw * kRawBytes);
 
@@ -271,11 +222,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < kAcc; ++i) {
       mbar_init(&S.accfull[i], 1);
-      mbar_init(&S.accempty[i], 4 * 32);
+      mbar_init(&S.accempty[i], kEpiWarps * 32);
     }
     mbar_init(&S.mma_done, 1);
     abort_of(S) = 0;
     fence_barrier_init();
+    prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_q);
   }
   if (warp == 1) {
@@ -289,88 +241,93 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // a tile's codes are contiguous in the plane (rows of 64 B): one bulk
-    // copy for the codes and one for the scales (Full), or one pair per
-    // pool block of 8 rows (Reindex), cut to the rows the planes hold
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();   // codes are read once
-      int prev_b = -1, qi = -1;
-      int32_t nv = 0;
-      int n_issued = 0;
-      TileCursor cur(it0, a.tiles_per_seq);
-      Ring<kRaw> rr;
-      for (int li = 0; li < n_tiles; ++li, cur.next(), rr.next()) {
-        const int b = cur.b, t = cur.t;
-        if (b != prev_b) {
-          if (qi >= 0 && abort_of(S)) break;
-          ++qi;
-          const int qs = qi & 1;
-          if (!mbar_wait(&S.qempty[qs], ((qi >> 1) & 1) ^ 1)) { abort_of(S) = 1; break; }
-          mbar_arrive_expect_tx(&S.qfull[qs], kQBytes);
-#pragma unroll
-          for (int j = 0; j < kQRows / HI; ++j)   // the 32 head rows, four times
-            tma_load_2d(qbuf + qs * kQBytes + j * HI * DI, &tm_q, 0, b * HI, &S.qfull[qs]);
-          nv = clamp_nvis_fp4(a.n_vis, b, a.n_max);
-          prev_b = b;
+    // lane 0 drives the rings and copies a Full tile: one tensor copy of the
+    // tile's code rows (zero-filled past the last row, counted in full) and
+    // one bulk copy of its scales; in a pool tile (Reindex) lane j fetches
+    // pool block j, its 8 code rows and its scales.  Scale copies are cut to
+    // the rows the planes hold.
+    const uint64_t pol = l2_policy_evict_first();   // codes are read once
+    int prev_b = -1, q_issued = 0;
+    int32_t nv = 0;
+    int n_issued = 0;
+    TileCursor cur(it0, a.tiles_per_seq);
+    Ring<kRaw> rr;
+    for (int li = 0; li < n_tiles; ++li, cur.next(), rr.next()) {
+      const int b = cur.b, t = cur.t;
+      int ok = 1;
+      if (b != prev_b) {
+        if (lane == 0) {
+          const int qs = q_issued & 1;
+          if (q_issued > 0 && abort_of(S)) {
+            ok = 0;
+          } else if (!mbar_wait(&S.qempty[qs], ((q_issued >> 1) & 1) ^ 1)) {
+            abort_of(S) = 1;
+            ok = 0;
+          } else {
+            mbar_arrive_expect_tx(&S.qfull[qs], kQBytes);
+            tma_load_2d(qbuf + qs * kQBytes, &tm_q, 0, b * HI, &S.qfull[qs]);
+            nv = clamp_nvis_fp4(a.n_vis, b, a.n_max);
+          }
         }
-        const int s = rr.slot;
-        if (!mbar_wait(&S.raw_empty[s], rr.phase ^ 1)) { abort_of(S) = 1; break; }
-        uint8_t *dst = raw + (size_t)s * kRawBytes;
-        const int64_t row0 = (int64_t)b * a.cap;
-        if (!kPool) {
+        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+        nv = __shfl_sync(0xffffffffu, nv, 0);
+        ++q_issued;
+        prev_b = b;
+      }
+      const int s = rr.slot;
+      if (lane == 0 && !mbar_wait(&S.raw_empty[s], rr.phase ^ 1)) {
+        abort_of(S) = 1;
+        ok = 0;
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      uint8_t *dst = raw + (size_t)s * kRawBytes;
+      const int64_t row0 = (int64_t)b * a.cap;
+      if (!kPool) {
+        if (lane == 0) {
           if ((int64_t)t * kKeys < nv) {
             const int64_t r0 = row0 + (int64_t)t * kKeys;
             const int64_t left = a.k_rows - r0;
             const uint32_t nrows = (uint32_t)(left < kKeys ? left : kKeys);   // a multiple of 4
-            mbar_arrive_expect_tx(&S.raw_full[s], nrows * (DI / 2 + 4));
-            bulk_g2s_hint(dst, a.k_codes + r0 * (DI / 2), nrows * (DI / 2), &S.raw_full[s], pol);
+            mbar_arrive_expect_tx(&S.raw_full[s], kRawCodes + nrows * 4);
+            tma_load_2d_hint(dst, &tm_k, 0, (int32_t)r0, &S.raw_full[s], pol);
             bulk_g2s(dst + kRawCodes, a.k_scales + r0 * 4, nrows * 4, &S.raw_full[s]);
           } else {
             mbar_arrive(&S.raw_full[s]);
           }
-        } else {
-          // the tile's pool blocks j0 .. j0 + nj - 1 (the last tile may hold fewer)
-          const int64_t j0 = (int64_t)t * (kKeys / BLOCK);
-          const int nj = (int)(a.pool_nb - j0 < kKeys / BLOCK ? a.pool_nb - j0 : kKeys / BLOCK);
-          const int32_t *pb = a.pool + (int64_t)b * a.pool_nb + j0;
-          const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
-          uint32_t valid = 0, bytes = 0;
-#pragma unroll 1
-          for (int j = 0; j < nj; ++j) {
-            const int32_t blk = __ldg(pb + j);
-            if (blk >= 0 && blk < nblk_vis) {
-              valid |= 1u << j;
-              const int64_t left = a.k_rows - (row0 + (int64_t)blk * BLOCK);
-              bytes += (uint32_t)(left < BLOCK ? left : BLOCK) * (DI / 2 + 4);
-            } else if (blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) {
-              set_error(CSA2_DEV_ERR_POOL);
-            }
-          }
-          if (valid) {
-            mbar_arrive_expect_tx(&S.raw_full[s], bytes);
-#pragma unroll 1
-            for (int j = 0; j < nj; ++j) {
-              if (!(valid >> j & 1)) continue;
-              const int64_t y = row0 + (int64_t)__ldg(pb + j) * BLOCK;
-              // a block past the last row when cap is not a multiple of 8
-              // (cap and y are multiples of 4)
-              const uint32_t nrows = (uint32_t)(a.k_rows - y < BLOCK ? a.k_rows - y : BLOCK);
-              bulk_g2s_hint(dst + j * BLOCK * (DI / 2), a.k_codes + y * (DI / 2), nrows * (DI / 2), &S.raw_full[s],
-                            pol);
-              bulk_g2s(dst + kRawCodes + j * BLOCK * 4, a.k_scales + y * 4, nrows * 4, &S.raw_full[s]);
-            }
-          } else {
-            mbar_arrive(&S.raw_full[s]);
-          }
         }
-        ++n_issued;
+      } else {
+        // the tile's pool blocks j0 .. j0 + nj - 1 (the last tile may hold fewer)
+        const int64_t j0 = (int64_t)t * (kKeys / BLOCK);
+        const int nj = (int)(a.pool_nb - j0 < kKeys / BLOCK ? a.pool_nb - j0 : kKeys / BLOCK);
+        const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
+        const int32_t blk = lane < nj ? __ldg(a.pool + (int64_t)b * a.pool_nb + j0 + lane) : -1;
+        const bool v = blk >= 0 && blk < nblk_vis;
+        if (lane < nj && !v && blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) set_error(CSA2_DEV_ERR_POOL);
+        const int64_t y = row0 + (int64_t)blk * BLOCK;
+        // a block past the last row when cap is not a multiple of 8 (cap and
+        // y are multiples of 4)
+        const uint32_t nrows = v ? (uint32_t)(a.k_rows - y < BLOCK ? a.k_rows - y : BLOCK) : 0u;
+        const uint32_t bytes = __reduce_add_sync(0xffffffffu, v ? BLOCK * (DI / 2) + nrows * 4 : 0u);
+        if (bytes) {
+          if (lane == 0) mbar_arrive_expect_tx(&S.raw_full[s], bytes);
+          __syncwarp();
+          if (v) {
+            tma_load_2d_hint(dst + lane * BLOCK * (DI / 2), &tm_k, 0, (int32_t)y, &S.raw_full[s], pol);
+            bulk_g2s(dst + kRawCodes + lane * BLOCK * 4, a.k_scales + y * 4, nrows * 4, &S.raw_full[s]);
+          }
+        } else if (lane == 0) {
+          mbar_arrive(&S.raw_full[s]);
+        }
       }
-      // every copy this thread issued has landed before the CTA can exit
+      ++n_issued;
+    }
+    // every copy this warp issued has landed before the CTA can exit
+    if (lane == 0) {
       for (int s = 0; s < kRaw && s < n_issued; ++s) {
         const int last = s + ((n_issued - 1 - s) / kRaw) * kRaw;
         mbar_wait(&S.raw_full[s], (uint32_t)((last / kRaw) & 1));
       }
-      if (qi >= 0) mbar_wait(&S.qfull[qi & 1], (qi >> 1) & 1);
+      if (q_issued > 0) mbar_wait(&S.qfull[(q_issued - 1) & 1], ((q_issued - 1) >> 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -396,20 +353,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t ka = tbase + (uint32_t)st * kTileBytes;
         const uint32_t qa = qbase + (uint32_t)(qi & 1) * kQBytes;
 #pragma unroll
-        for (int kk = 0; kk < DI / 32; ++kk)   // K = 32 E5M2 (32 B) per MMA
-          mma_f8f6f4(tmem + (uint32_t)(acc * kKeys), smem_desc(qa + kk * 32, 16, 1024),
-                     smem_desc(ka + kk * 32, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
+        for (int j = 0; j < 2; ++j)              // keys 128j .. 128j + 127 -> columns 32j .. 32j + 31
+#pragma unroll
+          for (int kk = 0; kk < DI / 32; ++kk)   // K = 32 E5M2 (32 B) per MMA
+            mma_f8f6f4(tmem + (uint32_t)(acc * 2 * HI + j * HI), smem_desc(ka + j * kHalfKeys * DI + kk * 32, 16, 1024),
+                       smem_desc(qa + kk * 32, 16, 1024), kIdesc, kk > 0 ? 1u : 0u);
         mma_commit(&S.tile_empty[st]);
         mma_commit(&S.accfull[acc]);
       }
       mma_commit(&S.mma_done);
       mbar_wait(&S.mma_done, 0);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------------------ dequant
     // thread = key row of the tile: 64 code bytes + 4 scale bytes -> 128
     // E5M2 bytes code x 2^(E - Emax); Emax goes to the epilogue
-    const int r = threadIdx.x - 6 * 32;   // 0..255
+    const int r = threadIdx.x - kDeqWarp0 * 32;   // 0..255
     Ring<kRaw> rr;
     Ring<kTiles> tr;
     Ring<kExpSlots> er;
@@ -418,9 +377,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int s = rr.slot, st = tr.slot;
       if (!mbar_wait(&S.raw_full[s], rr.phase)) { abort_of(S) = 1; break; }
       const uint8_t *src = raw + (size_t)s * kRawBytes;
+      // block q of the row: 16-byte chunk q ^ ((r >> 1) & 3) (64B swizzle)
       uint4 c[4];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const uint4 *>(src + r * (DI / 2) + q * 16);
+      for (int q = 0; q < 4; ++q)
+        c[q] = *reinterpret_cast<const uint4 *>(src + r * (DI / 2) + ((q ^ ((r >> 1) & 3)) << 4));
       const uint32_t sc = *reinterpret_cast<const uint32_t *>(src + kRawCodes + r * 4);
       mbar_arrive(&S.raw_empty[s]);
       const int emax = row_emax(sc);
@@ -444,11 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    // warp = TMEM lane quarter q (all 32 heads, lane = head): keys 64q..64q+63
+    // warp = TMEM lane quarter q: keys 32q + lane and 128 + 32q + lane
     const int quad = warp & 3;
     int prev_b = -1;
     int32_t nv = 0;
-    float wq = 0.0f;
+    float wv[HI];
     TileCursor cur(it0, a.tiles_per_seq);
     Ring<kAcc> ar;
     Ring<kExpSlots> er;
@@ -456,60 +417,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (abort_of(S)) break;
       const int b = cur.b, t = cur.t;
       if (b != prev_b) {
-        wq = __ldg(a.w + (int64_t)b * HI + lane);
+#pragma unroll
+        for (int h = 0; h < HI; ++h) wv[h] = __ldg(a.w + (int64_t)b * HI + h);
         nv = clamp_nvis_fp4(a.n_vis, b, a.n_max);
         prev_b = b;
       }
       const int acc = ar.slot;
       if (!mbar_wait(&S.exp_full[er.slot], er.phase)) { abort_of(S) = 1; break; }
-      const int kq = quad * 64 + 2 * lane;   // this lane's two keys after the reduction
-      const float f0 = exp2i(S.row_exp[er.slot][kq]), f1 = exp2i(S.row_exp[er.slot][kq + 1]);
+      const int k0 = quad * 32 + lane;
+      const float f0 = exp2i(S.row_exp[er.slot][k0]), f1 = exp2i(S.row_exp[er.slot][kHalfKeys + k0]);
       if (!mbar_wait(&S.accfull[acc], ar.phase)) { abort_of(S) = 1; break; }
       tc_fence_after();
       uint32_t v0[32], v1[32];
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kKeys + quad * 64);
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * 2 * HI);
       tmem_ld32(taddr, v0);
-      tmem_ld32(taddr + 32, v1);
+      tmem_ld32(taddr + HI, v1);
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&S.accempty[acc]);
-      float x[64];
+      float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        x[c] = wq * fmaxf(__uint_as_float(v0[c]), 0.0f);
-        x[c + 32] = wq * fmaxf(__uint_as_float(v1[c]), 0.0f);
+      for (int h = 0; h < HI; ++h) {
+        s0 = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), s0);
+        s1 = fmaf(wv[h], fmaxf(__uint_as_float(v1[h]), 0.0f), s1);
       }
-      float s0, s1;
-      transpose_reduce64(x, lane, s0, s1);
-      s0 *= f0;
-      s1 *= f1;
       float *srow = a.scores + (int64_t)b * a.row_len;
-      const int64_t slot = (int64_t)t * kKeys + kq;
-      if (!kPool) {
-        const bool ok0 = slot < nv, ok1 = slot + 1 < nv;
-        const float o0 = ok0 ? s0 : -INFINITY, o1 = ok1 ? s1 : -INFINITY;
-        *reinterpret_cast<float2 *>(srow + slot) = make_float2(o0, o1);
-        if (a.block_scores) {
-          // lanes 4j..4j+3 hold the 8 keys of block slot / 8
-          float bv;
-          if (a.block_reduce == 0) {
-            bv = fmaxf(o0, o1);
-            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 1));
-            bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 2));
-          } else {
-            bv = (ok0 ? s0 : 0.0f) + (ok1 ? s1 : 0.0f);
-            bv += __shfl_xor_sync(0xffffffffu, bv, 1);
-            bv += __shfl_xor_sync(0xffffffffu, bv, 2);
-            if ((slot & ~int64_t(BLOCK - 1)) >= nv) bv = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float sc = (j ? s1 : s0) * (j ? f1 : f0);
+        const int64_t slot = (int64_t)t * kKeys + j * kHalfKeys + k0;
+        if (!kPool) {
+          const bool ok = slot < nv;
+          const float o = ok ? sc : -INFINITY;
+          srow[slot] = o;
+          if (a.block_scores) {
+            // lanes 8i..8i+7 hold the keys of block slot / 8
+            float bv;
+            if (a.block_reduce == 0) {
+              bv = o;
+              bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 1));
+              bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 2));
+              bv = fmaxf(bv, __shfl_xor_sync(0xffffffffu, bv, 4));
+            } else {
+              bv = ok ? sc : 0.0f;
+              bv += __shfl_xor_sync(0xffffffffu, bv, 1);
+              bv += __shfl_xor_sync(0xffffffffu, bv, 2);
+              bv += __shfl_xor_sync(0xffffffffu, bv, 4);
+              if ((slot & ~int64_t(BLOCK - 1)) >= nv) bv = -INFINITY;
+            }
+            const int64_t blk = slot / BLOCK;
+            if ((lane & 7) == 0 && blk < a.nblk_stride) a.block_scores[(int64_t)b * a.nblk_stride + blk] = bv;
           }
-          const int64_t blk = slot / BLOCK;
-          if ((lane & 3) == 0 && blk < a.nblk_stride) a.block_scores[(int64_t)b * a.nblk_stride + blk] = bv;
+        } else if (slot < a.row_len) {   // pool_nb * 8 slots
+          const int32_t blk = __ldg(a.pool + (int64_t)b * a.pool_nb + slot / BLOCK);
+          const int64_t pos = (int64_t)blk * BLOCK + (slot & (BLOCK - 1));
+          srow[slot] = (blk >= 0 && pos < nv) ? sc : -INFINITY;
         }
-      } else if (slot < a.row_len) {   // pool_nb * 8 slots: whole blocks, so both keys exist
-        const int32_t blk = __ldg(a.pool + (int64_t)b * a.pool_nb + slot / BLOCK);
-        const int64_t pos = (int64_t)blk * BLOCK + (slot & (BLOCK - 1));
-        const bool ok0 = blk >= 0 && pos < nv, ok1 = blk >= 0 && pos + 1 < nv;
-        *reinterpret_cast<float2 *>(srow + slot) = make_float2(ok0 ? s0 : -INFINITY, ok1 ? s1 : -INFINITY);
       }
     }
   }
@@ -542,8 +505,8 @@ cudaError_t launch_indexer_q_fp4(const void *q, const float *w, int64_t rows, vo
   return cudaGetLastError();
 }
 
-cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_q, const SweepArgs &a, int num_sms, cudaStream_t stream,
-                                     int *launches) {
+cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
+                                     int num_sms, cudaStream_t stream, int *launches) {
   const int64_t total = (int64_t)a.batch * a.tiles_per_seq;
   if (total <= 0) return cudaSuccess;
   const int grid = (int)(total < num_sms ? total : num_sms);
@@ -554,12 +517,12 @@ cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_q, const SweepArgs &a
     err = cudaFuncSetAttribute(indexer_sweep_fp4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    indexer_sweep_fp4_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
+    indexer_sweep_fp4_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
   } else {
     err = cudaFuncSetAttribute(indexer_sweep_fp4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    indexer_sweep_fp4_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_q, a);
+    indexer_sweep_fp4_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
   }
   ++*launches;
   err = cudaGetLastError();

@@ -86,17 +86,18 @@ struct SweepArgs {
   int32_t pool_nb;
   int32_t nblk_stride;        // ceil(n_max / 8)
   int32_t block_reduce;       // 0 max, 1 sum
-  const uint8_t *k_codes;     // MXFP4 sweep: the code plane [k_rows][64]
   const uint8_t *k_scales;    // MXFP4 sweep: the scale plane [k_rows][4]
   int64_t k_rows;             // MXFP4 sweep: rows of the planes (batch * cap)
 };
 
 cudaError_t launch_indexer_sweep(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
                                  int num_sms, cudaStream_t stream, int *launches);
-// MXFP4 indexer: the planes through a.k_codes / a.k_scales, tm_q over the
-// queries' E5M2 rows (bytes [batch * 32][128], 128B swizzle, boxes of 32 rows).
-cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_q, const SweepArgs &a, int num_sms, cudaStream_t stream,
-                                     int *launches);
+// MXFP4 indexer: tm_k over the code plane (bytes [k_rows][64], 64B swizzle,
+// boxes of FP4_SWEEP_TILE rows, or of 8 rows for a pool), the scales through
+// a.k_scales, tm_q over the queries' E5M2 rows (bytes [batch * 32][128], 128B
+// swizzle, boxes of 32 rows).
+cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
+                                     int num_sms, cudaStream_t stream, int *launches);
 cudaError_t launch_indexer_k_quant(const void *k, int64_t n, const int64_t *slot, uint8_t *k_fp4, int64_t rows,
                                    cudaStream_t stream);
 // The queries' MXFP4 values as E5M2 bytes [rows][128] (code x 2^(E - Emax) per
@@ -107,7 +108,9 @@ cudaError_t launch_indexer_q_fp4(const void *q, const float *w, int64_t rows, vo
 // Single-kernel top-K with one thread-block cluster per row (no scratch);
 // for k <= 2048.
 bool topk_cluster_supported(const TopkRows &r);
-cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches);
+// profiled: record the CSA2_KERNEL_TOPK events (the indexer's top-K), not for
+// the HSI pool selection.
+cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled = true);
 
 // Chunked prefill: multi-query indexer over the causally visible entries.
 struct PrefillIdxArgs {
@@ -130,6 +133,10 @@ cudaError_t launch_prefill_indexer(const CUtensorMap &tm_k, const CUtensorMap &t
 
 size_t topk_scratch_bytes(int32_t rows, int64_t row_len, int32_t k);
 TopkScratch carve_topk_scratch(void *base, int32_t rows, int64_t row_len, int32_t k);
+// The HSI pool selection: for k <= 2048 the cluster top-K over a copy of the
+// rows with the forced block set to +inf (in `scratch`, which must hold
+// topk_scratch_bytes(rows, row_len, k)); the multi-pass top-K above that.
+cudaError_t launch_pool_topk(const TopkRows &r, void *scratch, int num_sms, cudaStream_t stream, int *launches);
 cudaError_t launch_topk(const TopkRows &r, const TopkScratch &s, int num_sms, cudaStream_t stream, int *launches);
 
 struct AttnArgs {

@@ -78,8 +78,7 @@ extern "C" csa2_status csa2_hier_pool_select_static(const float *block_scores, c
   r.pool = nullptr;
   r.pool_stride = 0;
   r.out = pool_blocks;
-  const TopkScratch s = carve_topk_scratch(scratch, batch, nblk, r.k);
   int launches = 0;
-  const cudaError_t e = launch_topk(r, s, 0, reinterpret_cast<cudaStream_t>(stream), &launches);
+  const cudaError_t e = launch_pool_topk(r, scratch, 0, reinterpret_cast<cudaStream_t>(stream), &launches);
   return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
 }

@@ -135,16 +135,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void *dst, const void *tmap, in
       : "memory");
 }
 
-// bulk_g2s under an L2 cache policy.
-__device__ __forceinline__ void bulk_g2s_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
-                                              uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
-          "r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-
 // L2 policy: lines loaded under it are the first to be evicted (data read
 // once, streamed past what should stay resident).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {

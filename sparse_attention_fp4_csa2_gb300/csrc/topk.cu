@@ -18,7 +18,8 @@
 //      (through the HSI pool for Reindex rows), sorted ascending and written,
 //      -1 padded.
 // Rows are streamed once by passes 1 and 2 (4 B per position each, against
-// the sweep's 256 B).
+// the sweep's 256 B).  The HSI pool (k <= 2048) goes to the cluster top-K
+// instead (launch_pool_topk); this path serves larger pools.
 #include "kernels.cuh"
 
 namespace csa2 {
@@ -327,7 +328,41 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(const TopkRows
   for (int i = threadIdx.x; i < r.k; i += kFinThreads) out[i] = (i < (int)n_final) ? list[i] : -1;
 }
 
+// Rows of block scores with the forced block set to +inf, padded with -inf
+// to `stride` (a multiple of 4) values: the input of the cluster top-K.
+__global__ void __launch_bounds__(256) pool_force_copy_kernel(const TopkRows r, float *dst, int64_t stride) {
+  const int row = blockIdx.y;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= stride) return;
+  const uint32_t force = row_force_index(r, row);
+  float v = -INFINITY;
+  if (i < r.row_len) v = (uint32_t)i == force ? INFINITY : __ldg(r.vals + (int64_t)row * r.row_stride + i);
+  dst[(int64_t)row * stride + i] = v;
+}
+
 }  // namespace
+
+cudaError_t launch_pool_topk(const TopkRows &r, void *scratch, int num_sms, cudaStream_t stream, int *launches) {
+  if (r.rows <= 0) return cudaSuccess;
+  if (r.k > 2048) return launch_topk(r, carve_topk_scratch(scratch, r.rows, r.row_len, r.k), num_sms, stream, launches);
+  // the cluster top-K over a forced copy (rows x stride floats fit in the
+  // scratch: topk_scratch_bytes holds 8 B per value plus 8 KB per row)
+  const int64_t stride = (r.row_len + 3) & ~int64_t(3);
+  float *copy = static_cast<float *>(scratch);
+  if (stride > 0) {
+    dim3 grid((unsigned)((stride + 255) / 256), (unsigned)r.rows);
+    pool_force_copy_kernel<<<grid, 256, 0, stream>>>(r, copy, stride);
+    ++*launches;
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  TopkRows c = r;
+  c.vals = copy;
+  c.row_len = stride;
+  c.row_stride = stride;
+  c.force_nvis = nullptr;
+  return launch_topk_cluster(c, stream, launches, /*profiled*/ false);
+}
 
 size_t topk_scratch_bytes(int32_t rows, int64_t row_len, int32_t k) {
   size_t b = 0;

@@ -483,7 +483,7 @@ bool topk_cluster_supported(const TopkRows &r) {
          (reinterpret_cast<uintptr_t>(r.vals) & 15u) == 0;
 }
 
-cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches) {
+cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled) {
   if (r.rows <= 0) return cudaSuccess;
   if (!topk_cluster_supported(r)) return cudaErrorInvalidValue;
   static int max_cluster = 0;
@@ -522,7 +522,8 @@ cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *lau
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const ProfileEvents &pe = profile_events(CSA2_KERNEL_TOPK);
+  static const ProfileEvents kNone;
+  const ProfileEvents &pe = profiled ? profile_events(CSA2_KERNEL_TOPK) : kNone;
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
   err = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, r);
   if (err != cudaSuccess) return err;
