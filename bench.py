@@ -107,13 +107,24 @@ def parse():
     return ap.parse_args()
 
 
+def kv_write_bytes(m):
+    """One new entry: m source latents (+ m compression logits at m = 2) in,
+    the 288 B entry out, position and slot."""
+    return m * 1024 + (m * 1024 if m == 2 else 0) + 288 + 16
+
+
+SWA_ATTN_BYTES = ATTN_BYTES - 512 * 288 - 512 * 4   # a SWA-only layer: no selected entries
+
+
 def algorithmic_bytes(cfg, hsi, fp4=False):
-    B, N, kb = cfg.batch, cfg.n_ctx, K_BYTES[fp4]
-    total = B * KVW_BYTES + (B * (256 + 68) if fp4 else 0)    # + the new indexer-K entry
+    B, E, kb = cfg.batch, cfg.n_ctx // cfg.m, K_BYTES[fp4]
+    total = 0
     for m in cfg.schedule:
-        total += B * ATTN_BYTES
+        total += B * (SWA_ATTN_BYTES if m == "swa" else ATTN_BYTES)
         if m == "full":
-            total += B * (kb * N + SWEEP_FIXED + 512 * 4)
+            # the copy's new entry (and its MXFP4 indexer-K entry), then the sweep
+            total += B * (kv_write_bytes(cfg.m) + (256 + 68 if fp4 else 0))
+            total += B * (kb * E + SWEEP_FIXED + 512 * 4)
         elif m == "reindex":
             total += B * (REINDEX_BYTES - 16384 * (256 - kb))
     return total
@@ -179,44 +190,64 @@ class Workload:
         import synth
         import sparse_attention_fp4_csa2_gb300 as c2
         self.c2, self.cfg, self.dev = c2, cfg, device
-        B, N = cfg.batch, cfg.n_ctx
-        self.B, self.N = B, N
+        B, N, m = cfg.batch, cfg.n_ctx, cfg.m
+        # m = 2: the context's N tokens are E = N / 2 entries and the step's
+        # token completes entry E - 1; every Full layer keeps its own copy
+        E = N // m
+        self.B, self.N, self.m, self.E = B, N, m, E
+        self.copies = max(1, sum(x == "full" for x in cfg.schedule))
         self.hsi = 1 if cfg.hsi else 0
         self.fp4 = INDEXER_FP4
         self.params = c2.Params.make(hsi=self.hsi, attn_kernel=ATTN_KERNEL, indexer_fp4=int(self.fp4))
         seed = cfg.layer_seeds[0]
-        # context: latents -> FP4 main KV with this library's writer; indexer K bf16
-        self.kv = torch.empty(B, N, 288, dtype=torch.uint8, device=device)
-        chunk = max(1, (1 << 22) // N)       # sequences per writer call (bounded temporary)
-        for b0 in range(0, B, chunk):
-            nb = min(chunk, B - b0)
-            lat = synth.context_latent(seed * 977 + b0, nb, N, device=device)
-            pos = torch.arange(N, dtype=torch.int64, device=device).repeat(nb)
-            slot = torch.arange(b0 * N, (b0 + nb) * N, dtype=torch.int64, device=device)
-            c2.kv_quant_write(lat.reshape(nb * N, 512), None, 1, pos, slot, self.kv.view(B * N, 288))
-            del lat
-        self.k_idx = synth.indexer_keys(seed, B, N, device=device)
-        if cfg.planted_blocks:
-            li0 = synth.layer_inputs(cfg.layer_seeds[0], B, device=device)
-            synth.plant_blocks(self.k_idx, li0.q_idx, li0.w, N, cfg.planted_blocks, seed)
+        # context: latents (pairs and logits at m = 2) -> FP4 main KV with this
+        # library's writer; indexer K bf16 (or MXFP4 through its writer)
+        self.kv, self.k_idx, self.new_in = [], [], []
+        chunk = max(1, (1 << 22) // (E * m))   # sequences per writer call (bounded temporary)
+        for c in range(self.copies):
+            cs = seed + 101 * c
+            kv = torch.empty(B, E, 288, dtype=torch.uint8, device=device)
+            for b0 in range(0, B, chunk):
+                nb = min(chunk, B - b0)
+                lat = synth.context_latent(cs * 977 + b0, nb, E, device=device, m=m)
+                z = synth.compression_logits(cs * 991 + b0, nb, E, device=device, m=m) if m == 2 else None
+                pos = (torch.arange(E, dtype=torch.int64, device=device) * m + (m - 1)).repeat(nb)
+                slot = torch.arange(b0 * E, (b0 + nb) * E, dtype=torch.int64, device=device)
+                c2.kv_quant_write(lat.reshape(nb * E, m, 512) if m == 2 else lat.reshape(nb * E, 512),
+                                  z.reshape(nb * E, m, 512) if m == 2 else None, m, pos, slot, kv.view(B * E, 288))
+                del lat, z
+            k = synth.indexer_keys(cs, B, E, device=device)
+            if cfg.planted_blocks and c == 0:
+                li0 = synth.layer_inputs(cfg.layer_seeds[0], B, device=device)
+                synth.plant_blocks(k, li0.q_idx, li0.w, E, cfg.planted_blocks, seed)
+            if self.fp4:
+                # the same keys through this library's MXFP4 writer; every
+                # Full layer also writes its new token's entry
+                kf = c2.indexer_k_fp4_cache(B * E, device=device)
+                c2.indexer_k_quant(k.view(B * E, 128), torch.arange(B * E, device=device), kf)
+                k = kf
+            self.kv.append(kv)
+            self.k_idx.append(k)
+            # the new entry's inputs: its latent (m = 1) or the completed pair
+            # and its logits (m = 2), and its indexer key (MXFP4 only)
+            new = {"latent": synth.normal((B, m, 512) if m == 2 else (B, 512), cs + 7, 0, device)}
+            if m == 2:
+                new["z"] = synth.normal((B, m, 512), cs + 9, 0, device)
+            if self.fp4:
+                new["k"] = synth.normal((B, 128), cs + 11, 0, device)
+            self.new_in.append(new)
         if self.fp4:
-            # the same keys through this library's MXFP4 writer; every step
-            # also writes the new token's entry
-            self.k_fp4 = c2.indexer_k_fp4_cache(B * N, device=device)
-            c2.indexer_k_quant(self.k_idx.view(B * N, 128), torch.arange(B * N, device=device), self.k_fp4)
-            self.k_idx = self.k_fp4
-            self.new_k = synth.normal((B, 128), seed + 11, 0, device)
             self.PROFILED = ((0, "indexer_sweep_fp4_kernel"), (3, "topk_cluster_kernel"), (1, "sparse_attn_kernel"))
         self.layers = [synth.layer_inputs(s, B, device=device) for s in cfg.layer_seeds]
-        self.new_latent = synth.normal((B, 512), seed + 7, 0, device)
-        self.new_pos = torch.full((B,), N - 1, dtype=torch.int64, device=device)
-        self.new_slot = torch.arange(B, dtype=torch.int64, device=device) * N + (N - 1)
-        self.n_vis = torch.full((B,), N, dtype=torch.int32, device=device)
+        self.new_pos = torch.full((B,), (E - 1) * m + (m - 1), dtype=torch.int64, device=device)
+        self.new_slot = torch.arange(B, dtype=torch.int64, device=device) * E + (E - 1)
+        self.n_vis = torch.full((B,), E, dtype=torch.int32, device=device)
         self.topk = torch.zeros(B, 512, dtype=torch.int32, device=device)
+        self.topk_none = torch.full((B, 512), -1, dtype=torch.int32, device=device)   # SWA-only layers
         self.pool = torch.zeros(B, 2048, dtype=torch.int32, device=device)
         self.out = torch.empty(len(cfg.schedule), B, 64, 512, device=device)
         self.lse = torch.empty(len(cfg.schedule), B, 64, device=device)
-        self.ws = c2.workspace(c2.OP_DECODE, B, N, self.params, device=device)
+        self.ws = c2.workspace(c2.OP_DECODE, B, E, self.params, device=device)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
@@ -231,25 +262,27 @@ class Workload:
     def rooflines(self, launch_ms, peaks_):
         """HBM rooflines of the Full layer's indexer sweep and top-K and of one
         layer's sparse attention (launch_ms: kernel name -> ms per launch)."""
-        sch, B, N, wl = self.cfg.schedule, self.B, self.N, self.cfg.name
+        sch, B, E, wl = self.cfg.schedule, self.B, self.E, self.cfg.name
         n_full = sum(m == "full" for m in sch)
+        n_attn = sum(m != "swa" for m in sch)   # layers with a top-K (the profiled launch's shape)
         out = []
         sweep = self.PROFILED[0][1]
         if launch_ms.get(sweep) and n_full:
-            out.append(roof_entry(sweep, wl, "hbm", B * (K_BYTES[self.fp4] * N + SWEEP_FIXED),
+            out.append(roof_entry(sweep, wl, "hbm", B * (K_BYTES[self.fp4] * E + SWEEP_FIXED),
                                   launch_ms[sweep], n_full, peaks_))
         if launch_ms.get("topk_cluster_kernel") and n_full:
-            out.append(roof_entry("topk_cluster_kernel", wl, "hbm", B * (4 * N + 4 * 512),
+            out.append(roof_entry("topk_cluster_kernel", wl, "hbm", B * (4 * E + 4 * 512),
                                   launch_ms["topk_cluster_kernel"], n_full, peaks_))
         if launch_ms.get("sparse_attn_kernel"):
             out.append(roof_entry("sparse_attn_kernel", wl, "hbm", B * ATTN_BYTES,
-                                  launch_ms["sparse_attn_kernel"], len(sch), peaks_))
+                                  launch_ms["sparse_attn_kernel"], n_attn, peaks_))
         return out
 
     def config(self, ms):
         step_bytes = algorithmic_bytes(self.cfg, self.hsi, self.fp4)
         ik = "MXFP4 indexer K and Q" if self.fp4 else "bf16 indexer K"
-        return {"workload": self.cfg.name, "batch": self.B, "context": self.N, "layers": "+".join(self.cfg.schedule),
+        return {"workload": self.cfg.name, "batch": self.B, "context": self.N, "m": self.m, "entries": self.E,
+                "cache_copies": self.copies, "layers": "+".join(self.cfg.schedule),
                 "hsi": bool(self.hsi), "storage": f"FP4 E2M1+E4M3/16 main KV, {ik}, E4M3 SWA",
                 "step_alg_bytes": step_bytes, "step_hbm_gbs": round(step_bytes / (ms / 1e3) / 1e9, 1)}
 
@@ -259,36 +292,43 @@ class Workload:
         one layer's attention launch (the first Reuse layer's, else the last
         layer's) are bracketed by those events; with io (a HostIO), every
         layer's inputs arrive from pinned host memory on a copy stream and its
-        outputs go back on another while later layers compute."""
-        c2, L = self.c2, self.layers
+        outputs go back on another while later layers compute.  A Full layer
+        first writes its cache copy's new entry; a SWA-only layer attends to
+        its window alone (no selected entries)."""
+        c2, L, m = self.c2, self.layers, self.m
         launches = 0
         if io:
             io.start()
-            io.wait_in(0)
-        c2.kv_quant_write(self.new_latent, None, 1, self.new_pos, self.new_slot, self.kv.view(-1, 288))
-        launches += c2.last_launch_count()
-        if self.fp4:
-            c2.indexer_k_quant(self.new_k, self.new_slot, self.k_fp4)
-            launches += c2.last_launch_count()
+        copy = -1
         for i, mode in enumerate(self.cfg.schedule):
             if io:
                 io.wait_in(i)
             li = L[i]
-            idx_args = {} if mode == "reuse" else dict(q_idx=li.q_idx, w=li.w, k_idx=self.k_idx)
+            if mode == "full":
+                copy += 1
+                new = self.new_in[copy]
+                c2.kv_quant_write(new["latent"], new.get("z"), m, self.new_pos, self.new_slot,
+                                  self.kv[copy].view(-1, 288))
+                launches += c2.last_launch_count()
+                if self.fp4:
+                    c2.indexer_k_quant(new["k"], self.new_slot, self.k_idx[copy])
+                    launches += c2.last_launch_count()
+            cc = max(copy, 0)
+            idx_args = {} if mode in ("reuse", "swa") else dict(q_idx=li.q_idx, w=li.w, k_idx=self.k_idx[cc])
             on = []
             if prof:
                 sch = self.cfg.schedule
                 if "full" in sch and i == sch.index("full"):
                     on += [c2.KERNEL_INDEXER_SWEEP, c2.KERNEL_TOPK]
-                reuse = [j for j, m in enumerate(sch) if m == "reuse"]
+                reuse = [j for j, x in enumerate(sch) if x == "reuse"]
                 if i == (reuse[0] if reuse else len(sch) - 1):
                     on.append(c2.KERNEL_SPARSE_ATTN)
                 on = [k for k in on if k in prof]
                 for k in on:
                     c2.set_profile_events(k, *prof[k])
-            c2.sparse_decode(mode, self.params, li.q, self.kv, self.n_vis, self.N, li.swa, li.swa_scale,
-                             li.swa_len, self.topk, self.out[i], self.ws, pool_blocks=self.pool,
-                             lse=self.lse[i], **idx_args)
+            c2.sparse_decode("reuse" if mode == "swa" else mode, self.params, li.q, self.kv[cc], self.n_vis, self.E,
+                             li.swa, li.swa_scale, li.swa_len, self.topk_none if mode == "swa" else self.topk,
+                             self.out[i], self.ws, pool_blocks=self.pool, lse=self.lse[i], **idx_args)
             for k in on:
                 c2.set_profile_events(k, None, None)
             launches += c2.last_launch_count()
@@ -300,12 +340,15 @@ class Workload:
 
     def io_groups(self):
         """Per layer: the tensors it reads that a caller supplies every step
-        (the new token's latent goes with layer 0), and the ones it returns."""
+        (a Full layer's new entry inputs go with it), and the ones it returns."""
         ins, outs = [], []
+        copy = -1
         for i, (li, m) in enumerate(zip(self.layers, self.cfg.schedule)):
-            g = ([self.new_latent] + ([self.new_k] if self.fp4 else []) if i == 0 else []) + [li.q, li.swa,
-                                                                                            li.swa_scale]
-            if m != "reuse":
+            g = [li.q, li.swa, li.swa_scale]
+            if m == "full":
+                copy += 1
+                g = list(self.new_in[copy].values()) + g
+            if m in ("full", "reindex"):
                 g += [li.q_idx, li.w]
             ins.append(g)
             outs.append([self.out[i], self.lse[i]])
@@ -636,40 +679,55 @@ class HostIO:
 
 def cpu_baseline(args, cfg, seconds=12.0):
     """The oracle, as it stands, on the host cores: whole decode steps of
-    single sequences of the same workload until ~`seconds` elapse."""
+    single sequences of the same workload until ~`seconds` elapse (each cache
+    copy's context drawn outside the timed region)."""
     import numpy as np
-    import torch
 
     import oracle
     import synth
     oracle.build()
-    B, N = cfg.batch, cfg.n_ctx
+    B, m = cfg.batch, cfg.m
+    E = cfg.n_ctx // m
     seed = cfg.layer_seeds[0]
+    copies = max(1, sum(x == "full" for x in cfg.schedule))
     fp4 = getattr(args, "indexer_fp4", False)
     layers = [synth.layer_inputs(s, 1) for s in cfg.layer_seeds]
+    no_rows = np.zeros((0, 288), np.uint8)
     done, t_total, b = 0, 0.0, 0
     while b < B and (t_total < seconds or done == 0):
-        k = synth.indexer_keys(seed * 31 + b, 1, N)[0]
-        lat = synth.context_latent(seed * 37 + b, 1, N)[0]
-        kq = oracle.mxfp4_quantise(k) if fp4 else None      # the cached MXFP4 entries
+        ctx = []
+        for c in range(copies):
+            cs = seed + 101 * c
+            k = synth.indexer_keys(cs * 31 + b, 1, E)[0]
+            lat = synth.context_latent(cs * 37 + b, 1, E, m=m)[0]
+            z = synth.compression_logits(cs * 41 + b, 1, E, m=m)[0] if m == 2 else None
+            kq = oracle.mxfp4_quantise(k) if fp4 else None      # the cached MXFP4 entries
+            ctx.append((k, lat, z, kq))
         t0 = time.perf_counter()
         sel = pool = None
+        copy = -1
         for i, mode in enumerate(cfg.schedule):
             li = layers[i]
+            if mode == "swa":
+                oracle.sparse_attn(li.q[0], no_rows, np.arange(0), li.swa[0], li.swa_scale[0], 128)
+                continue
+            if mode == "full":
+                copy += 1
+            k, lat, z, kq = ctx[max(copy, 0)]
             if mode == "full":
                 s = (oracle.index_scores_mxfp4(li.q_idx[0], li.w[0], *kq) if fp4
                      else oracle.index_scores(li.q_idx[0], li.w[0], k))
                 sel = oracle.topk(s, 512)
                 if cfg.hsi:
-                    pool = oracle.hsi_pool(s, N, 8, 2048)
+                    pool = oracle.hsi_pool(s, E, 8, 2048)
             elif mode == "reindex" and fp4:
-                pos = oracle.pool_positions(pool, N)
+                pos = oracle.pool_positions(pool, E)
                 sp = oracle.topk(oracle.index_scores_mxfp4(li.q_idx[0], li.w[0], kq[0][pos], kq[1][pos]), 512)
                 sel = np.where(sp >= 0, pos[np.clip(sp, 0, None)], -1)
             elif mode == "reindex":
-                sel = oracle.reindex_topk(li.q_idx[0], li.w[0], k, pool, N, 512)
+                sel = oracle.reindex_topk(li.q_idx[0], li.w[0], k, pool, E, 512)
             valid = sel[sel >= 0]
-            rows = oracle.kv_entries(lat[valid], None, 1, valid)
+            rows = oracle.kv_entries(lat[valid], z[valid] if m == 2 else None, m, valid * m + m - 1)
             oracle.sparse_attn(li.q[0], rows, np.arange(len(valid)), li.swa[0], li.swa_scale[0], 128)
         t_total += time.perf_counter() - t0
         done += 1

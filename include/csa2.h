@@ -89,6 +89,10 @@ csa2_params csa2_default_params(void);
  * scales (scale g covers channels 16g..16g+15).  = 288. */
 int32_t csa2_entry_bytes(void);
 
+/* Bytes of one indexer-K entry: 256 (bf16, 128 dims) or, with fp4 != 0, 68
+ * (MXFP4: 64 B of E2M1 codes and 4 UE8M0 scale bytes, [A] 3.1). */
+int32_t csa2_indexer_entry_bytes(int32_t fp4);
+
 /*
  * csa2_kv_quant_write -- write new main-KV entries ([A] 2.4.4 "quantized after
  * RoPE"; [N] section 4; the compressor of [A] 2.3.1 at m = 2).

@@ -64,6 +64,7 @@ def lib():
         PP = ctypes.POINTER(Params)
         L.csa2_default_params.argtypes, L.csa2_default_params.restype = [], Params
         L.csa2_entry_bytes.argtypes, L.csa2_entry_bytes.restype = [], i32
+        L.csa2_indexer_entry_bytes.argtypes, L.csa2_indexer_entry_bytes.restype = [i32], i32
         L.csa2_last_launch_count.argtypes, L.csa2_last_launch_count.restype = [], i32
         L.csa2_status_string.argtypes, L.csa2_status_string.restype = [ctypes.c_int], ctypes.c_char_p
         L.csa2_workspace_bytes.argtypes, L.csa2_workspace_bytes.restype = [ctypes.c_int, i32, i64, PP], sz
@@ -114,6 +115,10 @@ def default_params() -> Params:
 
 def entry_bytes() -> int:
     return lib().csa2_entry_bytes()
+
+
+def indexer_entry_bytes(fp4: bool = False) -> int:
+    return lib().csa2_indexer_entry_bytes(int(bool(fp4)))
 
 
 def last_launch_count() -> int:

@@ -321,6 +321,8 @@ csa2_status csa2_set_profile_events(csa2_kernel kernel, void *start, void *stop)
   return CSA2_OK;
 }
 
+int32_t csa2_indexer_entry_bytes(int32_t fp4) { return fp4 ? DI / 2 + DI / 32 : DI * 2; }
+
 const char *csa2_status_string(csa2_status s) {
   switch (s) {
     case CSA2_OK: return "ok";

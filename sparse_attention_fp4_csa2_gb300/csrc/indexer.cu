@@ -18,8 +18,7 @@
 // CUDA-core FMA rate.
 //
 // Persistent, warp-specialised CTA (one per SM): warp 0 issues TMA loads of
-// the K tiles into a ring of shared-memory stages (a lane per pool block in a
-// Reindex tile), warp 1 issues the MMAs into
+// the K tiles into a ring of shared-memory stages, warp 1 issues the MMAs into
 // two TMEM accumulators, warps 2-5 drain the accumulators.  Every CTA owns a
 // contiguous run of (sequence, tile) work items.
 #include "pipeline.cuh"
@@ -117,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t total = (int64_t)a.batch * a.tiles_per_seq;
   const int64_t it0 = total * blockIdx.x / gridDim.x;
-  const int n_tiles = (int)(total * (blockIdx.x + 1) / gridDim.x - it0);
+  const int64_t it1 = total * (blockIdx.x + 1) / gridDim.x;
+  const int n_tiles = (int)(it1 - it0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -147,49 +147,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    // lane 0 drives the rings and loads a Full tile; in a pool tile
-    // (Reindex) lane j fetches pool block j and its 8 rows.  K rows are read
-    // once: evict them first, so that the scores this kernel writes stay in
-    // L2 for the top-K that reads them next.
-    const uint64_t pol = l2_policy_evict_first();
-    int prev_b = -1, q_issued = 0;
-    int32_t nv = 0;
-    int n_issued = 0;
-    TileCursor cur(it0, a.tiles_per_seq);
-    Ring<kStages> kr;
-    for (int li = 0; li < n_tiles; ++li, cur.next(), kr.next()) {
-      const int b = cur.b, t = cur.t;
-      int ok = 1;
-      if (b != prev_b) {
-        if (lane == 0) {
-          const int qs = q_issued & 1;
-          if (q_issued > 0 && abort_flag(S)) {
-            ok = 0;
-          } else if (!mbar_wait(&S.qempty[qs], ((q_issued >> 1) & 1) ^ 1)) {
-            abort_flag(S) = 1;
-            ok = 0;
-          } else {
+    // Full tiles: lane 0 alone; pool tiles (Reindex): the whole warp, a lane
+    // per pool block
+    if (!kPool) {
+      if (lane == 0) {
+        // K rows are read once: evict them first, so that the scores this
+        // kernel writes stay in L2 for the top-K that reads them next
+        const uint64_t pol = l2_policy_evict_first();
+        int prev_b = -1, qi = -1;
+        int32_t nv = 0;
+        int64_t n_issued = 0;
+        for (int64_t it = it0; it < it1; ++it) {
+          const int b = (int)(it / a.tiles_per_seq);
+          const int t = (int)(it % a.tiles_per_seq);
+          if (b != prev_b) {
+            if (qi >= 0 && abort_flag(S)) break;
+            ++qi;
+            const int qs = qi & 1;
+            if (!mbar_wait(&S.qempty[qs], ((qi >> 1) & 1) ^ 1)) { abort_flag(S) = 1; break; }
             mbar_arrive_expect_tx(&S.qfull[qs], kQBytes);
             tma_load_2d(qbuf + qs * kQBytes, &tm_q, 0, b * HI, &S.qfull[qs]);
             tma_load_2d(qbuf + qs * kQBytes + kQBytes / 2, &tm_q, 64, b * HI, &S.qfull[qs]);
             nv = clamp_nvis(a.n_vis, b, a.n_max);
+            prev_b = b;
           }
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        nv = __shfl_sync(0xffffffffu, nv, 0);
-        ++q_issued;
-        prev_b = b;
-      }
-      const int s = kr.slot;
-      if (lane == 0 && !mbar_wait(&S.empty[s], kr.phase ^ 1)) {
-        abort_flag(S) = 1;
-        ok = 0;
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      uint8_t *dst = kbuf + (size_t)s * kTileBytes;
-      const int64_t row0 = (int64_t)b * a.cap;
-      if (!kPool) {
-        if (lane == 0) {
+          const int64_t li = it - it0;
+          const int s = (int)(li % kStages);
+          const uint32_t ph = (uint32_t)((li / kStages) & 1);
+          if (!mbar_wait(&S.empty[s], ph ^ 1)) { abort_flag(S) = 1; break; }
+          uint8_t *dst = kbuf + (size_t)s * kTileBytes;
+          const int64_t row0 = (int64_t)b * a.cap;
           if ((int64_t)t * SWEEP_TILE < nv) {
             mbar_arrive_expect_tx(&S.full[s], kTileBytes);
             tma_load_2d_hint(dst, &tm_k, 0, (int32_t)(row0 + (int64_t)t * SWEEP_TILE), &S.full[s], pol);
@@ -198,58 +185,108 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             mbar_arrive(&S.full[s]);
           }
+          ++n_issued;
         }
-      } else {
-        constexpr int kBlocks = SWEEP_TILE / BLOCK;   // pool blocks per tile
-        const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
-        const int32_t blk =
-            lane < kBlocks ? __ldg(a.pool + (int64_t)b * a.pool_nb + (int64_t)t * kBlocks + lane) : -1;
-        const bool v = blk >= 0 && blk < nblk_vis;
-        if (lane < kBlocks && !v && blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) set_error(CSA2_DEV_ERR_POOL);
-        const uint32_t valid = __ballot_sync(0xffffffffu, v);
-        if (valid) {
-          if (lane == 0) mbar_arrive_expect_tx(&S.full[s], (uint32_t)__popc(valid) * (BLOCK * DI * 2));
-          __syncwarp();
-          if (v) {
-            const int32_t y = (int32_t)(row0 + (int64_t)blk * BLOCK);
-            tma_load_2d_hint(dst + lane * 1024, &tm_k, 0, y, &S.full[s], pol);
-            tma_load_2d_hint(dst + kTileBytes / 2 + lane * 1024, &tm_k, 64, y, &S.full[s], pol);
+        // Drain: every load this thread issued has landed before the CTA can
+        // exit (returns at once unless a wait above gave up).
+        for (int s = 0; s < kStages && s < n_issued; ++s) {
+          const int64_t last = s + ((n_issued - 1 - s) / kStages) * kStages;
+          mbar_wait(&S.full[s], (uint32_t)((last / kStages) & 1));
+        }
+        if (qi >= 0) mbar_wait(&S.qfull[qi & 1], (qi >> 1) & 1);
+      }
+    } else {
+      // lane 0 drives the rings; lane j fetches pool block j and its 8 rows
+      const uint64_t pol = l2_policy_evict_first();
+      int prev_b = -1, q_issued = 0;
+      int32_t nv = 0;
+      int n_issued = 0;
+      TileCursor cur(it0, a.tiles_per_seq);
+      Ring<kStages> kr;
+      for (int li = 0; li < n_tiles; ++li, cur.next(), kr.next()) {
+        const int b = cur.b, t = cur.t;
+        int ok = 1;
+        if (b != prev_b) {
+          if (lane == 0) {
+            const int qs = q_issued & 1;
+            if (q_issued > 0 && abort_flag(S)) {
+              ok = 0;
+            } else if (!mbar_wait(&S.qempty[qs], ((q_issued >> 1) & 1) ^ 1)) {
+              abort_flag(S) = 1;
+              ok = 0;
+            } else {
+              mbar_arrive_expect_tx(&S.qfull[qs], kQBytes);
+              tma_load_2d(qbuf + qs * kQBytes, &tm_q, 0, b * HI, &S.qfull[qs]);
+              tma_load_2d(qbuf + qs * kQBytes + kQBytes / 2, &tm_q, 64, b * HI, &S.qfull[qs]);
+              nv = clamp_nvis(a.n_vis, b, a.n_max);
+            }
           }
-        } else if (lane == 0) {
-          mbar_arrive(&S.full[s]);
+          if (!warp_bcast<kPool>(ok)) break;
+          nv = warp_bcast<kPool>(nv);
+          ++q_issued;
+          prev_b = b;
         }
+        const int s = kr.slot;
+        if (lane == 0 && !mbar_wait(&S.empty[s], kr.phase ^ 1)) {
+          abort_flag(S) = 1;
+          ok = 0;
+        }
+        if (!warp_bcast<kPool>(ok)) break;
+        uint8_t *dst = kbuf + (size_t)s * kTileBytes;
+        const int64_t row0 = (int64_t)b * a.cap;
+        {
+          constexpr int kBlocks = SWEEP_TILE / BLOCK;   // pool blocks per tile
+          const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
+          const int32_t blk =
+              lane < kBlocks ? __ldg(a.pool + (int64_t)b * a.pool_nb + (int64_t)t * kBlocks + lane) : -1;
+          const bool v = blk >= 0 && blk < nblk_vis;
+          if (lane < kBlocks && !v && blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) set_error(CSA2_DEV_ERR_POOL);
+          const uint32_t valid = __ballot_sync(0xffffffffu, v);
+          if (valid) {
+            if (lane == 0) mbar_arrive_expect_tx(&S.full[s], (uint32_t)__popc(valid) * (BLOCK * DI * 2));
+            __syncwarp();
+            if (v) {
+              const int32_t y = (int32_t)(row0 + (int64_t)blk * BLOCK);
+              tma_load_2d_hint(dst + lane * 1024, &tm_k, 0, y, &S.full[s], pol);
+              tma_load_2d_hint(dst + kTileBytes / 2 + lane * 1024, &tm_k, 64, y, &S.full[s], pol);
+            }
+          } else if (lane == 0) {
+            mbar_arrive(&S.full[s]);
+          }
+        }
+        ++n_issued;
       }
-      ++n_issued;
-    }
-    // Drain: every load this warp issued has landed before the CTA can exit
-    // (returns at once unless a wait above gave up).
-    if (lane == 0) {
-      for (int s = 0; s < kStages && s < n_issued; ++s) {
-        const int last = s + ((n_issued - 1 - s) / kStages) * kStages;
-        mbar_wait(&S.full[s], (uint32_t)((last / kStages) & 1));
+      // Drain: every load this warp issued has landed before the CTA can exit
+      // (returns at once unless a wait above gave up).
+      if (lane == 0) {
+        for (int s = 0; s < kStages && s < n_issued; ++s) {
+          const int last = s + ((n_issued - 1 - s) / kStages) * kStages;
+          mbar_wait(&S.full[s], (uint32_t)((last / kStages) & 1));
+        }
+        if (q_issued > 0) mbar_wait(&S.qfull[(q_issued - 1) & 1], ((q_issued - 1) >> 1) & 1);
       }
-      if (q_issued > 0) mbar_wait(&S.qfull[(q_issued - 1) & 1], ((q_issued - 1) >> 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       int prev_b = -1, qi = -1;
       const uint32_t kbase = smem_u32(kbuf), qbase = smem_u32(qbuf);
-      TileCursor cur(it0, a.tiles_per_seq);
-      Ring<kStages> kr;
-      Ring<2> ar;
-      for (int li = 0; li < n_tiles; ++li, cur.next(), kr.next(), ar.next()) {
+      for (int64_t it = it0; it < it1; ++it) {
         if (abort_flag(S)) break;
-        const int b = cur.b;
+        const int b = (int)(it / a.tiles_per_seq);
         if (b != prev_b) {
           if (qi >= 0) mma_commit(&S.qempty[qi & 1]);
           ++qi;
           if (!mbar_wait(&S.qfull[qi & 1], (qi >> 1) & 1)) { abort_flag(S) = 1; break; }
           prev_b = b;
         }
-        const int s = kr.slot, acc = ar.slot;
-        if (!mbar_wait(&S.full[s], kr.phase)) { abort_flag(S) = 1; break; }
-        if (!mbar_wait(&S.accempty[acc], ar.phase ^ 1)) { abort_flag(S) = 1; break; }
+        const int64_t li = it - it0;
+        const int s = (int)(li % kStages);
+        const uint32_t ph = (uint32_t)((li / kStages) & 1);
+        const int acc = (int)(li & 1);
+        const uint32_t aph = (uint32_t)((li >> 1) & 1);
+        if (!mbar_wait(&S.full[s], ph)) { abort_flag(S) = 1; break; }
+        if (!mbar_wait(&S.accempty[acc], aph ^ 1)) { abort_flag(S) = 1; break; }
         tc_fence_after();
         const uint32_t ka = kbase + (uint32_t)s * kTileBytes;
         const uint32_t qa = qbase + (uint32_t)(qi & 1) * kQBytes;
@@ -273,19 +310,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int prev_b = -1;
     int32_t nv = 0;
     float wv[HI];
-    TileCursor cur(it0, a.tiles_per_seq);
-    Ring<2> ar;
-    for (int li = 0; li < n_tiles; ++li, cur.next(), ar.next()) {
+    for (int64_t it = it0; it < it1; ++it) {
       if (abort_flag(S)) break;
-      const int b = cur.b, t = cur.t;
+      const int b = (int)(it / a.tiles_per_seq);
+      const int t = (int)(it % a.tiles_per_seq);
       if (b != prev_b) {
 #pragma unroll
         for (int h = 0; h < HI; ++h) wv[h] = __ldg(a.w + (int64_t)b * HI + h);
         nv = clamp_nvis(a.n_vis, b, a.n_max);
         prev_b = b;
       }
-      const int acc = ar.slot;
-      if (!mbar_wait(&S.accfull[acc], ar.phase)) { abort_flag(S) = 1; break; }
+      const int64_t li = it - it0;
+      const int acc = (int)(li & 1);
+      const uint32_t aph = (uint32_t)((li >> 1) & 1);
+      if (!mbar_wait(&S.accfull[acc], aph)) { abort_flag(S) = 1; break; }
       tc_fence_after();
       uint32_t v[32];
       tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * HI), v);

@@ -240,94 +240,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    // lane 0 drives the rings and copies a Full tile: one tensor copy of the
-    // tile's code rows (zero-filled past the last row, counted in full) and
-    // one bulk copy of its scales; in a pool tile (Reindex) lane j fetches
-    // pool block j, its 8 code rows and its scales.  Scale copies are cut to
-    // the rows the planes hold.
-    const uint64_t pol = l2_policy_evict_first();   // codes are read once
-    int prev_b = -1, q_issued = 0;
-    int32_t nv = 0;
-    int n_issued = 0;
-    TileCursor cur(it0, a.tiles_per_seq);
-    Ring<kRaw> rr;
-    for (int li = 0; li < n_tiles; ++li, cur.next(), rr.next()) {
-      const int b = cur.b, t = cur.t;
-      int ok = 1;
-      if (b != prev_b) {
-        if (lane == 0) {
-          const int qs = q_issued & 1;
-          if (q_issued > 0 && abort_of(S)) {
-            ok = 0;
-          } else if (!mbar_wait(&S.qempty[qs], ((q_issued >> 1) & 1) ^ 1)) {
-            abort_of(S) = 1;
-            ok = 0;
-          } else {
-            mbar_arrive_expect_tx(&S.qfull[qs], kQBytes);
-            tma_load_2d(qbuf + qs * kQBytes, &tm_q, 0, b * HI, &S.qfull[qs]);
-            nv = clamp_nvis_fp4(a.n_vis, b, a.n_max);
+    // Full tiles: lane 0 alone runs the producer; pool tiles: the whole warp
+    if (kPool || lane == 0) {
+      // ------------------------------------------------------------ producer
+      // lane 0 drives the rings and copies a Full tile: one tensor copy of the
+      // tile's code rows (zero-filled past the last row, counted in full) and
+      // one bulk copy of its scales; in a pool tile (Reindex) lane j fetches
+      // pool block j, its 8 code rows and its scales.  Scale copies are cut to
+      // the rows the planes hold.
+      const uint64_t pol = l2_policy_evict_first();   // codes are read once
+      int prev_b = -1, q_issued = 0;
+      int32_t nv = 0;
+      int n_issued = 0;
+      TileCursor cur(it0, a.tiles_per_seq);
+      Ring<kRaw> rr;
+      for (int li = 0; li < n_tiles; ++li, cur.next(), rr.next()) {
+        const int b = cur.b, t = cur.t;
+        int ok = 1;
+        if (b != prev_b) {
+          if (lane == 0) {
+            const int qs = q_issued & 1;
+            if (q_issued > 0 && abort_of(S)) {
+              ok = 0;
+            } else if (!mbar_wait(&S.qempty[qs], ((q_issued >> 1) & 1) ^ 1)) {
+              abort_of(S) = 1;
+              ok = 0;
+            } else {
+              mbar_arrive_expect_tx(&S.qfull[qs], kQBytes);
+              tma_load_2d(qbuf + qs * kQBytes, &tm_q, 0, b * HI, &S.qfull[qs]);
+              nv = clamp_nvis_fp4(a.n_vis, b, a.n_max);
+            }
           }
+          if (!warp_bcast<kPool>(ok)) break;
+          nv = warp_bcast<kPool>(nv);
+          ++q_issued;
+          prev_b = b;
         }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-        nv = __shfl_sync(0xffffffffu, nv, 0);
-        ++q_issued;
-        prev_b = b;
-      }
-      const int s = rr.slot;
-      if (lane == 0 && !mbar_wait(&S.raw_empty[s], rr.phase ^ 1)) {
-        abort_of(S) = 1;
-        ok = 0;
-      }
-      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      uint8_t *dst = raw + (size_t)s * kRawBytes;
-      const int64_t row0 = (int64_t)b * a.cap;
-      if (!kPool) {
-        if (lane == 0) {
-          if ((int64_t)t * kKeys < nv) {
-            const int64_t r0 = row0 + (int64_t)t * kKeys;
-            const int64_t left = a.k_rows - r0;
-            const uint32_t nrows = (uint32_t)(left < kKeys ? left : kKeys);   // a multiple of 4
-            mbar_arrive_expect_tx(&S.raw_full[s], kRawCodes + nrows * 4);
-            tma_load_2d_hint(dst, &tm_k, 0, (int32_t)r0, &S.raw_full[s], pol);
-            bulk_g2s(dst + kRawCodes, a.k_scales + r0 * 4, nrows * 4, &S.raw_full[s]);
-          } else {
+        const int s = rr.slot;
+        if (lane == 0 && !mbar_wait(&S.raw_empty[s], rr.phase ^ 1)) {
+          abort_of(S) = 1;
+          ok = 0;
+        }
+        if (!warp_bcast<kPool>(ok)) break;
+        uint8_t *dst = raw + (size_t)s * kRawBytes;
+        const int64_t row0 = (int64_t)b * a.cap;
+        if (!kPool) {
+          if (lane == 0) {
+            if ((int64_t)t * kKeys < nv) {
+              const int64_t r0 = row0 + (int64_t)t * kKeys;
+              const int64_t left = a.k_rows - r0;
+              const uint32_t nrows = (uint32_t)(left < kKeys ? left : kKeys);   // a multiple of 4
+              mbar_arrive_expect_tx(&S.raw_full[s], kRawCodes + nrows * 4);
+              tma_load_2d_hint(dst, &tm_k, 0, (int32_t)r0, &S.raw_full[s], pol);
+              bulk_g2s(dst + kRawCodes, a.k_scales + r0 * 4, nrows * 4, &S.raw_full[s]);
+            } else {
+              mbar_arrive(&S.raw_full[s]);
+            }
+          }
+        } else {
+          // the tile's pool blocks j0 .. j0 + nj - 1 (the last tile may hold fewer)
+          const int64_t j0 = (int64_t)t * (kKeys / BLOCK);
+          const int nj = (int)(a.pool_nb - j0 < kKeys / BLOCK ? a.pool_nb - j0 : kKeys / BLOCK);
+          const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
+          const int32_t blk = lane < nj ? __ldg(a.pool + (int64_t)b * a.pool_nb + j0 + lane) : -1;
+          const bool v = blk >= 0 && blk < nblk_vis;
+          if (lane < nj && !v && blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) set_error(CSA2_DEV_ERR_POOL);
+          const int64_t y = row0 + (int64_t)blk * BLOCK;
+          // a block past the last row when cap is not a multiple of 8 (cap and
+          // y are multiples of 4)
+          const uint32_t nrows = v ? (uint32_t)(a.k_rows - y < BLOCK ? a.k_rows - y : BLOCK) : 0u;
+          const uint32_t bytes = __reduce_add_sync(0xffffffffu, v ? BLOCK * (DI / 2) + nrows * 4 : 0u);
+          if (bytes) {
+            if (lane == 0) mbar_arrive_expect_tx(&S.raw_full[s], bytes);
+            __syncwarp();
+            if (v) {
+              tma_load_2d_hint(dst + lane * BLOCK * (DI / 2), &tm_k, 0, (int32_t)y, &S.raw_full[s], pol);
+              bulk_g2s(dst + kRawCodes + lane * BLOCK * 4, a.k_scales + y * 4, nrows * 4, &S.raw_full[s]);
+            }
+          } else if (lane == 0) {
             mbar_arrive(&S.raw_full[s]);
           }
         }
-      } else {
-        // the tile's pool blocks j0 .. j0 + nj - 1 (the last tile may hold fewer)
-        const int64_t j0 = (int64_t)t * (kKeys / BLOCK);
-        const int nj = (int)(a.pool_nb - j0 < kKeys / BLOCK ? a.pool_nb - j0 : kKeys / BLOCK);
-        const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
-        const int32_t blk = lane < nj ? __ldg(a.pool + (int64_t)b * a.pool_nb + j0 + lane) : -1;
-        const bool v = blk >= 0 && blk < nblk_vis;
-        if (lane < nj && !v && blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) set_error(CSA2_DEV_ERR_POOL);
-        const int64_t y = row0 + (int64_t)blk * BLOCK;
-        // a block past the last row when cap is not a multiple of 8 (cap and
-        // y are multiples of 4)
-        const uint32_t nrows = v ? (uint32_t)(a.k_rows - y < BLOCK ? a.k_rows - y : BLOCK) : 0u;
-        const uint32_t bytes = __reduce_add_sync(0xffffffffu, v ? BLOCK * (DI / 2) + nrows * 4 : 0u);
-        if (bytes) {
-          if (lane == 0) mbar_arrive_expect_tx(&S.raw_full[s], bytes);
-          __syncwarp();
-          if (v) {
-            tma_load_2d_hint(dst + lane * BLOCK * (DI / 2), &tm_k, 0, (int32_t)y, &S.raw_full[s], pol);
-            bulk_g2s(dst + kRawCodes + lane * BLOCK * 4, a.k_scales + y * 4, nrows * 4, &S.raw_full[s]);
-          }
-        } else if (lane == 0) {
-          mbar_arrive(&S.raw_full[s]);
+        ++n_issued;
+      }
+      // every copy this warp issued has landed before the CTA can exit
+      if (lane == 0) {
+        for (int s = 0; s < kRaw && s < n_issued; ++s) {
+          const int last = s + ((n_issued - 1 - s) / kRaw) * kRaw;
+          mbar_wait(&S.raw_full[s], (uint32_t)((last / kRaw) & 1));
         }
+        if (q_issued > 0) mbar_wait(&S.qfull[(q_issued - 1) & 1], ((q_issued - 1) >> 1) & 1);
       }
-      ++n_issued;
-    }
-    // every copy this warp issued has landed before the CTA can exit
-    if (lane == 0) {
-      for (int s = 0; s < kRaw && s < n_issued; ++s) {
-        const int last = s + ((n_issued - 1 - s) / kRaw) * kRaw;
-        mbar_wait(&S.raw_full[s], (uint32_t)((last / kRaw) & 1));
-      }
-      if (q_issued > 0) mbar_wait(&S.qfull[(q_issued - 1) & 1], ((q_issued - 1) >> 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer

@@ -31,4 +31,12 @@ struct TileCursor {
   }
 };
 
+// Lane 0's value for the whole warp when the warp runs the loop together
+// (pool tiles); the value itself when lane 0 runs it alone (Full tiles).
+template <bool kWarp>
+__device__ __forceinline__ int warp_bcast(int v) {
+  if constexpr (kWarp) return __shfl_sync(0xffffffffu, v, 0);
+  return v;
+}
+
 }  // namespace csa2

@@ -48,3 +48,21 @@ def validate(modes) -> None:
             seen_full = True
         elif m in (Mode.REINDEX, Mode.REUSE) and not seen_full:
             raise ValueError(f"layer {i}: {m.value} before any Full layer")
+
+
+def cache_copies(modes) -> int:
+    """Main-KV / indexer-K copies a stack keeps: one per Full layer (Reindex
+    and Reuse layers read the latest one)."""
+    return sum(Mode(m) == Mode.FULL for m in modes)
+
+
+def global_kv_bytes_per_token(entry_bytes: int, indexer_entry_bytes: int, encoder=None, decoder=None,
+                              m_encoder: int = 2, m_decoder: int = 1) -> float:
+    """Global cache growth per token ("DeepSeek-v4.1 Flash: Pushing the Limits
+    of KV Cache Compression", section 3.1): every cache copy adds one main-KV
+    entry and one indexer-K entry per m tokens.  The encoder keeps a copy per
+    Full layer at m = 2, the decoder its own at m = 1."""
+    enc = encoder_modes() if encoder is None else encoder
+    dec = decoder_modes() if decoder is None else decoder
+    per_entry = entry_bytes + indexer_entry_bytes
+    return cache_copies(enc) * per_entry / m_encoder + cache_copies(dec) * per_entry / m_decoder

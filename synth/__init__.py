@@ -142,7 +142,7 @@ class Config:
     name: str
     batch: int
     n_ctx: int
-    schedule: list = field(default_factory=list)   # list of "full" / "reindex" / "reuse"
+    schedule: list = field(default_factory=list)   # list of "full" / "reindex" / "reuse" / "swa"
     hsi: bool = False
     planted_blocks: int = 0
     m: int = 1
@@ -161,6 +161,18 @@ def decoder_layer_modes(groups: int = 5, per_group: int = 4, first: str = "full"
     return modes
 
 
+def encoder_layer_modes(swa_layers: int = 2, groups: int = 3, per_group: int = 6):
+    """The encoder's schedule: SWA-only layers, then groups of one Full layer
+    (its own m = 2 cache copy) and Reuse layers ("DeepSeek-V4.1-Flash -
+    Architecture", section 2; "DeepSeek-v4.1 Flash: Pushing the Limits of KV
+    Cache Compression", section 2.3.3)."""
+    modes = ["swa"] * swa_layers
+    for _ in range(groups):
+        modes.append("full")
+        modes.extend(["reuse"] * (per_group - 1))
+    return modes
+
+
 CONFIGS = {
     # tiny single-layer Full decode, seed 0
     "decode_1x4k": Config("decode_1x4k", 1, 4096, ["full"], layer_seeds=[0]),
@@ -173,6 +185,11 @@ CONFIGS = {
     # long-context full 20-layer decoder step
     "decoder20_4x1m": Config("decoder20_4x1m", 4, 1048576, decoder_layer_modes(), hsi=True,
                  layer_seeds=[3000 + i for i in range(20)]),
+    # the encoder's 20 layers at decode: 2 SWA-only, 3 x [Full + 5 Reuse] over
+    # three m=2 cache copies; a 65,536-token context (32,768 entries per copy)
+    # and a step whose token completes an entry pair
+    "encoder_decode_32x64k": Config("encoder_decode_32x64k", 32, 65536, encoder_layer_modes(), m=2,
+                 layer_seeds=[5000 + i for i in range(20)]),
     # chunked prefill at m=2: 131072-token context + 16384-token chunk
     "prefill_m2_2x128k": Config("prefill_m2_2x128k+16k", 2, 131072, ["full"], m=2, chunk=16384,
                  layer_seeds=[4000]),

@@ -37,6 +37,7 @@ def test_defaults_and_sizes(c2):
     assert (p.index_topk, p.sliding_window, p.candidate_block_size, p.candidate_topk_blocks, p.block_reduce,
             p.hsi, p.attn_kernel, p.indexer_fp4) == (512, 128, 8, 2048, 0, 1, 0, 0)
     assert c2.entry_bytes() == 288
+    assert c2.indexer_entry_bytes(False) == 256 and c2.indexer_entry_bytes(True) == 68 == c2.FP4_ENTRY_BYTES
     assert c2.lib().csa2_status_string(3) == b"workspace too small"
 
 
@@ -105,6 +106,21 @@ def test_host_validation_rejects_without_launch(c2):
                                 fake, fake, fake, fake, None, P(0x1000), 1 << 30, None) == 1
 
 
+def test_encoder_decode_workload_schedule():
+    """The encoder decode workload follows the pages' schedule: two SWA-only
+    layers, then three groups of Full + five Reuse, each Full layer with its
+    own cache copy, at m = 2 ("DeepSeek-V4.1-Flash - Architecture", section 2)."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import synth
+    from sparse_attention_fp4_csa2_gb300 import schedule as s
+    cfg = synth.CONFIGS["encoder_decode_32x64k"]
+    assert cfg.m == 2 and cfg.n_ctx % 2 == 0 and len(cfg.schedule) == 20 and len(cfg.layer_seeds) == 20
+    assert cfg.schedule[:2] == ["swa", "swa"]
+    assert cfg.schedule[2:] == (["full"] + ["reuse"] * 5) * 3
+    assert cfg.schedule == [m.value for m in s.encoder_modes()]
+
+
 def test_schedule_host_logic():
     from sparse_attention_fp4_csa2_gb300 import schedule as s
     dec = s.decoder_modes()
@@ -115,3 +131,22 @@ def test_schedule_host_logic():
     s.validate(dec)
     with pytest.raises(ValueError):
         s.validate(["reuse", "full"])
+
+
+def test_global_cache_bytes_per_token_from_library_sizes(c2):
+    """The pages' 890 B/token ("DeepSeek-v4.1 Flash: Pushing the Limits of KV
+    Cache Compression", section 3.1): three encoder copies at m = 2 and one
+    decoder copy at m = 1, each adding a main-KV and an MXFP4 indexer-K entry,
+    from this library's own entry sizes and schedules."""
+    import json
+    from sparse_attention_fp4_csa2_gb300 import schedule as s
+    facts = json.load(open(os.path.join(ROOT, "tests", "golden", "pages_facts.json")))
+    lay = facts["model_layers"]
+    enc, dec = s.encoder_modes(), s.decoder_modes()
+    assert len(enc) == lay["encoder_layers"] and len(dec) == lay["decoder_layers"]
+    assert s.cache_copies(enc) == lay["encoder_groups"] and s.cache_copies(dec) == 1
+    got = s.global_kv_bytes_per_token(c2.entry_bytes(), c2.indexer_entry_bytes(True), enc, dec,
+                                      m_encoder=lay["encoder_m"], m_decoder=lay["decoder_m"])
+    assert got == facts["global_kv_bytes_per_token"]["value"]
+    # with the bf16 indexer entry the same schedule grows 1,360 B per token
+    assert s.global_kv_bytes_per_token(c2.entry_bytes(), c2.indexer_entry_bytes(False), enc, dec) == 1360
