@@ -39,7 +39,7 @@ SWEEP_FIXED = 32 * 128 * 2 + 32 * 4        # q_idx + w per sequence
 # DRAM bytes (read + write) per launch from one ncu capture of the current
 # kernel code on that workload (profiles/<kernel>_<workload>.md); absent: null
 TRAFFIC = {
-    ("indexer_sweep_kernel", "group_decode_32x64k"): None,   # kernel changed since its capture
+    ("indexer_sweep_kernel", "group_decode_32x64k"): 537181184 + 6408192,
     ("sparse_attn_kernel", "group_decode_32x64k"): 10633984,
     # captured at 16 sequences, scaled by the rows read to the 32-sequence launch
     ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411200 + 915968),
