@@ -62,6 +62,8 @@ def lib():
         L.csa2o_fp4_dequant.argtypes, L.csa2o_fp4_dequant.restype = [P, P], None
         L.csa2o_kv_entry.argtypes, L.csa2o_kv_entry.restype = [P, P, i32, i64, f64, P], None
         L.csa2o_kv_entries.argtypes, L.csa2o_kv_entries.restype = [P, P, i32, i64, P, f64, P], None
+        L.csa2o_indexer_k_project.argtypes = [P, P, i32, i64, P, f64, P, P]
+        L.csa2o_indexer_k_project.restype = None
         L.csa2o_index_scores.argtypes, L.csa2o_index_scores.restype = [P, P, P, i64, P], None
         L.csa2o_mxfp4_quantise.argtypes, L.csa2o_mxfp4_quantise.restype = [P, P, P], None
         L.csa2o_mxfp4_quantise_rows.argtypes, L.csa2o_mxfp4_quantise_rows.restype = [P, i64, P, P], None
@@ -155,6 +157,21 @@ def kv_entries(latent, z, m: int, pos, base: float = 10000.0) -> np.ndarray:
     out = np.empty((n, ENTRY_BYTES), np.uint8)
     lib().csa2o_kv_entries(_p(lat), _p(zz), int(m), int(n), _p(pp), float(base), _p(out))
     return out
+
+
+def indexer_k_project(latent, z, m: int, pos, w, base: float = 10000.0):
+    """The Full layer's indexer keys: latent (and z) bf16 [n, m, 512] (or
+    [n, 512] at m=1), pos int64 [n], w bf16 [128, 512] -> bf16 [n, 128]
+    (a torch tensor)."""
+    import torch
+    lat = _u16(latent).reshape(-1, m * D)
+    n = lat.shape[0]
+    zz = _u16(z).reshape(n, m * D) if z is not None else None
+    pp = _np(pos, np.int64).reshape(n)
+    ww = _u16(w).reshape(DI * D)
+    out = np.empty((n, DI), np.uint16)
+    lib().csa2o_indexer_k_project(_p(lat), _p(zz), int(m), int(n), _p(pp), float(base), _p(ww), _p(out))
+    return torch.from_numpy(out.view(np.int16)).view(torch.bfloat16)
 
 
 # ---------------------------------------------------------------- indexer

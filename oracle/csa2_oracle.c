@@ -212,6 +212,44 @@ void csa2o_kv_entries(const uint16_t *latent, const uint16_t *z, int m, int64_t 
                        entries + i * O_ENTRY);
 }
 
+/* A real number rounded to the nearest bf16 (ties to even), as its bits:
+ * 8 significant bits, quantum 2^-133 below the normal range, overflow to inf. */
+static uint16_t f64_to_bf16_rne(double v) {
+    if (v != v) return 0x7FC0;
+    if (v == 0.0) return signbit(v) ? 0x8000 : 0x0000;
+    int e;
+    frexp(fabs(v), &e);                     /* |v| in [2^(e-1), 2^e) */
+    int qexp = e - 8;
+    if (qexp < -133) qexp = -133;
+    double r = ldexp(rint(ldexp(fabs(v), -qexp)), qexp);
+    float rf = r > 3.3895313892515355e38 ? INFINITY : (float)r;   /* exact when finite */
+    if (signbit(v)) rf = -rf;
+    uint32_t u;
+    memcpy(&u, &rf, 4);
+    return (uint16_t)(u >> 16);
+}
+
+/* The Full layer's indexer key of an entry ("DeepSeek-v4.1 Flash: Pushing
+ * the Limits of KV Cache Compression", section 2.3.1: CSA2 obtains the Indexer
+ * K by projecting the main KV entry).  READING: the projected entry is the
+ * main-KV entry as written, before its FP4 quantisation (compressed at m = 2,
+ * RoPE on the tail channels, fp32); k = W e with W bf16 [128][512], in fp64,
+ * rounded once to bf16. */
+void csa2o_indexer_k_project(const uint16_t *latent, const uint16_t *z, int m, int64_t n, const int64_t *pos,
+                             double rope_base, const uint16_t *w, uint16_t *k) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < n; ++i) {
+        float e[O_D], r[O_D];
+        csa2o_compress(latent + i * m * O_D, z ? z + i * m * O_D : NULL, m, e);
+        csa2o_rope_tail(e, pos[i], rope_base, r);
+        for (int o = 0; o < O_DI; ++o) {
+            double acc = 0.0;
+            for (int c = 0; c < O_D; ++c) acc += (double)bf16_to_f32(w[o * O_D + c]) * (double)r[c];
+            k[i * O_DI + o] = f64_to_bf16_rne(acc);
+        }
+    }
+}
+
 /* -------------------------------------------------------------- indexer */
 
 /* Lightning-indexer score of each key row: s_n = sum_h w_h * ReLU(q_h . k_n)
