@@ -104,6 +104,9 @@ def parse():
                     help="readout kernel: 0 automatic, 1 chunk-parallel, 2 streaming")
     ap.add_argument("--indexer-fp4", action="store_true",
                     help="MXFP4 indexer K cache and query (decode workloads)")
+    ap.add_argument("--project-ik", action="store_true",
+                    help="a Full layer writes its new indexer key as the projection of its main-KV entry "
+                         "(csa2_kv_quant_write_ik; decode workloads)")
     return ap.parse_args()
 
 
@@ -116,14 +119,20 @@ def kv_write_bytes(m):
 SWA_ATTN_BYTES = ATTN_BYTES - 512 * 288 - 512 * 4   # a SWA-only layer: no selected entries
 
 
-def algorithmic_bytes(cfg, hsi, fp4=False):
+def algorithmic_bytes(cfg, hsi, fp4=False, project=False):
     B, E, kb = cfg.batch, cfg.n_ctx // cfg.m, K_BYTES[fp4]
     total = 0
     for m in cfg.schedule:
         total += B * (SWA_ATTN_BYTES if m == "swa" else ATTN_BYTES)
         if m == "full":
-            # the copy's new entry (and its MXFP4 indexer-K entry), then the sweep
-            total += B * (kv_write_bytes(cfg.m) + (256 + 68 if fp4 else 0))
+            # the copy's new entry and its indexer key (projected: W_ik read
+            # once, the key written; else the MXFP4 writer's bf16 key in and
+            # entry out), then the sweep
+            total += B * kv_write_bytes(cfg.m)
+            if project:
+                total += 128 * 512 * 2 + B * kb
+            elif fp4:
+                total += B * (256 + 68)
             total += B * (kb * E + SWEEP_FIXED + 512 * 4)
         elif m == "reindex":
             total += B * (REINDEX_BYTES - 16384 * (256 - kb))
@@ -233,9 +242,13 @@ class Workload:
             new = {"latent": synth.normal((B, m, 512) if m == 2 else (B, 512), cs + 7, 0, device)}
             if m == 2:
                 new["z"] = synth.normal((B, m, 512), cs + 9, 0, device)
-            if self.fp4:
+            if self.fp4 and not PROJECT_IK:
                 new["k"] = synth.normal((B, 128), cs + 11, 0, device)
             self.new_in.append(new)
+        # --project-ik: every copy's W_ik (a synthetic projection of the main-KV entry)
+        self.project = PROJECT_IK
+        self.w_ik = [synth.normal((128, 512), seed + 101 * c + 13, 0, device, std=512 ** -0.5)
+                     for c in range(self.copies)] if PROJECT_IK else None
         if self.fp4:
             self.PROFILED = ((0, "indexer_sweep_fp4_kernel"), (3, "topk_cluster_kernel"), (1, "sparse_attn_kernel"))
         self.layers = [synth.layer_inputs(s, B, device=device) for s in cfg.layer_seeds]
@@ -279,8 +292,10 @@ class Workload:
         return out
 
     def config(self, ms):
-        step_bytes = algorithmic_bytes(self.cfg, self.hsi, self.fp4)
+        step_bytes = algorithmic_bytes(self.cfg, self.hsi, self.fp4, self.project)
         ik = "MXFP4 indexer K and Q" if self.fp4 else "bf16 indexer K"
+        if self.project:
+            ik += " (new keys projected from the main-KV entry)"
         return {"workload": self.cfg.name, "batch": self.B, "context": self.N, "m": self.m, "entries": self.E,
                 "cache_copies": self.copies, "layers": "+".join(self.cfg.schedule),
                 "hsi": bool(self.hsi), "storage": f"FP4 E2M1+E4M3/16 main KV, {ik}, E4M3 SWA",
@@ -307,12 +322,20 @@ class Workload:
             if mode == "full":
                 copy += 1
                 new = self.new_in[copy]
-                c2.kv_quant_write(new["latent"], new.get("z"), m, self.new_pos, self.new_slot,
-                                  self.kv[copy].view(-1, 288))
-                launches += c2.last_launch_count()
-                if self.fp4:
-                    c2.indexer_k_quant(new["k"], self.new_slot, self.k_idx[copy])
+                if self.project:
+                    # the main-KV entry and its projected indexer key in one write
+                    c2.kv_quant_write_ik(new["latent"], new.get("z"), m, self.new_pos, self.new_slot,
+                                         self.kv[copy].view(-1, 288), self.w_ik[copy],
+                                         self.k_idx[copy] if self.fp4 else self.k_idx[copy].view(-1, 128),
+                                         indexer_fp4=self.fp4)
                     launches += c2.last_launch_count()
+                else:
+                    c2.kv_quant_write(new["latent"], new.get("z"), m, self.new_pos, self.new_slot,
+                                      self.kv[copy].view(-1, 288))
+                    launches += c2.last_launch_count()
+                    if self.fp4:
+                        c2.indexer_k_quant(new["k"], self.new_slot, self.k_idx[copy])
+                        launches += c2.last_launch_count()
             cc = max(copy, 0)
             idx_args = {} if mode in ("reuse", "swa") else dict(q_idx=li.q_idx, w=li.w, k_idx=self.k_idx[cc])
             on = []
@@ -468,12 +491,14 @@ class PrefillWorkload:
 
 ATTN_KERNEL = 0       # csa2_params.attn_kernel of the workloads (--attn-kernel)
 INDEXER_FP4 = False   # csa2_params.indexer_fp4 of the decode workloads (--indexer-fp4)
+PROJECT_IK = False    # Full layers project their new indexer key (--project-ik)
 
 
 def run_ours(args, rank, world, local_rank):
-    global ATTN_KERNEL, INDEXER_FP4
+    global ATTN_KERNEL, INDEXER_FP4, PROJECT_IK
     ATTN_KERNEL = args.attn_kernel
     INDEXER_FP4 = args.indexer_fp4
+    PROJECT_IK = args.project_ik
     import torch
 
     import synth
@@ -486,8 +511,8 @@ def run_ours(args, rank, world, local_rank):
     if args.batch:
         import dataclasses
         cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}[batch={args.batch}]")
-    if cfg.chunk and INDEXER_FP4:
-        raise SystemExit("--indexer-fp4: the MXFP4 indexer is decode-only")
+    if cfg.chunk and (INDEXER_FP4 or PROJECT_IK):
+        raise SystemExit("--indexer-fp4 / --project-ik: decode workloads only")
     wl = PrefillWorkload(cfg, dev) if cfg.chunk else Workload(cfg, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)

@@ -116,6 +116,25 @@ csa2_status csa2_kv_quant_write(const void *latent, const void *z, int32_t m, in
                                 int64_t kv_rows, float rope_theta, csa2_stream_t stream);
 
 /*
+ * csa2_kv_quant_write_ik -- csa2_kv_quant_write that also writes each
+ * entry's indexer key, the Full layer's projection of its main-KV entry
+ * ([A] 2.3.1: "obtains the Indexer K by projecting the main KV entries").
+ *   k = W_ik e, e the entry before FP4 quantisation (compressed at m = 2,
+ *   RoPE'd, fp32), fp32 accumulation, rounded to bf16 (nearest even); with
+ *   indexer_fp4 the bf16 row is then written as MXFP4 exactly as
+ *   csa2_indexer_k_quant writes it.
+ *   w_ik   bf16 [128][512] (row-major), 16-byte aligned
+ *   k_idx  bf16 [k_rows][128], or with indexer_fp4 the MXFP4 planes of k_rows
+ *          rows (k_rows a multiple of 4); 16-byte aligned
+ *   row slot[i] of both caches is written; slot[i] >= k_rows is skipped and
+ *   sets CSA2_DEV_ERR_INDEX.  Other arguments as csa2_kv_quant_write.
+ */
+csa2_status csa2_kv_quant_write_ik(const void *latent, const void *z, int32_t m, int64_t n_entries,
+                                   const int64_t *entry_pos, const int64_t *slot, uint8_t *kv, int64_t kv_rows,
+                                   float rope_theta, const void *w_ik, void *k_idx, int64_t k_rows,
+                                   int32_t indexer_fp4, csa2_stream_t stream);
+
+/*
  * csa2_indexer_k_quant -- write MXFP4 indexer-K entries (OCP Microscaling:
  * blocks of 32 dims share one UE8M0 scale 2^E, E = floor(log2(max |x|)) - 2
  * clamped to [-127, 127] (-127 for an all-zero block); codes =

@@ -72,6 +72,7 @@ def lib():
         L.csa2_get_device_status.restype = ctypes.c_int
         L.csa2_kv_quant_write.argtypes = [P, P, i32, i64, P, P, P, i64, f32, P]
         L.csa2_indexer_k_quant.argtypes = [P, i64, P, P, i64, P]
+        L.csa2_kv_quant_write_ik.argtypes = [P, P, i32, i64, P, P, P, i64, f32, P, P, i64, i32, P]
         L.csa2_indexer_score_topk.argtypes = [P, P, P, i32, i64, P, i64, P, PP, P, P, P, sz, P]
         L.csa2_hier_pool_select.argtypes = [P, P, i32, i64, PP, P, P, sz, P]
         L.csa2_sparse_attn.argtypes = [PP, i32, P, P, i64, P, P, P, P, P, P, P, sz, P]
@@ -80,7 +81,7 @@ def lib():
         L.csa2_prefill_chunk.argtypes = [PP, i32, i32, i64, i32, P, P, P, P, P, i64, P, P, i64, i64, P, P, P, P, sz, P]
         L.csa2_prefill_chunk.restype = ctypes.c_int
         L.csa2_set_profile_events.argtypes, L.csa2_set_profile_events.restype = [ctypes.c_int, P, P], ctypes.c_int
-        for f in ("csa2_kv_quant_write", "csa2_indexer_k_quant", "csa2_indexer_score_topk", "csa2_hier_pool_select",
+        for f in ("csa2_kv_quant_write", "csa2_kv_quant_write_ik", "csa2_indexer_k_quant", "csa2_indexer_score_topk", "csa2_hier_pool_select",
                   "csa2_sparse_attn", "csa2_sparse_decode"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
@@ -154,6 +155,23 @@ def kv_quant_write(latent, z, m, entry_pos, slot, kv, rope_theta=10000.0, stream
                                      _ptr(entry_pos, torch.int64, "entry_pos"), _ptr(slot, torch.int64, "slot"),
                                      _ptr(kv, torch.uint8, "kv"), kv.numel() // ENTRY_BYTES, float(rope_theta),
                                      _stream(stream)), "csa2_kv_quant_write")
+
+
+def kv_quant_write_ik(latent, z, m, entry_pos, slot, kv, w_ik, k_idx, indexer_fp4=False, rope_theta=10000.0,
+                     stream=None):
+    """kv_quant_write plus each entry's indexer key W_ik e: w_ik bf16 [128, 512];
+    k_idx bf16 [rows, 128] or, with indexer_fp4, an MXFP4 cache of
+    ``indexer_k_fp4_cache``."""
+    n = entry_pos.numel()
+    if indexer_fp4:
+        k_ptr, k_rows = _ptr(k_idx, torch.uint8, "k_idx"), k_idx.numel() // FP4_ENTRY_BYTES
+    else:
+        k_ptr, k_rows = _ptr(k_idx, torch.bfloat16, "k_idx"), k_idx.numel() // 128
+    _check(lib().csa2_kv_quant_write_ik(_ptr(latent, torch.bfloat16, "latent"), _ptr(z, torch.bfloat16, "z"), m, n,
+                                        _ptr(entry_pos, torch.int64, "entry_pos"), _ptr(slot, torch.int64, "slot"),
+                                        _ptr(kv, torch.uint8, "kv"), kv.numel() // ENTRY_BYTES, float(rope_theta),
+                                        _ptr(w_ik, torch.bfloat16, "w_ik"), k_ptr, k_rows, int(bool(indexer_fp4)),
+                                        _stream(stream)), "csa2_kv_quant_write_ik")
 
 
 FP4_ENTRY_BYTES = 68

@@ -373,6 +373,28 @@ csa2_status csa2_kv_quant_write(const void *latent, const void *z, int32_t m, in
   return CSA2_OK;
 }
 
+csa2_status csa2_kv_quant_write_ik(const void *latent, const void *z, int32_t m, int64_t n_entries,
+                                   const int64_t *entry_pos, const int64_t *slot, uint8_t *kv, int64_t kv_rows,
+                                   float rope_theta, const void *w_ik, void *k_idx, int64_t k_rows, int32_t indexer_fp4,
+                                   csa2_stream_t stream) {
+  g_last_launches = 0;
+  if (n_entries < 0 || kv_rows < 0 || k_rows < 0 || (m != 1 && m != 2) || (indexer_fp4 != 0 && indexer_fp4 != 1))
+    return CSA2_ERR_INVALID_ARG;
+  if (indexer_fp4 && k_rows % 4 != 0) return CSA2_ERR_INVALID_ARG;
+  if (n_entries == 0) return CSA2_OK;
+  if (!latent || !entry_pos || !slot || !kv || (m == 2 && !z) || !w_ik || !k_idx) return CSA2_ERR_INVALID_ARG;
+  if (!aligned16(latent) || !aligned16(kv) || (z && !aligned16(z)) || !aligned16(w_ik) || !aligned16(k_idx))
+    return CSA2_ERR_INVALID_ARG;
+  if (!(rope_theta > 1.0f)) return CSA2_ERR_INVALID_ARG;
+  if (n_entries > ((int64_t)1 << 34)) return CSA2_ERR_UNSUPPORTED;
+  const cudaError_t e =
+      launch_kv_quant_write(latent, m == 2 ? z : nullptr, m, n_entries, entry_pos, slot, kv, kv_rows, rope_theta,
+                            reinterpret_cast<cudaStream_t>(stream), w_ik, k_idx, k_rows, indexer_fp4);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  g_last_launches = 1;
+  return CSA2_OK;
+}
+
 csa2_status csa2_indexer_k_quant(const void *k, int64_t n, const int64_t *slot, uint8_t *k_fp4, int64_t rows,
                                  csa2_stream_t stream) {
   g_last_launches = 0;

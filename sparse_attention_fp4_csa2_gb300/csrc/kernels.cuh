@@ -66,11 +66,13 @@ cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream);
 
 // 2-D bf16 tensor map over rows of `inner` elements, box {64, box_rows}, 128B swizzle.
 bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t inner, int64_t rows, uint32_t box_rows);
-// 2-D byte tensor map over rows of 64 bytes, box {64, box_rows}, no swizzle.
 
+// w_ik != NULL: also the entry's indexer key k = W_ik e into k_out (bf16 rows,
+// or the MXFP4 planes with fp4), row slot[i] of k_rows.
 cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int64_t n_entries, const int64_t *pos,
                                   const int64_t *slot, uint8_t *kv, int64_t kv_rows, float rope_theta,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const void *w_ik = nullptr, void *k_out = nullptr,
+                                  int64_t k_rows = 0, int fp4 = 0);
 
 struct SweepArgs {
   const float *w;             // [B][32]

@@ -11,6 +11,17 @@
 // bytes and 32 contiguous scale bytes.  Decode writes one entry per sequence,
 // so the kernel is latency-bound; the m = 2 chunked-prefill write streams
 // 4 KB of input per entry and is bandwidth-bound.
+//
+// With a projection (csa2_kv_quant_write_ik) the same warp also writes the
+// entry's indexer key: k = W_ik e over the entry before FP4 quantisation
+// ("DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression", 2.3.1:
+// the Indexer K is a projection of the main KV entry).  Each lane forms the
+// partial dot products of its 16 channels with 32 rows of W_ik at a time
+// (W_ik read as 32-byte row pieces, one per lane, coalesced), a transposed
+// warp reduction leaves row 32g + l on lane l (four warps per entry, one per
+// block of 32 rows, the entry staged in shared memory), and the row is stored as bf16
+// (round to nearest even) or, for the MXFP4 indexer, quantised per block of
+// 32 (one block per group of 32 rows) exactly like csa2_indexer_k_quant.
 #include <cmath>
 
 #include "kernels.cuh"
@@ -45,19 +56,101 @@ constexpr double kTwoPi2 = 0x1.0b4611a6p-32;
 constexpr double kTwoPi3 = 0x1.3198a2e037073p-67;
 constexpr double kInvTwoPi = 0.15915494309189535;
 
+// The indexer-key output of the projecting write.
+struct IkOut {
+  const __nv_bfloat16 *w;   // W_ik [128][512]
+  void *k;                  // bf16 [k_rows][128], or the MXFP4 planes of k_rows rows
+  int64_t k_rows;
+  int fp4;
+};
+
+// One halving step of the transposed reduction: lanes with bit HALF set keep
+// the upper N of their 2N columns and add the partner's, the others the
+// lower N.
+template <int N, int HALF>
+__device__ __forceinline__ void reduce_step(float (&x)[32], int lane) {
+  const bool up = lane & HALF;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const float send = up ? x[i] : x[i + N];
+    const float keep = up ? x[i + N] : x[i];
+    x[i] = keep + __shfl_xor_sync(0xffffffffu, send, HALF);
+  }
+}
+
+// Sum over the 32 lanes of each of 32 columns: lane l returns column l.
+__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
+  reduce_step<16, 16>(x, lane);
+  reduce_step<8, 8>(x, lane);
+  reduce_step<4, 4>(x, lane);
+  reduce_step<2, 2>(x, lane);
+  reduce_step<1, 1>(x, lane);
+  return x[0];
+}
+
+// Rows 32g .. 32g + 31 of k = W_ik e for the entry whose channels 16 lane ..
+// +15 this lane holds in x, stored at row `row` of the indexer-K cache.
+__device__ __forceinline__ void project_indexer_block(const IkOut &ik, const float (&x)[16], int lane, int64_t row,
+                                                      int g) {
+  const int c0 = lane * 16;
+  {
+    float part[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      float wv[16];
+      load_bf16x16(ik.w + (int64_t)(g * 32 + j) * D + c0, wv);
+      float acc = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) acc = fmaf(wv[i], x[i], acc);
+      part[j] = acc;
+    }
+    const __nv_bfloat16 kb = __float2bfloat16_rn(transpose_reduce32(part, lane));   // row 32 g + lane
+    if (!ik.fp4) {
+      static_cast<__nv_bfloat16 *>(ik.k)[row * DI + g * 32 + lane] = kb;
+      return;
+    }
+    // MXFP4 block g: E = floor(log2 max|k|) - 2 in [-127, 127] (-127 for a
+    // zero or subnormal maximum), codes E2M1_rne_satfinite(k / 2^E)
+    const float v = __bfloat162float(kb);
+    float am = fabsf(v);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+    const int ef = (int)((__float_as_uint(am) >> 23) & 0xFFu);
+    const int E = (am > 0.0f && ef > 0) ? max(-127, min(127, ef - 127 - 2)) : -127;
+    const float inv = -E >= -126 ? __uint_as_float((uint32_t)(-E + 127) << 23) : __uint_as_float(0x00400000u);
+    const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+    uint8_t *planes = static_cast<uint8_t *>(ik.k);
+    if ((lane & 1) == 0)   // element 2j (this lane) in the low nibble, 2j + 1 in the high one
+      planes[row * (DI / 2) + g * 16 + (lane >> 1)] = (uint8_t)cvt_e2m1x2(partner * inv, v * inv);
+    if (lane == 0) planes[ik.k_rows * (DI / 2) + row * 4 + g] = (uint8_t)(E + 127);
+  }
+}
+
+template <bool kProject>
 __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16 *__restrict__ latent,
                                                              const __nv_bfloat16 *__restrict__ z, int m,
                                                              int64_t n_entries, const int64_t *__restrict__ pos,
                                                              const int64_t *__restrict__ slot,
                                                              uint8_t *__restrict__ kv, int64_t kv_rows,
-                                                             const RopeFreqs freqs) {
+                                                             const RopeFreqs freqs, const IkOut ik) {
   const int lane = threadIdx.x & 31;
-  const int64_t e = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (e >= n_entries) return;   // warp-uniform
+  // one entry per warp; when projecting, one entry per block of 4 warps:
+  // warp 0 writes the entry, then each warp projects 32 rows of W_ik
+  const int64_t e = kProject ? (int64_t)blockIdx.x : (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (e >= n_entries) return;   // uniform over the warp (the block, when projecting)
   const int64_t row = slot[e];
   const int64_t p = pos[e];
-  if (row < 0 || row >= kv_rows || p < 0 || p >= kMaxRopePos) {
-    if (lane == 0) set_error(CSA2_DEV_ERR_INDEX);
+  if (row < 0 || row >= kv_rows || p < 0 || p >= kMaxRopePos || (kProject && row >= ik.k_rows)) {
+    if (lane == 0 && (!kProject || threadIdx.x == 0)) set_error(CSA2_DEV_ERR_INDEX);
+    return;
+  }
+  __shared__ float e_s[kProject ? D : 1];
+  if (kProject && threadIdx.x >= 32) {
+    __syncthreads();   // the entry is staged in e_s
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = e_s[lane * 16 + i];
+    project_indexer_block(ik, x, lane, row, threadIdx.x >> 5);
     return;
   }
   // Lane j evaluates the rotation of pair j: angle = pos * inv_freq_j (exact
@@ -113,6 +206,12 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
       x[2 * i + 1] = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
     }
   }
+  if (kProject) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) e_s[lane * 16 + i] = x[i];
+    __syncthreads();
+    project_indexer_block(ik, x, lane, row, 0);
+  }
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(x[i]));
@@ -135,19 +234,29 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
 
 cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int64_t n_entries, const int64_t *pos,
                                   const int64_t *slot, uint8_t *kv, int64_t kv_rows, float rope_theta,
-                                  cudaStream_t stream) {
+                                  cudaStream_t stream, const void *w_ik, void *k_out, int64_t k_rows, int fp4) {
   // inverse frequencies fl32(theta^(-2j/64)), j = 0..31, evaluated on the host
   RopeFreqs freqs;
   for (int j = 0; j < ROPE_DIM / 2; ++j)
     freqs.inv[j] = (float)std::pow((double)rope_theta, -(2.0 * j) / (double)ROPE_DIM);
+  IkOut ik;
+  ik.w = static_cast<const __nv_bfloat16 *>(w_ik);
+  ik.k = k_out;
+  ik.k_rows = k_rows;
+  ik.fp4 = fp4;
   // Few entries (decode): one warp per block, so that the double-precision
   // rotations of different entries run on different SMs (FP64 throughput per
   // SM is low); many entries: 8 warps per block.
   const int warps = n_entries <= 1024 ? 1 : 8;
   const int64_t blocks = (n_entries + warps - 1) / warps;
-  kv_quant_write_kernel<<<(unsigned)blocks, warps * 32, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
-      kv, kv_rows, freqs);
+  if (w_ik)
+    kv_quant_write_kernel<true><<<(unsigned)n_entries, (DI / 32) * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
+        kv, kv_rows, freqs, ik);
+  else
+    kv_quant_write_kernel<false><<<(unsigned)blocks, warps * 32, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
+        kv, kv_rows, freqs, ik);
   return cudaGetLastError();
 }
 

@@ -85,6 +85,13 @@ def test_host_validation_rejects_without_launch(c2):
     # n_max above the cache capacity
     assert L.csa2_indexer_score_topk(fake, fake, fake, 1, 100, fake, 200, None, ctypes.byref(p), fake, None,
                                      P(0x1000), 1 << 30, None) == 1
+    # the projecting KV write needs W_ik and a key cache; MXFP4 rows a multiple of 4
+    assert L.csa2_kv_quant_write_ik(fake, None, 1, 4, fake, fake, fake, 4, 10000.0, None, fake, 8, 0, None) == 1
+    assert L.csa2_kv_quant_write_ik(fake, None, 1, 4, fake, fake, fake, 4, 10000.0, fake, None, 8, 0, None) == 1
+    assert L.csa2_kv_quant_write_ik(fake, None, 1, 4, fake, fake, fake, 4, 10000.0, odd, fake, 8, 0, None) == 1
+    assert L.csa2_kv_quant_write_ik(fake, None, 1, 4, fake, fake, fake, 4, 10000.0, fake, fake, 6, 1, None) == 1
+    assert L.csa2_kv_quant_write_ik(None, None, 1, 0, None, None, None, 0, 10000.0, None, None, 0, 0, None) == 0
+    assert c2.last_launch_count() == 0
     # MXFP4 indexer-K write: rows must be a multiple of 4, pointers aligned; n = 0 is a no-op
     assert L.csa2_indexer_k_quant(fake, 4, fake, fake, 6, None) == 1
     assert L.csa2_indexer_k_quant(odd, 4, fake, fake, 8, None) == 1

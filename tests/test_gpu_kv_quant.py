@@ -110,3 +110,59 @@ def test_empty_is_noop(c2):
     e = torch.empty(0, dtype=torch.int64, device="cuda")
     c2.kv_quant_write(torch.empty(0, 512, dtype=torch.bfloat16, device="cuda"), None, 1, e, e, kv)
     assert c2.last_launch_count() == 0
+
+
+@pytest.mark.parametrize("m", [1, 2])
+def test_kv_write_with_indexer_projection(c2, orc, m):
+    """csa2_kv_quant_write_ik: the main-KV entry equals the plain writer's and
+    the oracle's bit for bit; the indexer key W_ik e is the oracle's fp64
+    projection rounded to bf16 (within one bf16 step, equal almost
+    everywhere: the GPU sums in fp32); its MXFP4 form equals the oracle's
+    codec of the oracle's key wherever the two bf16 keys agree."""
+    n, rows = 300, 512
+    g = torch.Generator().manual_seed(70 + m)
+    lat = torch.randn((n, m, 512) if m == 2 else (n, 512), generator=g).to(torch.bfloat16)
+    z = torch.randn(n, 2, 512, generator=g).to(torch.bfloat16) if m == 2 else None
+    w_ik = (torch.randn(128, 512, generator=g) / 512 ** 0.5).to(torch.bfloat16)
+    pos = torch.randint(0, 1 << 20, (n,), generator=g, dtype=torch.int64)
+    slot = torch.randperm(rows, generator=g)[:n].to(torch.int64)
+    slot[7] = rows + 3                                        # skipped, flags an index error
+    kv_plain = torch.zeros(rows, 288, dtype=torch.uint8, device="cuda")
+    kv = torch.zeros_like(kv_plain)
+    kv4 = torch.zeros_like(kv_plain)
+    k_bf = torch.zeros(rows, 128, dtype=torch.bfloat16, device="cuda")
+    k_f4 = c2.indexer_k_fp4_cache(rows)
+    zz = z.cuda() if z is not None else None
+    c2.kv_quant_write(lat.cuda(), zz, m, pos.cuda(), slot.cuda(), kv_plain)
+    assert c2.get_device_status() == 0x2
+    c2.kv_quant_write_ik(lat.cuda(), zz, m, pos.cuda(), slot.cuda(), kv, w_ik.cuda(), k_bf)
+    assert c2.get_device_status() == 0x2
+    c2.kv_quant_write_ik(lat.cuda(), zz, m, pos.cuda(), slot.cuda(), kv4, w_ik.cuda(), k_f4, indexer_fp4=True)
+    assert c2.get_device_status() == 0x2
+    ok = np.arange(n) != 7
+    okt = torch.from_numpy(ok)
+    s = slot.numpy()[ok]
+    assert torch.equal(kv, kv_plain) and torch.equal(kv4, kv_plain)
+    want = orc.kv_entries(lat[okt], z[okt] if z is not None else None, m, pos.numpy()[ok])
+    assert np.array_equal(kv.cpu().numpy()[s], want)
+    k_or = orc.indexer_k_project(lat[okt], z[okt] if z is not None else None, m, pos.numpy()[ok], w_ik)
+    got = k_bf.cpu()[s]
+    a, b = got.float().numpy().astype(np.float64), k_or.float().numpy().astype(np.float64)
+    # the oracle's own pre-quantisation entries e, for the fp32 sum's error
+    # bound: both sides round to bf16 once (half a step each), and the GPU's
+    # fp32 sum of 512 products (16-term chains, then a 5-level tree) is
+    # within 32 u sum |w e| of the exact one
+    lat_ok, z_ok = lat[okt], (z[okt] if z is not None else None)
+    e = np.stack([orc.rope_tail(orc.compress(lat_ok[i].reshape(m, 512),
+                                             z_ok[i] if z_ok is not None else None, m), int(p))
+                  for i, p in enumerate(pos.numpy()[ok])]).astype(np.float64)
+    bound = np.abs(e) @ np.abs(w_ik.double().numpy()).T * 32 * 2.0 ** -24
+    step = lambda x: np.exp2(np.floor(np.log2(np.maximum(np.abs(x), 1e-30))) - 7)
+    assert np.all(np.abs(a - b) <= 0.5 * step(a) + 0.5 * step(b) + bound)
+    same_row = (got.view(torch.int16) == k_or.view(torch.int16)).all(dim=1).numpy()
+    assert same_row.mean() > 0.8
+    oc, os_ = orc.mxfp4_quantise(k_or)
+    codes, scales = (t.cpu().numpy() for t in c2.indexer_k_fp4_planes(k_f4))
+    assert np.array_equal(codes[s][same_row], oc[same_row]) and np.array_equal(scales[s][same_row], os_[same_row])
+    untouched = np.setdiff1d(np.arange(rows), s)
+    assert not k_bf.cpu()[untouched].float().abs().sum() and not codes[untouched].any()
