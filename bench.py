@@ -27,6 +27,7 @@ import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -598,8 +599,7 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with Clocks(os.path.join(ROOT, "gpurun_out", f"clocks_r{rank}.csv") if os.path.isdir(
-            os.path.join(ROOT, "gpurun_out")) else f"/tmp/csa2_clocks_r{rank}.csv") as clk:
+    with Clocks(os.path.join(tempfile.gettempdir(), f"csa2_clocks_r{rank}.csv")) as clk:
         total_ms, live_ms = timed(args.steps, g, live)
     torch.cuda.synchronize()
     total_ms = max_over_ranks([total_ms], dev)[0]
