@@ -19,7 +19,8 @@
 // partial dot products of its 16 channels with 32 rows of W_ik at a time
 // (W_ik read as 32-byte row pieces, one per lane, coalesced), a transposed
 // warp reduction leaves row 32g + l on lane l (four warps per entry, one per
-// block of 32 rows, the entry staged in shared memory), and the row is stored as bf16
+// block of 32 rows; warps 1-3 stage W_ik in shared memory while warp 0
+// computes the entry), and the row is stored as bf16
 // (round to nearest even) or, for the MXFP4 indexer, quantised per block of
 // 32 (one block per group of 32 rows) exactly like csa2_indexer_k_quant.
 #include <cmath>
@@ -88,17 +89,30 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
   return x[0];
 }
 
+// 16 bf16 from shared memory as floats.
+__device__ __forceinline__ void lds_bf16x16(const __nv_bfloat16 *p, float (&x)[16]) {
+  const uint4 *v = reinterpret_cast<const uint4 *>(p);
+  uint4 a = v[0], b = v[1];
+  uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
 // Rows 32g .. 32g + 31 of k = W_ik e for the entry whose channels 16 lane ..
-// +15 this lane holds in x, stored at row `row` of the indexer-K cache.
-__device__ __forceinline__ void project_indexer_block(const IkOut &ik, const float (&x)[16], int lane, int64_t row,
-                                                      int g) {
+// +15 this lane holds in x (W_ik staged in shared memory as w_s), stored at
+// row `row` of the indexer-K cache.
+__device__ __forceinline__ void project_indexer_block(const IkOut &ik, const __nv_bfloat16 *w_s, const float (&x)[16],
+                                                      int lane, int64_t row, int g) {
   const int c0 = lane * 16;
   {
     float part[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) {
       float wv[16];
-      load_bf16x16(ik.w + (int64_t)(g * 32 + j) * D + c0, wv);
+      lds_bf16x16(w_s + (g * 32 + j) * D + c0, wv);
       float acc = 0.0f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) acc = fmaf(wv[i], x[i], acc);
@@ -145,12 +159,21 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
     return;
   }
   __shared__ float e_s[kProject ? D : 1];
+  extern __shared__ __align__(16) uint8_t w_dyn[];   // projecting: W_ik [128][512] bf16
+  const __nv_bfloat16 *w_s = reinterpret_cast<const __nv_bfloat16 *>(w_dyn);
   if (kProject && threadIdx.x >= 32) {
-    __syncthreads();   // the entry is staged in e_s
+    // warps 1..3 stage W_ik while warp 0 computes the entry
+    // (asynchronous 16-byte copies: all of a thread's copies in flight)
+    const uint4 *src = reinterpret_cast<const uint4 *>(ik.w);
+    uint4 *dst = reinterpret_cast<uint4 *>(w_dyn);
+    for (int i = threadIdx.x - 32; i < DI * D / 8; i += blockDim.x - 32) cp_async16(dst + i, src + i);
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();   // the entry is in e_s, W_ik in w_dyn
     float x[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) x[i] = e_s[lane * 16 + i];
-    project_indexer_block(ik, x, lane, row, threadIdx.x >> 5);
+    project_indexer_block(ik, w_s, x, lane, row, threadIdx.x >> 5);
     return;
   }
   // Lane j evaluates the rotation of pair j: angle = pos * inv_freq_j (exact
@@ -210,7 +233,7 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
 #pragma unroll
     for (int i = 0; i < 16; ++i) e_s[lane * 16 + i] = x[i];
     __syncthreads();
-    project_indexer_block(ik, x, lane, row, 0);
+    project_indexer_block(ik, w_s, x, lane, row, 0);
   }
   float amax = 0.0f;
 #pragma unroll
@@ -249,14 +272,19 @@ cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int6
   // SM is low); many entries: 8 warps per block.
   const int warps = n_entries <= 1024 ? 1 : 8;
   const int64_t blocks = (n_entries + warps - 1) / warps;
-  if (w_ik)
-    kv_quant_write_kernel<true><<<(unsigned)n_entries, (DI / 32) * 32, 0, stream>>>(
+  if (w_ik) {
+    const int smem = DI * D * 2;   // W_ik staged per block
+    cudaError_t err = cudaFuncSetAttribute(kv_quant_write_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           smem);
+    if (err != cudaSuccess) return err;
+    kv_quant_write_kernel<true><<<(unsigned)n_entries, (DI / 32) * 32, smem, stream>>>(
         static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
         kv, kv_rows, freqs, ik);
-  else
+  } else {
     kv_quant_write_kernel<false><<<(unsigned)blocks, warps * 32, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
         kv, kv_rows, freqs, ik);
+  }
   return cudaGetLastError();
 }
 
