@@ -199,13 +199,19 @@ def indexer_k_quant(k, slot, k_fp4, stream=None):
                                       _stream(stream)), "csa2_indexer_k_quant")
 
 
-def _k_idx(k_idx, params, cap):
+def _k_idx(k_idx, params, batch, cap):
     """Pointer to the indexer K cache: bf16 [B, cap, 128], or with
-    params.indexer_fp4 the uint8 MXFP4 cache of B * cap rows."""
+    params.indexer_fp4 the uint8 MXFP4 cache of exactly B * cap rows (its
+    scale plane starts after B * cap rows of codes)."""
     if k_idx is None:
         return None
     if params.indexer_fp4:
+        if k_idx.numel() != batch * cap * FP4_ENTRY_BYTES:
+            raise Csa2Error(f"k_idx: an MXFP4 cache of {batch} x {cap} rows has {batch * cap * FP4_ENTRY_BYTES} "
+                            f"bytes, got {k_idx.numel()}")
         return _ptr(k_idx, torch.uint8, "k_idx")
+    if k_idx.numel() != batch * cap * 128:
+        raise Csa2Error(f"k_idx: expected bf16 [{batch}, {cap}, 128]")
     return _ptr(k_idx, torch.bfloat16, "k_idx")
 
 
@@ -217,7 +223,7 @@ def indexer_score_topk(q_idx, w, k_idx, n_vis, n_max, params, topk_idx, ws, pool
     B = q_idx.shape[0]
     cap = k_idx.numel() // (B * FP4_ENTRY_BYTES) if params.indexer_fp4 else k_idx.shape[1]
     _check(lib().csa2_indexer_score_topk(
-        _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w, torch.float32, "w"), _k_idx(k_idx, params, cap),
+        _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w, torch.float32, "w"), _k_idx(k_idx, params, B, cap),
         B, cap, _ptr(n_vis, torch.int32, "n_vis"), int(n_max), _ptr(pool_blocks, torch.int32, "pool_blocks"),
         ctypes.byref(params), _ptr(topk_idx, torch.int32, "topk_idx"),
         _ptr(block_scores, torch.float32, "block_scores"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
@@ -252,7 +258,7 @@ def sparse_decode(mode, params, q, kv, n_vis, n_max, swa, swa_scale, swa_len, to
     _check(lib().csa2_sparse_decode(
         MODE[mode] if isinstance(mode, str) else int(mode), ctypes.byref(params), B,
         _ptr(q, torch.bfloat16, "q"), _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w, torch.float32, "w"),
-        _ptr(kv, torch.uint8, "kv"), _k_idx(k_idx, params, cap), cap,
+        _ptr(kv, torch.uint8, "kv"), _k_idx(k_idx, params, B, cap), cap,
         _ptr(n_vis, torch.int32, "n_vis"), int(n_max), _ptr(swa, torch.uint8, "swa"),
         _ptr(swa_scale, torch.float32, "swa_scale"), _ptr(swa_len, torch.int32, "swa_len"),
         _ptr(topk_idx, torch.int32, "topk_idx"), _ptr(pool_blocks, torch.int32, "pool_blocks"),
