@@ -4,12 +4,24 @@
  * The calls follow the pages' statement of the decode-time CSA2 global
  * attention of DeepSeek-V4.1-Flash:
  *   [A] "DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression"
- *       (en.mycoding.id): 2.3.2 cross-layer KV/index reuse, 2.3.4
- *       Hierarchical Sparse Indexer, 2.4.4 FP4 Main KV Cache, 3.3.1-3.3.3
- *       sparse readout and the Full/Reindex/Reuse modes.
+ *       (en.mycoding.id): 2.3.1 the compressor and the projected Indexer K,
+ *       2.3.2 cross-layer KV/index reuse, 2.3.3 the encoder's groups, 2.3.4
+ *       Hierarchical Sparse Indexer, 2.4.4 FP4 Main KV Cache and FP4 indexer
+ *       Q/K, 3.1 entry sizes, 3.3.1-3.3.3 sparse readout and the
+ *       Full/Reindex/Reuse modes.
  *   [N] "DeepSeek-V4.1-Flash - Architecture" (notes.nimendra.online):
  *       section 2 (CSA2 modes table, layer schedule, main attention settings),
  *       section 3 (Hierarchical Sparse Indexer), section 4 (KV cache formats).
+ *
+ * Calls: csa2_kv_quant_write (new main-KV entries), csa2_kv_quant_write_ik
+ * (the same plus each entry's projected indexer key), csa2_indexer_k_quant
+ * (MXFP4 indexer-K entries), csa2_indexer_score_topk (indexer + top-K, Full
+ * or Reindex), csa2_hier_pool_select (+ _static: the HSI pool),
+ * csa2_sparse_attn (the readout), csa2_sparse_decode (one layer in a mode),
+ * csa2_prefill_chunk (a chunk at m = 2); helpers csa2_workspace_bytes,
+ * csa2_get_device_status, csa2_status_string, csa2_default_params,
+ * csa2_entry_bytes, csa2_indexer_entry_bytes, csa2_last_launch_count,
+ * csa2_set_profile_events.
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers, caller-owned; the library never
