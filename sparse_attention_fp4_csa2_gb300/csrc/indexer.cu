@@ -234,25 +234,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!warp_bcast<kPool>(ok)) break;
         uint8_t *dst = kbuf + (size_t)s * kTileBytes;
         const int64_t row0 = (int64_t)b * a.cap;
-        {
-          constexpr int kBlocks = SWEEP_TILE / BLOCK;   // pool blocks per tile
-          const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
-          const int32_t blk =
-              lane < kBlocks ? __ldg(a.pool + (int64_t)b * a.pool_nb + (int64_t)t * kBlocks + lane) : -1;
-          const bool v = blk >= 0 && blk < nblk_vis;
-          if (lane < kBlocks && !v && blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) set_error(CSA2_DEV_ERR_POOL);
-          const uint32_t valid = __ballot_sync(0xffffffffu, v);
-          if (valid) {
-            if (lane == 0) mbar_arrive_expect_tx(&S.full[s], (uint32_t)__popc(valid) * (BLOCK * DI * 2));
-            __syncwarp();
-            if (v) {
-              const int32_t y = (int32_t)(row0 + (int64_t)blk * BLOCK);
-              tma_load_2d_hint(dst + lane * 1024, &tm_k, 0, y, &S.full[s], pol);
-              tma_load_2d_hint(dst + kTileBytes / 2 + lane * 1024, &tm_k, 64, y, &S.full[s], pol);
-            }
-          } else if (lane == 0) {
-            mbar_arrive(&S.full[s]);
+        constexpr int kBlocks = SWEEP_TILE / BLOCK;   // pool blocks per tile
+        const int64_t nblk_vis = ((int64_t)nv + BLOCK - 1) / BLOCK;
+        const int32_t blk =
+            lane < kBlocks ? __ldg(a.pool + (int64_t)b * a.pool_nb + (int64_t)t * kBlocks + lane) : -1;
+        const bool v = blk >= 0 && blk < nblk_vis;
+        if (lane < kBlocks && !v && blk >= nblk_vis && (int64_t)blk * BLOCK >= a.n_max) set_error(CSA2_DEV_ERR_POOL);
+        const uint32_t valid = __ballot_sync(0xffffffffu, v);
+        if (valid) {
+          if (lane == 0) mbar_arrive_expect_tx(&S.full[s], (uint32_t)__popc(valid) * (BLOCK * DI * 2));
+          __syncwarp();
+          if (v) {
+            const int32_t y = (int32_t)(row0 + (int64_t)blk * BLOCK);
+            tma_load_2d_hint(dst + lane * 1024, &tm_k, 0, y, &S.full[s], pol);
+            tma_load_2d_hint(dst + kTileBytes / 2 + lane * 1024, &tm_k, 64, y, &S.full[s], pol);
           }
+        } else if (lane == 0) {
+          mbar_arrive(&S.full[s]);
         }
         ++n_issued;
       }

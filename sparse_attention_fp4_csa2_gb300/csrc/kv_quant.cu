@@ -107,37 +107,35 @@ __device__ __forceinline__ void lds_bf16x16(const __nv_bfloat16 *p, float (&x)[1
 __device__ __forceinline__ void project_indexer_block(const IkOut &ik, const __nv_bfloat16 *w_s, const float (&x)[16],
                                                       int lane, int64_t row, int g) {
   const int c0 = lane * 16;
-  {
-    float part[32];
+  float part[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      float wv[16];
-      lds_bf16x16(w_s + (g * 32 + j) * D + c0, wv);
-      float acc = 0.0f;
+  for (int j = 0; j < 32; ++j) {
+    float wv[16];
+    lds_bf16x16(w_s + (g * 32 + j) * D + c0, wv);
+    float acc = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) acc = fmaf(wv[i], x[i], acc);
-      part[j] = acc;
-    }
-    const __nv_bfloat16 kb = __float2bfloat16_rn(transpose_reduce32(part, lane));   // row 32 g + lane
-    if (!ik.fp4) {
-      static_cast<__nv_bfloat16 *>(ik.k)[row * DI + g * 32 + lane] = kb;
-      return;
-    }
-    // MXFP4 block g: E = floor(log2 max|k|) - 2 in [-127, 127] (-127 for a
-    // zero or subnormal maximum), codes E2M1_rne_satfinite(k / 2^E)
-    const float v = __bfloat162float(kb);
-    float am = fabsf(v);
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
-    const int ef = (int)((__float_as_uint(am) >> 23) & 0xFFu);
-    const int E = (am > 0.0f && ef > 0) ? max(-127, min(127, ef - 127 - 2)) : -127;
-    const float inv = -E >= -126 ? __uint_as_float((uint32_t)(-E + 127) << 23) : __uint_as_float(0x00400000u);
-    const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-    uint8_t *planes = static_cast<uint8_t *>(ik.k);
-    if ((lane & 1) == 0)   // element 2j (this lane) in the low nibble, 2j + 1 in the high one
-      planes[row * (DI / 2) + g * 16 + (lane >> 1)] = (uint8_t)cvt_e2m1x2(partner * inv, v * inv);
-    if (lane == 0) planes[ik.k_rows * (DI / 2) + row * 4 + g] = (uint8_t)(E + 127);
+    for (int i = 0; i < 16; ++i) acc = fmaf(wv[i], x[i], acc);
+    part[j] = acc;
   }
+  const __nv_bfloat16 kb = __float2bfloat16_rn(transpose_reduce32(part, lane));   // row 32 g + lane
+  if (!ik.fp4) {
+    static_cast<__nv_bfloat16 *>(ik.k)[row * DI + g * 32 + lane] = kb;
+    return;
+  }
+  // MXFP4 block g: E = floor(log2 max|k|) - 2 in [-127, 127] (-127 for a
+  // zero or subnormal maximum), codes E2M1_rne_satfinite(k / 2^E)
+  const float v = __bfloat162float(kb);
+  float am = fabsf(v);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  const int ef = (int)((__float_as_uint(am) >> 23) & 0xFFu);
+  const int E = (am > 0.0f && ef > 0) ? max(-127, min(127, ef - 127 - 2)) : -127;
+  const float inv = -E >= -126 ? __uint_as_float((uint32_t)(-E + 127) << 23) : __uint_as_float(0x00400000u);
+  const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+  uint8_t *planes = static_cast<uint8_t *>(ik.k);
+  if ((lane & 1) == 0)   // element 2j (this lane) in the low nibble, 2j + 1 in the high one
+    planes[row * (DI / 2) + g * 16 + (lane >> 1)] = (uint8_t)cvt_e2m1x2(partner * inv, v * inv);
+  if (lane == 0) planes[ik.k_rows * (DI / 2) + row * 4 + g] = (uint8_t)(E + 127);
 }
 
 template <bool kProject>
