@@ -142,7 +142,9 @@ size_t pool_ws(int32_t batch, int64_t n_max, const csa2_params *p) {
   return topk_scratch_bytes(batch, nblk, p->candidate_topk_blocks);
 }
 
-size_t attn_ws(int32_t batch, const csa2_params *p) { return attn_scratch_bytes(batch, p->index_topk, p->sliding_window); }
+size_t attn_ws(int32_t batch, const csa2_params *p) {
+  return attn_scratch_bytes(batch, p->index_topk, p->sliding_window, p->attn_kernel);
+}
 
 size_t decode_ws(int32_t batch, int64_t n_max, const csa2_params *p) {
   const int64_t nblk = (n_max + BLOCK - 1) / BLOCK;
@@ -158,7 +160,7 @@ constexpr int64_t kPrefillBlock = 1024;   // query tokens per indexer / top-K / 
 size_t prefill_ws(int32_t batch, int64_t cap, const csa2_params *p) {
   const int64_t qb = kPrefillBlock;
   size_t b = (size_t)round_up(qb * round_up(cap, SWEEP_TILE) * 4, 256);
-  b += attn_scratch_bytes((int32_t)qb, p->index_topk, p->sliding_window);
+  b += attn_scratch_bytes((int32_t)qb, p->index_topk, p->sliding_window, p->attn_kernel);
   (void)batch;
   return b;
 }

@@ -7,103 +7,216 @@
 // 3.3.1-3.3.2: key = value = content, a convex combination of the selected
 // entries; "DeepSeek-V4.1-Flash - Architecture", section 2: 64 heads x 512,
 // top-512 + SWA-128).  FP4 stores the cache; the values are dequantised before
-// the products (section 2.4.4: FP4 reduces storage, not matmul cost).
+// the products (section 2.4.4: FP4 reduces storage, not matmul cost).  E2M1 x
+// E4M3 is exact in fp16, so the tensor cores see the dequantised values.
 //
-// Work split (flash-decoding): a CTA owns 128 keys of one query token -- one
-// chunk of the top-K list or of the SWA window -- and produces a partial (row
-// max, row sum, output).  With up to 8 chunks (the pages' 512 + 128 keys make
-// 5) the chunks of a token form one thread-block cluster and merge in shared
-// memory: each CTA pushes to every other one, by bulk shared-to-shared copies,
-// the slice of its normalised fp16 partial that CTA owns, and sums its own
-// slice into the output; with more chunks the partials go to the workspace
-// and a separate combine kernel merges them.  Inside a CTA:
-//   gather   Q arrives by TMA and the SWA rows by one bulk copy (mbarrier);
-//            every thread issues 16-byte cp.async copies of the selected FP4
-//            entries (18 per 288-byte entry) into a shared staging area;
-//   dequant  every thread turns its share of codes into fp16 (E2M1 x E4M3 is
-//            exact in fp16) in a 128B-swizzled K-major tile [128 keys x 512];
-//            SWA rows (E4M3) likewise from their staging area;
-//   S^T      = K Q^T: 32 tcgen05 MMAs (M=128 keys, N=64 heads, K=16), fp32 in
-//            TMEM; Q (bf16 -> fp16) sits in shared memory K-major;
-//   softmax  each thread owns one key row of S^T for 32 heads; per-head max
-//            and sum over the 128 keys by warp butterfly transposes + shared
-//            memory; P = exp2(S - m) (times the SWA row scale) in fp16 written
-//            MN-major [128 keys x 64 heads];
-//   O        = P V: P as A (heads as M), the same shared tile read MN-major as
-//            B (N = 2 x 256 dims, K = 128 keys); fp32 in TMEM with the heads
-//            as lanes, so a thread reads 32 consecutive dims of one head;
-//   merge    as above.
-// Shared memory: 128 KB tile (the FP4 staging area lives in its tail and is
-// consumed through registers before the tile is written; later the fp16
-// partial), 64 KB Q (reused for P, then as the merge's receive area),
-// reductions; one CTA per SM.  TMEM: 512 columns (S^T uses 128 of them, two
-// accumulation chains, and is dead before O is written).
+// Work split.  An item is one token's keys, or -- when the tokens are too few
+// to fill the SMs -- one of C <= 8 chunks of them (a chunk takes an equal
+// share of the top-K list and of the SWA rows).  With C = 1 the CTAs are
+// persistent and walk the items; with C > 1 the C chunks of a token are the
+// CTAs of one thread-block cluster and merge their partial results through L2
+// after a cluster barrier.
+//
+// Inside a CTA an item's keys go through in blocks of up to 128 (a single
+// block of up to 160 when every CTA holds one item).  Per block:
+//   dequant   8 worker warps load the block's rows (FP4 entries through the
+//             index list, or E4M3 SWA rows) into registers one block ahead,
+//             then write them as fp16 into a 128B-swizzled K-major tile
+//             [8 columns of 64 dims][rows][128 B], one column pair at a time;
+//   S = Q K^T one thread of the MMA warp issues M = 64 (heads) x N = rows x
+//             K = 512 as the column pairs land (S in TMEM, heads on lanes);
+//   softmax   the workers read S per head (thread = head, two warps per head
+//             split the keys), keep a running reference max per head that is
+//             raised only when a block exceeds it by 2^8 (then O^T is rescaled
+//             in TMEM), and write P (fp16, times the SWA row scale) K-major as
+//             [64 heads][rows];
+//   O^T      += V^T P^T: M = 128 dims (four blocks) x N = 64 heads x K = rows,
+//             V^T read MN-major from the same tile; each 128-dim block's
+//             commit frees its column pair for the next block's dequant.
+// Every MMA issue sequence is unrolled with descriptors advanced by
+// constants.  At an item's end the workers normalise O^T and write the output
+// (C = 1) or the partial (C > 1) while the next item's first block is
+// already multiplying.
+//
+// Every wait is bounded.  After a wait runs out the kernel records
+// CSA2_DEV_ERR_TIMEOUT and falls through every later wait, so that all
+// threads still meet at the same named and cluster barriers and the CTA
+// exits; its output is then undefined.
 #include "kernels.cuh"
 
 namespace csa2 {
 
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kQBytes = H * D * 2;                  // 64 KB fp16
-constexpr int kQAtomCol = H * 128;                  // 8 KB
-constexpr int kMixSwa = 32;                         // SWA rows per chunk of the mixed layout
-constexpr int kRedOff = 32768;                      // softmax reductions: in the Q region, past P
-
-// Chunk layouts.  Split (kSwa = 0): a chunk is 128 top-K entries or 128 SWA
-// rows.  Mixed (kSwa = 32): a chunk is 128 top-K entries and 32 SWA rows, so
-// the pages' 512 + 128 keys make 4 chunks instead of 5 -- chosen when the
-// chunks outnumber the SMs.  The tile is [8 columns of 64 dims][rows][128 B].
-template <int kSwa>
-struct Layout {
-  static constexpr int kRows = ATTN_CHUNK + kSwa;
-  static constexpr int kTileBytes = kRows * D * 2;                          // fp16 tile
-  static constexpr int kAtomCol = kRows * 128;                             // one 64-dim column
-  static constexpr int kStageOff = kTileBytes - ATTN_CHUNK * ENTRY_BYTES;  // FP4 staging at the tile's tail
-  static constexpr int kSwaStageOff = kTileBytes - ATTN_CHUNK * D;         // split: SWA staging, upper half
-};
+constexpr int kWorkers = 256;                    // 8 worker warps
+constexpr int kThreads = kWorkers + 32;          // + the MMA warp
+constexpr int kMmaWarp = kWorkers / 32;
+constexpr int kMaxBk = 160;                      // rows of a single-block item
+constexpr int kBlockRows = 128;                  // rows of a block of a multi-block item
+constexpr int kTileRegion = kMaxBk * D * 2;      // 160 KB
+constexpr int kQBytes = H * D * 2;               // 64 KB fp16 Q
+constexpr int kAtom = H * 128;                   // 8 KB: a 64-row atom column (Q, P^T)
+constexpr int kPOffMulti = kBlockRows * D * 2;   // P^T of multi-block items: in the tile region's tail
+constexpr int kRedOffMulti = kPOffMulti + 3 * kAtom;
+constexpr int kRedOffSingle = 3 * kAtom;         // single-block items: P^T and reductions in the Q region
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kIdescQK = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ H, /*M*/ ATTN_CHUNK);
-// O = P V: A = P (M = 128 rows: the 64 heads, then 64 rows nobody reads), B = V
-// read MN-major from the tile, N = 256 dims per instruction
-constexpr uint32_t kPVN = 256;
-constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B MN-major*/ 1, /*N*/ kPVN, /*M*/ 128);
+constexpr uint32_t kColO = 256;                  // O^T: columns 256 + 64 mt + head, lanes = dims
+constexpr float kLazy = 8.0f;                    // log2 margin before the reference max is raised
+constexpr float kLogit = 0.06375871295460785f;   // log2(e) / sqrt(512)
+constexpr float kLn2 = 0.69314718055994531f;
+constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B K-major*/ 0, /*N*/ H, /*M*/ 128);
 
-constexpr int kMaxClusterChunks = 8;   // portable cluster size
-// cluster merge: the [64 heads x 512 dims] fp16 partial is 512 groups of 128 B
-constexpr int kRowBytes = D * 2;
-constexpr int kGroups = H * kRowBytes / 128;
-
-struct __align__(16) AttnSmem {
-  float mfin[H];   // mfin, lfin adjacent: one 512-byte (m, l) record per chunk
-  float lfin[H];
-  uint64_t bar_load;
-  uint64_t bar_mma;
-  uint64_t bar_ml;
-  uint64_t bar_merge;
+struct __align__(8) Ctl {
+  uint64_t q_full, q_ready, s_full, p_full, done;
+  uint64_t cols_full[4], cols_free[4];
   uint32_t tmem_base;
-  uint32_t vmask[(ATTN_CHUNK + kMixSwa) / 32];
-  int32_t ids[ATTN_CHUNK];
-  float row_scale[ATTN_CHUNK + kMixSwa];
+  volatile uint32_t abort;
+  float rs[kMaxBk];        // per row: 1 (main entry) or the SWA row scale
+  uint8_t vld[kMaxBk];     // per row: holds a key
+  float fac[H];            // O^T rescale factor per head (block being processed)
+  float inv_l[H];          // per head at an item's end: 1 / row sum (0 if empty)
+  float mfin[H];           // per head at an item's end: reference max (log2 units)
+  float lfin[H];           // per head at an item's end: row sum
 };
 
-// cluster merge scratch, in the tile region behind the 64 KB fp16 partial
-struct MergeSmem {
-  float ml_in[kMaxClusterChunks][2][H];   // every chunk's (m, l)
-  float wgt[kMaxClusterChunks][H];        // every chunk's per-head weight
+constexpr size_t kSmemBytes = 1024 + (size_t)kTileRegion + kQBytes + sizeof(Ctl);
+static_assert(kSmemBytes <= 232448, "attention exceeds the shared-memory limit");
+static_assert(kRedOffMulti + 2 * H * 4 <= kTileRegion, "multi-block reductions overflow the tile region");
+static_assert(kRedOffSingle >= (kMaxBk / 64 + 1) * kAtom && kRedOffSingle + 2 * H * 4 <= kQBytes,
+              "single-block P^T overlaps the reductions");
+
+// One item: a token and its chunk of keys.  Item key e < nW is SWA row
+// w0 + e of the token's window; e >= nW is top-K slot k0 + e - nW.  (SWA rows
+// first: in a block of more than 128 rows the rows past 128 are then entries.)
+struct Item {
+  int64_t gp;          // token (global problem index)
+  int64_t seq_row0;    // first main-KV row of the token's sequence
+  int64_t swa_row0;    // first SWA row of the token's window
+  int swa_len;         // valid rows of the window
+  int k0, nW, w0, R, nb;
 };
 
-template <int kSwa>
-constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Layout<kSwa>::kTileBytes + kQBytes + sizeof(AttnSmem);
+__device__ __forceinline__ Item item_info(const AttnArgs &a, int item) {
+  Item it;
+  const int C = a.C;
+  const int tok = item / C, c = item - tok * C;
+  it.gp = a.p0 + tok;
+  it.seq_row0 = (it.gp / a.tokens) * a.cap;
+  it.k0 = (c * a.K) / C;
+  it.w0 = (c * a.W) / C;
+  it.nW = ((c + 1) * a.W) / C - it.w0;
+  it.R = it.nW + ((c + 1) * a.K) / C - it.k0;
+  it.nb = it.R > a.Bk ? (it.R + a.Bk - 1) / a.Bk : 1;
+  if (a.causal_swa) {
+    const int64_t seq = it.gp / a.tokens;
+    const int64_t pos = a.first_pos + it.gp % a.tokens;
+    const int64_t start = pos - a.W + 1 > 0 ? pos - a.W + 1 : 0;
+    it.swa_row0 = seq * a.swa_seq_rows + (start - a.swa_first_pos);
+    it.swa_len = (int)(pos - start + 1);
+  } else {
+    it.swa_row0 = it.gp * a.W;
+    it.swa_len = a.W > 0 ? min(__ldg(a.swa_len + it.gp), a.W) : 0;
+  }
+  return it;
 }
-static_assert(smem_bytes<kMixSwa>() <= 232448, "mixed layout exceeds the shared-memory limit");
-static_assert(kRedOff >= (ATTN_CHUNK + kMixSwa) * 128 && kRedOff + 4 * H * 4 <= kQBytes, "reductions overlap P");
 
-// byte offset of 16-byte chunk `c` (0..63 along 512 fp16 channels) of row r in a
-// K-major SW128 tile made of 64-channel columns of `col_bytes` each
-__device__ __forceinline__ uint32_t swz_off(int r, int c, int col_bytes) {
-  return (uint32_t)((c >> 3) * col_bytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// A row's data, loaded one block ahead.  FP4 entry: v[2p], v[2p+1] are the
+// codes of column cp + 2p (32 bytes), v[8].{x,y,z,w} the scale words of the
+// four columns.  SWA row: v[4p .. 4p+3] are the 64 E4M3 bytes of column cp + 2p.
+template <int N>
+struct RowBufN {
+  uint4 v[N];
+  float scale;
+  int kind;   // 0 none, 1 FP4 entry, 2 SWA row
+};
+using RowBuf = RowBufN<16>;    // an entry or a SWA row
+using EntryBuf = RowBufN<9>;   // an entry only
+
+// Top-K slot of item key e, or -1 (also for SWA rows).
+__device__ __forceinline__ int32_t row_slot(const AttnArgs &a, const Item &it, int e) {
+  if (e < it.nW || e >= it.R) return -1;
+  return __ldg(a.idx + it.gp * a.K + it.k0 + (e - it.nW));
+}
+
+template <int N>
+__device__ __forceinline__ void load_row(const AttnArgs &a, const Item &it, int e, int32_t id, int cp,
+                                         RowBufN<N> &b) {
+  b.kind = 0;
+  b.scale = 0.0f;
+  if (e >= it.R) return;
+  if (e >= it.nW) {
+    if (id < 0) return;
+    if (id >= a.cap) {
+      set_error(CSA2_DEV_ERR_INDEX);
+      return;
+    }
+    const uint8_t *src = a.kv + (it.seq_row0 + id) * ENTRY_BYTES;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const int c = cp + 2 * p;
+      b.v[2 * p] = __ldg(reinterpret_cast<const uint4 *>(src + 32 * c));
+      b.v[2 * p + 1] = __ldg(reinterpret_cast<const uint4 *>(src + 32 * c + 16));
+    }
+    const uint32_t *sp = reinterpret_cast<const uint32_t *>(src + 256);
+    b.v[8] = make_uint4(__ldg(sp + cp), __ldg(sp + cp + 2), __ldg(sp + cp + 4), __ldg(sp + cp + 6));
+    b.scale = 1.0f;
+    b.kind = 1;
+  } else if constexpr (N == 16) {
+    const int t = it.w0 + e;
+    if (t >= it.swa_len) return;
+    const uint8_t *src = a.swa + (it.swa_row0 + t) * D;
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        b.v[4 * p + u] = __ldg(reinterpret_cast<const uint4 *>(src + 64 * (cp + 2 * p) + 16 * u));
+    b.scale = __ldg(a.swa_scale + it.swa_row0 + t);
+    b.kind = 2;
+  }
+}
+
+// Column c = cp + 2p of row r as fp16 into the tile (16-byte chunk i of the
+// row's 128-byte segment at (i ^ (r & 7)) * 16).
+template <int P, int N>
+__device__ __forceinline__ void dequant_col(uint8_t *tile, uint32_t col_stride, int r, int cp, const RowBufN<N> &b) {
+  uint8_t *rowp = tile + (uint32_t)(cp + 2 * P) * col_stride + (uint32_t)r * 128;
+  const int sw = r & 7;
+  if (b.kind == 1) {
+    const uint32_t sc = P == 0 ? b.v[8].x : P == 1 ? b.v[8].y : P == 2 ? b.v[8].z : b.v[8].w;
+    const uint32_t w[8] = {b.v[2 * P].x, b.v[2 * P].y, b.v[2 * P].z, b.v[2 * P].w,
+                           b.v[2 * P + 1].x, b.v[2 * P + 1].y, b.v[2 * P + 1].z, b.v[2 * P + 1].w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      // 8 codes = 8 dims of scale group i / 2
+      const uint32_t sb = (sc >> (8 * (i >> 1))) & 0xFFu;
+      const uint32_t s2 = e4m3x2_to_half2((uint16_t)(sb | (sb << 8)));
+      uint32_t h[4];
+      e2m1x8_to_half2x4(w[i], h);
+      const uint4 o = make_uint4(hmul2_u32(h[0], s2), hmul2_u32(h[1], s2), hmul2_u32(h[2], s2), hmul2_u32(h[3], s2));
+      *reinterpret_cast<uint4 *>(rowp + ((i ^ sw) << 4)) = o;
+    }
+    return;
+  }
+  if constexpr (N == 16) {
+    if (b.kind == 2) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 raw = b.v[4 * P + u];
+        const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+        const uint4 o0 =
+            make_uint4(e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)), e4m3x2_to_half2((uint16_t)(w[0] >> 16)),
+                       e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)), e4m3x2_to_half2((uint16_t)(w[1] >> 16)));
+        const uint4 o1 =
+            make_uint4(e4m3x2_to_half2((uint16_t)(w[2] & 0xFFFF)), e4m3x2_to_half2((uint16_t)(w[2] >> 16)),
+                       e4m3x2_to_half2((uint16_t)(w[3] & 0xFFFF)), e4m3x2_to_half2((uint16_t)(w[3] >> 16)));
+        *reinterpret_cast<uint4 *>(rowp + (((2 * u) ^ sw) << 4)) = o0;
+        *reinterpret_cast<uint4 *>(rowp + (((2 * u + 1) ^ sw) << 4)) = o1;
+      }
+      return;
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4 *>(rowp + ((i ^ sw) << 4)) = make_uint4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
@@ -111,60 +224,143 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Butterfly transpose-reduction over the 32 lanes of a warp: on entry every
-// lane holds v[0..31] (one value per head column); on exit v[0] of lane l holds
-// the reduction over all lanes of column l.
-template <bool kMax>
-__device__ __forceinline__ void warp_transpose_reduce(float (&v)[32], int lane) {
+// Bounded wait that falls through once any role has given up.
+__device__ __forceinline__ void wait_ft(Ctl &S, uint64_t *bar, uint32_t parity) {
+  if (S.abort) return;
+  if (!mbar_wait(bar, parity)) S.abort = 1;
+}
+
+// The next block a worker loads: with C = 1 the CTA strides through the
+// items; with C > 1 it holds exactly one.
+struct Cursor {
+  int item, j;
+  Item it;
+  __device__ __forceinline__ void advance(const AttnArgs &a, int stride, int items) {
+    if (++j >= it.nb) {
+      j = 0;
+      item += stride;
+      if (item < items) it = item_info(a, item);
+    }
+  }
+};
+
+// The finished item's output: out = O^T / l (C = 1), or (C > 1) this chunk's
+// (m, l) and its normalised partial (fp16, [dim][head]) for the dims the other
+// chunks own; the merge follows a cluster barrier.
+__device__ __forceinline__ void item_epilogue(const AttnArgs &a, Ctl &S, int item, uint32_t s_row, int tid, int q4,
+                                              int wh, int lane) {
+  const int64_t gp = a.p0 + item / a.C;
+  bar_named(1, kWorkers);   // inv_l / mfin / lfin of the item are visible
+  tc_fence_after();
+  if (a.C == 1) {
+    float *outp = a.out + gp * H * D;
+#pragma unroll 1
+    for (int mm = 0; mm < 2; ++mm) {
+      const int mt = 2 * wh + mm;
+      const int d = mt * 128 + 32 * q4 + lane;
+#pragma unroll 1
+      for (int hb = 0; hb < 2; ++hb) {
+        uint32_t v[32];
+        tmem_ld32(s_row + kColO + (uint32_t)(mt * H + hb * 32), v);
+        tmem_ld_wait();
 #pragma unroll
-  for (int o = 16, n = 32; o >= 1; o >>= 1, n >>= 1) {
-    const bool upper = (lane & o) != 0;
+        for (int i = 0; i < 32; ++i) {
+          const int hh = hb * 32 + i;
+          outp[hh * D + d] = S.abort ? 0.0f : __uint_as_float(v[i]) * S.inv_l[hh];
+        }
+      }
+    }
+    if (tid < H && a.lse)
+      a.lse[gp * H + tid] = S.lfin[tid] > 0.0f ? (S.mfin[tid] + log2f(S.lfin[tid])) * kLn2 : -INFINITY;
+    return;
+  }
+  const int rank = item % a.C;
+  const int dc = D / a.C;   // dims per owner
+  __half *po = a.part_o + (int64_t)item * D * H;
+  if (tid < H) {
+    a.part_ml[(int64_t)item * 2 * H + tid] = S.mfin[tid];
+    a.part_ml[(int64_t)item * 2 * H + H + tid] = S.lfin[tid];
+  }
+#pragma unroll 1
+  for (int mm = 0; mm < 2; ++mm) {
+    const int mt = 2 * wh + mm;
+    const int d = mt * 128 + 32 * q4 + lane;
+#pragma unroll 1
+    for (int hb = 0; hb < 2; ++hb) {
+      uint32_t v[32];
+      tmem_ld32(s_row + kColO + (uint32_t)(mt * H + hb * 32), v);
+      tmem_ld_wait();
+      if (d / dc != rank) {
+        uint4 *dst = reinterpret_cast<uint4 *>(po + (int64_t)d * H + hb * 32);
+        const float *il = S.inv_l + hb * 32;
 #pragma unroll
-    for (int i = 0; i < n / 2; ++i) {
-      const float send = upper ? v[i] : v[i + n / 2];
-      const float keep = upper ? v[i + n / 2] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, o);
-      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+        for (int k = 0; k < 4; ++k)
+          dst[k] = make_uint4(pack_half2(__uint_as_float(v[8 * k + 0]) * il[8 * k + 0],
+                                         __uint_as_float(v[8 * k + 1]) * il[8 * k + 1]),
+                              pack_half2(__uint_as_float(v[8 * k + 2]) * il[8 * k + 2],
+                                         __uint_as_float(v[8 * k + 3]) * il[8 * k + 3]),
+                              pack_half2(__uint_as_float(v[8 * k + 4]) * il[8 * k + 4],
+                                         __uint_as_float(v[8 * k + 5]) * il[8 * k + 5]),
+                              pack_half2(__uint_as_float(v[8 * k + 6]) * il[8 * k + 6],
+                                         __uint_as_float(v[8 * k + 7]) * il[8 * k + 7]));
+      }
     }
   }
 }
 
-template <int kSwa>
+// Q of an item: bf16 -> fp16 in place (the same 2-byte slots of the swizzled
+// layout; |q| < 65504 assumed), once its copy has landed.
+__device__ __forceinline__ void convert_q(uint8_t *qs, int tid) {
+  for (int i = tid; i < kQBytes / 16; i += kWorkers) {
+    uint4 *ptr = reinterpret_cast<uint4 *>(qs) + i;
+    const uint4 v = *ptr;
+    *ptr = make_uint4(pack_half2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)),
+                      pack_half2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)),
+                      pack_half2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u)),
+                      pack_half2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)));
+  }
+  fence_proxy_async_smem();
+}
+
+// Q of an item's token by TMA (bf16, 8 boxes of [64 heads x 64 dims], 128B swizzle).
+__device__ __forceinline__ void load_q(const AttnArgs &a, Ctl &S, const CUtensorMap &tm_q, uint8_t *qs, int item) {
+  const int64_t gp = a.p0 + item / a.C;
+  mbar_arrive_expect_tx(&S.q_full, (uint32_t)kQBytes);
+#pragma unroll
+  for (int c = 0; c < D / 64; ++c) tma_load_2d(qs + c * kAtom, &tm_q, c * 64, (int32_t)(gp * H), &S.q_full);
+}
+
+template <bool kSingle>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a) {
-  using Lay = Layout<kSwa>;
-  constexpr bool kMixed = kSwa > 0;
-  constexpr int kAtomCol = Lay::kAtomCol;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *tile = base;                  // [8 cols][rows][128 B] fp16, SW128
-  uint8_t *qs = base + Lay::kTileBytes;  // [8 cols][64 heads][128 B] fp16, SW128; later P
-  AttnSmem &S = *reinterpret_cast<AttnSmem *>(qs + kQBytes);
-  MergeSmem &MS = *reinterpret_cast<MergeSmem *>(tile + H * D * 2);
-  float(*red)[H] = reinterpret_cast<float(*)[H]>(qs + kRedOff);   // [4][64]: live only in the softmax
+  uint8_t *tile = base;
+  uint8_t *qs = base + kTileRegion;
+  Ctl &S = *reinterpret_cast<Ctl *>(qs + kQBytes);
+  // kSingle: every CTA holds one item of one block (up to 160 rows), and P^T
+  // and the reductions live in the Q region once S has read Q
+  uint8_t *pbuf = kSingle ? qs : tile + kPOffMulti;
+  float(*red)[H] = reinterpret_cast<float(*)[H]>(kSingle ? qs + kRedOffSingle : tile + kRedOffMulti);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk = blockIdx.x, p = blockIdx.y;   // p: this launch's problem (block-local)
-  const int64_t gp = a.p0 + p;                     // the query token it serves
-  const bool is_swa = !kMixed && chunk >= a.n_kchunks;   // split layout: a chunk of SWA rows
-  const int64_t seq = gp / a.tokens;
-  const int64_t seq_row0 = seq * a.cap;           // the token's sequence in the main-KV cache
+  const int items = a.problems * a.C;
+  const int first_item = blockIdx.x;
+  const int stride = gridDim.x;
 
   if (tid == 0) {
-    mbar_init(&S.bar_load, 1);
-    mbar_init(&S.bar_mma, 1);
-    mbar_init(&S.bar_ml, 1);
-    mbar_init(&S.bar_merge, 1);
-    if (a.cluster) {
-      // armed before the first cluster barrier, so before any peer's copy
-      // into this CTA can start: every other chunk sends its (m, l) record
-      // and this CTA's slice of its partial
-      const uint32_t crank = cluster_ctarank(), nct = cluster_nctarank();
-      const uint32_t slice = ((crank + 1) * kGroups / nct - crank * kGroups / nct) * 128;
-      mbar_arrive_expect_tx(&S.bar_ml, (nct - 1) * (2 * H * 4));
-      mbar_arrive_expect_tx(&S.bar_merge, (nct - 1) * slice);
+    mbar_init(&S.q_full, 1);
+    mbar_init(&S.q_ready, kWorkers);
+    mbar_init(&S.s_full, 1);
+    mbar_init(&S.p_full, kWorkers);
+    mbar_init(&S.done, 1);
+    for (int p = 0; p < 4; ++p) {
+      mbar_init(&S.cols_full[p], kWorkers);
+      mbar_init(&S.cols_free[p], 1);
     }
+    S.abort = 0;
     fence_barrier_init();
+    prefetch_tmap(&tm_q);
   }
   if (warp == 0) {
     tmem_alloc(&S.tmem_base, kTmemCols);
@@ -174,447 +370,339 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
-  bool ok = true;
+  const uint32_t col_stride = (uint32_t)a.Bk * 128;   // bytes per 64-dim column of the tile
 
-  // ------------------------------------------------------------------ loads
-  // One mbarrier counts the bulk bytes: Q (8 TMA boxes of [64 heads x 64
-  // dims] bf16 into the SW128 K-major layout) and the chunk's SWA rows (split:
-  // one contiguous copy into the tile's upper half; mixed: 8-row pieces into
-  // the SWA-row areas of tile columns 0-3, which the top-K rows never touch).
-  // The selected FP4 entries arrive by cp.async into the tile's tail.
-  constexpr int kSwaPer = kMixed ? kSwa : ATTN_CHUNK;   // SWA rows per chunk
-  constexpr int kSwaRow = kMixed ? ATTN_CHUNK : 0;      // their first tile row
-  const int t0 = kMixed ? chunk * kSwa : (chunk - a.n_kchunks) * ATTN_CHUNK;   // first SWA row of this chunk
-  int swa_rows = 0;
-  int64_t swa_row0 = 0;                              // first SWA row of the token's window
-  if (kMixed || is_swa) {
-    int len;
-    if (a.causal_swa) {
-      const int64_t pos = a.first_pos + gp % a.tokens;
-      const int64_t start = pos - a.W + 1 > 0 ? pos - a.W + 1 : 0;
-      swa_row0 = seq * a.swa_seq_rows + (start - a.swa_first_pos);
-      len = (int)(pos - start + 1);
-    } else {
-      swa_row0 = gp * a.W;
-      len = min(__ldg(a.swa_len + gp), a.W);
-    }
-    swa_rows = max(0, min(kSwaPer, len - t0));
-    if (tid < kSwaPer)
-      S.row_scale[kSwaRow + tid] = (tid < swa_rows) ? __ldg(a.swa_scale + swa_row0 + t0 + tid) : 0.0f;
-  }
-  if (!is_swa && tid < ATTN_CHUNK) S.row_scale[tid] = 1.0f;
-  if (tid == 0) {
-    // Q and the SWA rows first: their latency overlaps the index loads below
-    const uint32_t bytes = (uint32_t)kQBytes + (uint32_t)swa_rows * D;
-    mbar_arrive_expect_tx(&S.bar_load, bytes);
+  if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA
+    if (lane == 0) {
+      const uint32_t id_s = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ (uint32_t)a.Bk, /*M*/ 64);
+      const uint64_t qd = smem_desc(smem_u32(qs), 16, 1024);
+      const uint64_t td = smem_desc(smem_u32(tile), 16, 1024);
+      const uint64_t vd = smem_desc(smem_u32(tile), col_stride, 1024);
+      const uint64_t pd = smem_desc(smem_u32(pbuf), 16, 1024);
+      const uint64_t cs16 = col_stride >> 4;
+      const int nks = a.Bk / 16;
+      uint32_t g = 0, n_item = 0;
+      if (first_item < items) load_q(a, S, tm_q, qs, first_item);
+      for (int item = first_item; item < items; item += stride, ++n_item) {
+        const Item it = item_info(a, item);
+        for (int j = 0; j < it.nb; ++j, ++g) {
+          const uint32_t ph = g & 1u;
+          if (j == 0) wait_ft(S, &S.q_ready, n_item & 1u);
+          // (no MMA sits under a per-instruction condition: a conditional
+          // tcgen05.mma in unrolled code was observed to issue wrongly)
 #pragma unroll
-    for (int j = 0; j < D / 64; ++j) tma_load_2d(qs + j * kQAtomCol, &tm_q, j * 64, (int32_t)(gp * H), &S.bar_load);
-    if (kMixed) {
-      for (int i = 0; i * 8 < swa_rows; ++i)
-        bulk_g2s(tile + i * kAtomCol + ATTN_CHUNK * 128, a.swa + (swa_row0 + t0 + 8 * i) * D,
-                 (uint32_t)min(8, swa_rows - 8 * i) * D, &S.bar_load);
-    } else if (is_swa && swa_rows > 0) {
-      bulk_g2s(tile + Lay::kSwaStageOff, a.swa + (swa_row0 + t0) * D, (uint32_t)swa_rows * D, &S.bar_load);
-    }
-  }
-  if (tid < ATTN_CHUNK) {
-    bool v;
-    if (!is_swa) {
-      const int j = chunk * ATTN_CHUNK + tid;
-      int32_t id = (j < a.K) ? __ldg(a.idx + gp * a.K + j) : -1;
-      if (id >= a.cap) {
-        set_error(CSA2_DEV_ERR_INDEX);
-        id = -1;
+          for (int p = 0; p < 4; ++p) {
+            wait_ft(S, &S.cols_full[p], ph);
+            tc_fence_after();
+            const uint64_t a0 = qd + (uint64_t)(p * 2 * kAtom >> 4), a1 = a0 + (kAtom >> 4);
+            const uint64_t b0 = td + 2 * p * cs16, b1 = b0 + cs16;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mma_f16(tmem, a0 + 2 * i, b0 + 2 * i, id_s, (p | i) ? 1u : 0u);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) mma_f16(tmem, a1 + 2 * i, b1 + 2 * i, id_s, 1u);
+          }
+          mma_commit(&S.s_full);
+          if (j == it.nb - 1 && item + stride < items) {
+            // Q is read by the last block's S: reload it for the next item
+            wait_ft(S, &S.s_full, ph);
+            if (!S.abort) load_q(a, S, tm_q, qs, item + stride);
+          }
+          wait_ft(S, &S.p_full, ph);
+          tc_fence_after();
+          const uint32_t acc0 = j > 0 ? 1u : 0u;
+#pragma unroll
+          for (int mt = 0; mt < 4; ++mt) {
+            const uint64_t va = vd + 2 * mt * cs16;
+            const uint32_t dt = tmem + kColO + (uint32_t)(mt * H);
+            // 16 keys per step; nks varies with the block size, so a plain loop
+#pragma unroll 1
+            for (int ks = 0; ks < nks; ++ks)
+              mma_f16(dt, va + (uint64_t)ks * 128, pd + (uint64_t)((ks >> 2) * (kAtom >> 4) + (ks & 3) * 2), kIdescPV,
+                      (acc0 | (uint32_t)ks) ? 1u : 0u);
+            mma_commit(&S.cols_free[mt]);
+          }
+        }
       }
-      S.ids[tid] = id;
-      v = id >= 0;
-    } else {
-      v = tid < swa_rows;
-    }
-    const uint32_t m = __ballot_sync(0xffffffffu, v);
-    if (lane == 0) S.vmask[warp] = m;
-  } else if (kMixed && warp == ATTN_CHUNK / 32) {
-    const uint32_t m = __ballot_sync(0xffffffffu, lane < swa_rows);
-    if (lane == 0) S.vmask[warp] = m;
-  }
-  if (!is_swa) {
-    // gather: the selected entries' 288 bytes as 18 16-byte pieces each, all
-    // threads issuing their cp.async copies at once
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < (ATTN_CHUNK * ENTRY_BYTES / 16) / kThreads; ++j) {
-      const int c = tid + j * kThreads;
-      const int e = c / (ENTRY_BYTES / 16), piece = c % (ENTRY_BYTES / 16);
-      const int32_t id = S.ids[e];
-      if (id >= 0)
-        cp_async16(tile + Lay::kStageOff + e * ENTRY_BYTES + piece * 16,
-                   a.kv + (seq_row0 + id) * ENTRY_BYTES + piece * 16);
-    }
-    cp_async_commit();
-  }
-  ok = mbar_wait(&S.bar_load, 0);
-
-  // Q: bf16 -> fp16 in place (same 2-byte slots of the swizzled layout;
-  // |q| < 65504 assumed)
-#pragma unroll 4
-  for (int i = tid; i < kQBytes / 16; i += kThreads) {
-    uint4 *ptr = reinterpret_cast<uint4 *>(qs) + i;
-    const uint4 v = *ptr;
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint4 o;
-    o.x = pack_half2(__uint_as_float(w[0] << 16), __uint_as_float(w[0] & 0xFFFF0000u));
-    o.y = pack_half2(__uint_as_float(w[1] << 16), __uint_as_float(w[1] & 0xFFFF0000u));
-    o.z = pack_half2(__uint_as_float(w[2] << 16), __uint_as_float(w[2] & 0xFFFF0000u));
-    o.w = pack_half2(__uint_as_float(w[3] << 16), __uint_as_float(w[3] & 0xFFFF0000u));
-    *ptr = o;
-  }
-
-  // ---------------------------------------------------------------- dequant
-  const int row = tid >> 1, half = tid & 1;   // 2 threads per key, 256 channels each
-  if (!is_swa) {
-    cp_async_wait_all();
-    __syncthreads();   // every thread's gathered pieces have landed
-    const bool valid = (S.vmask[row >> 5] >> (row & 31)) & 1;
-    uint4 codes[8];
-    uint4 scl;
-    const uint8_t *src = tile + Lay::kStageOff + row * ENTRY_BYTES;
-    if (valid && ok) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) codes[k] = *reinterpret_cast<const uint4 *>(src + half * 128 + k * 16);
-      scl = *reinterpret_cast<const uint4 *>(src + 256 + half * 16);
-    } else {
-#pragma unroll
-      for (int k = 0; k < 8; ++k) codes[k] = make_uint4(0, 0, 0, 0);
-      scl = make_uint4(0, 0, 0, 0);
-    }
-    // mixed: the 32 SWA rows -- thread (r, j) takes dims 64j..64j+63 of row r
-    // from its staging piece (column r / 8, slot r % 8); read now, so that
-    // one barrier covers both staging areas
-    const int sr = tid >> 3, sj = tid & 7;
-    uint4 sraw[4];
-    if (kMixed) {
-      const bool sv = sr < swa_rows && ok;
-      const uint4 *ssrc =
-          reinterpret_cast<const uint4 *>(tile + (sr >> 3) * kAtomCol + ATTN_CHUNK * 128 + (sr & 7) * D + sj * 64);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sraw[k] = sv ? ssrc[k] : make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();   // the staging areas are read; the tile may now be written over them
-    const uint32_t sw[4] = {scl.x, scl.y, scl.z, scl.w};
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      // 16 bytes of codes = 32 channels = scale groups 2k, 2k+1 of this half
-      const uint32_t cw[4] = {codes[k].x, codes[k].y, codes[k].z, codes[k].w};
-#pragma unroll
-      for (int g = 0; g < 2; ++g) {
-        const uint32_t sb = (sw[k >> 1] >> (8 * ((k & 1) * 2 + g))) & 0xFFu;
-        const uint32_t s2 = e4m3x2_to_half2((uint16_t)(sb | (sb << 8)));
-        uint32_t h0[4], h1[4];
-        e2m1x8_to_half2x4(cw[2 * g], h0);
-        e2m1x8_to_half2x4(cw[2 * g + 1], h1);
-        uint4 o0, o1;
-        o0.x = hmul2_u32(h0[0], s2); o0.y = hmul2_u32(h0[1], s2);
-        o0.z = hmul2_u32(h0[2], s2); o0.w = hmul2_u32(h0[3], s2);
-        o1.x = hmul2_u32(h1[0], s2); o1.y = hmul2_u32(h1[1], s2);
-        o1.z = hmul2_u32(h1[2], s2); o1.w = hmul2_u32(h1[3], s2);
-        const int ch16 = half * 32 + k * 4 + g * 2;   // 16-byte chunk index of the first 8 channels
-        *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16, kAtomCol)) = o0;
-        *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16 + 1, kAtomCol)) = o1;
-      }
-    }
-    if (kMixed) {
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t w[4] = {sraw[k].x, sraw[k].y, sraw[k].z, sraw[k].w};
-        uint4 o0, o1;
-        o0.x = e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)); o0.y = e4m3x2_to_half2((uint16_t)(w[0] >> 16));
-        o0.z = e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)); o0.w = e4m3x2_to_half2((uint16_t)(w[1] >> 16));
-        o1.x = e4m3x2_to_half2((uint16_t)(w[2] & 0xFFFF)); o1.y = e4m3x2_to_half2((uint16_t)(w[2] >> 16));
-        o1.z = e4m3x2_to_half2((uint16_t)(w[3] & 0xFFFF)); o1.w = e4m3x2_to_half2((uint16_t)(w[3] >> 16));
-        const int ch16 = sj * 8 + k * 2;
-        *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + sr, ch16, kAtomCol)) = o0;
-        *reinterpret_cast<uint4 *>(tile + swz_off(ATTN_CHUNK + sr, ch16 + 1, kAtomCol)) = o1;
-      }
+      // every MMA of this CTA has completed before the teardown
+      mma_commit(&S.done);
+      wait_ft(S, &S.done, 0);
     }
   } else {
-    // SWA rows (E4M3) staged in the tile's upper half: through registers, then
-    // converted to fp16 (exact) into the tile
-    const bool valid = row < swa_rows && ok;
-    uint4 raw[16];
-    const uint4 *src = reinterpret_cast<const uint4 *>(tile + Lay::kSwaStageOff + row * D + half * 256);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) raw[k] = valid ? src[k] : make_uint4(0, 0, 0, 0);
-    __syncthreads();   // the staging area is read; the tile may now be written over it
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-      uint4 o0, o1;
-      o0.x = e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)); o0.y = e4m3x2_to_half2((uint16_t)(w[0] >> 16));
-      o0.z = e4m3x2_to_half2((uint16_t)(w[1] & 0xFFFF)); o0.w = e4m3x2_to_half2((uint16_t)(w[1] >> 16));
-      o1.x = e4m3x2_to_half2((uint16_t)(w[2] & 0xFFFF)); o1.y = e4m3x2_to_half2((uint16_t)(w[2] >> 16));
-      o1.z = e4m3x2_to_half2((uint16_t)(w[3] & 0xFFFF)); o1.w = e4m3x2_to_half2((uint16_t)(w[3] >> 16));
-      const int ch16 = half * 32 + k * 2;
-      *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16, kAtomCol)) = o0;
-      *reinterpret_cast<uint4 *>(tile + swz_off(row, ch16 + 1, kAtomCol)) = o1;
-    }
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
+    // -------------------------------------------------------------- workers
+    const int cp = tid & 1;                          // columns cp, cp + 2, cp + 4, cp + 6
+    const int r0 = tid >> 1;                         // rows r0 and (single blocks > 128 rows) 128 + r0
+    const bool two_rows = kSingle && (128 + r0) < a.Bk;
+    const int q4 = warp & 3, wh = warp >> 2;         // TMEM lane quadrant, warp half
+    const bool head_lane = lane < 16;                // S lanes 0-15 of each quadrant hold heads
+    const int h = 16 * q4 + (lane & 15);             // head of this thread in the softmax
+    const uint32_t s_row = tmem + ((uint32_t)(32 * q4) << 16);
+    const int nslab = a.Bk / 16;
 
-  // ------------------------------------------------------------- S^T = K Q^T
-  if (tid == 0 && ok) {
-    tc_fence_after();
-    const uint32_t ta = smem_u32(tile), qa = smem_u32(qs);
-    // even and odd K steps accumulate into two column blocks, two
-    // independent chains that the softmax adds
-#pragma unroll 4
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t aa = ta + (kk >> 2) * kAtomCol + (kk & 3) * 32;
-      const uint64_t bd = smem_desc(qa + (kk >> 2) * kQAtomCol + (kk & 3) * 32, 16, 1024);
-      mma_f16(tmem + (uint32_t)((kk & 1) * H), smem_desc(aa, 16, 1024), bd, kIdescQK, kk > 1 ? 1u : 0u);
-      // mixed: the same over tile rows 32..159, whose D lanes 96..127 are the SWA rows
-      if (kMixed)
-        mma_f16(tmem + (uint32_t)((2 + (kk & 1)) * H), smem_desc(aa + 32 * 128, 16, 1024), bd, kIdescQK,
-                kk > 1 ? 1u : 0u);
+    // `cur`: the block being processed; `ld`: the next block to load into
+    // registers, whose top-K slot `ld_id` was requested one block earlier
+    Cursor cur;
+    cur.item = first_item;
+    cur.j = 0;
+    if (cur.item < items) cur.it = item_info(a, cur.item);
+    RowBuf b0;
+    EntryBuf b1;   // kSingle: row 128 + r0 (an entry: SWA rows come first)
+    Cursor ld = cur;
+    int32_t ld_id = -1;
+    if (cur.item < items) {
+      load_row(a, cur.it, r0, row_slot(a, cur.it, r0), cp, b0);
+      if (two_rows) load_row(a, cur.it, 128 + r0, row_slot(a, cur.it, 128 + r0), cp, b1);
+      if constexpr (!kSingle) {
+        ld.advance(a, stride, items);
+        if (ld.item < items) ld_id = row_slot(a, ld.it, ld.j * a.Bk + r0);
+      }
     }
-    mma_commit(&S.bar_mma);
-  }
-  if (ok) ok = mbar_wait(&S.bar_mma, 0);
-  tc_fence_after();
 
-  // ---------------------------------------------------------------- softmax
-  // Warp w owns key rows 32 (w % 4) .. + 31 (its TMEM lane quadrant) for heads
-  // 32 (w / 4) .. + 31; in the mixed layout warps 3 and 7 also own the SWA
-  // rows 128..159 (lanes 96..127 of the second accumulator).
-  const int quad = warp & 3, hh = warp >> 2;
-  const int key = quad * 32 + lane;
-  const bool extra = kMixed && quad == 3;
-  const int key2 = ATTN_CHUNK + lane;
-  // log2(e) / sqrt(512), times the SWA row scale (the key is code x scale)
-  constexpr float kLogit = 0.06375871295460785f;
-  float s[32], s2[32];
-  {
-    uint32_t v[32], v2[32];
-    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(hh * 32), v);
-    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(H + hh * 32), v2);
-    tmem_ld_wait();
-    const bool valid = ok && ((S.vmask[key >> 5] >> (key & 31)) & 1);
-    const float f = kLogit * S.row_scale[key];
+    uint32_t g = 0, n_item = 0;
+    bool epi_pending = false;
+    int epi_item = 0;
+    float m_ref = -INFINITY, l_part = 0.0f;
+
+    for (; cur.item < items; ++g) {
+      const uint32_t ph = g & 1u;
+      const int j = cur.j;
+      // ------------------------------------------------------ Q of a new item
+      if (j == 0 && n_item == 0) {
+        wait_ft(S, &S.q_full, 0);
+        convert_q(qs, tid);
+        mbar_arrive(&S.q_ready);
+      }
+      // --------------------------------------------------------- dequant
 #pragma unroll
-    for (int i = 0; i < 32; ++i) s[i] = valid ? (__uint_as_float(v[i]) + __uint_as_float(v2[i])) * f : -INFINITY;
-  }
-  if (extra) {
-    uint32_t v[32], v2[32];
-    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(2 * H + hh * 32), v);
-    tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(3 * H + hh * 32), v2);
-    tmem_ld_wait();
-    const bool valid = ok && ((S.vmask[key2 >> 5] >> (key2 & 31)) & 1);
-    const float f = kLogit * S.row_scale[key2];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) s2[i] = valid ? (__uint_as_float(v[i]) + __uint_as_float(v2[i])) * f : -INFINITY;
-  }
-  {
-    float t[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) t[i] = extra ? fmaxf(s[i], s2[i]) : s[i];
-    warp_transpose_reduce<true>(t, lane);
-    red[quad][hh * 32 + lane] = t[0];
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (tid < H) S.mfin[tid] = fmaxf(fmaxf(red[0][tid], red[1][tid]), fmaxf(red[2][tid], red[3][tid]));
-  __syncthreads();
-  {
-    // P = 2^(s - m) per head, times the row scale, as fp16 [rows][64 heads],
-    // MN-major SW128 (row r at byte 128 r, 16-byte chunks XOR r % 8)
-    float t[32];
-    auto write_p = [&](const float(&sv)[32], int k, bool acc) {
-      const float rs = S.row_scale[k];
-      uint8_t *prow = qs + k * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i0 = c * 8 + 2 * q;
-          const float m0 = S.mfin[hh * 32 + i0], m1 = S.mfin[hh * 32 + i0 + 1];
-          const float p0 = (m0 == -INFINITY) ? 0.0f : exp2f(sv[i0] - m0);
-          const float p1 = (m1 == -INFINITY) ? 0.0f : exp2f(sv[i0 + 1] - m1);
-          t[i0] = acc ? t[i0] + p0 : p0;
-          t[i0 + 1] = acc ? t[i0 + 1] + p1 : p1;
-          w[q] = pack_half2(p0 * rs, p1 * rs);
+      for (int p = 0; p < 4; ++p) {
+        if (g > 0) wait_ft(S, &S.cols_free[p], (g - 1) & 1u);
+        if (p == 0 && cp == 0) {
+          if (r0 < a.Bk) {
+            S.rs[r0] = b0.scale;
+            S.vld[r0] = b0.kind != 0 ? 1 : 0;
+          }
+          if (two_rows) {
+            S.rs[128 + r0] = b1.scale;
+            S.vld[128 + r0] = b1.kind != 0 ? 1 : 0;
+          }
         }
-        *reinterpret_cast<uint4 *>(prow + (((hh * 4 + c) ^ (k & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (r0 < a.Bk) {
+          if (p == 0) dequant_col<0>(tile, col_stride, r0, cp, b0);
+          if (p == 1) dequant_col<1>(tile, col_stride, r0, cp, b0);
+          if (p == 2) dequant_col<2>(tile, col_stride, r0, cp, b0);
+          if (p == 3) dequant_col<3>(tile, col_stride, r0, cp, b0);
+        }
+        if (two_rows) {
+          if (p == 0) dequant_col<0>(tile, col_stride, 128 + r0, cp, b1);
+          if (p == 1) dequant_col<1>(tile, col_stride, 128 + r0, cp, b1);
+          if (p == 2) dequant_col<2>(tile, col_stride, 128 + r0, cp, b1);
+          if (p == 3) dequant_col<3>(tile, col_stride, 128 + r0, cp, b1);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&S.cols_full[p]);
       }
-    };
-    write_p(s, key, false);
-    if (extra) write_p(s2, key2, true);
-    warp_transpose_reduce<false>(t, lane);
-    __syncthreads();   // every thread has read mfin/red before red is reused
-    red[quad][hh * 32 + lane] = t[0];
-  }
-  fence_proxy_async_smem();
-  __syncthreads();
-  if (tid < H) S.lfin[tid] = (red[0][tid] + red[1][tid]) + (red[2][tid] + red[3][tid]);
-
-  // --------------------------------------------------------------- O = P V
-  // P as A, MN-major (heads contiguous): rows 0-63 are the heads, and the
-  // second 64-row atom is the same P (leading offset 0), so D lanes 64-127
-  // repeat lanes 0-63 and all four TMEM lane quadrants hold heads.  V as B,
-  // MN-major: 4 of the tile's 64-dim columns per instruction.  D overwrites S
-  // in TMEM (S has been read into registers): lane = head, column = dim.
-  if (tid == 0 && ok) {
-    tc_fence_after();
-    const uint32_t ta = smem_u32(tile), pa = smem_u32(qs);
-#pragma unroll
-    for (int kk = 0; kk < Lay::kRows / 16; ++kk) {
-      const uint64_t ad = smem_desc(pa + kk * 2048, 0, 1024);
-#pragma unroll
-      for (int nh = 0; nh < D / (int)kPVN; ++nh) {
-        const uint64_t bd = smem_desc(ta + (nh * (kPVN / 64)) * kAtomCol + kk * 2048, kAtomCol, 1024);
-        mma_f16(tmem + nh * kPVN, ad, bd, kIdescPV, kk > 0 ? 1u : 0u);
+      // the finished item's epilogue overlaps this block's S = Q K^T
+      if (epi_pending) {
+        item_epilogue(a, S, epi_item, s_row, tid, q4, wh, lane);
+        epi_pending = false;
       }
-    }
-    mma_commit(&S.bar_mma);
-  }
-  if (ok) ok = mbar_wait(&S.bar_mma, 1);
-  tc_fence_after();
-  const bool all_ok = __syncthreads_and(ok) != 0;
-
-  // Warp w reads TMEM lane quadrant w % 4, i.e. heads 32 (w & 1) + lane; the
-  // four warps on the same heads take one quarter of the 512 dims each.
-  const int eh = (warp & 1) * 32 + lane;                       // head of this thread's TMEM lane
-  const int ec0 = (((warp >> 1) & 1) * 2 + (warp >> 2)) * 128;  // first dim of its quarter
-  const uint32_t etm = tmem + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)ec0;
-
-  // ---------------------------------------------------------------- merge
-  if (a.cluster) {
-    // The token's chunks are the CTAs of one cluster.  Each CTA normalises
-    // its partial (O / l) into fp16 (a convex combination of values: |.| <=
-    // 6 x 448), then pushes to every other CTA, by bulk shared-to-shared
-    // copies, its (m, l) record and the slice of the [head][dim] partial that
-    // CTA owns.  Each CTA then sums its slice over the chunks with weights
-    // l_c 2^(m_c - M) / L straight into the output.
-    const uint32_t crank = cluster_ctarank(), nct = cluster_nctarank();
-    cluster_arrive();   // this CTA's Q/P region is free to receive
-    if (tid < H && !all_ok) {
-      S.mfin[tid] = -INFINITY;
-      S.lfin[tid] = 0.0f;
-    }
-    uint8_t *sendb = tile;   // [64 heads][1024 B] fp16, 16-byte chunks XOR-swizzled by (head & 7)
-    {
-      const float l = S.lfin[eh];
-      const float inv = (all_ok && l > 0.0f) ? 1.0f / l : 0.0f;
+      // ------------------------------------------ next block into registers
+      if constexpr (!kSingle) {
+        if (ld.item < items) {
+          load_row(a, ld.it, ld.j * a.Bk + r0, ld_id, cp, b0);
+          ld.advance(a, stride, items);
+          if (ld.item < items) ld_id = row_slot(a, ld.it, ld.j * a.Bk + r0);
+        }
+      }
+      const int this_item = cur.item;
+      const int this_nb = cur.it.nb;
+      cur.advance(a, stride, items);
+      // ---------------------------------------------------------- softmax
+      wait_ft(S, &S.s_full, ph);
+      tc_fence_after();
+      bar_named(1, kWorkers);   // rs / vld of every row are visible
+      if (j == 0) {
+        m_ref = -INFINITY;
+        l_part = 0.0f;
+      }
+      float mx = -INFINITY;
 #pragma unroll 1
-      for (int j = 0; j < 4; j += 2) {
-        uint32_t v[2][32];
-        tmem_ld32(etm + (uint32_t)(j * 32), v[0]);
-        tmem_ld32(etm + (uint32_t)(j * 32 + 32), v[1]);
+      for (int s = wh; s < nslab; s += 2) {
+        uint32_t v[16];
+        tmem_ld16(s_row + (uint32_t)(16 * s), v);
         tmem_ld_wait();
 #pragma unroll
-        for (int u = 0; u < 2; ++u)
+        for (int i = 0; i < 16; ++i) {
+          const int k = 16 * s + i;
+          const float x = S.vld[k] ? __uint_as_float(v[i]) * (kLogit * S.rs[k]) : -INFINITY;
+          mx = fmaxf(mx, x);
+        }
+      }
+      if (head_lane) red[wh][h] = mx;
+      bar_named(1, kWorkers);
+      const float mc = fmaxf(red[0][h], red[1][h]);
+      float f = 1.0f;
+      if (m_ref == -INFINITY) {
+        m_ref = mc;   // nothing accumulated yet
+      } else if (mc > m_ref + kLazy) {
+        f = exp2f(m_ref - mc);
+        m_ref = mc;
+      }
+      if (head_lane && wh == 0) S.fac[h] = f;
+      const bool any = bar_named_or(2, kWorkers, head_lane && f != 1.0f);
+      if (any) {
+        // O^T holds every earlier block (the dequant above waited for the
+        // previous block's products): scale its head columns
+        tc_fence_after();
+#pragma unroll 1
+        for (int mm = 0; mm < 2; ++mm) {
+          const int mt = 2 * wh + mm;
+#pragma unroll 1
+          for (int hb = 0; hb < 2; ++hb) {
+            uint32_t v[32];
+            const uint32_t ta = s_row + kColO + (uint32_t)(mt * H + hb * 32);
+            tmem_ld32(ta, v);
+            tmem_ld_wait();
 #pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            uint4 o;
-            o.x = pack_half2(__uint_as_float(v[u][8 * t + 0]) * inv, __uint_as_float(v[u][8 * t + 1]) * inv);
-            o.y = pack_half2(__uint_as_float(v[u][8 * t + 2]) * inv, __uint_as_float(v[u][8 * t + 3]) * inv);
-            o.z = pack_half2(__uint_as_float(v[u][8 * t + 4]) * inv, __uint_as_float(v[u][8 * t + 5]) * inv);
-            o.w = pack_half2(__uint_as_float(v[u][8 * t + 6]) * inv, __uint_as_float(v[u][8 * t + 7]) * inv);
-            const int cr = (ec0 + (j + u) * 32) / 8 + t;   // 16-byte chunk of the head's row
-            *reinterpret_cast<uint4 *>(sendb + eh * kRowBytes + (((cr & ~7) | ((cr & 7) ^ (eh & 7))) << 4)) = o;
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * S.fac[hb * 32 + i]);
+            tmem_st32(ta, v);
           }
+        }
+        tmem_st_wait();
+      }
+      l_part *= f;
+#pragma unroll 1
+      for (int s = wh; s < nslab; s += 2) {
+        uint32_t v[16];
+        tmem_ld16(s_row + (uint32_t)(16 * s), v);
+        tmem_ld_wait();
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          const int k = 16 * s + i;
+          float p0 = 0.0f, p1 = 0.0f;
+          if (m_ref != -INFINITY) {
+            if (S.vld[k]) p0 = exp2f(__uint_as_float(v[i]) * (kLogit * S.rs[k]) - m_ref);
+            if (S.vld[k + 1]) p1 = exp2f(__uint_as_float(v[i + 1]) * (kLogit * S.rs[k + 1]) - m_ref);
+          }
+          l_part += p0 + p1;
+          pk[i >> 1] = pack_half2(p0 * S.rs[k], p1 * S.rs[k + 1]);
+        }
+        if (head_lane) {
+          // P^T K-major: [64-key atom column][64 heads][128 B]
+          const int k0 = 16 * s;
+          uint8_t *prow = pbuf + (k0 >> 6) * kAtom + h * 128;
+          const int c0 = (k0 & 63) >> 3;
+          *reinterpret_cast<uint4 *>(prow + (((c0) ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4 *>(prow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&S.p_full);
+
+      if (j == this_nb - 1) {
+        // ---------------------------------------------------- item finished
+        if (head_lane) red[wh][h] = l_part;
+        bar_named(1, kWorkers);
+        if (head_lane && wh == 0) {
+          const float L = red[0][h] + red[1][h];
+          S.lfin[h] = L;
+          S.mfin[h] = m_ref;
+          S.inv_l[h] = L > 0.0f ? 1.0f / L : 0.0f;
+        }
+        epi_pending = true;
+        epi_item = this_item;
+        ++n_item;
+        if (cur.item < items) {
+          // the next item's Q (loaded once this item's last S had read Q)
+          wait_ft(S, &S.q_full, n_item & 1u);
+          convert_q(qs, tid);
+          mbar_arrive(&S.q_ready);
+        }
       }
     }
-    fence_proxy_async_smem();   // the bulk copies read what the threads wrote
-    __syncthreads();
-    cluster_wait();             // every CTA of the cluster may now receive
-    if (tid < (int)nct && tid != (int)crank) {
-      const uint32_t s = (uint32_t)tid;
-      const uint32_t g0 = s * kGroups / nct, bytes = ((s + 1) * kGroups / nct - g0) * 128;
-      const uint32_t slot = crank < s ? crank : crank - 1;
-      bulk_s2s_cluster(dsmem_addr(&MS.ml_in[crank][0][0], s), S.mfin, 2 * H * 4, dsmem_addr(&S.bar_ml, s));
-      bulk_s2s_cluster(dsmem_addr(qs + slot * bytes, s), sendb + g0 * 128, bytes, dsmem_addr(&S.bar_merge, s));
+    if (epi_pending) {
+      // the last item: wait for its products, then write
+      wait_ft(S, &S.cols_free[3], (g - 1) & 1u);
+      item_epilogue(a, S, epi_item, s_row, tid, q4, wh, lane);
     }
-    // warps 0-1 wait for the (m, l) records and compute the weights while
-    // warp 2 waits for the partial slices
-    if (warp == 2) mbar_wait(&S.bar_merge, 0);
-    if (tid < H) {
-      mbar_wait(&S.bar_ml, 0);
-      float mc[kMaxClusterChunks], lc[kMaxClusterChunks];
-      float M = -INFINITY;
+  }
+
+  // ------------------------------------------------------------ cluster merge
+  if (a.C > 1) {
+    cluster_arrive();
+    cluster_wait();
+    if (warp < kMmaWarp && first_item < items) {
+      const int item = first_item;
+      const int C = a.C;
+      const int tok = item / C;
+      const uint32_t rank = (uint32_t)(item - tok * C);
+      const int64_t gp = a.p0 + tok;
+      const int dc = D / C;
+      float(*wgt)[H] = reinterpret_cast<float(*)[H]>(tile);   // [C][H]: the tile is free now
+      if (tid < H) {
+        float mc[8], lc[8];
+        float M = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c)
-        if (c < (int)nct) {
-          mc[c] = c == (int)crank ? S.mfin[tid] : MS.ml_in[c][0][tid];
-          lc[c] = c == (int)crank ? S.lfin[tid] : MS.ml_in[c][1][tid];
-          M = fmaxf(M, mc[c]);
-        }
-      float L = 0.0f;
-#pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c)
-        if (c < (int)nct && mc[c] != -INFINITY) L += lc[c] * exp2f(mc[c] - M);
-      const float invL = L > 0.0f ? 1.0f / L : 0.0f;
-#pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c)
-        if (c < (int)nct) MS.wgt[c][tid] = mc[c] == -INFINITY ? 0.0f : lc[c] * exp2f(mc[c] - M) * invL;
-      if (crank == 0 && a.lse)
-        a.lse[gp * H + tid] = (L > 0.0f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-    }
-    __syncthreads();
-    cluster_arrive();   // everything this CTA needs has arrived: its peers' buffers are free
-    const uint32_t g0 = crank * kGroups / nct, g1 = (crank + 1) * kGroups / nct;
-    const uint32_t bytes = (g1 - g0) * 128;
-    float *outp = a.out + gp * H * D;
-    for (int k = (int)g0 * 8 + tid; k < (int)g1 * 8; k += kThreads) {
-      const int h = k >> 6, cr = k & 63;   // head, 16-byte chunk (8 dims) of its row
-      const uint32_t off = (uint32_t)(h * kRowBytes + (((cr & ~7) | ((cr & 7) ^ (h & 7))) << 4));
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-#pragma unroll
-      for (int c = 0; c < kMaxClusterChunks; ++c)
-        if (c < (int)nct) {
-          const uint8_t *src = c == (int)crank ? sendb + off
-                                               : qs + (uint32_t)(c < (int)crank ? c : c - 1) * bytes + off - g0 * 128;
-          const uint4 v = *reinterpret_cast<const uint4 *>(src);
-          const float w = MS.wgt[c][h];
-          const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&u[i]));
-            acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
-            acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+        for (int c = 0; c < 8; ++c)
+          if (c < C) {
+            const int64_t pi = (int64_t)(tok * C + c) * 2 * H;
+            mc[c] = ld_cg_f32(a.part_ml + pi + tid);
+            lc[c] = ld_cg_f32(a.part_ml + pi + H + tid);
+            M = fmaxf(M, mc[c]);
           }
-        }
-      float4 *dst = reinterpret_cast<float4 *>(outp + h * D + cr * 8);
-      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-    }
-    cluster_wait();   // no CTA leaves while a peer's copy may still read its buffer
-  } else {
-    // unnormalised partial O of this chunk, with its per-head (max, sum), to
-    // the workspace for the combine kernel
-    const int64_t pc = (int64_t)p * a.n_chunks + chunk;
-    {
-      float *po = a.part_o + (pc * H + eh) * D + ec0;
+        float L = 0.0f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < C && mc[c] != -INFINITY) L += lc[c] * exp2f(mc[c] - M);
+        const float invL = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          if (c < C) wgt[c][tid] = mc[c] == -INFINITY ? 0.0f : lc[c] * exp2f(mc[c] - M) * invL;
+        if (rank == 0 && a.lse) a.lse[gp * H + tid] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+      }
+      bar_named(1, kWorkers);
+      tc_fence_after();
+      // the dims this CTA owns: lanes of quadrant q4 in each 128-dim block
+      const int q4 = warp & 3, hh = warp >> 2;   // heads 32 hh .. + 31
+      const uint32_t s_row = tmem + ((uint32_t)(32 * q4) << 16);
+      float *outp = a.out + gp * H * D;
 #pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
+      for (int mt = 0; mt < 4; ++mt) {
+        const int d = mt * 128 + 32 * q4 + lane;
+        const bool own = d / dc == (int)rank;
+        if (!__any_sync(0xffffffffu, own)) continue;
         uint32_t v[32];
-        tmem_ld32(etm + (uint32_t)(j * 32), v);
+        tmem_ld32(s_row + kColO + (uint32_t)(mt * H + hh * 32), v);
         tmem_ld_wait();
+        if (!own) continue;
+        float acc[32];
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          reinterpret_cast<float4 *>(po + j * 32)[t] =
-              all_ok ? make_float4(__uint_as_float(v[4 * t]), __uint_as_float(v[4 * t + 1]),
-                                   __uint_as_float(v[4 * t + 2]), __uint_as_float(v[4 * t + 3]))
-                     : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < 32; ++i)
+          acc[i] = __uint_as_float(v[i]) * S.inv_l[hh * 32 + i] * wgt[rank][hh * 32 + i];
+#pragma unroll 1
+        for (int c = 0; c < C; ++c) {
+          if (c == (int)rank) continue;
+          const __half *src = a.part_o + ((int64_t)(tok * C + c) * D + d) * H + hh * 32;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 u = ld_cg_v4(src + 8 * k);
+            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
+              acc[8 * k + 2 * e] = fmaf(wgt[c][hh * 32 + 8 * k + 2 * e], fv.x, acc[8 * k + 2 * e]);
+              acc[8 * k + 2 * e + 1] = fmaf(wgt[c][hh * 32 + 8 * k + 2 * e + 1], fv.y, acc[8 * k + 2 * e + 1]);
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) outp[(hh * 32 + i) * D + d] = S.abort ? 0.0f : acc[i];
       }
     }
-    if (tid < H) {
-      a.part_ml[pc * 2 * H + tid] = all_ok ? S.mfin[tid] : -INFINITY;
-      a.part_ml[pc * 2 * H + H + tid] = all_ok ? S.lfin[tid] : 0.0f;
-    }
   }
+
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -623,131 +711,75 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merge the chunk partials of each (token, head): m = max_c m_c,
-// l = sum_c l_c 2^(m_c - m), o = sum_c o_c 2^(m_c - m) / l; lse in natural log.
-__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
-  const int p = blockIdx.y;
-  const int h = blockIdx.x;
-  const int n = a.n_chunks;
-  __shared__ float wgt[64];
-  __shared__ float inv_l;
-  if (threadIdx.x == 0) {
-    float m = -INFINITY;
-    for (int c = 0; c < n; ++c) m = fmaxf(m, a.part_ml[((int64_t)p * n + c) * 2 * H + h]);
-    float l = 0.0f;
-    for (int c = 0; c < n; ++c) {
-      const float mc = a.part_ml[((int64_t)p * n + c) * 2 * H + h];
-      const float w = (mc == -INFINITY) ? 0.0f : exp2f(mc - m);
-      wgt[c] = w;
-      l += w * a.part_ml[((int64_t)p * n + c) * 2 * H + H + h];
-    }
-    inv_l = (l > 0.0f) ? 1.0f / l : 0.0f;
-    if (a.lse) a.lse[(a.p0 + p) * H + h] = (l > 0.0f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
-  }
-  __syncthreads();
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {
-    float acc = 0.0f;
-    for (int c = 0; c < n; ++c) acc += wgt[c] * a.part_o[(((int64_t)p * n + c) * H + h) * D + d];
-    a.out[((a.p0 + p) * H + h) * D + d] = acc * inv_l;
-  }
+int device_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+  return n;
+}
+
+// Chunks per token: the most (1, 2, 4 or 8) whose clusters all fit on the
+// GPU at once, keeping at least 16 keys per chunk; 1 once the tokens fill the SMs.
+// kernel 1 forces a split (C >= 2), kernel 2 a single chunk.
+int choose_chunks(int problems, int K, int W, int kernel, int sms) {
+  if (kernel == 2) return 1;
+  int c = 1;
+  for (int cand : {2, 4, 8})
+    if ((int64_t)problems * cand <= sms && (K + W) / cand >= 16) c = cand;
+  if (kernel == 1 && c == 1) c = (K + W) >= 32 ? 2 : 1;
+  return c;
 }
 
 }  // namespace
 
-size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W) {
-  const int n_chunks = (K + ATTN_CHUNK - 1) / ATTN_CHUNK + (W + ATTN_CHUNK - 1) / ATTN_CHUNK;
-  size_t b = (size_t)problems * n_chunks * H * D * 4;
-  b = (b + 255) & ~size_t(255);
-  b += (size_t)problems * n_chunks * 2 * H * 4;
+size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W, int32_t kernel) {
+  const int C = choose_chunks(problems, K, W, kernel, device_sms());
+  if (C <= 1) return 256;
+  const size_t items = (size_t)problems * C;
+  size_t b = (items * D * H * 2 + 255) & ~size_t(255);
+  b += items * 2 * H * 4;
   return (b + 255) & ~size_t(255);
 }
 
-namespace {
-
-template <int kSwa>
-cudaError_t launch_layout(const AttnArgs &a, const CUtensorMap &tm_q, cudaStream_t stream, int *launches) {
-  constexpr size_t smem = smem_bytes<kSwa>();
-  cudaError_t err =
-      cudaFuncSetAttribute(sparse_attn_kernel<kSwa>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  if (a.cluster) {
-    // one cluster per token: its chunks merge in shared memory
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.n_chunks, (unsigned)a.problems, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)a.n_chunks;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, sparse_attn_kernel<kSwa>, tm_q, a);
-    *launches += 1;
-    return err;
-  }
-  sparse_attn_kernel<kSwa><<<dim3(a.n_chunks, a.problems), kThreads, smem, stream>>>(tm_q, a);
-  *launches += 1;
-  return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches) {
   if (a.problems <= 0) return cudaSuccess;
-  const int n_top = (a.K + ATTN_CHUNK - 1) / ATTN_CHUNK;
-  const int n_split = n_top + (a.W + ATTN_CHUNK - 1) / ATTN_CHUNK;
-  const int n_mixed = max(n_top, (a.W + kMixSwa - 1) / kMixSwa);
+  const int sms = device_sms();
+  a.C = choose_chunks(a.problems, a.K, a.W, a.kernel, sms);
+  const int max_r = (a.K + a.C - 1) / a.C + (a.W + a.C - 1) / a.C;
+  const int items = a.problems * a.C;
+  const int grid = a.C > 1 ? items : (a.problems < sms ? a.problems : sms);
+  const bool one_item = grid >= items;
+  const int r16 = max_r > 16 ? (max_r + 15) / 16 * 16 : 16;
+  // one block per CTA (its rows past 128 must be entries: SWA rows come first)
+  const bool single = one_item && r16 <= kMaxBk && (a.W + a.C - 1) / a.C <= kBlockRows;
+  a.Bk = single ? r16 : kBlockRows;
   uint8_t *p = static_cast<uint8_t *>(scratch);
-  a.part_o = reinterpret_cast<float *>(p);
-  size_t off = ((size_t)a.problems * n_split * H * D * 4 + 255) & ~size_t(255);
-  a.part_ml = reinterpret_cast<float *>(p + off);
-  if (n_split == 0) {
-    // no key at all: out = 0, lse = -inf
-    cudaError_t e = cudaMemsetAsync(a.out + a.p0 * H * D, 0, (size_t)a.problems * H * D * 4, stream);
-    if (e != cudaSuccess || !a.lse) return e;
-    a.n_chunks = 0;
-    attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
-    ++*launches;
-    return cudaGetLastError();
-  }
-  int dev = 0, sms = 0;
-  cudaError_t err = cudaGetDevice(&dev);
-  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (err != cudaSuccess) return err;
-  // Streaming (a CTA pipelines whole tokens) once the tokens alone fill the
-  // SMs -- it keeps every SM's tensor cores busy without a merge; below that,
-  // chunk-parallel (a token's chunks on a cluster of CTAs) for latency.
-  if (a.kernel == 2 || (a.kernel == 0 && a.problems >= sms)) {
-    const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
-    if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-    err = launch_sparse_attn_stream(a, sms, stream, launches);
-    if (err == cudaSuccess && pe.stop) err = record_profile_event(pe.stop, stream);
-    return err;
-  }
-  // The mixed layout (4 chunks for 512 + 128 keys) when the split layout's
-  // chunks would not fit in one wave of CTAs (one per SM); the split layout
-  // (5 chunks, each less work) otherwise.
-  const bool mixed = a.W > 0 && n_mixed < n_split && n_mixed <= kMaxClusterChunks &&
-                     (int64_t)a.problems * n_split > (int64_t)sms;
-  a.n_chunks = mixed ? n_mixed : n_split;
-  a.n_kchunks = mixed ? n_mixed : n_top;
-  a.cluster = a.n_chunks <= kMaxClusterChunks ? 1 : 0;
+  a.part_o = reinterpret_cast<__half *>(p);
+  a.part_ml = reinterpret_cast<float *>(p + (((size_t)items * D * H * 2 + 255) & ~size_t(255)));
   CUtensorMap tm_q;
   if (!make_tmap_bf16(&tm_q, a.q, D, (a.p0 + a.problems) * H, H)) return cudaErrorInvalidValue;
+  auto kern = single ? sparse_attn_kernel<true> : sparse_attn_kernel<false>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (err != cudaSuccess) return err;
   const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-  err = mixed ? launch_layout<kMixSwa>(a, tm_q, stream, launches) : launch_layout<0>(a, tm_q, stream, launches);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)a.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, tm_q, a);
   if (err != cudaSuccess) return err;
+  ++*launches;
   if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;
-  if (!a.cluster) {
-    attn_combine_kernel<<<dim3(H, a.problems), 256, 0, stream>>>(a);
-    ++*launches;
-    err = cudaGetLastError();
-  }
-  return err;
+  return cudaSuccess;
 }
 
 }  // namespace csa2

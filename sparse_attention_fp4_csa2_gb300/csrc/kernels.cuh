@@ -23,8 +23,6 @@ constexpr int BLOCK = 8;           // HSI candidate block width
 // Indexer sweep: 128 positions per tile (the MMA M dimension).
 constexpr int SWEEP_TILE = 128;
 constexpr int FP4_SWEEP_TILE = 256;   // keys per tile of the MXFP4 sweep
-// Attention: 128 keys per CTA (the MMA M dimension of S^T = K Q^T).
-constexpr int ATTN_CHUNK = 128;
 // Radix select: 11-bit first digit.
 constexpr int TOPK_BINS = 2048;
 constexpr int TOPK_MAX_K = 8192;
@@ -148,17 +146,16 @@ struct AttnArgs {
   const uint8_t *swa;         // [P][W][512] (E4M3)
   const float *swa_scale;     // [P][W]
   const int32_t *swa_len;     // [P]
-  float *part_o;              // [P][n_chunks][64][512]
-  float *part_ml;             // [P][n_chunks][2][64]
   float *out;                 // [P][64][512]
   float *lse;                 // [P][64] or NULL
+  __half *part_o;             // chunked tokens: [P * C][512][64] normalised partials (workspace)
+  float *part_ml;             // chunked tokens: [P * C][2][64] (reference max, row sum) (workspace)
   int64_t cap;
   int32_t problems;
   int32_t K;
   int32_t W;
-  int32_t n_kchunks;
-  int32_t n_chunks;
-  int32_t cluster;            // 1: the chunks of a token form a cluster and merge after one barrier
+  int32_t C;                  // chunks per token (1, 2, 4, 8): the CTAs of one cluster when > 1
+  int32_t Bk;                 // rows per key block (<= 128, or <= 160 with one block per CTA)
   // Problem p of this launch is token gp = p0 + p; it reads the caches of
   // sequence gp / tokens.  Decode: tokens = 1, SWA rows [gp*W, gp*W + swa_len[gp]).
   // Prefill (causal_swa): token i of its sequence sits at position
@@ -170,11 +167,11 @@ struct AttnArgs {
   int64_t first_pos;
   int64_t swa_first_pos;
   int64_t swa_seq_rows;
-  int32_t kernel;             // 0 automatic, 1 chunk-parallel, 2 streaming
+  int32_t kernel;             // 0 automatic, 1 split into chunks, 2 one chunk per token
 };
 
-size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W);
+// Workspace of one readout launch (the chunk partials when tokens are split).
+size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W, int32_t kernel);
 cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches);
-cudaError_t launch_sparse_attn_stream(const AttnArgs &a, int num_sms, cudaStream_t stream, int *launches);
 
 }  // namespace csa2
