@@ -48,9 +48,15 @@ namespace csa2 {
 
 namespace {
 
-constexpr int kWorkers = 256;                    // 8 worker warps
-constexpr int kThreads = kWorkers + 32;          // + the MMA warp
+constexpr int kWorkers = 256;                    // 8 worker warps (warpgroups 0 and 1)
+constexpr int kThreads = kWorkers + 128;         // + warpgroup 2: the MMA warp and 3 idle warps
 constexpr int kMmaWarp = kWorkers / 32;
+// Register split (setmaxnreg): launched at 65536 / 384 -> 168 per thread; the
+// MMA warpgroup gives up to 80, the workers take 208 (256 x 208 + 128 x 80
+// = 63,488 <= 384 x 168 = 64,512; per scheduler 2 x 208 + 80 = 496 <= 512).
+constexpr uint32_t kRegsMma = 80, kRegsWork = 208;
+constexpr int kQThreads = 96;                    // warps 9-11: convert each item's Q
+static_assert(kWorkers * kRegsWork + 128 * kRegsMma <= kThreads * 168, "register split exceeds the launch budget");
 constexpr int kMaxBk = 160;                      // rows of a single-block item
 constexpr int kBlockRows = 128;                  // rows of a block of a multi-block item
 constexpr int kTileRegion = kMaxBk * D * 2;      // 160 KB
@@ -66,13 +72,13 @@ constexpr float kLogit = 0.06375871295460785f;   // log2(e) / sqrt(512)
 constexpr float kLn2 = 0.69314718055994531f;
 constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B K-major*/ 0, /*N*/ H, /*M*/ 128);
 
-struct __align__(8) Ctl {
+struct __align__(16) Ctl {
   uint64_t q_full, q_ready, s_full, p_full, done;
   uint64_t cols_full[4], cols_free[4];
   uint32_t tmem_base;
   volatile uint32_t abort;
-  float rs[kMaxBk];        // per row: 1 (main entry) or the SWA row scale
-  uint8_t vld[kMaxBk];     // per row: holds a key
+  __align__(16) float rs[kMaxBk];      // per row: 1 (main entry) or the SWA row scale
+  __align__(16) uint8_t vld[kMaxBk];   // per row: holds a key
   float fac[H];            // O^T rescale factor per head (block being processed)
   float inv_l[H];          // per head at an item's end: 1 / row sum (0 if empty)
   float mfin[H];           // per head at an item's end: reference max (log2 units)
@@ -118,6 +124,13 @@ __device__ __forceinline__ Item item_info(const AttnArgs &a, int item) {
     it.swa_len = a.W > 0 ? min(__ldg(a.swa_len + it.gp), a.W) : 0;
   }
   return it;
+}
+
+// Blocks of an item (its key count over the block size, at least one).
+__device__ __forceinline__ int item_blocks(const AttnArgs &a, int item) {
+  const int c = item % a.C;
+  const int R = ((c + 1) * a.W) / a.C - (c * a.W) / a.C + ((c + 1) * a.K) / a.C - (c * a.K) / a.C;
+  return R > a.Bk ? (R + a.Bk - 1) / a.Bk : 1;
 }
 
 // A row's data, loaded one block ahead.  FP4 entry: v[2p], v[2p+1] are the
@@ -258,17 +271,13 @@ __device__ __forceinline__ void item_epilogue(const AttnArgs &a, Ctl &S, int ite
     for (int mm = 0; mm < 2; ++mm) {
       const int mt = 2 * wh + mm;
       const int d = mt * 128 + 32 * q4 + lane;
-#pragma unroll 1
-      for (int hb = 0; hb < 2; ++hb) {
-        uint32_t v[32];
-        tmem_ld32(s_row + kColO + (uint32_t)(mt * H + hb * 32), v);
-        tmem_ld_wait();
+      uint32_t v[2][32];
+      tmem_ld32(s_row + kColO + (uint32_t)(mt * H), v[0]);
+      tmem_ld32(s_row + kColO + (uint32_t)(mt * H + 32), v[1]);
+      tmem_ld_wait();
+      const float keep = S.abort ? 0.0f : 1.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int hh = hb * 32 + i;
-          outp[hh * D + d] = S.abort ? 0.0f : __uint_as_float(v[i]) * S.inv_l[hh];
-        }
-      }
+      for (int hh = 0; hh < H; ++hh) outp[hh * D + d] = __uint_as_float(v[hh >> 5][hh & 31]) * (S.inv_l[hh] * keep);
     }
     if (tid < H && a.lse)
       a.lse[gp * H + tid] = S.lfin[tid] > 0.0f ? (S.mfin[tid] + log2f(S.lfin[tid])) * kLn2 : -INFINITY;
@@ -285,24 +294,21 @@ __device__ __forceinline__ void item_epilogue(const AttnArgs &a, Ctl &S, int ite
   for (int mm = 0; mm < 2; ++mm) {
     const int mt = 2 * wh + mm;
     const int d = mt * 128 + 32 * q4 + lane;
-#pragma unroll 1
-    for (int hb = 0; hb < 2; ++hb) {
-      uint32_t v[32];
-      tmem_ld32(s_row + kColO + (uint32_t)(mt * H + hb * 32), v);
-      tmem_ld_wait();
-      if (d / dc != rank) {
-        uint4 *dst = reinterpret_cast<uint4 *>(po + (int64_t)d * H + hb * 32);
-        const float *il = S.inv_l + hb * 32;
+    uint32_t v[2][32];
+    tmem_ld32(s_row + kColO + (uint32_t)(mt * H), v[0]);
+    tmem_ld32(s_row + kColO + (uint32_t)(mt * H + 32), v[1]);
+    tmem_ld_wait();
+    if (d / dc != rank) {
+      // [d / 32][h / 8][d % 32][h % 8]: a warp's store covers 512 contiguous bytes
+      uint4 *dst = reinterpret_cast<uint4 *>(po) + (d >> 5) * 256 + (d & 31);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[k] = make_uint4(pack_half2(__uint_as_float(v[8 * k + 0]) * il[8 * k + 0],
-                                         __uint_as_float(v[8 * k + 1]) * il[8 * k + 1]),
-                              pack_half2(__uint_as_float(v[8 * k + 2]) * il[8 * k + 2],
-                                         __uint_as_float(v[8 * k + 3]) * il[8 * k + 3]),
-                              pack_half2(__uint_as_float(v[8 * k + 4]) * il[8 * k + 4],
-                                         __uint_as_float(v[8 * k + 5]) * il[8 * k + 5]),
-                              pack_half2(__uint_as_float(v[8 * k + 6]) * il[8 * k + 6],
-                                         __uint_as_float(v[8 * k + 7]) * il[8 * k + 7]));
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t *w = &v[k >> 2][(k & 3) * 8];
+        const float *il = S.inv_l + 8 * k;
+        dst[32 * k] = make_uint4(pack_half2(__uint_as_float(w[0]) * il[0], __uint_as_float(w[1]) * il[1]),
+                            pack_half2(__uint_as_float(w[2]) * il[2], __uint_as_float(w[3]) * il[3]),
+                            pack_half2(__uint_as_float(w[4]) * il[4], __uint_as_float(w[5]) * il[5]),
+                            pack_half2(__uint_as_float(w[6]) * il[6], __uint_as_float(w[7]) * il[7]));
       }
     }
   }
@@ -310,8 +316,8 @@ __device__ __forceinline__ void item_epilogue(const AttnArgs &a, Ctl &S, int ite
 
 // Q of an item: bf16 -> fp16 in place (the same 2-byte slots of the swizzled
 // layout; |q| < 65504 assumed), once its copy has landed.
-__device__ __forceinline__ void convert_q(uint8_t *qs, int tid) {
-  for (int i = tid; i < kQBytes / 16; i += kWorkers) {
+__device__ __forceinline__ void convert_q(uint8_t *qs, int t, int nthreads) {
+  for (int i = t; i < kQBytes / 16; i += nthreads) {
     uint4 *ptr = reinterpret_cast<uint4 *>(qs) + i;
     const uint4 v = *ptr;
     *ptr = make_uint4(pack_half2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)),
@@ -320,6 +326,41 @@ __device__ __forceinline__ void convert_q(uint8_t *qs, int tid) {
                       pack_half2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)));
   }
   fence_proxy_async_smem();
+}
+
+// O^T (+)= V^T P^T for one block of NKS x 16 keys: four 128-dim blocks, each
+// committed to its cols_free barrier (its tile columns are then free).  The
+// sequence is fully unrolled per block size; no MMA is issued under a
+// per-instruction condition.
+template <int NKS>
+__device__ __forceinline__ void issue_pv(Ctl &S, uint32_t tmem, uint64_t vd, uint64_t pd, uint64_t cs16,
+                                         uint32_t acc0) {
+#pragma unroll
+  for (int mt = 0; mt < 4; ++mt) {
+    const uint64_t va = vd + 2 * mt * cs16;
+    const uint32_t dt = tmem + kColO + (uint32_t)(mt * H);
+#pragma unroll
+    for (int ks = 0; ks < NKS; ++ks)
+      mma_f16(dt, va + (uint64_t)ks * 128, pd + (uint64_t)((ks >> 2) * (kAtom >> 4) + (ks & 3) * 2), kIdescPV,
+              (acc0 | (uint32_t)ks) ? 1u : 0u);
+    mma_commit(&S.cols_free[mt]);
+  }
+}
+
+__device__ __forceinline__ void issue_pv_n(int nks, Ctl &S, uint32_t tmem, uint64_t vd, uint64_t pd, uint64_t cs16,
+                                           uint32_t acc0) {
+  switch (nks) {
+    case 1: issue_pv<1>(S, tmem, vd, pd, cs16, acc0); break;
+    case 2: issue_pv<2>(S, tmem, vd, pd, cs16, acc0); break;
+    case 3: issue_pv<3>(S, tmem, vd, pd, cs16, acc0); break;
+    case 4: issue_pv<4>(S, tmem, vd, pd, cs16, acc0); break;
+    case 5: issue_pv<5>(S, tmem, vd, pd, cs16, acc0); break;
+    case 6: issue_pv<6>(S, tmem, vd, pd, cs16, acc0); break;
+    case 7: issue_pv<7>(S, tmem, vd, pd, cs16, acc0); break;
+    case 8: issue_pv<8>(S, tmem, vd, pd, cs16, acc0); break;
+    case 9: issue_pv<9>(S, tmem, vd, pd, cs16, acc0); break;
+    default: issue_pv<10>(S, tmem, vd, pd, cs16, acc0); break;
+  }
 }
 
 // Q of an item's token by TMA (bf16, 8 boxes of [64 heads x 64 dims], 128B swizzle).
@@ -350,12 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     mbar_init(&S.q_full, 1);
-    mbar_init(&S.q_ready, kWorkers);
+    mbar_init(&S.q_ready, kQThreads);
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, kWorkers);
     mbar_init(&S.done, 1);
     for (int p = 0; p < 4; ++p) {
-      mbar_init(&S.cols_full[p], kWorkers);
+      // kSingle: warps 9 and 10 also write the rows past 128
+      mbar_init(&S.cols_full[p], kSingle ? kWorkers + 64 : kWorkers);
       mbar_init(&S.cols_free[p], 1);
     }
     S.abort = 0;
@@ -371,8 +413,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   const uint32_t col_stride = (uint32_t)a.Bk * 128;   // bytes per 64-dim column of the tile
+  if (warp >= kMmaWarp)
+    setmaxnreg_dec<kRegsMma>();
+  else
+    setmaxnreg_inc<kRegsWork>();
 
-  if (warp == kMmaWarp) {
+  if (warp > kMmaWarp) {
+    // the other warps of the MMA warpgroup: every item's Q, bf16 -> fp16 in
+    // place once it has landed (the MMA thread reloads it after an item's
+    // last S); then, in a single block of more than 128 rows, warps 9 and 10
+    // write rows 128 .. (entries: SWA rows come first)
+    const int ht = tid - (kMmaWarp + 1) * 32;   // 0 .. 95
+    const int r = 128 + (ht >> 1), hcp = ht & 1;
+    const bool rows = kSingle && ht < 64 && first_item < items && r < a.Bk;
+    EntryBuf eb;
+    Item it0;
+    if (rows) {   // the rows' loads go out before the wait for Q
+      it0 = item_info(a, first_item);
+      load_row(a, it0, r, row_slot(a, it0, r), hcp, eb);
+    }
+    {
+      uint32_t n = 0;
+      for (int item = first_item; item < items; item += stride, ++n) {
+        wait_ft(S, &S.q_full, n & 1u);
+        convert_q(qs, ht, kQThreads);
+        mbar_arrive(&S.q_ready);
+      }
+    }
+    if constexpr (kSingle) {
+      if (ht < 64 && first_item < items) {
+        if (rows && hcp == 0) {
+          S.rs[r] = eb.scale;
+          S.vld[r] = eb.kind != 0 ? 1 : 0;
+        }
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          if (rows) {
+            if (p == 0) dequant_col<0>(tile, col_stride, r, hcp, eb);
+            if (p == 1) dequant_col<1>(tile, col_stride, r, hcp, eb);
+            if (p == 2) dequant_col<2>(tile, col_stride, r, hcp, eb);
+            if (p == 3) dequant_col<3>(tile, col_stride, r, hcp, eb);
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&S.cols_full[p]);
+        }
+      }
+    }
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ (uint32_t)a.Bk, /*M*/ 64);
@@ -410,18 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           wait_ft(S, &S.p_full, ph);
           tc_fence_after();
-          const uint32_t acc0 = j > 0 ? 1u : 0u;
-#pragma unroll
-          for (int mt = 0; mt < 4; ++mt) {
-            const uint64_t va = vd + 2 * mt * cs16;
-            const uint32_t dt = tmem + kColO + (uint32_t)(mt * H);
-            // 16 keys per step; nks varies with the block size, so a plain loop
-#pragma unroll 1
-            for (int ks = 0; ks < nks; ++ks)
-              mma_f16(dt, va + (uint64_t)ks * 128, pd + (uint64_t)((ks >> 2) * (kAtom >> 4) + (ks & 3) * 2), kIdescPV,
-                      (acc0 | (uint32_t)ks) ? 1u : 0u);
-            mma_commit(&S.cols_free[mt]);
-          }
+          issue_pv_n(nks, S, tmem, vd, pd, cs16, j > 0 ? 1u : 0u);
         }
       }
       // every MMA of this CTA has completed before the teardown
@@ -431,27 +507,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // -------------------------------------------------------------- workers
     const int cp = tid & 1;                          // columns cp, cp + 2, cp + 4, cp + 6
-    const int r0 = tid >> 1;                         // rows r0 and (single blocks > 128 rows) 128 + r0
-    const bool two_rows = kSingle && (128 + r0) < a.Bk;
+    const int r0 = tid >> 1;                         // row r0 of the block (rows past 128: warps 9, 10)
     const int q4 = warp & 3, wh = warp >> 2;         // TMEM lane quadrant, warp half
-    const bool head_lane = lane < 16;                // S lanes 0-15 of each quadrant hold heads
+    const int th = lane >> 4;                        // thread half of the warp
     const int h = 16 * q4 + (lane & 15);             // head of this thread in the softmax
     const uint32_t s_row = tmem + ((uint32_t)(32 * q4) << 16);
-    const int nslab = a.Bk / 16;
 
-    // `cur`: the block being processed; `ld`: the next block to load into
-    // registers, whose top-K slot `ld_id` was requested one block earlier
-    Cursor cur;
-    cur.item = first_item;
-    cur.j = 0;
-    if (cur.item < items) cur.it = item_info(a, cur.item);
+    // the block being processed (item, block, blocks of the item); `ld`: the
+    // next block to load into registers, whose top-K slot `ld_id` was
+    // requested one block earlier
+    int cur_item = first_item, cur_j = 0, cur_nb = 1;
+    Cursor ld;
+    ld.item = first_item;
+    ld.j = 0;
     RowBuf b0;
-    EntryBuf b1;   // kSingle: row 128 + r0 (an entry: SWA rows come first)
-    Cursor ld = cur;
     int32_t ld_id = -1;
-    if (cur.item < items) {
-      load_row(a, cur.it, r0, row_slot(a, cur.it, r0), cp, b0);
-      if (two_rows) load_row(a, cur.it, 128 + r0, row_slot(a, cur.it, 128 + r0), cp, b1);
+    if (ld.item < items) {
+      ld.it = item_info(a, ld.item);
+      cur_nb = ld.it.nb;
+      load_row(a, ld.it, r0, row_slot(a, ld.it, r0), cp, b0);
       if constexpr (!kSingle) {
         ld.advance(a, stride, items);
         if (ld.item < items) ld_id = row_slot(a, ld.it, ld.j * a.Bk + r0);
@@ -463,40 +537,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     int epi_item = 0;
     float m_ref = -INFINITY, l_part = 0.0f;
 
-    for (; cur.item < items; ++g) {
+    for (; cur_item < items; ++g) {
       const uint32_t ph = g & 1u;
-      const int j = cur.j;
+      const int j = cur_j;
       // ------------------------------------------------------ Q of a new item
-      if (j == 0 && n_item == 0) {
-        wait_ft(S, &S.q_full, 0);
-        convert_q(qs, tid);
-        mbar_arrive(&S.q_ready);
-      }
       // --------------------------------------------------------- dequant
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
         if (g > 0) wait_ft(S, &S.cols_free[p], (g - 1) & 1u);
-        if (p == 0 && cp == 0) {
-          if (r0 < a.Bk) {
-            S.rs[r0] = b0.scale;
-            S.vld[r0] = b0.kind != 0 ? 1 : 0;
-          }
-          if (two_rows) {
-            S.rs[128 + r0] = b1.scale;
-            S.vld[128 + r0] = b1.kind != 0 ? 1 : 0;
-          }
+        if (p == 0 && cp == 0 && r0 < a.Bk) {
+          S.rs[r0] = b0.scale;
+          S.vld[r0] = b0.kind != 0 ? 1 : 0;
         }
         if (r0 < a.Bk) {
           if (p == 0) dequant_col<0>(tile, col_stride, r0, cp, b0);
           if (p == 1) dequant_col<1>(tile, col_stride, r0, cp, b0);
           if (p == 2) dequant_col<2>(tile, col_stride, r0, cp, b0);
           if (p == 3) dequant_col<3>(tile, col_stride, r0, cp, b0);
-        }
-        if (two_rows) {
-          if (p == 0) dequant_col<0>(tile, col_stride, 128 + r0, cp, b1);
-          if (p == 1) dequant_col<1>(tile, col_stride, 128 + r0, cp, b1);
-          if (p == 2) dequant_col<2>(tile, col_stride, 128 + r0, cp, b1);
-          if (p == 3) dequant_col<3>(tile, col_stride, 128 + r0, cp, b1);
         }
         fence_proxy_async_smem();
         mbar_arrive(&S.cols_full[p]);
@@ -514,10 +571,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ld.item < items) ld_id = row_slot(a, ld.it, ld.j * a.Bk + r0);
         }
       }
-      const int this_item = cur.item;
-      const int this_nb = cur.it.nb;
-      cur.advance(a, stride, items);
+      const int this_item = cur_item;
+      const int this_nb = cur_nb;
+      if (++cur_j >= cur_nb) {
+        cur_j = 0;
+        cur_item += stride;
+        if (cur_item < items) cur_nb = item_blocks(a, cur_item);
+      }
       // ---------------------------------------------------------- softmax
+      // Thread (warp w, lane l) owns head h = 16 (w % 4) + l % 16 and the
+      // 16-key slabs 2m + l / 16 of the slab pairs m = 2 mi + w / 4; one
+      // 16x32bx2 load per pair brings both halves of the warp their slab.
       wait_ft(S, &S.s_full, ph);
       tc_fence_after();
       bar_named(1, kWorkers);   // rs / vld of every row are visible
@@ -525,20 +589,53 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_ref = -INFINITY;
         l_part = 0.0f;
       }
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int s = wh; s < nslab; s += 2) {
-        uint32_t v[16];
-        tmem_ld16(s_row + (uint32_t)(16 * s), v);
+      constexpr int kPairs = kSingle ? 3 : 2;   // slab pairs per warp half (blocks of <= 160 / 128 rows)
+      // The slabs' row scales and valid flags by 16-byte loads (no loads
+      // under a condition: those serialise); slabs past the block read
+      // neighbouring Ctl bytes, masked by k < Bk.
+      float x[kPairs][16];
+      {
+        float rsv[kPairs][16];
+        uint32_t u[kPairs][16];
+#pragma unroll
+        for (int mi = 0; mi < kPairs; ++mi) tmem_ld16x2(s_row + (uint32_t)(32 * (2 * mi + wh)), u[mi]);
+        uint32_t vb[kPairs][4];
+#pragma unroll
+        for (int mi = 0; mi < kPairs; ++mi) {
+          const int k0 = 16 * (2 * (2 * mi + wh) + th);
+          const float4 *r4 = reinterpret_cast<const float4 *>(S.rs + k0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 f4 = r4[q];
+            rsv[mi][4 * q] = f4.x;
+            rsv[mi][4 * q + 1] = f4.y;
+            rsv[mi][4 * q + 2] = f4.z;
+            rsv[mi][4 * q + 3] = f4.w;
+          }
+          const uint4 v4 = *reinterpret_cast<const uint4 *>(S.vld + k0);
+          vb[mi][0] = v4.x;
+          vb[mi][1] = v4.y;
+          vb[mi][2] = v4.z;
+          vb[mi][3] = v4.w;
+        }
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k = 16 * s + i;
-          const float x = S.vld[k] ? __uint_as_float(v[i]) * (kLogit * S.rs[k]) : -INFINITY;
-          mx = fmaxf(mx, x);
+        for (int mi = 0; mi < kPairs; ++mi) {
+          const int k0 = 16 * (2 * (2 * mi + wh) + th);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const bool ok = (k0 + i < a.Bk) && ((vb[mi][i >> 2] >> (8 * (i & 3))) & 0xFFu);
+            x[mi][i] = ok ? __uint_as_float(u[mi][i]) * (kLogit * rsv[mi][i]) : -INFINITY;
+          }
         }
       }
-      if (head_lane) red[wh][h] = mx;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int mi = 0; mi < kPairs; ++mi)
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, x[mi][i]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      if (th == 0) red[wh][h] = mx;
       bar_named(1, kWorkers);
       const float mc = fmaxf(red[0][h], red[1][h]);
       float f = 1.0f;
@@ -548,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         f = exp2f(m_ref - mc);
         m_ref = mc;
       }
-      if (head_lane && wh == 0) S.fac[h] = f;
-      const bool any = bar_named_or(2, kWorkers, head_lane && f != 1.0f);
+      if (th == 0 && wh == 0) S.fac[h] = f;
+      const bool any = bar_named_or(2, kWorkers, f != 1.0f);
       if (any) {
         // O^T holds every earlier block (the dequant above waited for the
         // previous block's products): scale its head columns
@@ -571,29 +668,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_wait();
       }
       l_part *= f;
-#pragma unroll 1
-      for (int s = wh; s < nslab; s += 2) {
-        uint32_t v[16];
-        tmem_ld16(s_row + (uint32_t)(16 * s), v);
-        tmem_ld_wait();
+      const float mref_s = m_ref == -INFINITY ? 0.0f : m_ref;
+#pragma unroll
+      for (int mi = 0; mi < kPairs; ++mi) {
+        const int k0 = 16 * (2 * (2 * mi + wh) + th);
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
-          const int k = 16 * s + i;
-          float p0 = 0.0f, p1 = 0.0f;
-          if (m_ref != -INFINITY) {
-            if (S.vld[k]) p0 = exp2f(__uint_as_float(v[i]) * (kLogit * S.rs[k]) - m_ref);
-            if (S.vld[k + 1]) p1 = exp2f(__uint_as_float(v[i + 1]) * (kLogit * S.rs[k + 1]) - m_ref);
-          }
+          // masked keys hold -inf: 2^-inf = 0 (no branch); m_ref = -inf only when all are masked
+          const float p0 = ex2_approx(x[mi][i] - mref_s), p1 = ex2_approx(x[mi][i + 1] - mref_s);
           l_part += p0 + p1;
-          pk[i >> 1] = pack_half2(p0 * S.rs[k], p1 * S.rs[k + 1]);
+          const float2 r2 = *reinterpret_cast<const float2 *>(S.rs + k0 + i);
+          pk[i >> 1] = pack_half2(p0 * r2.x, p1 * r2.y);
         }
-        if (head_lane) {
+        if (k0 < a.Bk) {
           // P^T K-major: [64-key atom column][64 heads][128 B]
-          const int k0 = 16 * s;
           uint8_t *prow = pbuf + (k0 >> 6) * kAtom + h * 128;
           const int c0 = (k0 & 63) >> 3;
-          *reinterpret_cast<uint4 *>(prow + (((c0) ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4 *>(prow + ((c0 ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
           *reinterpret_cast<uint4 *>(prow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
         }
       }
@@ -603,9 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (j == this_nb - 1) {
         // ---------------------------------------------------- item finished
-        if (head_lane) red[wh][h] = l_part;
+        const float lp = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
+        if (th == 0) red[wh][h] = lp;
         bar_named(1, kWorkers);
-        if (head_lane && wh == 0) {
+        if (th == 0 && wh == 0) {
           const float L = red[0][h] + red[1][h];
           S.lfin[h] = L;
           S.mfin[h] = m_ref;
@@ -614,12 +707,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         epi_pending = true;
         epi_item = this_item;
         ++n_item;
-        if (cur.item < items) {
-          // the next item's Q (loaded once this item's last S had read Q)
-          wait_ft(S, &S.q_full, n_item & 1u);
-          convert_q(qs, tid);
-          mbar_arrive(&S.q_ready);
-        }
       }
     }
     if (epi_pending) {
@@ -645,13 +732,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mc[8], lc[8];
         float M = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < C) {
-            const int64_t pi = (int64_t)(tok * C + c) * 2 * H;
-            mc[c] = ld_cg_f32(a.part_ml + pi + tid);
-            lc[c] = ld_cg_f32(a.part_ml + pi + H + tid);
-            M = fmaxf(M, mc[c]);
-          }
+        for (int c = 0; c < 8; ++c) {
+          const int64_t pi = (int64_t)(tok * C + (c < C ? c : 0)) * 2 * H;   // loads not under a condition
+          mc[c] = ld_cg_f32(a.part_ml + pi + tid);
+          lc[c] = ld_cg_f32(a.part_ml + pi + H + tid);
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) M = fmaxf(M, c < C ? mc[c] : -INFINITY);
         float L = 0.0f;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -681,24 +768,42 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i)
           acc[i] = __uint_as_float(v[i]) * S.inv_l[hh * 32 + i] * wgt[rank][hh * 32 + i];
+        // the peers' partials, four chunks' loads in flight at a time
 #pragma unroll 1
-        for (int c = 0; c < C; ++c) {
-          if (c == (int)rank) continue;
-          const __half *src = a.part_o + ((int64_t)(tok * C + c) * D + d) * H + hh * 32;
+        for (int c0 = 0; c0 < C; c0 += 4) {
+          uint4 pv[4][4];
+          // chunks past C or this CTA's own read a written slot and count 0
+          const int cfill = rank == 0 ? 1 : 0;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint4 u = ld_cg_v4(src + 8 * k);
-            const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c = c0 + cc;
+            const int cl = (c < C && c != (int)rank) ? c : cfill;
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.part_o + (int64_t)(tok * C + cl) * D * H) +
+                               (d >> 5) * 256 + (hh * 4) * 32 + (d & 31);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
-              acc[8 * k + 2 * e] = fmaf(wgt[c][hh * 32 + 8 * k + 2 * e], fv.x, acc[8 * k + 2 * e]);
-              acc[8 * k + 2 * e + 1] = fmaf(wgt[c][hh * 32 + 8 * k + 2 * e + 1], fv.y, acc[8 * k + 2 * e + 1]);
+            for (int k = 0; k < 4; ++k) pv[cc][k] = ld_cg_v4(src + 32 * k);
+          }
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c = c0 + cc;
+            const bool use = c < C && c != (int)rank;
+            const float *wc = wgt[use ? c : 0] + hh * 32;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t w4[4] = {pv[cc][k].x, pv[cc][k].y, pv[cc][k].z, pv[cc][k].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
+                const float w0 = use ? wc[8 * k + 2 * e] : 0.0f, w1 = use ? wc[8 * k + 2 * e + 1] : 0.0f;
+                acc[8 * k + 2 * e] = fmaf(w0, use ? fv.x : 0.0f, acc[8 * k + 2 * e]);
+                acc[8 * k + 2 * e + 1] = fmaf(w1, use ? fv.y : 0.0f, acc[8 * k + 2 * e + 1]);
+              }
             }
           }
         }
+        const float keep = S.abort ? 0.0f : 1.0f;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) outp[(hh * 32 + i) * D + d] = S.abort ? 0.0f : acc[i];
+        for (int i = 0; i < 32; ++i) outp[(hh * 32 + i) * D + d] = acc[i] * keep;
       }
     }
   }

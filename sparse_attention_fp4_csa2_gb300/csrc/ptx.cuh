@@ -229,6 +229,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "r"(taddr));
 }
 
+// 16 lanes x 16 consecutive 32-bit columns, twice: threads 0-15 read lanes
+// taddr.lane + i at columns taddr.col .. +15, threads 16-31 the same lanes at
+// columns taddr.col + 16 .. +31.
+__device__ __forceinline__ void tmem_ld16x2(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 16;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
 // 32 lanes x 32 consecutive 32-bit columns, registers -> TMEM (thread i -> lane taddr.lane + i).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -267,6 +279,19 @@ constexpr uint32_t kFmtE4M3 = 0, kFmtE5M2 = 1;
 // both K-major, N, M (the same fields as kind::f16).
 __host__ __device__ constexpr uint32_t idesc_f8f6f4(uint32_t a_fmt, uint32_t b_fmt, uint32_t n, uint32_t m) {
   return (1u << 4) | (a_fmt << 7) | (b_fmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// ------------------------------------------------------- register split
+// Per-warpgroup register budget (all 4 warps of the warpgroup execute it).
+// An increase waits until other warpgroups have released enough registers, so
+// the shares must fit the block's launch total.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ------------------------------------------------------- named CTA barriers
@@ -426,6 +451,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_half2(uint16_t two) {
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// 2^x by the hardware approximation (ex2.approx.ftz: a few ulp; 2^-inf = +0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Order-preserving map of fp32 to uint32 (larger float -> larger key); -0 == +0.
