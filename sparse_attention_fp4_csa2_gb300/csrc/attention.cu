@@ -52,9 +52,10 @@ constexpr int kWorkers = 256;                    // 8 worker warps (warpgroups 0
 constexpr int kThreads = kWorkers + 128;         // + warpgroup 2: the MMA warp and 3 idle warps
 constexpr int kMmaWarp = kWorkers / 32;
 // Register split (setmaxnreg): launched at 65536 / 384 -> 168 per thread; the
-// MMA warpgroup gives up to 80, the workers take 208 (256 x 208 + 128 x 80
-// = 63,488 <= 384 x 168 = 64,512; per scheduler 2 x 208 + 80 = 496 <= 512).
-constexpr uint32_t kRegsMma = 80, kRegsWork = 208;
+// MMA warpgroup gives up to 136, the workers take 184 (256 x 184 + 128 x 136
+// = 64,512 = 384 x 168; per scheduler 2 x 184 + 136 = 504 <= 512).  Both
+// roles then compile without spills.
+constexpr uint32_t kRegsMma = 136, kRegsWork = 184;
 constexpr int kQThreads = 96;                    // warps 9-11: convert each item's Q
 static_assert(kWorkers * kRegsWork + 128 * kRegsMma <= kThreads * 168, "register split exceeds the launch budget");
 constexpr int kMaxBk = 160;                      // rows of a single-block item
@@ -65,6 +66,11 @@ constexpr int kAtom = H * 128;                   // 8 KB: a 64-row atom column (
 constexpr int kPOffMulti = kBlockRows * D * 2;   // P^T of multi-block items: in the tile region's tail
 constexpr int kRedOffMulti = kPOffMulti + 3 * kAtom;
 constexpr int kRedOffSingle = 3 * kAtom;         // single-block items: P^T and reductions in the Q region
+// cluster combine, in the tile region: received [8][2][64] max / sum and
+// [C][D / C rows][128 B] partials, [8][64] weights, staged rows to send
+constexpr uint32_t kCombineParts = 8 * 2 * H * 4;
+constexpr uint32_t kCombineWgt = kCombineParts + D * 128;
+constexpr uint32_t kCombineStage = kCombineWgt + 8 * H * 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 256;                  // O^T: columns 256 + 64 mt + head, lanes = dims
 constexpr float kLazy = 8.0f;                    // log2 margin before the reference max is raised
@@ -73,7 +79,7 @@ constexpr float kLn2 = 0.69314718055994531f;
 constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B K-major*/ 0, /*N*/ H, /*M*/ 128);
 
 struct __align__(16) Ctl {
-  uint64_t q_full, q_ready, s_full, p_full, done;
+  uint64_t q_full, q_ready, s_full, p_full, done, comb;
   uint64_t cols_full[4], cols_free[4];
   uint32_t tmem_base;
   volatile uint32_t abort;
@@ -88,6 +94,7 @@ struct __align__(16) Ctl {
 constexpr size_t kSmemBytes = 1024 + (size_t)kTileRegion + kQBytes + sizeof(Ctl);
 static_assert(kSmemBytes <= 232448, "attention exceeds the shared-memory limit");
 static_assert(kRedOffMulti + 2 * H * 4 <= kTileRegion, "multi-block reductions overflow the tile region");
+static_assert(kCombineStage + D * 128 <= kTileRegion, "cluster combine overflows the tile region");
 static_assert(kRedOffSingle >= (kMaxBk / 64 + 1) * kAtom && kRedOffSingle + 2 * H * 4 <= kQBytes,
               "single-block P^T overlaps the reductions");
 
@@ -136,6 +143,7 @@ __device__ __forceinline__ int item_blocks(const AttnArgs &a, int item) {
 // A row's data, loaded one block ahead.  FP4 entry: v[2p], v[2p+1] are the
 // codes of column cp + 2p (32 bytes), v[8].{x,y,z,w} the scale words of the
 // four columns.  SWA row: v[4p .. 4p+3] are the 64 E4M3 bytes of column cp + 2p.
+// (dequant_front consumes the columns in order, shifting the rest forward.)
 template <int N>
 struct RowBufN {
   uint4 v[N];
@@ -167,11 +175,11 @@ __device__ __forceinline__ void load_row(const AttnArgs &a, const Item &it, int 
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
       const int c = cp + 2 * p;
-      b.v[2 * p] = __ldg(reinterpret_cast<const uint4 *>(src + 32 * c));
-      b.v[2 * p + 1] = __ldg(reinterpret_cast<const uint4 *>(src + 32 * c + 16));
+      b.v[2 * p] = ld_nc_v4(src + 32 * c);
+      b.v[2 * p + 1] = ld_nc_v4(src + 32 * c + 16);
     }
-    const uint32_t *sp = reinterpret_cast<const uint32_t *>(src + 256);
-    b.v[8] = make_uint4(__ldg(sp + cp), __ldg(sp + cp + 2), __ldg(sp + cp + 4), __ldg(sp + cp + 6));
+    const uint8_t *sp = src + 256 + 4 * cp;
+    b.v[8] = make_uint4(ld_nc_u32(sp), ld_nc_u32(sp + 8), ld_nc_u32(sp + 16), ld_nc_u32(sp + 24));
     b.scale = 1.0f;
     b.kind = 1;
   } else if constexpr (N == 16) {
@@ -181,23 +189,24 @@ __device__ __forceinline__ void load_row(const AttnArgs &a, const Item &it, int 
 #pragma unroll
     for (int p = 0; p < 4; ++p)
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        b.v[4 * p + u] = __ldg(reinterpret_cast<const uint4 *>(src + 64 * (cp + 2 * p) + 16 * u));
-    b.scale = __ldg(a.swa_scale + it.swa_row0 + t);
+      for (int u = 0; u < 4; ++u) b.v[4 * p + u] = ld_nc_v4(src + 64 * (cp + 2 * p) + 16 * u);
+    b.scale = __uint_as_float(ld_nc_u32(a.swa_scale + it.swa_row0 + t));
     b.kind = 2;
   }
 }
 
-// Column c = cp + 2p of row r as fp16 into the tile (16-byte chunk i of the
-// row's 128-byte segment at (i ^ (r & 7)) * 16).
-template <int P, int N>
-__device__ __forceinline__ void dequant_col(uint8_t *tile, uint32_t col_stride, int r, int cp, const RowBufN<N> &b) {
-  uint8_t *rowp = tile + (uint32_t)(cp + 2 * P) * col_stride + (uint32_t)r * 128;
+// The buffer's front column as fp16 into column c of row r of the tile
+// (16-byte chunk i of the row's 128-byte segment at (i ^ (r & 7)) * 16);
+// the buffer's next column then moves to the front.  (One instantiation
+// walked four times: the kernel's code stays small enough for the
+// instruction cache.)
+template <int N>
+__device__ __forceinline__ void dequant_front(uint8_t *tile, uint32_t col_stride, int r, int c, RowBufN<N> &b) {
+  uint8_t *rowp = tile + (uint32_t)c * col_stride + (uint32_t)r * 128;
   const int sw = r & 7;
   if (b.kind == 1) {
-    const uint32_t sc = P == 0 ? b.v[8].x : P == 1 ? b.v[8].y : P == 2 ? b.v[8].z : b.v[8].w;
-    const uint32_t w[8] = {b.v[2 * P].x, b.v[2 * P].y, b.v[2 * P].z, b.v[2 * P].w,
-                           b.v[2 * P + 1].x, b.v[2 * P + 1].y, b.v[2 * P + 1].z, b.v[2 * P + 1].w};
+    const uint32_t sc = b.v[8].x;
+    const uint32_t w[8] = {b.v[0].x, b.v[0].y, b.v[0].z, b.v[0].w, b.v[1].x, b.v[1].y, b.v[1].z, b.v[1].w};
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       // 8 codes = 8 dims of scale group i / 2
@@ -208,13 +217,16 @@ __device__ __forceinline__ void dequant_col(uint8_t *tile, uint32_t col_stride, 
       const uint4 o = make_uint4(hmul2_u32(h[0], s2), hmul2_u32(h[1], s2), hmul2_u32(h[2], s2), hmul2_u32(h[3], s2));
       *reinterpret_cast<uint4 *>(rowp + ((i ^ sw) << 4)) = o;
     }
+#pragma unroll
+    for (int i = 0; i < 6; ++i) b.v[i] = b.v[i + 2];
+    b.v[8] = make_uint4(b.v[8].y, b.v[8].z, b.v[8].w, 0u);
     return;
   }
   if constexpr (N == 16) {
     if (b.kind == 2) {
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const uint4 raw = b.v[4 * P + u];
+        const uint4 raw = b.v[u];
         const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
         const uint4 o0 =
             make_uint4(e4m3x2_to_half2((uint16_t)(w[0] & 0xFFFF)), e4m3x2_to_half2((uint16_t)(w[0] >> 16)),
@@ -225,6 +237,8 @@ __device__ __forceinline__ void dequant_col(uint8_t *tile, uint32_t col_stride, 
         *reinterpret_cast<uint4 *>(rowp + (((2 * u) ^ sw) << 4)) = o0;
         *reinterpret_cast<uint4 *>(rowp + (((2 * u + 1) ^ sw) << 4)) = o1;
       }
+#pragma unroll
+      for (int i = 0; i < 12; ++i) b.v[i] = b.v[i + 4];
       return;
     }
   }
@@ -238,7 +252,7 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 }
 
 // Bounded wait that falls through once any role has given up.
-__device__ __forceinline__ void wait_ft(Ctl &S, uint64_t *bar, uint32_t parity) {
+__device__ __noinline__ void wait_ft(Ctl &S, uint64_t *bar, uint32_t parity) {
   if (S.abort) return;
   if (!mbar_wait(bar, parity)) S.abort = 1;
 }
@@ -262,34 +276,10 @@ struct Cursor {
 // chunks own; the merge follows a cluster barrier.
 __device__ __forceinline__ void item_epilogue(const AttnArgs &a, Ctl &S, int item, uint32_t s_row, int tid, int q4,
                                               int wh, int lane) {
-  const int64_t gp = a.p0 + item / a.C;
+  const int64_t gp = a.p0 + item;   // C = 1: an item is a token
   bar_named(1, kWorkers);   // inv_l / mfin / lfin of the item are visible
   tc_fence_after();
-  if (a.C == 1) {
-    float *outp = a.out + gp * H * D;
-#pragma unroll 1
-    for (int mm = 0; mm < 2; ++mm) {
-      const int mt = 2 * wh + mm;
-      const int d = mt * 128 + 32 * q4 + lane;
-      uint32_t v[2][32];
-      tmem_ld32(s_row + kColO + (uint32_t)(mt * H), v[0]);
-      tmem_ld32(s_row + kColO + (uint32_t)(mt * H + 32), v[1]);
-      tmem_ld_wait();
-      const float keep = S.abort ? 0.0f : 1.0f;
-#pragma unroll
-      for (int hh = 0; hh < H; ++hh) outp[hh * D + d] = __uint_as_float(v[hh >> 5][hh & 31]) * (S.inv_l[hh] * keep);
-    }
-    if (tid < H && a.lse)
-      a.lse[gp * H + tid] = S.lfin[tid] > 0.0f ? (S.mfin[tid] + log2f(S.lfin[tid])) * kLn2 : -INFINITY;
-    return;
-  }
-  const int rank = item % a.C;
-  const int dc = D / a.C;   // dims per owner
-  __half *po = a.part_o + (int64_t)item * D * H;
-  if (tid < H) {
-    a.part_ml[(int64_t)item * 2 * H + tid] = S.mfin[tid];
-    a.part_ml[(int64_t)item * 2 * H + H + tid] = S.lfin[tid];
-  }
+  float *outp = a.out + gp * H * D;
 #pragma unroll 1
   for (int mm = 0; mm < 2; ++mm) {
     const int mt = 2 * wh + mm;
@@ -298,20 +288,141 @@ __device__ __forceinline__ void item_epilogue(const AttnArgs &a, Ctl &S, int ite
     tmem_ld32(s_row + kColO + (uint32_t)(mt * H), v[0]);
     tmem_ld32(s_row + kColO + (uint32_t)(mt * H + 32), v[1]);
     tmem_ld_wait();
-    if (d / dc != rank) {
-      // [d / 32][h / 8][d % 32][h % 8]: a warp's store covers 512 contiguous bytes
-      uint4 *dst = reinterpret_cast<uint4 *>(po) + (d >> 5) * 256 + (d & 31);
+    const float keep = S.abort ? 0.0f : 1.0f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint32_t *w = &v[k >> 2][(k & 3) * 8];
-        const float *il = S.inv_l + 8 * k;
-        dst[32 * k] = make_uint4(pack_half2(__uint_as_float(w[0]) * il[0], __uint_as_float(w[1]) * il[1]),
-                            pack_half2(__uint_as_float(w[2]) * il[2], __uint_as_float(w[3]) * il[3]),
-                            pack_half2(__uint_as_float(w[4]) * il[4], __uint_as_float(w[5]) * il[5]),
-                            pack_half2(__uint_as_float(w[6]) * il[6], __uint_as_float(w[7]) * il[7]));
-      }
+    for (int hh = 0; hh < H; ++hh) outp[hh * D + d] = __uint_as_float(v[hh >> 5][hh & 31]) * (S.inv_l[hh] * keep);
+  }
+  if (tid < H && a.lse)
+    a.lse[gp * H + tid] = S.lfin[tid] > 0.0f ? (S.mfin[tid] + log2f(S.lfin[tid])) * kLn2 : -INFINITY;
+}
+
+// C > 1: the C chunks of a token are the CTAs of one cluster (rank = chunk),
+// each the owner of D / C dims of the output.  Each CTA stages, in its own
+// tile region, its row-normalised O for every other owner's dims (fp16,
+// 128-byte rows [dim][64 heads], 16-byte chunks XOR-swizzled by the row) and
+// its per-head reference max and row sum.  Once every CTA's products are done
+// (a cluster barrier: the tile regions are free), one thread sends each
+// owner its rows and the max / sum by bulk shared-to-shared copies that
+// complete on the owner's `comb` barrier.  Each owner then combines the C
+// partials with the weights l_c 2^(m_c - M) / L -- one softmax over the union
+// of the chunks' keys -- and writes its dims; rank 0 also writes the
+// log-sum-exp.  A second cluster barrier, arrived once a CTA has received
+// everything and awaited at its end, keeps every CTA resident until the
+// copies out of it are complete.
+__device__ __forceinline__ void cluster_combine(const AttnArgs &a, Ctl &S, uint8_t *tile, uint32_t tmem, int item,
+                                                int tid, int warp, int lane) {
+  const int C = a.C;
+  const int tok = item / C;
+  const uint32_t rank = (uint32_t)(item - tok * C);
+  const int64_t gp = a.p0 + tok;
+  const int dc = D / C;                              // dims per owner (>= 64: a warp's 32 dims have one owner)
+  const uint32_t slot = (uint32_t)dc * 128;          // one source's rows
+  float(*mlr)[2][H] = reinterpret_cast<float(*)[2][H]>(tile);            // received: [source][max, sum][head]
+  uint8_t *parts = tile + kCombineParts;                                  // received: [source][row][128 B]
+  float(*wgt)[H] = reinterpret_cast<float(*)[H]>(tile + kCombineWgt);     // [source][head]
+  uint8_t *stage = tile + kCombineStage;                                  // sent: [owner][row][128 B]
+  const int q4 = warp & 3, wh = warp >> 2;
+  const uint32_t s_row = tmem + ((uint32_t)(32 * q4) << 16);
+
+  if (tid == 0) mbar_arrive_expect_tx(&S.comb, (uint32_t)(C - 1) * (slot + 2 * H * 4));
+  if (tid < H) {
+    mlr[rank][0][tid] = S.mfin[tid];   // sent to the peers from here, and this CTA's own
+    mlr[rank][1][tid] = S.lfin[tid];
+  }
+  tc_fence_after();
+#pragma unroll 1
+  for (int mm = 0; mm < 2; ++mm) {
+    const int mt = 2 * wh + mm;
+    const int d = mt * 128 + 32 * q4 + lane;
+    const int owner = d / dc;
+    if (owner == (int)rank) continue;
+    uint32_t v[2][32];
+    tmem_ld32(s_row + kColO + (uint32_t)(mt * H), v[0]);
+    tmem_ld32(s_row + kColO + (uint32_t)(mt * H + 32), v[1]);
+    tmem_ld_wait();
+    const int row = d - owner * dc;
+    uint8_t *dst = stage + owner * slot + (uint32_t)row * 128;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t *w = &v[k >> 2][(k & 3) * 8];
+      const float *il = S.inv_l + 8 * k;
+      *reinterpret_cast<uint4 *>(dst + ((k ^ (row & 7)) << 4)) =
+          make_uint4(pack_half2(__uint_as_float(w[0]) * il[0], __uint_as_float(w[1]) * il[1]),
+                     pack_half2(__uint_as_float(w[2]) * il[2], __uint_as_float(w[3]) * il[3]),
+                     pack_half2(__uint_as_float(w[4]) * il[4], __uint_as_float(w[5]) * il[5]),
+                     pack_half2(__uint_as_float(w[6]) * il[6], __uint_as_float(w[7]) * il[7]));
     }
   }
+  fence_proxy_async_smem();
+  __syncwarp();
+  cluster_arrive();
+  cluster_wait();   // every CTA's products are done and its rows staged
+  if (tid == 0) {
+#pragma unroll 1
+    for (int c = 0; c < C; ++c) {
+      if (c == (int)rank) continue;
+      const uint32_t bar = dsmem_addr(&S.comb, (uint32_t)c);
+      bulk_s2s_cluster(dsmem_addr(parts + rank * slot, (uint32_t)c), stage + c * slot, slot, bar);
+      bulk_s2s_cluster(dsmem_addr(&mlr[rank][0][0], (uint32_t)c), &mlr[rank][0][0], 2 * H * 4, bar);
+    }
+  }
+  wait_ft(S, &S.comb, 0);   // every peer's rows and max / sum have landed
+  __syncwarp();
+  cluster_arrive();         // (awaited at the end)
+  if (tid < H) {
+    float M = -INFINITY;
+#pragma unroll 1
+    for (int c = 0; c < C; ++c) M = fmaxf(M, mlr[c][0][tid]);
+    float L = 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < C; ++c) {
+      const float mc = mlr[c][0][tid];
+      const float w = mc == -INFINITY ? 0.0f : mlr[c][1][tid] * exp2f(mc - M);
+      wgt[c][tid] = w;
+      L += w;
+    }
+    const float invL = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll 1
+    for (int c = 0; c < C; ++c) wgt[c][tid] *= invL;
+    if (rank == 0 && a.lse) a.lse[gp * H + tid] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
+  }
+  bar_named(1, kWorkers);
+  // this CTA's dims d, heads 32 wh .. + 31
+  float *outp = a.out + gp * H * D;
+  const float keep = S.abort ? 0.0f : 1.0f;
+#pragma unroll 1
+  for (int mt = 0; mt < 4; ++mt) {
+    const int d = mt * 128 + 32 * q4 + lane;
+    if (d / dc != (int)rank) continue;
+    uint32_t v[32];
+    tmem_ld32(s_row + kColO + (uint32_t)(mt * H + wh * 32), v);
+    tmem_ld_wait();
+    float acc[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]) * S.inv_l[wh * 32 + i] * wgt[rank][wh * 32 + i];
+    const int row = d - (int)rank * dc;
+#pragma unroll 1
+    for (int c = 0; c < C; ++c) {
+      if (c == (int)rank) continue;
+      const uint8_t *src = parts + c * slot + (uint32_t)row * 128;
+      const float *wc = wgt[c] + wh * 32;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 q = *reinterpret_cast<const uint4 *>(src + (((4 * wh + k) ^ (row & 7)) << 4));
+        const uint32_t q2[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&q2[e]));
+          acc[8 * k + 2 * e] = fmaf(wc[8 * k + 2 * e], f.x, acc[8 * k + 2 * e]);
+          acc[8 * k + 2 * e + 1] = fmaf(wc[8 * k + 2 * e + 1], f.y, acc[8 * k + 2 * e + 1]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) outp[(wh * 32 + i) * D + d] = acc[i] * keep;
+  }
+  __syncwarp();
+  cluster_wait();
 }
 
 // Q of an item: bf16 -> fp16 in place (the same 2-byte slots of the swizzled
@@ -328,38 +439,30 @@ __device__ __forceinline__ void convert_q(uint8_t *qs, int t, int nthreads) {
   fence_proxy_async_smem();
 }
 
-// O^T (+)= V^T P^T for one block of NKS x 16 keys: four 128-dim blocks, each
-// committed to its cols_free barrier (its tile columns are then free).  The
-// sequence is fully unrolled per block size; no MMA is issued under a
-// per-instruction condition.
-template <int NKS>
-__device__ __forceinline__ void issue_pv(Ctl &S, uint32_t tmem, uint64_t vd, uint64_t pd, uint64_t cs16,
+// O^T (+)= V^T P^T for one block of nks x 16 keys over the four 128-dim
+// blocks mt, in groups of G: within a group the key steps are the outer loop,
+// so consecutive MMAs go to different accumulators (back-to-back MMAs into
+// one accumulator wait for each other: 80-105 clocks per M128 N64 K16 MMA
+// against 58-76 when four accumulators alternate).  Each group's commit frees
+// its column pairs.  The key steps are a runtime loop with descriptors
+// advanced by constants (no MMA sits under a per-instruction condition).
+template <int G>
+__device__ __forceinline__ void issue_pv(int nks, Ctl &S, uint32_t tmem, uint64_t vd, uint64_t pd, uint64_t cs16,
                                          uint32_t acc0) {
+#pragma unroll 1
+  for (int g0 = 0; g0 < 4; g0 += G) {
+    uint64_t va = vd + 2 * g0 * cs16, pk = pd;
+#pragma unroll 1
+    for (int ks = 0; ks < nks; ++ks) {
+      const uint32_t acc = (acc0 | (uint32_t)ks) ? 1u : 0u;
 #pragma unroll
-  for (int mt = 0; mt < 4; ++mt) {
-    const uint64_t va = vd + 2 * mt * cs16;
-    const uint32_t dt = tmem + kColO + (uint32_t)(mt * H);
+      for (int mt = 0; mt < G; ++mt)
+        mma_f16(tmem + kColO + (uint32_t)((g0 + mt) * H), va + 2 * mt * cs16, pk, kIdescPV, acc);
+      va += 128;   // 16 keys of the MN-major V^T
+      pk += (ks & 3) == 3 ? (uint64_t)((kAtom >> 4) - 6) : 2ull;   // 16 keys of P^T; next atom after 64
+    }
 #pragma unroll
-    for (int ks = 0; ks < NKS; ++ks)
-      mma_f16(dt, va + (uint64_t)ks * 128, pd + (uint64_t)((ks >> 2) * (kAtom >> 4) + (ks & 3) * 2), kIdescPV,
-              (acc0 | (uint32_t)ks) ? 1u : 0u);
-    mma_commit(&S.cols_free[mt]);
-  }
-}
-
-__device__ __forceinline__ void issue_pv_n(int nks, Ctl &S, uint32_t tmem, uint64_t vd, uint64_t pd, uint64_t cs16,
-                                           uint32_t acc0) {
-  switch (nks) {
-    case 1: issue_pv<1>(S, tmem, vd, pd, cs16, acc0); break;
-    case 2: issue_pv<2>(S, tmem, vd, pd, cs16, acc0); break;
-    case 3: issue_pv<3>(S, tmem, vd, pd, cs16, acc0); break;
-    case 4: issue_pv<4>(S, tmem, vd, pd, cs16, acc0); break;
-    case 5: issue_pv<5>(S, tmem, vd, pd, cs16, acc0); break;
-    case 6: issue_pv<6>(S, tmem, vd, pd, cs16, acc0); break;
-    case 7: issue_pv<7>(S, tmem, vd, pd, cs16, acc0); break;
-    case 8: issue_pv<8>(S, tmem, vd, pd, cs16, acc0); break;
-    case 9: issue_pv<9>(S, tmem, vd, pd, cs16, acc0); break;
-    default: issue_pv<10>(S, tmem, vd, pd, cs16, acc0); break;
+    for (int mt = 0; mt < G; ++mt) mma_commit(&S.cols_free[g0 + mt]);
   }
 }
 
@@ -395,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, kWorkers);
     mbar_init(&S.done, 1);
+    mbar_init(&S.comb, 1);
     for (int p = 0; p < 4; ++p) {
       // kSingle: warps 9 and 10 also write the rows past 128
       mbar_init(&S.cols_full[p], kSingle ? kWorkers + 64 : kWorkers);
@@ -413,12 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
   const uint32_t col_stride = (uint32_t)a.Bk * 128;   // bytes per 64-dim column of the tile
-  if (warp >= kMmaWarp)
-    setmaxnreg_dec<kRegsMma>();
-  else
-    setmaxnreg_inc<kRegsWork>();
-
-  if (warp > kMmaWarp) {
+  // Each role sets its register budget at the head of its own branch (a
+  // setmaxnreg before a join would bound the code after it by the lower one).
+  if (warp >= kMmaWarp) {
+   setmaxnreg_dec<kRegsMma>();
+   if (warp > kMmaWarp) {
     // the other warps of the MMA warpgroup: every item's Q, bf16 -> fp16 in
     // place once it has landed (the MMA thread reloads it after an item's
     // last S); then, in a single block of more than 128 rows, warps 9 and 10
@@ -446,20 +549,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           S.rs[r] = eb.scale;
           S.vld[r] = eb.kind != 0 ? 1 : 0;
         }
-#pragma unroll
+#pragma unroll 1
         for (int p = 0; p < 4; ++p) {
-          if (rows) {
-            if (p == 0) dequant_col<0>(tile, col_stride, r, hcp, eb);
-            if (p == 1) dequant_col<1>(tile, col_stride, r, hcp, eb);
-            if (p == 2) dequant_col<2>(tile, col_stride, r, hcp, eb);
-            if (p == 3) dequant_col<3>(tile, col_stride, r, hcp, eb);
-          }
+          if (rows) dequant_front(tile, col_stride, r, hcp + 2 * p, eb);
           fence_proxy_async_smem();
           mbar_arrive(&S.cols_full[p]);
         }
       }
     }
-  } else if (warp == kMmaWarp) {
+   } else {
     // ------------------------------------------------------------------ MMA
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(/*fp16*/ 0, /*A K-major*/ 0, /*B K-major*/ 0, /*N*/ (uint32_t)a.Bk, /*M*/ 64);
@@ -478,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == 0) wait_ft(S, &S.q_ready, n_item & 1u);
           // (no MMA sits under a per-instruction condition: a conditional
           // tcgen05.mma in unrolled code was observed to issue wrongly)
-#pragma unroll
+#pragma unroll 1
           for (int p = 0; p < 4; ++p) {
             wait_ft(S, &S.cols_full[p], ph);
             tc_fence_after();
@@ -497,14 +595,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           wait_ft(S, &S.p_full, ph);
           tc_fence_after();
-          issue_pv_n(nks, S, tmem, vd, pd, cs16, j > 0 ? 1u : 0u);
+          // single block: nothing waits for early column release; several
+          // blocks: the next block's dequant starts on columns 0-3 early
+          issue_pv<kSingle ? 4 : 2>(nks, S, tmem, vd, pd, cs16, j > 0 ? 1u : 0u);
         }
       }
       // every MMA of this CTA has completed before the teardown
       mma_commit(&S.done);
       wait_ft(S, &S.done, 0);
     }
+   }
+    if (a.C > 1) {   // the two cluster barriers of the combine
+      cluster_arrive();
+      cluster_wait();
+      cluster_arrive();
+      cluster_wait();
+    }
   } else {
+    setmaxnreg_inc<kRegsWork>();
     // -------------------------------------------------------------- workers
     const int cp = tid & 1;                          // columns cp, cp + 2, cp + 4, cp + 6
     const int r0 = tid >> 1;                         // row r0 of the block (rows past 128: warps 9, 10)
@@ -542,19 +650,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int j = cur_j;
       // ------------------------------------------------------ Q of a new item
       // --------------------------------------------------------- dequant
-#pragma unroll
+      if (cp == 0 && r0 < a.Bk) {
+        S.rs[r0] = b0.scale;
+        S.vld[r0] = b0.kind != 0 ? 1 : 0;
+      }
+#pragma unroll 1
       for (int p = 0; p < 4; ++p) {
         if (g > 0) wait_ft(S, &S.cols_free[p], (g - 1) & 1u);
-        if (p == 0 && cp == 0 && r0 < a.Bk) {
-          S.rs[r0] = b0.scale;
-          S.vld[r0] = b0.kind != 0 ? 1 : 0;
-        }
-        if (r0 < a.Bk) {
-          if (p == 0) dequant_col<0>(tile, col_stride, r0, cp, b0);
-          if (p == 1) dequant_col<1>(tile, col_stride, r0, cp, b0);
-          if (p == 2) dequant_col<2>(tile, col_stride, r0, cp, b0);
-          if (p == 3) dequant_col<3>(tile, col_stride, r0, cp, b0);
-        }
+        if (r0 < a.Bk) dequant_front(tile, col_stride, r0, cp + 2 * p, b0);
         fence_proxy_async_smem();
         mbar_arrive(&S.cols_full[p]);
       }
@@ -590,50 +693,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         l_part = 0.0f;
       }
       constexpr int kPairs = kSingle ? 3 : 2;   // slab pairs per warp half (blocks of <= 160 / 128 rows)
-      // The slabs' row scales and valid flags by 16-byte loads (no loads
-      // under a condition: those serialise); slabs past the block read
-      // neighbouring Ctl bytes, masked by k < Bk.
-      float x[kPairs][16];
-      {
-        float rsv[kPairs][16];
-        uint32_t u[kPairs][16];
+      // Logits of slab pair mi for this thread: 16 keys from one 16x32bx2
+      // load, the row scales and valid flags by 16-byte loads (no loads
+      // under a condition: those serialise).  Slabs past the block read
+      // neighbouring Ctl bytes, masked by k < Bk.  Two passes over TMEM (max,
+      // then exponents) keep only one pair's values in registers.
+      auto logits = [&](int mi, float (&x)[16]) {
+        uint32_t u[16];
+        tmem_ld16x2(s_row + (uint32_t)(32 * (2 * mi + wh)), u);
+        const int k0 = 16 * (2 * (2 * mi + wh) + th);
+        const float4 *r4 = reinterpret_cast<const float4 *>(S.rs + k0);
+        const uint4 v4 = *reinterpret_cast<const uint4 *>(S.vld + k0);
+        const uint32_t vb[4] = {v4.x, v4.y, v4.z, v4.w};
+        float rsv[16];
 #pragma unroll
-        for (int mi = 0; mi < kPairs; ++mi) tmem_ld16x2(s_row + (uint32_t)(32 * (2 * mi + wh)), u[mi]);
-        uint32_t vb[kPairs][4];
-#pragma unroll
-        for (int mi = 0; mi < kPairs; ++mi) {
-          const int k0 = 16 * (2 * (2 * mi + wh) + th);
-          const float4 *r4 = reinterpret_cast<const float4 *>(S.rs + k0);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 f4 = r4[q];
-            rsv[mi][4 * q] = f4.x;
-            rsv[mi][4 * q + 1] = f4.y;
-            rsv[mi][4 * q + 2] = f4.z;
-            rsv[mi][4 * q + 3] = f4.w;
-          }
-          const uint4 v4 = *reinterpret_cast<const uint4 *>(S.vld + k0);
-          vb[mi][0] = v4.x;
-          vb[mi][1] = v4.y;
-          vb[mi][2] = v4.z;
-          vb[mi][3] = v4.w;
+        for (int q = 0; q < 4; ++q) {
+          const float4 f4 = r4[q];
+          rsv[4 * q] = f4.x;
+          rsv[4 * q + 1] = f4.y;
+          rsv[4 * q + 2] = f4.z;
+          rsv[4 * q + 3] = f4.w;
         }
         tmem_ld_wait();
 #pragma unroll
-        for (int mi = 0; mi < kPairs; ++mi) {
-          const int k0 = 16 * (2 * (2 * mi + wh) + th);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const bool ok = (k0 + i < a.Bk) && ((vb[mi][i >> 2] >> (8 * (i & 3))) & 0xFFu);
-            x[mi][i] = ok ? __uint_as_float(u[mi][i]) * (kLogit * rsv[mi][i]) : -INFINITY;
-          }
+        for (int i = 0; i < 16; ++i) {
+          const bool ok = (k0 + i < a.Bk) && ((vb[i >> 2] >> (8 * (i & 3))) & 0xFFu);
+          x[i] = ok ? __uint_as_float(u[i]) * (kLogit * rsv[i]) : -INFINITY;
         }
-      }
+      };
       float mx = -INFINITY;
+#pragma unroll 1
+      for (int mi = 0; mi < kPairs; ++mi) {
+        float x[16];
+        logits(mi, x);
 #pragma unroll
-      for (int mi = 0; mi < kPairs; ++mi)
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, x[mi][i]);
+        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, x[i]);
+      }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
       if (th == 0) red[wh][h] = mx;
       bar_named(1, kWorkers);
@@ -669,14 +764,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       l_part *= f;
       const float mref_s = m_ref == -INFINITY ? 0.0f : m_ref;
-#pragma unroll
+#pragma unroll 1
       for (int mi = 0; mi < kPairs; ++mi) {
+        float x[16];
+        logits(mi, x);
         const int k0 = 16 * (2 * (2 * mi + wh) + th);
         uint32_t pk[8];
 #pragma unroll
         for (int i = 0; i < 16; i += 2) {
           // masked keys hold -inf: 2^-inf = 0 (no branch); m_ref = -inf only when all are masked
-          const float p0 = ex2_approx(x[mi][i] - mref_s), p1 = ex2_approx(x[mi][i + 1] - mref_s);
+          const float p0 = ex2_approx(x[i] - mref_s), p1 = ex2_approx(x[i + 1] - mref_s);
           l_part += p0 + p1;
           const float2 r2 = *reinterpret_cast<const float2 *>(S.rs + k0 + i);
           pk[i >> 1] = pack_half2(p0 * r2.x, p1 * r2.y);
@@ -710,102 +807,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (epi_pending) {
-      // the last item: wait for its products, then write
+      // the last item: wait for its products, then write (C = 1) or combine
+      // across the cluster (C > 1: the CTA's one item)
       wait_ft(S, &S.cols_free[3], (g - 1) & 1u);
-      item_epilogue(a, S, epi_item, s_row, tid, q4, wh, lane);
+      if (a.C == 1) item_epilogue(a, S, epi_item, s_row, tid, q4, wh, lane);
     }
-  }
-
-  // ------------------------------------------------------------ cluster merge
-  if (a.C > 1) {
-    cluster_arrive();
-    cluster_wait();
-    if (warp < kMmaWarp && first_item < items) {
-      const int item = first_item;
-      const int C = a.C;
-      const int tok = item / C;
-      const uint32_t rank = (uint32_t)(item - tok * C);
-      const int64_t gp = a.p0 + tok;
-      const int dc = D / C;
-      float(*wgt)[H] = reinterpret_cast<float(*)[H]>(tile);   // [C][H]: the tile is free now
-      if (tid < H) {
-        float mc[8], lc[8];
-        float M = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const int64_t pi = (int64_t)(tok * C + (c < C ? c : 0)) * 2 * H;   // loads not under a condition
-          mc[c] = ld_cg_f32(a.part_ml + pi + tid);
-          lc[c] = ld_cg_f32(a.part_ml + pi + H + tid);
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) M = fmaxf(M, c < C ? mc[c] : -INFINITY);
-        float L = 0.0f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < C && mc[c] != -INFINITY) L += lc[c] * exp2f(mc[c] - M);
-        const float invL = L > 0.0f ? 1.0f / L : 0.0f;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          if (c < C) wgt[c][tid] = mc[c] == -INFINITY ? 0.0f : lc[c] * exp2f(mc[c] - M) * invL;
-        if (rank == 0 && a.lse) a.lse[gp * H + tid] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
-      }
-      bar_named(1, kWorkers);
-      tc_fence_after();
-      // the dims this CTA owns: lanes of quadrant q4 in each 128-dim block
-      const int q4 = warp & 3, hh = warp >> 2;   // heads 32 hh .. + 31
-      const uint32_t s_row = tmem + ((uint32_t)(32 * q4) << 16);
-      float *outp = a.out + gp * H * D;
-#pragma unroll 1
-      for (int mt = 0; mt < 4; ++mt) {
-        const int d = mt * 128 + 32 * q4 + lane;
-        const bool own = d / dc == (int)rank;
-        if (!__any_sync(0xffffffffu, own)) continue;
-        uint32_t v[32];
-        tmem_ld32(s_row + kColO + (uint32_t)(mt * H + hh * 32), v);
-        tmem_ld_wait();
-        if (!own) continue;
-        float acc[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-          acc[i] = __uint_as_float(v[i]) * S.inv_l[hh * 32 + i] * wgt[rank][hh * 32 + i];
-        // the peers' partials, four chunks' loads in flight at a time
-#pragma unroll 1
-        for (int c0 = 0; c0 < C; c0 += 4) {
-          uint4 pv[4][4];
-          // chunks past C or this CTA's own read a written slot and count 0
-          const int cfill = rank == 0 ? 1 : 0;
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int c = c0 + cc;
-            const int cl = (c < C && c != (int)rank) ? c : cfill;
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.part_o + (int64_t)(tok * C + cl) * D * H) +
-                               (d >> 5) * 256 + (hh * 4) * 32 + (d & 31);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) pv[cc][k] = ld_cg_v4(src + 32 * k);
-          }
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int c = c0 + cc;
-            const bool use = c < C && c != (int)rank;
-            const float *wc = wgt[use ? c : 0] + hh * 32;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint32_t w4[4] = {pv[cc][k].x, pv[cc][k].y, pv[cc][k].z, pv[cc][k].w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float2 fv = __half22float2(*reinterpret_cast<const __half2 *>(&w4[e]));
-                const float w0 = use ? wc[8 * k + 2 * e] : 0.0f, w1 = use ? wc[8 * k + 2 * e + 1] : 0.0f;
-                acc[8 * k + 2 * e] = fmaf(w0, use ? fv.x : 0.0f, acc[8 * k + 2 * e]);
-                acc[8 * k + 2 * e + 1] = fmaf(w1, use ? fv.y : 0.0f, acc[8 * k + 2 * e + 1]);
-              }
-            }
-          }
-        }
-        const float keep = S.abort ? 0.0f : 1.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) outp[(hh * 32 + i) * D + d] = acc[i] * keep;
-      }
-    }
+    if (a.C > 1) cluster_combine(a, S, tile, tmem, first_item, tid, warp, lane);
   }
 
   tc_fence_before();
@@ -838,12 +845,11 @@ int choose_chunks(int problems, int K, int W, int kernel, int sms) {
 }  // namespace
 
 size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W, int32_t kernel) {
-  const int C = choose_chunks(problems, K, W, kernel, device_sms());
-  if (C <= 1) return 256;
-  const size_t items = (size_t)problems * C;
-  size_t b = (items * D * H * 2 + 255) & ~size_t(255);
-  b += items * 2 * H * 4;
-  return (b + 255) & ~size_t(255);
+  (void)problems;
+  (void)K;
+  (void)W;
+  (void)kernel;
+  return 256;   // the chunks of a token combine through distributed shared memory
 }
 
 cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches) {
@@ -858,9 +864,7 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
   // one block per CTA (its rows past 128 must be entries: SWA rows come first)
   const bool single = one_item && r16 <= kMaxBk && (a.W + a.C - 1) / a.C <= kBlockRows;
   a.Bk = single ? r16 : kBlockRows;
-  uint8_t *p = static_cast<uint8_t *>(scratch);
-  a.part_o = reinterpret_cast<__half *>(p);
-  a.part_ml = reinterpret_cast<float *>(p + (((size_t)items * D * H * 2 + 255) & ~size_t(255)));
+  (void)scratch;
   CUtensorMap tm_q;
   if (!make_tmap_bf16(&tm_q, a.q, D, (a.p0 + a.problems) * H, H)) return cudaErrorInvalidValue;
   auto kern = single ? sparse_attn_kernel<true> : sparse_attn_kernel<false>;

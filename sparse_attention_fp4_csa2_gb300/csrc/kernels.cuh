@@ -148,8 +148,6 @@ struct AttnArgs {
   const int32_t *swa_len;     // [P]
   float *out;                 // [P][64][512]
   float *lse;                 // [P][64] or NULL
-  __half *part_o;             // chunked tokens: [P * C][512][64] normalised partials (workspace)
-  float *part_ml;             // chunked tokens: [P * C][2][64] (reference max, row sum) (workspace)
   int64_t cap;
   int32_t problems;
   int32_t K;

@@ -114,6 +114,20 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// Read-only global loads the compiler keeps where they are written (volatile):
+// prefetches issued a block ahead must not be sunk to their first use.
+__device__ __forceinline__ uint4 ld_nc_v4(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_nc_u32(const void *p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 // 2-D tiled tensor copy global -> shared (box and swizzle from the tensor map).
 // x is the innermost coordinate in elements; x * elem_size must be a multiple
 // of 16 bytes.
@@ -394,6 +408,11 @@ __device__ __forceinline__ uint32_t dsmem_ld_u32(uint32_t addr) {
 
 __device__ __forceinline__ void dsmem_st_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_st_v4(uint32_t addr, uint4 v) {
+  asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v) {
