@@ -37,11 +37,12 @@ sys.path.insert(0, ROOT)
 METRIC = "CSA2 sparse-decode tokens/s at 64K/1M ctx; achieved HBM GB/s vs ~8 TB/s"
 ATTN_BYTES = 512 * 288 + (128 * 512 + 128 * 4) + 64 * 512 * 2 + 64 * 512 * 4 + 512 * 4   # per (seq, layer)
 SWEEP_FIXED = 32 * 128 * 2 + 32 * 4        # q_idx + w per sequence
-# DRAM bytes (read + write) per launch from one ncu capture of the current
-# kernel code on that workload (profiles/<kernel>_<workload>.md); absent: null
+# DRAM bytes (read + write) per launch, dram__bytes_read.sum +
+# dram__bytes_write.sum, from one ncu capture of the kernel code as it now
+# stands on that workload (stored, not measured by this run); a kernel changed
+# since its capture has no entry and reports null.
 TRAFFIC = {
     ("indexer_sweep_kernel", "group_decode_32x64k"): 537181184 + 6408192,
-    ("sparse_attn_kernel", "group_decode_32x64k"): 10633984,
     # captured at 16 sequences, scaled by the rows read to the 32-sequence launch
     ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411200 + 915968),
 }
@@ -87,6 +88,7 @@ def roof_entry(kernel, workload, bound, work, launch_ms, count, peaks_):
         ach, unit, key = work / (launch_ms / 1e3) / 1e9, "GB/s", "alg_bytes_per_launch"
     return {"kernel": kernel, "bound": bound, "achieved": round(ach, 1), "peak": peak, "peak_kind": kind,
             "unit": unit, "frac": round(ach / peak, 4), "traffic": TRAFFIC.get((kernel, workload)),
+            "traffic_source": "stored ncu capture of this kernel code" if (kernel, workload) in TRAFFIC else None,
             "launch_ms": round(launch_ms, 4), key: work, "launches_per_step": count,
             "step_ms_est": round(count * launch_ms, 4)}
 
@@ -97,7 +99,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=0,
                     help="timed steps (default: enough for about 1.5 s of timed work, 20 to 5000)")
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="group_decode_32x64k")
+    ap.add_argument("--config", default="group_decode_32x64k",
+                    help="workload (the default run also times decoder20_4x1m under ctx_1m)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
@@ -141,48 +144,62 @@ def algorithmic_bytes(cfg, hsi, fp4=False, project=False):
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling (every 50 ms, read-only queries) of SM clocks and
+    throttle reasons from the warm-up through the timed region."""
 
     def __init__(self, path):
         self.path = path
         self.proc = None
 
     def __enter__(self):
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+        import atexit
+        atexit.register(self.__exit__)   # never leave the sampler running
+        q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                                          "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                                          "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
         return self
 
     def __exit__(self, *a):
-        if self.proc:
+        if self.proc and self.proc.poll() is None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+        if self.proc and not self.f.closed:
             self.f.close()
 
-    def summary(self, device_index):
+    def summary(self, device_index, t0=None, t1=None):
+        """Median SM clock and the throttle reasons seen, over the samples
+        taken between host times t0 and t1 (seconds since the epoch)."""
+        import datetime
+        self.__exit__()
         if not self.proc or not os.path.exists(self.path):
             return None
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9 or not f[0].isdigit() or int(f[0]) != device_index:
+            if len(f) < 10 or not f[1].isdigit() or int(f[1]) != device_index:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if ts is not None and t0 is not None and not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            try:
+                sm.append(float(f[2]))
+                mx = float(f[3])
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
@@ -200,6 +217,7 @@ class Workload:
         import synth
         import sparse_attention_fp4_csa2_gb300 as c2
         self.c2, self.cfg, self.dev = c2, cfg, device
+        self.planted = None
         B, N, m = cfg.batch, cfg.n_ctx, cfg.m
         # m = 2: the context's N tokens are E = N / 2 entries and the step's
         # token completes entry E - 1; every Full layer keeps its own copy
@@ -229,7 +247,7 @@ class Workload:
             k = synth.indexer_keys(cs, B, E, device=device)
             if cfg.planted_blocks and c == 0:
                 li0 = synth.layer_inputs(cfg.layer_seeds[0], B, device=device)
-                synth.plant_blocks(k, li0.q_idx, li0.w, E, cfg.planted_blocks, seed)
+                self.planted = synth.plant_blocks(k, li0.q_idx, li0.w, E, cfg.planted_blocks, seed)
             if self.fp4:
                 # the same keys through this library's MXFP4 writer; every
                 # Full layer also writes its new token's entry
@@ -269,6 +287,14 @@ class Workload:
 
     def tokens(self):
         return self.B
+
+    def planted_recall(self):
+        """Recall of the planted high-score blocks (keys aligned to the Full
+        layer's query) in the HSI pool the last step built."""
+        pool = self.pool.cpu()
+        hit = sum(len(set(self.planted[b].tolist()) & set(pool[b].tolist())) for b in range(self.B))
+        return {"pool_blocks": round(hit / self.planted.numel(), 4), "planted_per_sequence": self.planted.shape[1],
+                "pool_size_blocks": pool.shape[1]}
 
     # kernels timed live inside the step: (library kernel id, kernel name)
     PROFILED = ((0, "indexer_sweep_kernel"), (3, "topk_cluster_kernel"), (1, "sparse_attn_kernel"))
@@ -490,30 +516,23 @@ class PrefillWorkload:
                 [[self.out, self.lse, self.topk]])
 
 
+DEFAULT_CONFIG = "group_decode_32x64k"   # the 64K workload the metric is quoted on
+LONG_CONFIG = "decoder20_4x1m"           # its 1M-context workload, timed beside it by default
 ATTN_KERNEL = 0       # csa2_params.attn_kernel of the workloads (--attn-kernel)
 INDEXER_FP4 = False   # csa2_params.indexer_fp4 of the decode workloads (--indexer-fp4)
 PROJECT_IK = False    # Full layers project their new indexer key (--project-ik)
 
 
-def run_ours(args, rank, world, local_rank):
-    global ATTN_KERNEL, INDEXER_FP4, PROJECT_IK
-    ATTN_KERNEL = args.attn_kernel
-    INDEXER_FP4 = args.indexer_fp4
-    PROJECT_IK = args.project_ik
+def measure(args, cfg, dev, rank, world, local_rank, steps):
+    """Build `cfg`'s workload on `dev`, capture its step in CUDA graphs and
+    time `steps` replays (0: about 1.5 s of timed work), then the end-to-end
+    replays; the fields of the JSON line that describe this workload."""
     import torch
 
-    import synth
     import sparse_attention_fp4_csa2_gb300 as c2
-    from sparse_attention_fp4_csa2_gb300 import build as b
-    b.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    cfg = synth.CONFIGS[args.config]
-    if args.batch:
-        import dataclasses
-        cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}[batch={args.batch}]")
-    if cfg.chunk and (INDEXER_FP4 or PROJECT_IK):
-        raise SystemExit("--indexer-fp4 / --project-ik: decode workloads only")
+    # the sampler starts now (nvidia-smi takes a moment to come up); only its
+    # samples from the first warm-up replay to the end of the timed region count
+    clk = Clocks(os.path.join(tempfile.gettempdir(), f"csa2_clocks_r{rank}.csv")).__enter__()
     wl = PrefillWorkload(cfg, dev) if cfg.chunk else Workload(cfg, dev)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -564,6 +583,7 @@ def run_ours(args, rank, world, local_rank):
                 per.setdefault(k, []).append(a.elapsed_time(b))
         return tot, per
 
+    t_warm = time.time()
     for _ in range(max(3, args.warmup)):
         with torch.cuda.stream(stream):
             flush_l2()
@@ -577,14 +597,18 @@ def run_ours(args, rank, world, local_rank):
     dom_k = [k for k, n in wl.PROFILED if dom and n == dom["kernel"]]
     live = events_for(dom_k)
     g = capture(live)
-    for _ in range(max(3, args.warmup)):
+    # at least W warm-up replays of the timed graph, and at least 0.4 s of
+    # them, so that the clock record holds samples under this load
+    n_warm, t_w = 0, time.time()
+    while n_warm < max(3, args.warmup) or time.time() - t_w < 0.4:
         with torch.cuda.stream(stream):
             flush_l2()
             g.replay()
-    stream.synchronize()
+        stream.synchronize()
+        n_warm += 1
 
-    if args.steps <= 0:
-        # enough steps for about 1.5 s of timed work (clock samples every 200 ms)
+    if steps <= 0:
+        # enough steps for about 1.5 s of timed work
         probe_ms, _ = timed(3, g)
         fl0, fl1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -593,15 +617,16 @@ def run_ours(args, rank, world, local_rank):
             fl1.record(stream)
         stream.synchronize()
         per = probe_ms / 3 + fl0.elapsed_time(fl1)
-        args.steps = int(min(5000, max(20, math.ceil(1500.0 / per))))
-        args.steps = int(max_over_ranks([args.steps], dev)[0])   # every rank times the same count
+        steps = int(min(5000, max(20, math.ceil(1500.0 / per))))
+        steps = int(max_over_ranks([steps], dev)[0])   # every rank times the same count
 
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with Clocks(os.path.join(tempfile.gettempdir(), f"csa2_clocks_r{rank}.csv")) as clk:
-        total_ms, live_ms = timed(args.steps, g, live)
+    total_ms, live_ms = timed(steps, g, live)
     torch.cuda.synchronize()
+    t_end = time.time()
+    clk.__exit__(None, None, None)
     total_ms = max_over_ranks([total_ms], dev)[0]
 
     # end to end: every step's inputs copied from pinned host memory and its
@@ -617,7 +642,7 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             g_io.replay()
     stream.synchronize()
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(steps, 20))
     if world > 1:
         torch.distributed.barrier()
     e2e_ms, _ = timed(e2e_steps, g_io)
@@ -625,7 +650,7 @@ def run_ours(args, rank, world, local_rank):
     h2d, d2h = io.h2d, io.d2h
     assert c2.get_device_status(stream) == 0
 
-    ms = total_ms / args.steps
+    ms = total_ms / steps
     tokens_per_s = whole_job_rate(world, wl.tokens(), ms)
     # the dominant kernel (largest estimated share of the step), its launch
     # time measured live over the timed region; every profiled kernel from
@@ -639,18 +664,58 @@ def run_ours(args, rank, world, local_rank):
         r["launch_timing"] = "profiling replays (events around every profiled kernel)"
     conf = wl.config(ms)
     conf["l2"] = "flushed between steps (512 MB write, then 512 MB read), outside the timed events"
-    line = {
-        "metric": METRIC, "value": round(tokens_per_s, 1), "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    clocks = clk.summary(local_rank, t_warm, t_end)
+    if clocks:
+        clocks["window"] = "nvidia-smi every 50 ms from the first warm-up replay to the end of the timed region"
+    res = {
+        "value": round(tokens_per_s, 1), "steps": steps, "ms_per_step": round(ms, 4),
         "config": conf,
         "roofline": roof,
         "roofline_kernels": roofs,
         "e2e": {"value": round(whole_job_rate(world, wl.tokens(), e2e_ms / e2e_steps), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches * args.steps,
-        "clocks": clk.summary(local_rank),
+        "gpu_launches": launches * steps,
+        "clocks": clocks,
     }
+    if getattr(wl, "planted", None) is not None:
+        res["hsi_recall"] = wl.planted_recall()
+    del g, g_prof, g_io, io, wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, rank, world, local_rank):
+    global ATTN_KERNEL, INDEXER_FP4, PROJECT_IK
+    ATTN_KERNEL = args.attn_kernel
+    INDEXER_FP4 = args.indexer_fp4
+    PROJECT_IK = args.project_ik
+    import torch
+
+    import synth
+    from sparse_attention_fp4_csa2_gb300 import build as b
+    b.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = synth.CONFIGS[args.config]
+    if args.batch:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}[batch={args.batch}]")
+    if cfg.chunk and (INDEXER_FP4 or PROJECT_IK):
+        raise SystemExit("--indexer-fp4 / --project-ik: decode workloads only")
+    res = measure(args, cfg, dev, rank, world, local_rank, args.steps)
+    line = {"metric": METRIC, "value": res.pop("value"), "unit": "tokens/s", "n_gpus": world,
+            "steps": res.pop("steps"), "warmup": args.warmup, "ms_per_step": res.pop("ms_per_step"),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic"}
+    line.update(res)
+    plain = not (args.batch or INDEXER_FP4 or PROJECT_IK or ATTN_KERNEL)
+    if args.config == DEFAULT_CONFIG and plain:
+        # the metric's other context: the 20-layer step at 1M tokens, same
+        # timing rules, reported beside the 64K line
+        r1 = measure(args, synth.CONFIGS[LONG_CONFIG], dev, rank, world, local_rank, args.steps)
+        r1["unit"] = "tokens/s"
+        line["ctx_1m"] = r1
     if rank == 0:
         line["cpu_baseline"] = (cpu_baseline_prefill if cfg.chunk else cpu_baseline)(args, cfg, seconds=args.cpu_seconds)
         print(json.dumps(line), flush=True)

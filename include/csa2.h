@@ -25,8 +25,11 @@
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers, caller-owned; the library never
- *    allocates or frees memory and keeps no state between calls except a
- *    per-device error word (see csa2_get_device_status).
+ *    allocates or frees memory.  Between calls it keeps only a per-device
+ *    error word (see csa2_get_device_status), the per-thread launch count of
+ *    the last call (csa2_last_launch_count) and, on each device that has run
+ *    csa2_hier_pool_select_static, that call's static scratch array, which
+ *    holds the last call's contents.
  *  - Every call is asynchronous on `stream` (NULL = legacy default stream) and
  *    returns CSA2_OK once its kernels are enqueued.  Host-side validation
  *    failures return an error code without launching anything.

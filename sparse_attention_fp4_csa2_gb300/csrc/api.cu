@@ -17,6 +17,12 @@ thread_local ProfileEvents g_profile[4];
 
 ProfileEvents &profile_events(int kernel) { return g_profile[kernel >= 0 && kernel < 4 ? kernel : 0]; }
 
+namespace {
+thread_local int32_t g_last_launches = 0;
+}
+
+void set_last_launch_count(int32_t n) { g_last_launches = n; }
+
 cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream) {
   cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(stream, &cs);
@@ -26,8 +32,6 @@ cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream) {
 }
 
 namespace {
-
-thread_local int32_t g_last_launches = 0;
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

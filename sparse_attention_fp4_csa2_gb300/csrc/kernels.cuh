@@ -58,6 +58,9 @@ struct ProfileEvents {
   cudaEvent_t start = nullptr, stop = nullptr;
 };
 ProfileEvents &profile_events(int kernel);
+// Kernel launches of the last successful call on this host thread
+// (csa2_last_launch_count); every entry point sets it.
+void set_last_launch_count(int32_t n);
 // Records `ev` on `stream`; inside a stream capture it becomes an event-record
 // node of the graph, so every replay records it.
 cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream);

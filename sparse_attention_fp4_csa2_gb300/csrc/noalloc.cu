@@ -57,6 +57,7 @@ using namespace csa2;
 extern "C" csa2_status csa2_hier_pool_select_static(const float *block_scores, const int32_t *n_vis,
                                                     int32_t batch, int64_t n_max, const csa2_params *params,
                                                     int32_t *pool_blocks, csa2_stream_t stream) {
+  set_last_launch_count(0);
   if (!params || params->candidate_block_size != BLOCK || params->candidate_topk_blocks < 16 ||
       params->candidate_topk_blocks > TOPK_MAX_K || params->candidate_topk_blocks % 16 != 0)
     return CSA2_ERR_UNSUPPORTED;
@@ -80,5 +81,7 @@ extern "C" csa2_status csa2_hier_pool_select_static(const float *block_scores, c
   r.out = pool_blocks;
   int launches = 0;
   const cudaError_t e = launch_pool_topk(r, scratch, 0, reinterpret_cast<cudaStream_t>(stream), &launches);
-  return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA;
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
+  set_last_launch_count(launches);
+  return CSA2_OK;
 }

@@ -85,13 +85,13 @@ def test_encoder_group_step_m2(c2, orc, fp4):
             s = orc.index_scores_mxfp4(li[1].q_idx[b], li[1].w[b], codes, scales)
         else:
             s = orc.index_scores(li[1].q_idx[b], li[1].w[b], k[b])
-        o_idx = orc.topk(s, 512)
-        ndiff = check_topk(topk_h[b], o_idx, s, n_valid=E)
-        if ndiff == 0:
-            rows = orc.kv_entries(lat[b][o_idx], z[b][o_idx], 2, o_idx * 2 + 1)
-            for i in (1, 2):
-                o, l = orc.sparse_attn(li[i].q[b], rows, np.arange(len(o_idx)), li[i].swa[b], li[i].swa_scale[b],
-                                       128)
-                check_attn(outs[i][b].cpu().numpy(), o)
-                check_lse(lses[i][b].cpu().numpy(), l)
+        check_topk(topk_h[b], orc.topk(s, 512), s, n_valid=E)
+        # the readouts are checked on the GPU's own selection (it may differ
+        # from the oracle's only inside the tie band bounded above)
+        sel = topk_h[b][topk_h[b] >= 0]
+        rows = orc.kv_entries(lat[b][sel], z[b][sel], 2, sel * 2 + 1)
+        for i in (1, 2):
+            o, l = orc.sparse_attn(li[i].q[b], rows, np.arange(len(sel)), li[i].swa[b], li[i].swa_scale[b], 128)
+            check_attn(outs[i][b].cpu().numpy(), o)
+            check_lse(lses[i][b].cpu().numpy(), l)
 

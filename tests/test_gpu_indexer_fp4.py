@@ -131,6 +131,35 @@ def test_fp4_full_indexer_topk_and_block_scores(c2, orc, B, cap, n_vis, K, wide)
         assert np.all(np.isneginf(bs[b, nb:]))
 
 
+def test_fp4_block_sum_reduction_and_pool(c2, orc):
+    """block_reduce = 1 with the MXFP4 sweep: block scores are sums of the 8
+    positions' MXFP4 scores, and the HSI pool follows the oracle's sum
+    reduction."""
+    B, cap = 2, 5000
+    n_vis = [5000, 2345]
+    q_idx, w, k, nv = _index_case(61, B, cap, n_vis)
+    p = c2.Params.make(candidate_topk_blocks=256, block_reduce=1, indexer_fp4=1)
+    ws = c2.workspace(c2.OP_DECODE, B, cap, p)
+    nblk = (cap + 7) // 8
+    bs = torch.empty(B, nblk, dtype=torch.float32, device="cuda")
+    topk = torch.empty(B, 512, dtype=torch.int32, device="cuda")
+    c2.indexer_score_topk(q_idx.cuda(), w.cuda(), _fp4_cache(c2, k), nv.cuda(), cap, p, topk, ws, block_scores=bs)
+    pool = torch.empty(B, 256, dtype=torch.int32, device="cuda")
+    c2.hier_pool_select(bs, nv.cuda(), cap, p, pool, ws)
+    assert c2.get_device_status() == 0
+    bs, pool = bs.cpu().numpy(), pool.cpu().numpy()
+    for b in range(B):
+        n = n_vis[b]
+        s = _oracle_scores(orc, q_idx[b], w[b], k[b, :n])
+        ob = orc.block_scores(s, n, 8, reduce_sum=True)
+        nb = len(ob)
+        assert np.allclose(bs[b, :nb], ob, rtol=1e-4, atol=1e-4 * np.abs(ob).max())
+        assert np.all(np.isneginf(bs[b, nb:]))
+        ob[(n - 1) // 8] = np.inf
+        check_topk(pool[b], orc.hsi_pool(s, n, 8, 256, reduce_sum=True), ob)
+        assert (n - 1) // 8 in set(pool[b].tolist())
+
+
 def test_fp4_ranking_follows_the_quantised_keys(c2, orc):
     """The FP4 path scores the quantised operands: keys whose dim-0 values
     2.75, 2.90625, 3.1875 all round to E2M1 3 (and 3.625 to 4) tie in MXFP4,

@@ -58,24 +58,21 @@ def _prefill_case(c2, seed, B, ctx_tokens, T, m=2, W=128, K=512):
 def _check_tokens(orc, d, samples):
     m, W, K = d["m"], d["W"], d["K"]
     kvh = {}
-    exact = 0
     for b, i in samples:
         pos = d["first_pos"] + i
         nvis = (pos + 1) // m
         s = orc.index_scores(d["q_idx"][b, i], d["w"][b, i], d["k_idx"][b, :nvis])
-        o_idx = orc.topk(s, K)
-        ndiff = check_topk(d["topk"][b, i], o_idx, s, n_valid=nvis)
-        if ndiff:
-            continue
-        exact += 1
+        check_topk(d["topk"][b, i], orc.topk(s, K), s, n_valid=nvis)
+        # every sampled token's readout is checked on the GPU's own selection
+        # (it may differ from the oracle's only inside the tie band above)
         if b not in kvh:
             kvh[b] = orc.kv_entries(d["lat"][b], d["z"][b], m, np.arange(d["E"]) * m + m - 1)
         start = max(pos - W + 1, 0)
         r0, r1 = start - d["swa_first"], pos - d["swa_first"] + 1
-        o, l = orc.sparse_attn(d["q"][b, i], kvh[b], o_idx, d["swa"][b, r0:r1], d["swa_scale"][b, r0:r1], r1 - r0)
+        o, l = orc.sparse_attn(d["q"][b, i], kvh[b], d["topk"][b, i], d["swa"][b, r0:r1], d["swa_scale"][b, r0:r1],
+                               r1 - r0)
         check_attn(d["out"][b, i], o)
         check_lse(d["lse"][b, i], l)
-    assert exact >= len(samples) // 2
 
 
 def _check_all_valid(d):

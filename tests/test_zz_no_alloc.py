@@ -49,8 +49,10 @@ def test_static_pool_select_matches_workspace_version_twice(c2, seed):
         p = c2.Params.make(candidate_topk_blocks=nb)
         ref = torch.empty(B, nb, dtype=torch.int32, device="cuda")
         c2.hier_pool_select(bs, nv, n_max, p, ref, c2.workspace(c2.OP_POOL, B, n_max, p))
+        ref_launches = c2.last_launch_count()
         got = torch.full((B, nb), -5, dtype=torch.int32, device="cuda")
         assert _static_call(c2, bs, nv, n_max, p, got) == 0
+        assert c2.last_launch_count() == ref_launches > 0   # the same kernels, counted for this call
         assert c2.get_device_status() == 0
         assert torch.equal(got, ref), f"call {i}: static-scratch pool differs"
 
@@ -65,3 +67,4 @@ def test_static_pool_select_refuses_oversize(c2):
         ctypes.c_void_p(bs.data_ptr()), ctypes.c_void_p(nv.data_ptr()), B, n_max, ctypes.byref(p),
         ctypes.c_void_p(pool.data_ptr()), None)
     assert st == 3      # CSA2_ERR_WORKSPACE: more than the static scratch holds
+    assert c2.last_launch_count() == 0
