@@ -79,7 +79,7 @@ constexpr float kLn2 = 0.69314718055994531f;
 constexpr uint32_t kIdescPV = idesc_f16(/*fp16*/ 0, /*A MN-major*/ 1, /*B K-major*/ 0, /*N*/ H, /*M*/ 128);
 
 struct __align__(16) Ctl {
-  uint64_t q_full, q_ready, s_full, p_full, done, comb;
+  uint64_t q_full[4], q_ready[4], s_full, p_full, done, comb;
   uint64_t cols_full[4], cols_free[4];
   uint32_t tmem_base;
   volatile uint32_t abort;
@@ -425,13 +425,15 @@ __device__ __forceinline__ void cluster_combine(const AttnArgs &a, Ctl &S, uint8
   cluster_wait();
 }
 
-// Q of an item: bf16 -> fp16 in place (the same 2-byte slots of the swizzled
-// layout; |q| < 65504 assumed), once its copy has landed.
-__device__ __forceinline__ void convert_q(uint8_t *qs, int t, int nthreads) {
-  for (int i = t; i < kQBytes / 16; i += nthreads) {
-    uint4 *ptr = reinterpret_cast<uint4 *>(qs) + i;
-    const uint4 v = *ptr;
-    *ptr = make_uint4(pack_half2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)),
+// Column pair p of an item's Q (16 KB: 64 heads x 128 dims): bf16 -> fp16 in
+// place (the same 2-byte slots of the swizzled layout; |q| < 65504 assumed),
+// once its copy has landed.
+__device__ __forceinline__ void convert_q_pair(uint8_t *qs, int p, int t, int nthreads) {
+  uint4 *q = reinterpret_cast<uint4 *>(qs + p * 2 * kAtom);
+#pragma unroll 4
+  for (int i = t; i < 2 * kAtom / 16; i += nthreads) {
+    const uint4 v = q[i];
+    q[i] = make_uint4(pack_half2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u)),
                       pack_half2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u)),
                       pack_half2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u)),
                       pack_half2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u)));
@@ -469,9 +471,12 @@ __device__ __forceinline__ void issue_pv(int nks, Ctl &S, uint32_t tmem, uint64_
 // Q of an item's token by TMA (bf16, 8 boxes of [64 heads x 64 dims], 128B swizzle).
 __device__ __forceinline__ void load_q(const AttnArgs &a, Ctl &S, const CUtensorMap &tm_q, uint8_t *qs, int item) {
   const int64_t gp = a.p0 + item / a.C;
-  mbar_arrive_expect_tx(&S.q_full, (uint32_t)kQBytes);
 #pragma unroll
-  for (int c = 0; c < D / 64; ++c) tma_load_2d(qs + c * kAtom, &tm_q, c * 64, (int32_t)(gp * H), &S.q_full);
+  for (int p = 0; p < 4; ++p) {   // one barrier per column pair: S starts on the first pair
+    mbar_arrive_expect_tx(&S.q_full[p], (uint32_t)(2 * kAtom));
+    tma_load_2d(qs + 2 * p * kAtom, &tm_q, 2 * p * 64, (int32_t)(gp * H), &S.q_full[p]);
+    tma_load_2d(qs + (2 * p + 1) * kAtom, &tm_q, (2 * p + 1) * 64, (int32_t)(gp * H), &S.q_full[p]);
+  }
 }
 
 template <bool kSingle>
@@ -493,8 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int stride = gridDim.x;
 
   if (tid == 0) {
-    mbar_init(&S.q_full, 1);
-    mbar_init(&S.q_ready, kQThreads);
+    for (int p = 0; p < 4; ++p) {
+      mbar_init(&S.q_full[p], 1);
+      mbar_init(&S.q_ready[p], kQThreads);
+    }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, kWorkers);
     mbar_init(&S.done, 1);
@@ -523,37 +530,35 @@ __global__ void __launch_bounds__(kThreads, 1)
    setmaxnreg_dec<kRegsMma>();
    if (warp > kMmaWarp) {
     // the other warps of the MMA warpgroup: every item's Q, bf16 -> fp16 in
-    // place once it has landed (the MMA thread reloads it after an item's
-    // last S); then, in a single block of more than 128 rows, warps 9 and 10
-    // write rows 128 .. (entries: SWA rows come first)
+    // place one column pair at a time as it lands (the MMA thread reloads Q
+    // after an item's last S); in a single block of more than 128 rows, warps
+    // 9 and 10 also write rows 128 .. (entries: SWA rows come first), each
+    // column pair right after Q's
     const int ht = tid - (kMmaWarp + 1) * 32;   // 0 .. 95
     const int r = 128 + (ht >> 1), hcp = ht & 1;
     const bool rows = kSingle && ht < 64 && first_item < items && r < a.Bk;
     EntryBuf eb;
-    Item it0;
     if (rows) {   // the rows' loads go out before the wait for Q
-      it0 = item_info(a, first_item);
+      const Item it0 = item_info(a, first_item);
       load_row(a, it0, r, row_slot(a, it0, r), hcp, eb);
-    }
-    {
-      uint32_t n = 0;
-      for (int item = first_item; item < items; item += stride, ++n) {
-        wait_ft(S, &S.q_full, n & 1u);
-        convert_q(qs, ht, kQThreads);
-        mbar_arrive(&S.q_ready);
+      if (hcp == 0) {
+        S.rs[r] = eb.scale;
+        S.vld[r] = eb.kind != 0 ? 1 : 0;
       }
     }
-    if constexpr (kSingle) {
-      if (ht < 64 && first_item < items) {
-        if (rows && hcp == 0) {
-          S.rs[r] = eb.scale;
-          S.vld[r] = eb.kind != 0 ? 1 : 0;
-        }
+    uint32_t n = 0;
+    for (int item = first_item; item < items; item += stride, ++n) {
 #pragma unroll 1
-        for (int p = 0; p < 4; ++p) {
-          if (rows) dequant_front(tile, col_stride, r, hcp + 2 * p, eb);
-          fence_proxy_async_smem();
-          mbar_arrive(&S.cols_full[p]);
+      for (int p = 0; p < 4; ++p) {
+        wait_ft(S, &S.q_full[p], n & 1u);
+        convert_q_pair(qs, p, ht, kQThreads);
+        mbar_arrive(&S.q_ready[p]);
+        if constexpr (kSingle) {   // one item
+          if (ht < 64) {
+            if (rows) dequant_front(tile, col_stride, r, hcp + 2 * p, eb);
+            fence_proxy_async_smem();
+            mbar_arrive(&S.cols_full[p]);
+          }
         }
       }
     }
@@ -573,11 +578,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Item it = item_info(a, item);
         for (int j = 0; j < it.nb; ++j, ++g) {
           const uint32_t ph = g & 1u;
-          if (j == 0) wait_ft(S, &S.q_ready, n_item & 1u);
+
           // (no MMA sits under a per-instruction condition: a conditional
           // tcgen05.mma in unrolled code was observed to issue wrongly)
 #pragma unroll 1
           for (int p = 0; p < 4; ++p) {
+            if (j == 0) wait_ft(S, &S.q_ready[p], n_item & 1u);
             wait_ft(S, &S.cols_full[p], ph);
             tc_fence_after();
             const uint64_t a0 = qd + (uint64_t)(p * 2 * kAtom >> 4), a1 = a0 + (kAtom >> 4);

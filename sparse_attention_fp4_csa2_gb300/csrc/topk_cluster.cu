@@ -7,23 +7,28 @@
 // Scores become order-preserving 32-bit keys (-inf marks an invalid slot).
 // The CTAs of the cluster split the row into contiguous slices; in a round
 // each warp covers 1024 consecutive values with 8 coalesced float4 loads in
-// flight per thread.
+// flight per thread (a slice of one round stays in registers throughout).
 //   1. sample: the first of every warp's 8 loads (1/8 of the values); a low
 //      threshold t_low with about twice the sample's share of k above it,
 //      located to 22 key bits by two histogram levels (the top 11 bits, then
 //      the next 11 inside the threshold bin);
 //   2. filter: every key >= t_low goes to the CTA's candidate list in shared
 //      memory, in index order (warp and CTA prefix sums of per-thread counts
-//      give every thread its output slots: no per-key atomics);
-//   3. exact radix select -- 11, 11 and 10 key bits -- on the candidate lists
-//      when together they hold >= k keys and none overflowed, else on the
-//      whole slices; a level stops early when its threshold bin holds exactly
-//      the count still needed; keys equal on all 32 bits are taken toward the
-//      lower index (each CTA its quota, in index order, after a cluster prefix
-//      of the per-CTA tie counts);
-//   4. each CTA sorts the indices it selected and writes them at its cluster
-//      prefix offset (slices are in index order), mapped through the HSI pool
-//      for Reindex rows; the last CTA pads with -1.
+//      give every thread its output slots: no per-key atomics), and then to a
+//      block of the leader's (rank 0) list reserved by a remote atomic add;
+//   3. when every list fits its slot and together they hold >= k keys, the
+//      leader alone finds the exact top k in the gathered list (three radix
+//      levels over local histograms, ties on the full key toward the lower
+//      index) and writes them in list order, which is index order;
+//   4. otherwise the cluster selects together: exact radix select -- 11, 11
+//      and 10 key bits -- on the candidate lists when together they hold >= k
+//      keys and none overflowed, else on the whole slices; a level stops early
+//      when its threshold bin holds exactly the count still needed; keys equal
+//      on all 32 bits are taken toward the lower index (each CTA its quota, in
+//      index order, after a cluster prefix of the per-CTA tie counts); each
+//      CTA sorts the indices it selected and writes them at its cluster prefix
+//      offset (slices are in index order); the last CTA pads with -1.
+// Selected positions are mapped through the HSI pool for Reindex rows.
 // Histograms are exchanged by pushing each CTA's non-zero bins into every
 // CTA's cluster total with remote atomic adds; all waiting is at cluster
 // barriers, which the hardware co-schedules.
@@ -39,9 +44,10 @@ constexpr int kBinsPerThread = kBins / kThreads;
 constexpr int kSelMax = 2048;          // index_topk limit
 constexpr int kVec = 8;                // float4 loads per thread per round (32 values)
 constexpr int kRound = kThreads * kVec * 4;   // values per CTA per round
-constexpr int kCand = 4096;            // per-CTA candidate list
+constexpr int kCand = 2048;            // per-CTA candidate list
 constexpr int kSampleEvery = 8;        // the sample: 1 of every warp's 8 loads
 constexpr int kMaxCluster = 16;        // CTAs per row (non-portable cluster size)
+constexpr int kGather = 2048;          // the leader's list of the whole row's candidates
 
 struct __align__(16) TopkClusterSmem {
   uint32_t hist[kBins];                // this CTA's histogram of the current level
@@ -49,6 +55,10 @@ struct __align__(16) TopkClusterSmem {
   uint32_t ckey[kCand];
   int32_t cidx[kCand];
   int32_t sel[kSelMax];                // this CTA's selected indices
+  uint32_t gkey[kGather];              // leader: every CTA's candidates, a block per CTA
+  int32_t gidx[kGather];
+  uint32_t cand_base[kMaxCluster];     // where each CTA's block starts in the leader's list
+  uint32_t g_used, g_base;             // leader: entries reserved; this CTA: its block
   uint32_t cand_cnt[kMaxCluster];      // per-CTA counts, pushed by the CTAs
   uint32_t tie_cnt[kMaxCluster];
   uint32_t sel_cnt[kMaxCluster];
@@ -58,6 +68,8 @@ struct __align__(16) TopkClusterSmem {
   int thr;
   uint32_t above, total, in_thr;
 };
+
+static_assert(3 * (sizeof(TopkClusterSmem) + 1024 + 16) <= 232448, "three CTAs must fit on an SM");
 
 __device__ __forceinline__ uint32_t score_key(float v) {
   return (v == -INFINITY || v != v) ? 0u : f32_key(v);
@@ -193,6 +205,33 @@ __device__ __forceinline__ void for_slice(const float *vals, int64_t lo, int64_t
   }
 }
 
+// The sample's histogram of level `lvl` (0: key bits 31..21; 1: bits 20..10
+// of the keys whose top bits are b0) into tot[lvl] of every CTA: load 0 of
+// every warp of every round, 1/8 of the values (v0, when have_v0: that load
+// of a slice of one round, already in registers).  Ends at a cluster barrier.
+__device__ __forceinline__ void sample_hist(TopkClusterSmem &S, const float *vals, int64_t lo, int64_t hi,
+                                            bool have_v0, float4 v0, int lvl, uint32_t b0, uint32_t nctas) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t base = lo; base < hi; base += kRound) {
+    const int64_t i = round_index(base, 0);
+    const float4 v = have_v0 ? v0
+                     : (i < hi) ? __ldca(reinterpret_cast<const float4 *>(vals + i))
+                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t key = score_key(x[e]);
+      const uint32_t bin = !key ? (uint32_t)kBins
+                           : lvl == 0 ? (key >> 21)
+                           : (key >> 21) == b0 ? ((key >> 10) & 2047u) : (uint32_t)kBins;
+      hist_add(S.hist, bin, lane);
+    }
+  }
+  __syncthreads();
+  push_hist(S, lvl, nctas);
+  cluster_sync();
+}
+
 // Exclusive prefix sum of one value per thread over the CTA; *total gets the
 // sum.  Uses S.scan; ends with the CTA synchronised.
 __device__ __forceinline__ uint32_t block_excl_scan(TopkClusterSmem &S, uint32_t v, uint32_t *total) {
@@ -276,135 +315,108 @@ __device__ uint32_t run_levels(TopkClusterSmem &S, const TopkRows &r, const floa
   return need;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r) {
-  extern __shared__ uint8_t smem_raw[];
-  TopkClusterSmem &S = *reinterpret_cast<TopkClusterSmem *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const uint32_t crank = cluster_ctarank(), nctas = cluster_nctarank();
-  const int row = blockIdx.y;
-  const float *vals = r.vals + (int64_t)row * r.row_stride;
-  const int64_t n4 = r.row_len / 4;
-  const int64_t lo = 4 * (n4 * crank / nctas), hi = 4 * (n4 * (crank + 1) / nctas);
-
-  for (int i = tid; i < kBins; i += kThreads) {
-    S.hist[i] = 0;
-    S.tot[0][i] = 0;
-    S.tot[1][i] = 0;
+// The leader's exact top-k of its row from the candidates every CTA pushed
+// into its gather list (CTA c's block: cand_cnt[c] entries at cand_base[c],
+// in index order; the CTAs' slices are in index order too).  The blocks are
+// compacted in CTA order into
+// one list, three radix levels over local histograms (11, 11 and 10 key
+// bits) locate the full key T of the k-th largest, and the keys above T plus
+// the lowest-index keys equal to T are written ascending (list order).
+__device__ void leader_select(TopkClusterSmem &S, const TopkRows &r, int row, uint32_t nctas) {
+  const uint32_t tid = threadIdx.x;
+  uint32_t n = 0;
+#pragma unroll 1
+  for (uint32_t c = 0; c < nctas; ++c) {
+    const uint32_t m = S.cand_cnt[c], b = S.cand_base[c];
+#pragma unroll 1
+    for (uint32_t i = tid; i < m; i += kThreads) {
+      S.ckey[n + i] = S.gkey[b + i];
+      S.cidx[n + i] = S.gidx[b + i];
+    }
+    n += m;
   }
-  if (tid < kMaxCluster) {
-    S.cand_cnt[tid] = 0;
-    S.tie_cnt[tid] = 0;
-    S.sel_cnt[tid] = 0;
-  }
-  if (tid == 0) {
-    S.ccount = 0;
-    S.n_sel = 0;
-    S.n_tie = 0;
-  }
-  cluster_sync();   // every CTA's totals are cleared before anyone pushes
-
-  // 1. sample: load 0 of every warp of every round, 1/8 of the values; the
-  // histogram of level `lvl` (0: key bits 31..21; 1: bits 20..10 of the keys
-  // whose top bits are b0) goes into tot[lvl] of every CTA
-  auto sample_hist = [&](int lvl, uint32_t b0) {
-    for (int64_t base = lo; base < hi; base += kRound) {
-      const int64_t i = round_index(base, 0);
-      const float4 v = (i < hi) ? __ldca(reinterpret_cast<const float4 *>(vals + i))
-                                : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-      const float x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t key = score_key(x[e]);
-        const uint32_t bin = !key ? (uint32_t)kBins
-                             : lvl == 0 ? (key >> 21)
-                             : (key >> 21) == b0 ? ((key >> 10) & 2047u) : (uint32_t)kBins;
-        hist_add(S.hist, bin, lane);
-      }
+  __syncthreads();
+  uint32_t need = (uint32_t)r.k, prefix = 0;   // k <= n: checked by the caller
+#pragma unroll 1
+  for (int L = 0; L < 3; ++L) {
+    const int sh = L == 0 ? 21 : L == 1 ? 10 : 0, width = L == 2 ? 10 : 11;
+    const uint32_t nb = 1u << width;
+    for (int b = tid; b < kBins; b += kThreads) S.hist[b] = 0;
+    __syncthreads();
+    // warp-aggregated adds: the candidates crowd into a few top bins
+#pragma unroll 1
+    for (uint32_t b0 = 0; b0 < n; b0 += kThreads) {
+      const uint32_t i = b0 + tid;
+      const uint32_t key = i < n ? S.ckey[i] : 0u;
+      const bool m = i < n && (L == 0 || (key >> (sh + width)) == prefix);
+      hist_add(S.hist, m ? ((key >> sh) & (nb - 1)) : (uint32_t)kBins, tid & 31);
     }
     __syncthreads();
-    push_hist(S, lvl, nctas);
-    cluster_sync();
-  };
-  // about twice the sample's share of k above the low threshold, located to
-  // 22 key bits: the level-0 bin, then the level-1 bin inside it
-  const uint32_t need_s = (uint32_t)(2 * r.k / kSampleEvery) + 16;
-  sample_hist(0, 0);
-  local_threshold(S, 0, need_s, kBins);
-  uint32_t t_low = 1u;
-  if (S.thr >= 0) {
-    const uint32_t b0 = (uint32_t)S.thr, above0 = S.above;
-    sample_hist(1, b0);
-    local_threshold(S, 1, need_s - above0, kBins);
-    t_low = S.thr < 0 ? (b0 << 21) : ((b0 << 21) | ((uint32_t)S.thr << 10));
-  }
-
-  // 2. filter into the candidate list, in index order.  Within a warp the
-  // order is (load j, lane, component): the per-lane counts of the 8 loads
-  // are packed into two words of 8-bit fields (a field sums to at most 128)
-  // and prefix-summed across the warp at once; warps are in index order, and
-  // a CTA prefix sum of the warp totals places them.
-  uint32_t n_cand = 0;
-  for (int64_t base = lo; base < hi; base += kRound) {
-    float4 v[kVec];
-    load_round(vals, base, hi, v);
-    uint32_t pk[2] = {0u, 0u};
+    // bins from the top, nb / kThreads per thread: the one where the count reaches `need`
+    const int per = (int)nb / kThreads;
+    uint32_t cnt[kBinsPerThread], loc = 0;
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
-      const uint32_t c = (score_key(v[j].x) >= t_low) + (score_key(v[j].y) >= t_low) +
-                         (score_key(v[j].z) >= t_low) + (score_key(v[j].w) >= t_low);
-      pk[j >> 2] |= c << (8 * (j & 3));
-    }
-    uint32_t inc[2] = {pk[0], pk[1]};
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t n0 = __shfl_up_sync(0xffffffffu, inc[0], o), n1 = __shfl_up_sync(0xffffffffu, inc[1], o);
-      if (lane >= o) {
-        inc[0] += n0;
-        inc[1] += n1;
-      }
-    }
-    const uint32_t tw0 = __shfl_sync(0xffffffffu, inc[0], 31), tw1 = __shfl_sync(0xffffffffu, inc[1], 31);
-    uint32_t wtot = 0, jbase[kVec];   // warp-local start of load j's candidates
-#pragma unroll
-    for (int j = 0; j < kVec; ++j) {
-      jbase[j] = wtot;
-      wtot += ((j < 4 ? tw0 : tw1) >> (8 * (j & 3))) & 0xFFu;
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      cnt[j] = j < per ? S.hist[nb - 1 - (per * tid + j)] : 0u;
+      loc += cnt[j];
     }
     uint32_t tot;
-    const uint32_t wbase = n_cand + block_excl_scan(S, lane == 0 ? wtot : 0u, &tot);
-    const uint32_t wb = __shfl_sync(0xffffffffu, wbase, 0);
+    uint32_t before = block_excl_scan(S, loc, &tot);
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
-      const uint32_t ex = (((j < 4 ? inc[0] - pk[0] : inc[1] - pk[1]) >> (8 * (j & 3))) & 0xFFu);
-      uint32_t pos = wb + jbase[j] + ex;
-      const int32_t i0 = (int32_t)round_index(base, j);
-      const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const uint32_t key = score_key(x[e]);
-        if (key >= t_low) {
-          if (pos < kCand) {
-            S.ckey[pos] = key;
-            S.cidx[pos] = i0 + e;
-          }
-          ++pos;
-        }
+    for (int j = 0; j < kBinsPerThread; ++j) {
+      if (j < per && before < need && before + cnt[j] >= need) {
+        S.thr = (int)(nb - 1 - (per * tid + j));
+        S.above = before;
       }
+      before += cnt[j];
     }
-    n_cand += tot;
+    __syncthreads();
+    need -= S.above;
+    prefix = (prefix << width) | (uint32_t)S.thr;
+    __syncthreads();   // S.thr and S.above are read before the next level sets them
   }
-  if (tid == 0) S.ccount = n_cand;
-  __syncthreads();
-  if (tid < (int)nctas) dsmem_st_u32(dsmem_addr(&S.cand_cnt[crank], (uint32_t)tid), S.ccount);
-  cluster_sync();
-  uint32_t total_cand = 0;
-  bool overflow = false;
-  for (uint32_t c = 0; c < nctas; ++c) {
-    total_cand += S.cand_cnt[c];
-    overflow |= S.cand_cnt[c] > (uint32_t)kCand;
+  // prefix is T; the `need` lowest-index keys equal to T are taken
+  const uint32_t T = prefix;
+  const uint32_t per = (n + kThreads - 1) / kThreads;   // a contiguous run of the list per thread
+  const uint32_t i0 = min(tid * per, n), i1 = min(i0 + per, n);
+  uint32_t eq = 0;
+#pragma unroll 1
+  for (uint32_t i = i0; i < i1; ++i) eq += S.ckey[i] == T;
+  uint32_t tot_eq, tot_sel;
+  const uint32_t eq_before = block_excl_scan(S, eq, &tot_eq);
+  uint32_t nsel = 0, e = eq_before;
+#pragma unroll 1
+  for (uint32_t i = i0; i < i1; ++i) {
+    const uint32_t key = S.ckey[i];
+    nsel += key > T || (key == T && e < need);
+    e += key == T;
   }
+  uint32_t o = block_excl_scan(S, nsel, &tot_sel);
+  int32_t *out = r.out + (int64_t)row * r.k;
+  e = eq_before;
+#pragma unroll 1
+  for (uint32_t i = i0; i < i1; ++i) {
+    const uint32_t key = S.ckey[i];
+    const bool f = key > T || (key == T && e < need);
+    e += key == T;
+    if (!f) continue;
+    const int32_t v = S.cidx[i];
+    int32_t pos = v;
+    if (r.pool) {
+      const int32_t blk = __ldg(r.pool + (int64_t)row * r.pool_stride + v / BLOCK);
+      pos = blk * BLOCK + (v & (BLOCK - 1));
+    }
+    if (o < (uint32_t)r.k) out[o] = pos;
+    ++o;
+  }
+}
 
+// The cluster's exact selection when the leader could not take the whole
+// row (steps 3 and 4 of the outline at the top of this file).
+__device__ __forceinline__ void select_together(TopkClusterSmem &S, const TopkRows &r, const float *vals, int64_t lo,
+                                                int64_t hi, int row, uint32_t crank, uint32_t nctas,
+                                                uint32_t total_cand, bool overflow) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   // 3. exact select, on the candidate lists when they are complete
   uint32_t need, full = 0;
   const bool fast = !overflow && total_cand >= (uint32_t)r.k;
@@ -476,6 +488,148 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
     for (int i = (int)min(all, (uint32_t)r.k) + tid; i < r.k; i += kThreads) out[i] = -1;
 }
 
+__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r) {
+  extern __shared__ uint8_t smem_raw[];
+  TopkClusterSmem &S = *reinterpret_cast<TopkClusterSmem *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const uint32_t crank = cluster_ctarank(), nctas = cluster_nctarank();
+  const int row = blockIdx.y;
+  const float *vals = r.vals + (int64_t)row * r.row_stride;
+  const int64_t n4 = r.row_len / 4;
+  const int64_t lo = 4 * (n4 * crank / nctas), hi = 4 * (n4 * (crank + 1) / nctas);
+  // a slice of one round stays in registers from here: the sample and the
+  // filter read it there
+  const bool one_round = hi - lo <= kRound;
+  float4 vr[kVec];
+  if (one_round) load_round(vals, lo, hi, vr);
+
+  for (int i = tid; i < kBins; i += kThreads) {
+    S.hist[i] = 0;
+    S.tot[0][i] = 0;
+    S.tot[1][i] = 0;
+  }
+  if (tid < kMaxCluster) {
+    S.cand_cnt[tid] = 0;
+    S.tie_cnt[tid] = 0;
+    S.sel_cnt[tid] = 0;
+  }
+  if (tid == 0) {
+    S.ccount = 0;
+    S.n_sel = 0;
+    S.n_tie = 0;
+    S.g_used = 0;
+  }
+  cluster_sync();   // every CTA's totals are cleared before anyone pushes
+
+  // 1. sample: load 0 of every warp of every round, 1/8 of the values
+  // about twice the sample's share of k above the low threshold, located to
+  // 22 key bits: the level-0 bin, then the level-1 bin inside it
+  const uint32_t need_s = (uint32_t)(2 * r.k / kSampleEvery) + 16;
+  sample_hist(S, vals, lo, hi, one_round, vr[0], 0, 0u, nctas);
+  local_threshold(S, 0, need_s, kBins);
+  uint32_t t_low = 1u;
+  if (S.thr >= 0) {
+    const uint32_t b0 = (uint32_t)S.thr, above0 = S.above;
+    sample_hist(S, vals, lo, hi, one_round, vr[0], 1, b0, nctas);
+    local_threshold(S, 1, need_s - above0, kBins);
+    t_low = S.thr < 0 ? (b0 << 21) : ((b0 << 21) | ((uint32_t)S.thr << 10));
+  }
+
+  // 2. filter into the candidate list, in index order.  Within a warp the
+  // order is (load j, lane, component): the per-lane counts of the 8 loads
+  // are packed into two words of 8-bit fields (a field sums to at most 128)
+  // and prefix-summed across the warp at once; warps are in index order, and
+  // a CTA prefix sum of the warp totals places them.
+  uint32_t n_cand = 0;
+  for (int64_t base = lo; base < hi; base += kRound) {
+    float4 v[kVec];
+    if (one_round) {
+#pragma unroll
+      for (int j = 0; j < kVec; ++j) v[j] = vr[j];
+    } else {
+      load_round(vals, base, hi, v);
+    }
+    uint32_t pk[2] = {0u, 0u};
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const uint32_t c = (score_key(v[j].x) >= t_low) + (score_key(v[j].y) >= t_low) +
+                         (score_key(v[j].z) >= t_low) + (score_key(v[j].w) >= t_low);
+      pk[j >> 2] |= c << (8 * (j & 3));
+    }
+    uint32_t inc[2] = {pk[0], pk[1]};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n0 = __shfl_up_sync(0xffffffffu, inc[0], o), n1 = __shfl_up_sync(0xffffffffu, inc[1], o);
+      if (lane >= o) {
+        inc[0] += n0;
+        inc[1] += n1;
+      }
+    }
+    const uint32_t tw0 = __shfl_sync(0xffffffffu, inc[0], 31), tw1 = __shfl_sync(0xffffffffu, inc[1], 31);
+    uint32_t wtot = 0, jbase[kVec];   // warp-local start of load j's candidates
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      jbase[j] = wtot;
+      wtot += ((j < 4 ? tw0 : tw1) >> (8 * (j & 3))) & 0xFFu;
+    }
+    uint32_t tot;
+    const uint32_t wbase = n_cand + block_excl_scan(S, lane == 0 ? wtot : 0u, &tot);
+    const uint32_t wb = __shfl_sync(0xffffffffu, wbase, 0);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const uint32_t ex = (((j < 4 ? inc[0] - pk[0] : inc[1] - pk[1]) >> (8 * (j & 3))) & 0xFFu);
+      uint32_t pos = wb + jbase[j] + ex;
+      const int32_t i0 = (int32_t)round_index(base, j);
+      const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t key = score_key(x[e]);
+        if (key >= t_low) {
+          if (pos < kCand) {
+            S.ckey[pos] = key;
+            S.cidx[pos] = i0 + e;
+          }
+          ++pos;
+        }
+      }
+    }
+    n_cand += tot;
+  }
+  if (tid == 0) S.ccount = n_cand;
+  __syncthreads();
+  // every CTA copies its candidates into a block of the leader's (rank 0)
+  // list, reserved by a remote atomic add; the blocks' places go to every CTA
+  const uint32_t mine_c = min(n_cand, (uint32_t)kCand);
+  if (tid == 0) S.g_base = dsmem_atom_add(dsmem_addr(&S.g_used, 0u), mine_c);
+  __syncthreads();
+  const uint32_t gb = S.g_base;
+  if (gb + mine_c <= (uint32_t)kGather)
+    for (uint32_t i = tid; i < mine_c; i += kThreads) {
+      dsmem_st_u32(dsmem_addr(&S.gkey[gb + i], 0u), S.ckey[i]);
+      dsmem_st_u32(dsmem_addr(&S.gidx[gb + i], 0u), (uint32_t)S.cidx[i]);
+    }
+  if (tid < (int)nctas) {
+    dsmem_st_u32(dsmem_addr(&S.cand_cnt[crank], (uint32_t)tid), S.ccount);
+    dsmem_st_u32(dsmem_addr(&S.cand_base[crank], (uint32_t)tid), gb);
+  }
+  cluster_sync();
+  uint32_t total_cand = 0;
+  bool overflow = false;
+  for (uint32_t c = 0; c < nctas; ++c) {
+    total_cand += S.cand_cnt[c];
+    overflow |= S.cand_cnt[c] > (uint32_t)kCand;
+  }
+  if (!overflow && total_cand >= (uint32_t)r.k && total_cand <= (uint32_t)kGather) {
+    // every candidate is in the leader, which selects alone; the other CTAs
+    // are done (nothing reads their memory any more)
+    if (crank == 0) leader_select(S, r, row, nctas);
+    return;
+  }
+
+  select_together(S, r, vals, lo, hi, row, crank, nctas, total_cand, overflow);
+}
+
 }  // namespace
 
 bool topk_cluster_supported(const TopkRows &r) {
@@ -507,7 +661,7 @@ cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *lau
   if (err != cudaSuccess) return err;
   int64_t c = (r.row_len + 8191) / 8192;
   if (c > max_cluster) c = max_cluster;
-  const int64_t fill = 3 * (int64_t)sms / r.rows;
+  const int64_t fill = 3 * (int64_t)sms / r.rows;   // three CTAs fit on an SM
   if (c > fill) c = fill;
   if (c < 1) c = 1;
   cudaLaunchConfig_t cfg = {};
