@@ -1,6 +1,7 @@
 """Builds libcsa2.so in-tree for sm_103a with nvcc (no cmake, no torch
 extension machinery): every .cu under csrc/ is compiled in parallel with
-relocatable device code, then device-linked into one shared library."""
+relocatable device code (except the units in WHOLE_PROGRAM), then
+device-linked into one shared library."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -17,6 +18,11 @@ LIB = os.path.join(BUILD, "libcsa2.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-rdc=true", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          f"-I{INCLUDE}", f"-I{CSRC}"]
+
+
+# units compiled as whole-program device code: ptxas ignores setmaxnreg under
+# separate compilation, and these kernels split their registers between roles
+WHOLE_PROGRAM = {"attention.cu"}
 
 
 def _nvcc():
@@ -46,7 +52,10 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
+        flags = FLAGS
+        if os.path.basename(src) in WHOLE_PROGRAM:
+            flags = [f for f in FLAGS if f != "-rdc=true"]
+        cmd = [nvcc, *ARCH, *flags, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")

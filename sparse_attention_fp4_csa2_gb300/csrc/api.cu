@@ -355,9 +355,11 @@ size_t csa2_workspace_bytes(csa2_op op, int32_t batch, int64_t n_max, const csa2
 
 csa2_status csa2_get_device_status(csa2_stream_t stream, uint32_t *bits) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return CSA2_ERR_CUDA;
-  unsigned int v = 0, zero = 0;
+  unsigned int v = 0, zero = 0, va = 0;
   if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(v)) != cudaSuccess) return CSA2_ERR_CUDA;
   if (v && cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero)) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (attn_take_error(&va) != cudaSuccess) return CSA2_ERR_CUDA;   // the readout's own word
+  v |= va;
   if (bits) *bits = v;
   return v ? CSA2_ERR_DEVICE : CSA2_OK;
 }

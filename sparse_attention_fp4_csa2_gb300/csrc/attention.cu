@@ -42,6 +42,10 @@
 // CSA2_DEV_ERR_TIMEOUT and falls through every later wait, so that all
 // threads still meet at the same named and cluster barriers and the CTA
 // exits; its output is then undefined.
+// This unit is compiled without relocatable device code, so that ptxas
+// allots each warp role the registers its setmaxnreg asks for (with
+// separate compilation it ignores setmaxnreg); it keeps its own error word.
+#define CSA2_WHOLE_PROGRAM_TU 1
 #include "kernels.cuh"
 
 namespace csa2 {
@@ -252,7 +256,7 @@ __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
 }
 
 // Bounded wait that falls through once any role has given up.
-__device__ __noinline__ void wait_ft(Ctl &S, uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ void wait_ft(Ctl &S, uint64_t *bar, uint32_t parity) {
   if (S.abort) return;
   if (!mbar_wait(bar, parity)) S.abort = 1;
 }
@@ -849,6 +853,14 @@ int choose_chunks(int problems, int K, int W, int kernel, int sms) {
 }
 
 }  // namespace
+
+cudaError_t attn_take_error(unsigned int *bits) {
+  unsigned int v = 0, zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_dev_error, sizeof(v));
+  if (e == cudaSuccess && v) e = cudaMemcpyToSymbol(g_dev_error, &zero, sizeof(zero));
+  *bits = v;
+  return e;
+}
 
 size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W, int32_t kernel) {
   (void)problems;

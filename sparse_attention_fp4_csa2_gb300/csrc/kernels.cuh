@@ -173,6 +173,9 @@ struct AttnArgs {
 
 // Workspace of one readout launch (the chunk partials when tokens are split).
 size_t attn_scratch_bytes(int32_t problems, int32_t K, int32_t W, int32_t kernel);
+// Reads and clears the readout's own device error word (that unit is
+// compiled as whole-program device code).
+cudaError_t attn_take_error(unsigned int *bits);
 cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, int *launches);
 
 }  // namespace csa2

@@ -13,8 +13,14 @@
 namespace csa2 {
 
 // Per-device error word (CSA2_DEV_ERR_* bits); read and cleared by
-// csa2_get_device_status.
+// csa2_get_device_status.  A translation unit compiled as whole-program
+// device code (no -rdc: its kernels then honour setmaxnreg) keeps a word of
+// its own, which the same call reads through that unit's host accessor.
+#ifdef CSA2_WHOLE_PROGRAM_TU
+static __device__ unsigned int g_dev_error = 0;
+#else
 extern __device__ unsigned int g_dev_error;
+#endif
 
 __device__ __forceinline__ void set_error(unsigned int bits) { atomicOr(&g_dev_error, bits); }
 
