@@ -105,7 +105,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
     ap.add_argument("--attn-kernel", type=int, default=0, choices=[0, 1, 2],
-                    help="readout kernel: 0 automatic, 1 chunk-parallel, 2 streaming")
+                    help="readout work split: 0 automatic, 1 keys split over a cluster, 2 one CTA per token")
     ap.add_argument("--indexer-fp4", action="store_true",
                     help="MXFP4 indexer K cache and query (decode workloads)")
     ap.add_argument("--project-ik", action="store_true",

@@ -85,10 +85,11 @@ typedef struct {
   int32_t candidate_topk_blocks; /* HSI pool blocks, 16..8192, multiple of 16; 2048 */
   int32_t block_reduce;          /* 0 = max over the block (pages), 1 = sum      */
   int32_t hsi;                   /* FULL: also build the candidate pool (1/0)    */
-  int32_t attn_kernel;           /* readout kernel: 0 automatic, 1 chunk-parallel
-                                    (a token's chunks on a cluster of CTAs),
-                                    2 streaming (a CTA pipelines a token's chunks);
-                                    the result is the same up to rounding      */
+  int32_t attn_kernel;           /* readout work split: 0 automatic, 1 a token's
+                                    keys split over a cluster of CTAs (at
+                                    least 2 chunks), 2 one CTA per token (its
+                                    keys in blocks of 128); the result is the
+                                    same up to rounding                        */
   int32_t indexer_fp4;           /* 0: indexer K cache bf16 [.][128]; 1: MXFP4
                                     (csa2_indexer_k_quant) and the indexer
                                     query quantised to MXFP4 as well ([A] 2.4.4:

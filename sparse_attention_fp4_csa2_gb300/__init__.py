@@ -35,7 +35,7 @@ class Csa2Error(RuntimeError):
 class Params(ctypes.Structure):
     """csa2_params: index_topk, sliding_window, candidate_block_size,
     candidate_topk_blocks, block_reduce (0 max, 1 sum), hsi, attn_kernel (0
-    automatic, 1 chunk-parallel, 2 streaming), indexer_fp4 (0 bf16 indexer K
+    automatic, 1 keys split over a cluster, 2 one CTA per token), indexer_fp4 (0 bf16 indexer K
     cache, 1 MXFP4 planes written by ``indexer_k_quant``)."""
     _fields_ = [("index_topk", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
                 ("candidate_block_size", ctypes.c_int32), ("candidate_topk_blocks", ctypes.c_int32),

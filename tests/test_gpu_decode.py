@@ -225,7 +225,7 @@ def _kv_cache(c2, lat):
     (1, 256, 200, [200], [256]),               # two SWA chunks
     (2, 1024, 128, [128, 5], [1024, 700]),     # 9 chunks: merged by the separate combine kernel
 ])
-@pytest.mark.parametrize("ak", [1, 2])            # chunk-parallel, streaming
+@pytest.mark.parametrize("ak", [1, 2])            # keys split over a cluster, one CTA per token
 def test_sparse_attn_reuse(c2, orc, B, K, W, swa_len, n_valid, ak):
     cap = 3000
     lat, li, idx, sl = _attn_inputs(41 + K, B, cap, K, W, swa_len, n_valid)
