@@ -502,7 +502,14 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
   // filter read it there
   const bool one_round = hi - lo <= kRound;
   float4 vr[kVec];
-  if (one_round) load_round(vals, lo, hi, vr);
+  if (one_round) {
+    load_round(vals, lo, hi, vr);
+  } else if (tid == 0) {
+    // a longer slice is read three times (two sample levels, the filter):
+    // bring all of it into L2 now, one round (32 KB) per bulk prefetch
+    for (int64_t b = lo; b < hi; b += kRound)
+      prefetch_l2_bulk(vals + b, (uint32_t)(4 * (hi - b < kRound ? hi - b : kRound)));
+  }
 
   for (int i = tid; i < kBins; i += kThreads) {
     S.hist[i] = 0;
