@@ -840,14 +840,45 @@ int device_sms() {
   return n;
 }
 
-// Chunks per token: the most (1, 2, 4 or 8) whose clusters all fit on the
-// GPU at once, keeping at least 16 keys per chunk; 1 once the tokens fill the SMs.
+// Clusters of `c` CTAs of the readout that can be resident at once (a
+// cluster lives inside one GPC; one CTA per SM), from the occupancy query;
+// the SM count over c when the query fails.  Cached per cluster size.
+int max_active_clusters(int c, int sms) {
+  static int cache[9] = {};
+  if (c < 1 || c > 8) return 0;
+  if (cache[c]) return cache[c];
+  int n = 0;
+  auto kern = sparse_attn_kernel<true>;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)c, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)c;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = sms / c;
+  }
+  cache[c] = n;
+  return n;
+}
+
+// Chunks per token: the most (1, 2, 4 or 8) whose clusters can all be
+// resident at once (a second wave of clusters would double the launch),
+// keeping at least 16 keys per chunk; 1 once the tokens fill the SMs.
 // kernel 1 forces a split (C >= 2), kernel 2 a single chunk.
 int choose_chunks(int problems, int K, int W, int kernel, int sms) {
   if (kernel == 2) return 1;
   int c = 1;
   for (int cand : {2, 4, 8})
-    if ((int64_t)problems * cand <= sms && (K + W) / cand >= 16) c = cand;
+    if ((int64_t)problems * cand <= sms && problems <= max_active_clusters(cand, sms) && (K + W) / cand >= 16)
+      c = cand;
   if (kernel == 1 && c == 1) c = (K + W) >= 32 ? 2 : 1;
   return c;
 }
