@@ -731,70 +731,94 @@ __global__ void __launch_bounds__(kThreads, 1)
           x[i] = ok ? __uint_as_float(u[i]) * (kLogit * rsv[i]) : -INFINITY;
         }
       };
-      float mx = -INFINITY;
+      // P = 2^(logit - m_ref) (x the SWA row scale) into P^T; the row sum
+      // gathers the unscaled exponents.  `over` flags a logit above
+      // m_ref + kLazy (the one-pass attempt below).
+      auto write_p = [&](float mref_s) {
+        bool over = false;
 #pragma unroll 1
-      for (int mi = 0; mi < kPairs; ++mi) {
-        float x[16];
-        logits(mi, x);
+        for (int mi = 0; mi < kPairs; ++mi) {
+          float x[16];
+          logits(mi, x);
+          const int k0 = 16 * (2 * (2 * mi + wh) + th);
+          uint32_t pk[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) mx = fmaxf(mx, x[i]);
-      }
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      if (th == 0) red[wh][h] = mx;
-      bar_named(1, kWorkers);
-      const float mc = fmaxf(red[0][h], red[1][h]);
-      float f = 1.0f;
-      if (m_ref == -INFINITY) {
-        m_ref = mc;   // nothing accumulated yet
-      } else if (mc > m_ref + kLazy) {
-        f = exp2f(m_ref - mc);
-        m_ref = mc;
-      }
-      if (th == 0 && wh == 0) S.fac[h] = f;
-      const bool any = bar_named_or(2, kWorkers, f != 1.0f);
-      if (any) {
-        // O^T holds every earlier block (the dequant above waited for the
-        // previous block's products): scale its head columns
-        tc_fence_after();
-#pragma unroll 1
-        for (int mm = 0; mm < 2; ++mm) {
-          const int mt = 2 * wh + mm;
-#pragma unroll 1
-          for (int hb = 0; hb < 2; ++hb) {
-            uint32_t v[32];
-            const uint32_t ta = s_row + kColO + (uint32_t)(mt * H + hb * 32);
-            tmem_ld32(ta, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * S.fac[hb * 32 + i]);
-            tmem_st32(ta, v);
+          for (int i = 0; i < 16; i += 2) {
+            // masked keys hold -inf: 2^-inf = 0 (no branch); m_ref = -inf only when all are masked
+            over |= (x[i] > mref_s + kLazy) | (x[i + 1] > mref_s + kLazy);
+            const float p0 = ex2_approx(x[i] - mref_s), p1 = ex2_approx(x[i + 1] - mref_s);
+            l_part += p0 + p1;
+            const float2 r2 = *reinterpret_cast<const float2 *>(S.rs + k0 + i);
+            pk[i >> 1] = pack_half2(p0 * r2.x, p1 * r2.y);
+          }
+          if (k0 < a.Bk) {
+            // P^T K-major: [64-key atom column][64 heads][128 B]
+            uint8_t *prow = pbuf + (k0 >> 6) * kAtom + h * 128;
+            const int c0 = (k0 & 63) >> 3;
+            *reinterpret_cast<uint4 *>(prow + ((c0 ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            *reinterpret_cast<uint4 *>(prow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
-        tmem_st_wait();
+        return over;
+      };
+      // After an item's first block the reference max is rarely raised: one
+      // pass writes P with the current reference, and only if some logit is
+      // above it by more than 2^kLazy (any thread) is the block redone by the
+      // two passes below (max, then exponents).  Whether a reference exists
+      // is the same for every head (it depends on which keys were valid).
+      bool done_p = false;
+      if constexpr (!kSingle) {
+        if (m_ref != -INFINITY) {
+          const float l_save = l_part;
+          const bool over = write_p(m_ref);
+          done_p = !bar_named_or(2, kWorkers, over);
+          if (!done_p) l_part = l_save;
+        }
       }
-      l_part *= f;
-      const float mref_s = m_ref == -INFINITY ? 0.0f : m_ref;
+      if (!done_p) {
+        float mx = -INFINITY;
 #pragma unroll 1
-      for (int mi = 0; mi < kPairs; ++mi) {
-        float x[16];
-        logits(mi, x);
-        const int k0 = 16 * (2 * (2 * mi + wh) + th);
-        uint32_t pk[8];
+        for (int mi = 0; mi < kPairs; ++mi) {
+          float x[16];
+          logits(mi, x);
 #pragma unroll
-        for (int i = 0; i < 16; i += 2) {
-          // masked keys hold -inf: 2^-inf = 0 (no branch); m_ref = -inf only when all are masked
-          const float p0 = ex2_approx(x[i] - mref_s), p1 = ex2_approx(x[i + 1] - mref_s);
-          l_part += p0 + p1;
-          const float2 r2 = *reinterpret_cast<const float2 *>(S.rs + k0 + i);
-          pk[i >> 1] = pack_half2(p0 * r2.x, p1 * r2.y);
+          for (int i = 0; i < 16; ++i) mx = fmaxf(mx, x[i]);
         }
-        if (k0 < a.Bk) {
-          // P^T K-major: [64-key atom column][64 heads][128 B]
-          uint8_t *prow = pbuf + (k0 >> 6) * kAtom + h * 128;
-          const int c0 = (k0 & 63) >> 3;
-          *reinterpret_cast<uint4 *>(prow + ((c0 ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-          *reinterpret_cast<uint4 *>(prow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (th == 0) red[wh][h] = mx;
+        bar_named(1, kWorkers);
+        const float mc = fmaxf(red[0][h], red[1][h]);
+        float f = 1.0f;
+        if (m_ref == -INFINITY) {
+          m_ref = mc;   // nothing accumulated yet
+        } else if (mc > m_ref + kLazy) {
+          f = exp2f(m_ref - mc);
+          m_ref = mc;
         }
+        if (th == 0 && wh == 0) S.fac[h] = f;
+        const bool any = bar_named_or(2, kWorkers, f != 1.0f);
+        if (any) {
+          // O^T holds every earlier block (the dequant above waited for the
+          // previous block's products): scale its head columns
+          tc_fence_after();
+#pragma unroll 1
+          for (int mm = 0; mm < 2; ++mm) {
+            const int mt = 2 * wh + mm;
+#pragma unroll 1
+            for (int hb = 0; hb < 2; ++hb) {
+              uint32_t v[32];
+              const uint32_t ta = s_row + kColO + (uint32_t)(mt * H + hb * 32);
+              tmem_ld32(ta, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * S.fac[hb * 32 + i]);
+              tmem_st32(ta, v);
+            }
+          }
+          tmem_st_wait();
+        }
+        l_part *= f;
+        (void)write_p(m_ref == -INFINITY ? 0.0f : m_ref);
       }
       fence_proxy_async_smem();
       tc_fence_before();
