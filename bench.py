@@ -43,6 +43,8 @@ SWEEP_FIXED = 32 * 128 * 2 + 32 * 4        # q_idx + w per sequence
 # since its capture has no entry and reports null.
 TRAFFIC = {
     ("indexer_sweep_kernel", "group_decode_32x64k"): 537181184 + 6408192,
+    ("sparse_attn_kernel", "group_decode_32x64k"): 10639872,      # the output stays in L2 during the capture
+    ("topk_cluster_kernel", "group_decode_32x64k"): 8454400,
     # captured at 16 sequences, scaled by the rows read to the 32-sequence launch
     ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411200 + 915968),
 }
@@ -104,6 +106,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (profiling runs)")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="override a prefill workload's chunk tokens (profiling runs; a multiple of 1024)")
     ap.add_argument("--attn-kernel", type=int, default=0, choices=[0, 1, 2],
                     help="readout work split: 0 automatic, 1 keys split over a cluster, 2 one CTA per token")
     ap.add_argument("--indexer-fp4", action="store_true",
@@ -701,6 +705,11 @@ def run_ours(args, rank, world, local_rank):
     if args.batch:
         import dataclasses
         cfg = dataclasses.replace(cfg, batch=args.batch, name=f"{cfg.name}[batch={args.batch}]")
+    if args.chunk:
+        import dataclasses
+        if not cfg.chunk or args.chunk % 1024:
+            raise SystemExit("--chunk: prefill workloads only, a multiple of 1024")
+        cfg = dataclasses.replace(cfg, chunk=args.chunk, name=f"{cfg.name}[chunk={args.chunk}]")
     if cfg.chunk and (INDEXER_FP4 or PROJECT_IK):
         raise SystemExit("--indexer-fp4 / --project-ik: decode workloads only")
     res = measure(args, cfg, dev, rank, world, local_rank, args.steps)
@@ -709,7 +718,7 @@ def run_ours(args, rank, world, local_rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic"}
     line.update(res)
-    plain = not (args.batch or INDEXER_FP4 or PROJECT_IK or ATTN_KERNEL)
+    plain = not (args.batch or args.chunk or INDEXER_FP4 or PROJECT_IK or ATTN_KERNEL)
     if args.config == DEFAULT_CONFIG and plain:
         # the metric's other context: the 20-layer step at 1M tokens, same
         # timing rules, reported beside the 64K line
