@@ -279,6 +279,39 @@ def test_sparse_attn_mixed_layout(c2, orc, K, W, ak):
         check_lse(lse[b].cpu().numpy(), l)
 
 
+def test_sparse_attn_more_tokens_than_sms(c2, orc):
+    """More tokens than SMs: one chunk per token, keys in blocks of 64 through
+    two tiles, CTAs walking several tokens (item boundaries inside a CTA).
+    Ragged top-K fills and SWA lengths, tokens with no key at all, every token
+    checked."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, cap, K, W = sms + 8, 1024, 512, 128
+    rng = np.random.default_rng(7)
+    swa_len = [int(x) for x in rng.integers(0, W + 1, B)]
+    n_valid = [int(x) for x in rng.integers(0, K + 1, B)]
+    swa_len[0], n_valid[0] = W, K
+    swa_len[1], n_valid[1] = 0, 0
+    swa_len[sms], n_valid[sms] = 3, 70          # the second item of CTA 0
+    lat, li, idx, sl = _attn_inputs(131, B, cap, K, W, swa_len, n_valid)
+    p = _params(c2, index_topk=K, sliding_window=W)
+    ws = c2.workspace(c2.OP_ATTN, B, cap, p)
+    kv = _kv_cache(c2, lat)
+    out = torch.empty(B, 64, 512, dtype=torch.float32, device="cuda")
+    lse = torch.empty(B, 64, dtype=torch.float32, device="cuda")
+    swa = li.swa[:, :W].contiguous()
+    sc = li.swa_scale[:, :W].contiguous()
+    c2.sparse_attn(p, li.q.cuda(), kv, idx.cuda(), swa.cuda(), sc.cuda(), sl.cuda(), out, ws, lse=lse)
+    assert c2.get_device_status() == 0
+    kvh = orc.kv_entries(lat.reshape(-1, 512), None, 1, np.tile(np.arange(cap), B)).reshape(B, cap, 288)
+    for b in range(B):
+        o, l = orc.sparse_attn(li.q[b], kvh[b], idx[b].numpy(), swa[b], sc[b], int(sl[b]))
+        if swa_len[b] == 0 and n_valid[b] == 0:
+            assert torch.all(out[b] == 0) and torch.all(torch.isneginf(lse[b]))
+            continue
+        check_attn(out[b].cpu().numpy(), o)
+        check_lse(lse[b].cpu().numpy(), l)
+
+
 @pytest.mark.parametrize("ak", [1, 2])
 def test_sparse_attn_no_keys(c2, ak):
     B, cap, K = 1, 64, 128
