@@ -93,9 +93,17 @@ __device__ __forceinline__ uint32_t level_digit(uint32_t key, int level) {
   return level == 0 ? (key >> 21) : level == 1 ? ((key >> 10) & 2047u) : (key & 1023u);
 }
 
+// Histogram add of the warp's 32 bins (kBins: none), aggregated over equal
+// bins -- for keys that crowd into a few bins (the top 11 key bits).
 __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, int lane) {
   const uint32_t peers = __match_any_sync(0xffffffffu, bin);
   if (bin < kBins && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+}
+
+// The same without aggregation -- for the finer levels, where a warp's bins
+// are mostly distinct and the match costs more than it saves.
+__device__ __forceinline__ void hist_add_plain(uint32_t *h, uint32_t bin) {
+  if (bin < kBins) atomicAdd(&h[bin], 1u);
 }
 
 // Appends the flagged indices of this warp to the CTA's selection list.
@@ -224,7 +232,10 @@ __device__ __forceinline__ void sample_hist(TopkClusterSmem &S, const float *val
       const uint32_t bin = !key ? (uint32_t)kBins
                            : lvl == 0 ? (key >> 21)
                            : (key >> 21) == b0 ? ((key >> 10) & 2047u) : (uint32_t)kBins;
-      hist_add(S.hist, bin, lane);
+      if (lvl == 0)
+        hist_add(S.hist, bin, lane);
+      else
+        hist_add_plain(S.hist, bin);
     }
   }
   __syncthreads();
@@ -343,13 +354,18 @@ __device__ void leader_select(TopkClusterSmem &S, const TopkRows &r, int row, ui
     const uint32_t nb = 1u << width;
     for (int b = tid; b < kBins; b += kThreads) S.hist[b] = 0;
     __syncthreads();
-    // warp-aggregated adds: the candidates crowd into a few top bins
+    // level 0: warp-aggregated adds (the candidates crowd into a few top
+    // bins); below it the bins are mostly distinct
 #pragma unroll 1
     for (uint32_t b0 = 0; b0 < n; b0 += kThreads) {
       const uint32_t i = b0 + tid;
       const uint32_t key = i < n ? S.ckey[i] : 0u;
       const bool m = i < n && (L == 0 || (key >> (sh + width)) == prefix);
-      hist_add(S.hist, m ? ((key >> sh) & (nb - 1)) : (uint32_t)kBins, tid & 31);
+      const uint32_t bin = m ? ((key >> sh) & (nb - 1)) : (uint32_t)kBins;
+      if (L == 0)
+        hist_add(S.hist, bin, tid & 31);
+      else
+        hist_add_plain(S.hist, bin);
     }
     __syncthreads();
     // bins from the top, nb / kThreads per thread: the one where the count reaches `need`
