@@ -280,8 +280,11 @@ class Workload:
         self.topk = torch.zeros(B, 512, dtype=torch.int32, device=device)
         self.topk_none = torch.full((B, 512), -1, dtype=torch.int32, device=device)   # SWA-only layers
         self.pool = torch.zeros(B, 2048, dtype=torch.int32, device=device)
-        self.out = torch.empty(len(cfg.schedule), B, 64, 512, device=device)
-        self.lse = torch.empty(len(cfg.schedule), B, 64, device=device)
+        # per layer its output then its log-sum-exp, adjacent: one read-back per layer
+        L, n_o = len(cfg.schedule), B * 64 * 512
+        self.out_arena = torch.empty(L, n_o + B * 64, device=device)
+        self.out = self.out_arena[:, :n_o].view(L, B, 64, 512)
+        self.lse = self.out_arena[:, n_o:].view(L, B, 64)
         self.ws = c2.workspace(c2.OP_DECODE, B, E, self.params, device=device)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -404,7 +407,7 @@ class Workload:
             if m in ("full", "reindex"):
                 g += [li.q_idx, li.w]
             ins.append(g)
-            outs.append([self.out[i], self.lse[i]])
+            outs.append([self.out_arena[i]])
         return ins, outs
 
 
@@ -449,9 +452,12 @@ class PrefillWorkload:
         self.swa_first = max(self.first_pos - W + 1, 0)
         rows = self.first_pos + T - self.swa_first
         self.swa, self.swa_scale = synth.fp8_rows(synth.normal((B, rows, 512), seed, 5, device, dtype=torch.float32))
-        self.topk = torch.empty(B, T, 512, dtype=torch.int32, device=device)
-        self.out = torch.empty(B, T, 64, 512, device=device)
-        self.lse = torch.empty(B, T, 64, device=device)
+        # the step's results side by side (output, log-sum-exp, top-K): one read-back
+        n_o, n_l = B * T * 64 * 512, B * T * 64
+        self.out_arena = torch.empty(n_o + n_l + B * T * 512, device=device)
+        self.out = self.out_arena[:n_o].view(B, T, 64, 512)
+        self.lse = self.out_arena[n_o:n_o + n_l].view(B, T, 64)
+        self.topk = self.out_arena[n_o + n_l:].view(torch.int32).view(B, T, 512)
         self.ws = c2.workspace(c2.OP_PREFILL, B, self.E, self.params, device=device)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
@@ -516,7 +522,7 @@ class PrefillWorkload:
 
     def io_groups(self):
         return ([[self.new_lat, self.new_z, self.q, self.q_idx, self.w, self.swa, self.swa_scale]],
-                [[self.out, self.lse, self.topk]])
+                [[self.out_arena]])
 
 
 DEFAULT_CONFIG = "group_decode_32x64k"   # the 64K workload the metric is quoted on
@@ -730,16 +736,24 @@ def run_ours(args, rank, world, local_rank):
 
 
 class HostIO:
-    """End-to-end copies of a step, captured with it: group i's inputs go
-    pinned host -> device on a copy stream (all groups issued up front, in
-    order) and layer i waits only for its own; layer i's outputs go device ->
-    pinned host on a second stream as soon as it is done.  The step's graph
-    joins both streams, so a replay covers every copy."""
+    """End-to-end copies of a step, captured with it: group i's inputs (one
+    contiguous block per group) go pinned host -> device on a copy stream (all
+    groups issued up front, in order) and layer i waits only for its own;
+    layer i's outputs go device -> pinned host on a second stream as soon as
+    it is done.  The step's graph joins both streams, so a replay covers every
+    copy.  Creating it re-points the input tensors into the blocks: graphs
+    captured before it are not replayed afterwards."""
 
     def __init__(self, ins, outs, device):
         import torch
         self.torch = torch
-        self.ins = [[(t.cpu().pin_memory(), t) for t in g] for g in ins]
+        # every group's inputs are moved into one contiguous device block (the
+        # tensors keep their identity and now view it), so that a group is
+        # one copy from one pinned host block
+        ptrs = [t.data_ptr() for g in ins for t in g]
+        assert len(set(ptrs)) == len(ptrs), "a tensor is supplied by two groups"
+        packed = [self._pack(g, device) for g in ins]
+        self.ins = [[(a.cpu().pin_memory(), a)] for a in packed]
         self.outs = [[(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for t in g] for g in outs]
         self.cin = torch.cuda.Stream(device=device)
         self.cout = torch.cuda.Stream(device=device)
@@ -747,6 +761,19 @@ class HostIO:
         self.ev_done = [torch.cuda.Event() for _ in self.outs]
         self.h2d = sum(h.numel() * h.element_size() for g in self.ins for h, _ in g)
         self.d2h = sum(h.numel() * h.element_size() for g in self.outs for h, _ in g)
+
+    def _pack(self, group, device):
+        torch = self.torch
+        sizes = [(t, (t.numel() * t.element_size() + 255) // 256 * 256) for t in group]
+        arena = torch.empty(sum(sz for _, sz in sizes), dtype=torch.uint8, device=device)
+        off = 0
+        for t, sz in sizes:
+            assert t.is_contiguous() and t.device == arena.device
+            nb = t.numel() * t.element_size()
+            arena[off:off + nb].copy_(t.reshape(-1).view(torch.uint8))
+            t.set_(arena.untyped_storage(), off // t.element_size(), t.shape, t.stride())
+            off += sz
+        return arena
 
     def start(self):
         main = self.torch.cuda.current_stream()
