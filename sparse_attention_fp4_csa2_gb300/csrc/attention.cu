@@ -14,8 +14,9 @@
 // to fill the SMs -- one of C <= 8 chunks of them (a chunk takes an equal
 // share of the top-K list and of the SWA rows).  With C = 1 the CTAs are
 // persistent and walk the items; with C > 1 the C chunks of a token are the
-// CTAs of one thread-block cluster and merge their partial results through L2
-// after a cluster barrier.
+// CTAs of one thread-block cluster: each loads a share of the token's Q for
+// all of them (TMA multicast), and they merge their partial results through
+// distributed shared memory.
 //
 // Inside a CTA an item's keys go through in blocks of up to 128 (a single
 // block of up to 160 when every CTA holds one item).  Per block:
@@ -33,8 +34,9 @@
 //   O^T      += V^T P^T: M = 128 dims (four blocks) x N = 64 heads x K = rows,
 //             V^T read MN-major from the same tile; each 128-dim block's
 //             commit frees its column pair for the next block's dequant.
-// Every MMA issue sequence is unrolled with descriptors advanced by
-// constants.  At an item's end the workers normalise O^T and write the output
+// The MMA issue sequences are runtime loops with descriptors advanced by
+// constants (small code: a CTA runs it once, with a cold instruction
+// cache).  At an item's end the workers normalise O^T and write the output
 // (C = 1) or the partial (C > 1) while the next item's first block is
 // already multiplying.
 //
@@ -99,7 +101,7 @@ constexpr size_t kSmemBytes = 1024 + (size_t)kTileRegion + kQBytes + sizeof(Ctl)
 static_assert(kSmemBytes <= 232448, "attention exceeds the shared-memory limit");
 static_assert(kRedOffMulti + 2 * H * 4 <= kTileRegion, "multi-block reductions overflow the tile region");
 static_assert(kCombineStage + D * 128 <= kTileRegion, "cluster combine overflows the tile region");
-static_assert(kRedOffSingle >= (kMaxBk / 64 + 1) * kAtom && kRedOffSingle + 2 * H * 4 <= kQBytes,
+static_assert(kRedOffSingle >= (kMaxBk / 64 + 1) * kAtom && kRedOffSingle + 4 * H * 4 <= kQBytes,
               "single-block P^T overlaps the reductions");
 
 // One item: a token and its chunk of keys.  Item key e < nW is SWA row
@@ -155,7 +157,6 @@ struct RowBufN {
   int kind;   // 0 none, 1 FP4 entry, 2 SWA row
 };
 using RowBuf = RowBufN<16>;    // an entry or a SWA row
-using EntryBuf = RowBufN<9>;   // an entry only
 
 // Top-K slot of item key e, or -1 (also for SWA rows).
 __device__ __forceinline__ int32_t row_slot(const AttnArgs &a, const Item &it, int e) {
@@ -305,14 +306,15 @@ __device__ __forceinline__ void item_epilogue(const AttnArgs &a, Ctl &S, int ite
 // tile region, its row-normalised O for every other owner's dims (fp16,
 // 128-byte rows [dim][64 heads], 16-byte chunks XOR-swizzled by the row) and
 // its per-head reference max and row sum.  Once every CTA's products are done
-// (a cluster barrier: the tile regions are free), one thread sends each
-// owner its rows and the max / sum by bulk shared-to-shared copies that
-// complete on the owner's `comb` barrier.  Each owner then combines the C
-// partials with the weights l_c 2^(m_c - M) / L -- one softmax over the union
-// of the chunks' keys -- and writes its dims; rank 0 also writes the
-// log-sum-exp.  A second cluster barrier, arrived once a CTA has received
-// everything and awaited at its end, keeps every CTA resident until the
-// copies out of it are complete.
+// (a cluster barrier: the tile regions are free), thread c sends owner c its
+// rows and the max / sum by bulk shared-to-shared copies that complete on the
+// owner's `comb` barrier (the copies to the C - 1 owners go out in
+// parallel).  Each owner then combines the C partials with the weights
+// l_c 2^(m_c - M) / L -- one softmax over the union of the chunks' keys --
+// and writes its dims; rank 0 also writes the log-sum-exp.  A second cluster
+// barrier, arrived once a CTA has received everything and awaited at its
+// end, keeps every CTA resident until the copies out of it are complete
+// (residency only: its arrive orders nothing).
 __device__ __forceinline__ void cluster_combine(const AttnArgs &a, Ctl &S, uint8_t *tile, uint32_t tmem, int item,
                                                 int tid, int warp, int lane) {
   const int C = a.C;
@@ -361,33 +363,33 @@ __device__ __forceinline__ void cluster_combine(const AttnArgs &a, Ctl &S, uint8
   __syncwarp();
   cluster_arrive();
   cluster_wait();   // every CTA's products are done and its rows staged
-  if (tid == 0) {
-#pragma unroll 1
-    for (int c = 0; c < C; ++c) {
-      if (c == (int)rank) continue;
-      const uint32_t bar = dsmem_addr(&S.comb, (uint32_t)c);
-      bulk_s2s_cluster(dsmem_addr(parts + rank * slot, (uint32_t)c), stage + c * slot, slot, bar);
-      bulk_s2s_cluster(dsmem_addr(&mlr[rank][0][0], (uint32_t)c), &mlr[rank][0][0], 2 * H * 4, bar);
-    }
+  if (tid < C && tid != (int)rank) {
+    const uint32_t bar = dsmem_addr(&S.comb, (uint32_t)tid);
+    bulk_s2s_cluster(dsmem_addr(parts + rank * slot, (uint32_t)tid), stage + tid * slot, slot, bar);
+    bulk_s2s_cluster(dsmem_addr(&mlr[rank][0][0], (uint32_t)tid), &mlr[rank][0][0], 2 * H * 4, bar);
   }
   wait_ft(S, &S.comb, 0);   // every peer's rows and max / sum have landed
   __syncwarp();
-  cluster_arrive();         // (awaited at the end)
+  cluster_arrive_relaxed();   // (awaited at the end)
   if (tid < H) {
+    float mc[8], lc[8];
     float M = -INFINITY;
-#pragma unroll 1
-    for (int c = 0; c < C; ++c) M = fmaxf(M, mlr[c][0][tid]);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      mc[c] = c < C ? mlr[c][0][tid] : -INFINITY;
+      lc[c] = c < C ? mlr[c][1][tid] : 0.0f;
+      M = fmaxf(M, mc[c]);
+    }
     float L = 0.0f;
-#pragma unroll 1
-    for (int c = 0; c < C; ++c) {
-      const float mc = mlr[c][0][tid];
-      const float w = mc == -INFINITY ? 0.0f : mlr[c][1][tid] * exp2f(mc - M);
-      wgt[c][tid] = w;
-      L += w;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      lc[c] = mc[c] == -INFINITY ? 0.0f : lc[c] * exp2f(mc[c] - M);
+      L += lc[c];
     }
     const float invL = L > 0.0f ? 1.0f / L : 0.0f;
-#pragma unroll 1
-    for (int c = 0; c < C; ++c) wgt[c][tid] *= invL;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if (c < C) wgt[c][tid] = lc[c] * invL;
     if (rank == 0 && a.lse) a.lse[gp * H + tid] = L > 0.0f ? (M + log2f(L)) * kLn2 : -INFINITY;
   }
   bar_named(1, kWorkers);
@@ -483,6 +485,22 @@ __device__ __forceinline__ void load_q(const AttnArgs &a, Ctl &S, const CUtensor
   }
 }
 
+// C > 1: the cluster's CTAs share one token, so CTA `rank` loads the column
+// pairs p = rank (mod C) once for all of them (multicast); every CTA armed
+// its four Q barriers before the cluster barrier that precedes this call.
+__device__ __forceinline__ void load_q_cluster(const AttnArgs &a, Ctl &S, const CUtensorMap &tm_q, uint8_t *qs,
+                                               int item) {
+  const int tok = item / a.C;
+  const int rank = item - tok * a.C;
+  const int64_t gp = a.p0 + tok;
+  const uint16_t mask = (uint16_t)((1u << a.C) - 1u);
+#pragma unroll 1
+  for (int p = rank; p < 4; p += a.C) {
+    tma_load_2d_mc(qs + 2 * p * kAtom, &tm_q, 2 * p * 64, (int32_t)(gp * H), &S.q_full[p], mask);
+    tma_load_2d_mc(qs + (2 * p + 1) * kAtom, &tm_q, (2 * p + 1) * 64, (int32_t)(gp * H), &S.q_full[p], mask);
+  }
+}
+
 template <bool kSingle>
 __global__ void __launch_bounds__(kThreads, 1)
     sparse_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnArgs a) {
@@ -501,10 +519,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int first_item = blockIdx.x;
   const int stride = gridDim.x;
 
-  if (tid == 0) {
+  // The MMA warp's lane 0 sets up the barriers first.  C > 1: a cluster
+  // barrier then orders every CTA's set-up before any Q multicast into it;
+  // every thread arrives at once and awaits it once later (before its next
+  // arrive).
+  if (warp == kMmaWarp && lane == 0) {
     for (int p = 0; p < 4; ++p) {
       mbar_init(&S.q_full[p], 1);
-      mbar_init(&S.q_ready[p], kQThreads);
+      // one item per CTA (kSingle): the workers convert a share of Q too
+      mbar_init(&S.q_ready[p], kSingle ? kWorkers + kQThreads : kQThreads);
     }
     mbar_init(&S.s_full, 1);
     mbar_init(&S.p_full, kWorkers);
@@ -516,13 +539,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.cols_free[p], 1);
     }
     S.abort = 0;
+    // C > 1: Q arrives by multicast from the cluster's CTAs (one item per CTA)
+    if (a.C > 1)
+      for (int p = 0; p < 4; ++p) mbar_arrive_expect_tx(&S.q_full[p], (uint32_t)(2 * kAtom));
     fence_barrier_init();
     prefetch_tmap(&tm_q);
   }
-  if (warp == 0) {
+  __syncwarp();
+  if (a.C > 1) cluster_arrive();
+
+  // The first block's row of this thread: row tid / 2 for the workers, and
+  // in a single block row 128 + (tid - 288) / 2 for warps 9 and 10
+  // (entries: SWA rows come first).  Its top-K slot is requested first; the
+  // MMA warp meanwhile sets up the barriers and TMEM and sends Q's loads.
+  int e0 = -1;
+  if (warp < kMmaWarp)
+    e0 = tid >> 1;
+  else if (kSingle && tid >= (kMmaWarp + 1) * 32 && tid < (kMmaWarp + 3) * 32)
+    e0 = 128 + ((tid - (kMmaWarp + 1) * 32) >> 1);
+  const bool row0 = first_item < items && e0 >= 0 && (warp < kMmaWarp || e0 < a.Bk);
+  Item it0;
+  int32_t id0 = -1;
+  if (row0) {
+    it0 = item_info(a, first_item);
+    id0 = row_slot(a, it0, e0);
+  }
+
+  if (warp == kMmaWarp) {
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
+    if (a.C > 1) cluster_wait();
+    if (lane == 0 && first_item < items) {
+      if (a.C > 1)
+        load_q_cluster(a, S, tm_q, qs, first_item);
+      else
+        load_q(a, S, tm_q, qs, first_item);
+    }
   }
+  RowBuf b0;
+  b0.kind = 0;
+  b0.scale = 0.0f;
+  if (row0) load_row(a, it0, e0, id0, tid & 1, b0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -535,34 +592,46 @@ __global__ void __launch_bounds__(kThreads, 1)
    if (warp > kMmaWarp) {
     // the other warps of the MMA warpgroup: every item's Q, bf16 -> fp16 in
     // place one column pair at a time as it lands (the MMA thread reloads Q
-    // after an item's last S); in a single block of more than 128 rows, warps
-    // 9 and 10 also write rows 128 .. (entries: SWA rows come first), each
-    // column pair right after Q's
+    // after an item's last S).  A single block (one item): Q lands before
+    // the gathered rows, so the workers convert it with these warps first;
+    // warps 9 and 10 then also write rows 128 .. (entries: SWA rows come
+    // first).
     const int ht = tid - (kMmaWarp + 1) * 32;   // 0 .. 95
-    const int r = 128 + (ht >> 1), hcp = ht & 1;
-    const bool rows = kSingle && ht < 64 && first_item < items && r < a.Bk;
-    EntryBuf eb;
-    if (rows) {   // the rows' loads go out before the wait for Q
-      const Item it0 = item_info(a, first_item);
-      load_row(a, it0, r, row_slot(a, it0, r), hcp, eb);
-      if (hcp == 0) {
-        S.rs[r] = eb.scale;
-        S.vld[r] = eb.kind != 0 ? 1 : 0;
-      }
-    }
-    uint32_t n = 0;
-    for (int item = first_item; item < items; item += stride, ++n) {
+    if constexpr (kSingle) {
+      const int r = 128 + (ht >> 1), hcp = ht & 1;
+      const bool rows = ht < 64 && first_item < items && r < a.Bk;   // loaded into b0 at the start
+      __syncwarp();
+      if (a.C > 1) cluster_wait();
+      if (first_item < items) {
 #pragma unroll 1
-      for (int p = 0; p < 4; ++p) {
-        wait_ft(S, &S.q_full[p], n & 1u);
-        convert_q_pair(qs, p, ht, kQThreads);
-        mbar_arrive(&S.q_ready[p]);
-        if constexpr (kSingle) {   // one item
-          if (ht < 64) {
-            if (rows) dequant_front(tile, col_stride, r, hcp + 2 * p, eb);
+        for (int p = 0; p < 4; ++p) {
+          wait_ft(S, &S.q_full[p], 0);
+          convert_q_pair(qs, p, kWorkers + ht, kWorkers + kQThreads);
+          mbar_arrive(&S.q_ready[p]);
+        }
+        if (ht < 64) {
+          if (rows && hcp == 0) {
+            S.rs[r] = b0.scale;
+            S.vld[r] = b0.kind != 0 ? 1 : 0;
+          }
+#pragma unroll 1
+          for (int p = 0; p < 4; ++p) {
+            if (rows) dequant_front(tile, col_stride, r, hcp + 2 * p, b0);
             fence_proxy_async_smem();
             mbar_arrive(&S.cols_full[p]);
           }
+        }
+      }
+    } else {
+      __syncwarp();
+      if (a.C > 1) cluster_wait();
+      uint32_t n = 0;
+      for (int item = first_item; item < items; item += stride, ++n) {
+#pragma unroll 1
+        for (int p = 0; p < 4; ++p) {
+          wait_ft(S, &S.q_full[p], n & 1u);
+          convert_q_pair(qs, p, ht, kQThreads);
+          mbar_arrive(&S.q_ready[p]);
         }
       }
     }
@@ -577,7 +646,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t cs16 = col_stride >> 4;
       const int nks = a.Bk / 16;
       uint32_t g = 0, n_item = 0;
-      if (first_item < items) load_q(a, S, tm_q, qs, first_item);
       for (int item = first_item; item < items; item += stride, ++n_item) {
         const Item it = item_info(a, item);
         for (int j = 0; j < it.nb; ++j, ++g) {
@@ -638,15 +706,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     Cursor ld;
     ld.item = first_item;
     ld.j = 0;
-    RowBuf b0;
     int32_t ld_id = -1;
-    if (ld.item < items) {
+    if (ld.item < items) {   // (the first block's row is in b0 already)
       ld.it = item_info(a, ld.item);
       cur_nb = ld.it.nb;
-      load_row(a, ld.it, r0, row_slot(a, ld.it, r0), cp, b0);
       if constexpr (!kSingle) {
         ld.advance(a, stride, items);
         if (ld.item < items) ld_id = row_slot(a, ld.it, ld.j * a.Bk + r0);
+      }
+    }
+    __syncwarp();
+    if (a.C > 1) cluster_wait();
+    if constexpr (kSingle) {
+      // Q (multicast or local TMA) lands before the gathered rows: this
+      // thread's share of it first, while the rows are on their way
+      if (first_item < items) {
+#pragma unroll 1
+        for (int p = 0; p < 4; ++p) {
+          wait_ft(S, &S.q_full[p], 0);
+          convert_q_pair(qs, p, tid, kWorkers + kQThreads);
+          mbar_arrive(&S.q_ready[p]);
+        }
       }
     }
 
@@ -708,14 +788,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // under a condition: those serialise).  Slabs past the block read
       // neighbouring Ctl bytes, masked by k < Bk.  Two passes over TMEM (max,
       // then exponents) keep only one pair's values in registers.
-      auto logits = [&](int mi, float (&x)[16]) {
-        uint32_t u[16];
-        tmem_ld16x2(s_row + (uint32_t)(32 * (2 * mi + wh)), u);
+      // The row scales and valid flags of slab pair mi's 16 keys, and the
+      // logits from its TMEM values u.
+      auto row_info = [&](int mi, float (&rsv)[16], uint32_t (&vb)[4]) {
         const int k0 = 16 * (2 * (2 * mi + wh) + th);
         const float4 *r4 = reinterpret_cast<const float4 *>(S.rs + k0);
         const uint4 v4 = *reinterpret_cast<const uint4 *>(S.vld + k0);
-        const uint32_t vb[4] = {v4.x, v4.y, v4.z, v4.w};
-        float rsv[16];
+        vb[0] = v4.x;
+        vb[1] = v4.y;
+        vb[2] = v4.z;
+        vb[3] = v4.w;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const float4 f4 = r4[q];
@@ -724,40 +806,56 @@ __global__ void __launch_bounds__(kThreads, 1)
           rsv[4 * q + 2] = f4.z;
           rsv[4 * q + 3] = f4.w;
         }
-        tmem_ld_wait();
+      };
+      auto apply = [&](int mi, const uint32_t (&u)[16], const float (&rsv)[16], const uint32_t (&vb)[4],
+                       float (&x)[16]) {
+        const int k0 = 16 * (2 * (2 * mi + wh) + th);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const bool ok = (k0 + i < a.Bk) && ((vb[i >> 2] >> (8 * (i & 3))) & 0xFFu);
           x[i] = ok ? __uint_as_float(u[i]) * (kLogit * rsv[i]) : -INFINITY;
         }
       };
+      auto logits = [&](int mi, float (&x)[16]) {
+        uint32_t u[16], vb[4];
+        float rsv[16];
+        tmem_ld16x2(s_row + (uint32_t)(32 * (2 * mi + wh)), u);
+        row_info(mi, rsv, vb);   // overlaps the TMEM load
+        tmem_ld_wait();
+        apply(mi, u, rsv, vb, x);
+      };
       // P = 2^(logit - m_ref) (x the SWA row scale) into P^T; the row sum
       // gathers the unscaled exponents.  `over` flags a logit above
       // m_ref + kLazy (the one-pass attempt below).
+      auto store_p = [&](int mi, const float (&x)[16], float mref_s) {
+        bool over = false;
+        const int k0 = 16 * (2 * (2 * mi + wh) + th);
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 16; i += 2) {
+          // masked keys hold -inf: 2^-inf = 0 (no branch); m_ref = -inf only when all are masked
+          over |= (x[i] > mref_s + kLazy) | (x[i + 1] > mref_s + kLazy);
+          const float p0 = ex2_approx(x[i] - mref_s), p1 = ex2_approx(x[i + 1] - mref_s);
+          l_part += p0 + p1;
+          const float2 r2 = *reinterpret_cast<const float2 *>(S.rs + k0 + i);
+          pk[i >> 1] = pack_half2(p0 * r2.x, p1 * r2.y);
+        }
+        if (k0 < a.Bk) {
+          // P^T K-major: [64-key atom column][64 heads][128 B]
+          uint8_t *prow = pbuf + (k0 >> 6) * kAtom + h * 128;
+          const int c0 = (k0 & 63) >> 3;
+          *reinterpret_cast<uint4 *>(prow + ((c0 ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          *reinterpret_cast<uint4 *>(prow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+        }
+        return over;
+      };
       auto write_p = [&](float mref_s) {
         bool over = false;
 #pragma unroll 1
         for (int mi = 0; mi < kPairs; ++mi) {
           float x[16];
           logits(mi, x);
-          const int k0 = 16 * (2 * (2 * mi + wh) + th);
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            // masked keys hold -inf: 2^-inf = 0 (no branch); m_ref = -inf only when all are masked
-            over |= (x[i] > mref_s + kLazy) | (x[i + 1] > mref_s + kLazy);
-            const float p0 = ex2_approx(x[i] - mref_s), p1 = ex2_approx(x[i + 1] - mref_s);
-            l_part += p0 + p1;
-            const float2 r2 = *reinterpret_cast<const float2 *>(S.rs + k0 + i);
-            pk[i >> 1] = pack_half2(p0 * r2.x, p1 * r2.y);
-          }
-          if (k0 < a.Bk) {
-            // P^T K-major: [64-key atom column][64 heads][128 B]
-            uint8_t *prow = pbuf + (k0 >> 6) * kAtom + h * 128;
-            const int c0 = (k0 & 63) >> 3;
-            *reinterpret_cast<uint4 *>(prow + ((c0 ^ (h & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            *reinterpret_cast<uint4 *>(prow + (((c0 + 1) ^ (h & 7)) << 4)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-          }
+          over |= store_p(mi, x, mref_s);
         }
         return over;
       };
@@ -767,7 +865,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       // two passes below (max, then exponents).  Whether a reference exists
       // is the same for every head (it depends on which keys were valid).
       bool done_p = false;
-      if constexpr (!kSingle) {
+      if constexpr (kSingle) {
+        // one block (nothing accumulated yet): every logit of this thread
+        // from one TMEM round trip, kept in registers for the max and the
+        // exponents
+        uint32_t u[kPairs][16];
+#pragma unroll
+        for (int mi = 0; mi < kPairs; ++mi) tmem_ld16x2(s_row + (uint32_t)(32 * (2 * mi + wh)), u[mi]);
+        tmem_ld_wait();
+        float x[kPairs][16];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int mi = 0; mi < kPairs; ++mi) {
+          uint32_t vb[4];
+          float rsv[16];
+          row_info(mi, rsv, vb);
+          apply(mi, u[mi], rsv, vb, x[mi]);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) mx = fmaxf(mx, x[mi][i]);
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        if (th == 0) red[wh][h] = mx;
+        bar_named(1, kWorkers);
+        m_ref = fmaxf(red[0][h], red[1][h]);
+        const float ms = m_ref == -INFINITY ? 0.0f : m_ref;
+#pragma unroll
+        for (int mi = 0; mi < kPairs; ++mi) (void)store_p(mi, x[mi], ms);
+        done_p = true;
+      } else {
         if (m_ref != -INFINITY) {
           const float l_save = l_part;
           const bool over = write_p(m_ref);
@@ -826,11 +951,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (j == this_nb - 1) {
         // ---------------------------------------------------- item finished
+        // (kSingle: the sums take the next two rows, as no barrier separates
+        // this from the reads of the maxima above)
+        float(*red_l)[H] = red + (kSingle ? 2 : 0);
         const float lp = l_part + __shfl_xor_sync(0xffffffffu, l_part, 16);
-        if (th == 0) red[wh][h] = lp;
+        if (th == 0) red_l[wh][h] = lp;
         bar_named(1, kWorkers);
         if (th == 0 && wh == 0) {
-          const float L = red[0][h] + red[1][h];
+          const float L = red_l[0][h] + red_l[1][h];
           S.lfin[h] = L;
           S.mfin[h] = m_ref;
           S.inv_l[h] = L > 0.0f ? 1.0f / L : 0.0f;
@@ -851,7 +979,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {   // the allocating warp
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

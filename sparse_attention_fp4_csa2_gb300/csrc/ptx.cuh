@@ -150,6 +150,18 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int32_t
       : "memory");
 }
 
+// The same box delivered to every CTA of the cluster in `mask`, at the same
+// shared-memory offset, each arrival counted on that CTA's barrier at `bar`'s
+// offset (so every destination's barrier must be initialised first).
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const void *tmap, int32_t x, int32_t y, uint64_t *bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], "
+      "[%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
 // The same with an L2 cache policy (createpolicy below) for the loaded lines.
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const void *tmap, int32_t x, int32_t y, uint64_t *bar,
                                                  uint64_t policy) {
@@ -378,6 +390,12 @@ __device__ __forceinline__ void cluster_sync() {
 // independent work can run between the two halves.
 __device__ __forceinline__ void cluster_arrive() {
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+// Arrive without ordering this thread's earlier memory accesses (for a
+// barrier that only keeps the cluster's CTAs resident).
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_wait() {
