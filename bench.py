@@ -466,7 +466,8 @@ class PrefillWorkload:
         return self.B * self.T
 
     # kernels timed live inside the step (the last 1024-token block's launches)
-    PROFILED = ((2, "prefill_indexer_kernel"), (3, "topk_cluster_kernel"), (1, "sparse_attn_kernel"))
+    # (a block's 1,024 rows fill every SM twice: the top-K runs one CTA per row)
+    PROFILED = ((2, "prefill_indexer_kernel"), (3, "topk_row_kernel"), (1, "sparse_attn_kernel"))
 
     def step(self, prof=None, io=None):
         c2 = self.c2
@@ -506,9 +507,9 @@ class PrefillWorkload:
         if launch_ms.get("prefill_indexer_kernel"):
             out.append(roof_entry("prefill_indexer_kernel", wl, "tensor", vis * 32 * 128 * 2,
                                   launch_ms["prefill_indexer_kernel"], n_blk, peaks_))
-        if launch_ms.get("topk_cluster_kernel"):
-            out.append(roof_entry("topk_cluster_kernel", wl, "hbm", 4 * vis + 1024 * 512 * 4,
-                                  launch_ms["topk_cluster_kernel"], n_blk, peaks_))
+        if launch_ms.get("topk_row_kernel"):
+            out.append(roof_entry("topk_row_kernel", wl, "hbm", 4 * vis + 1024 * 512 * 4,
+                                  launch_ms["topk_row_kernel"], n_blk, peaks_))
         if launch_ms.get("sparse_attn_kernel"):
             out.append(roof_entry("sparse_attn_kernel", wl, "hbm", 1024 * ATTN_BYTES,
                                   launch_ms["sparse_attn_kernel"], n_blk, peaks_))

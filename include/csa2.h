@@ -21,13 +21,14 @@
  * csa2_prefill_chunk (a chunk at m = 2); helpers csa2_workspace_bytes,
  * csa2_get_device_status, csa2_status_string, csa2_default_params,
  * csa2_entry_bytes, csa2_indexer_entry_bytes, csa2_last_launch_count,
- * csa2_set_profile_events.
+ * csa2_set_profile_events, csa2_set_topk_kernel.
  *
  * Conventions for every call:
  *  - All tensor pointers are DEVICE pointers, caller-owned; the library never
  *    allocates or frees memory.  Between calls it keeps only a per-device
  *    error word (see csa2_get_device_status), the per-thread launch count of
- *    the last call (csa2_last_launch_count) and, on each device that has run
+ *    the last call (csa2_last_launch_count), the process-wide top-K kernel
+ *    choice (csa2_set_topk_kernel) and, on each device that has run
  *    csa2_hier_pool_select_static, that call's static scratch array, which
  *    holds the last call's contents.
  *  - Every call is asynchronous on `stream` (NULL = legacy default stream) and
@@ -360,6 +361,17 @@ typedef enum {
   CSA2_KERNEL_TOPK = 3
 } csa2_kernel;
 csa2_status csa2_set_profile_events(csa2_kernel kernel, void *start, void *stop);
+
+/* Which kernel the top-K selections (index_topk of the Full and Reindex
+ * layers and of prefill, the HSI pool) run on, for tests and measurements:
+ * 0 = automatic (one CTA per row for rows of at most 131,072 scores when a
+ * call has at least twice as many rows as the GPU has SMs, else one
+ * thread-block cluster per row), 1 = one
+ * cluster per row, 2 = one CTA per row (a call whose rows do not fit then
+ * fails with CSA2_ERR_CUDA).  Both kernels are exact and give the same
+ * result.  Applies to later calls in this process;
+ * CSA2_ERR_INVALID_ARG for any other value. */
+csa2_status csa2_set_topk_kernel(int32_t which);
 
 #ifdef __cplusplus
 }

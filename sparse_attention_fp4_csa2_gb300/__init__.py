@@ -81,6 +81,7 @@ def lib():
         L.csa2_prefill_chunk.argtypes = [PP, i32, i32, i64, i32, P, P, P, P, P, i64, P, P, i64, i64, P, P, P, P, sz, P]
         L.csa2_prefill_chunk.restype = ctypes.c_int
         L.csa2_set_profile_events.argtypes, L.csa2_set_profile_events.restype = [ctypes.c_int, P, P], ctypes.c_int
+        L.csa2_set_topk_kernel.argtypes, L.csa2_set_topk_kernel.restype = [ctypes.c_int32], ctypes.c_int
         for f in ("csa2_kv_quant_write", "csa2_kv_quant_write_ik", "csa2_indexer_k_quant", "csa2_indexer_score_topk", "csa2_hier_pool_select",
                   "csa2_sparse_attn", "csa2_sparse_decode"):
             getattr(L, f).restype = ctypes.c_int
@@ -275,6 +276,16 @@ def set_profile_events(kernel: int, start=None, stop=None):
     sp = ctypes.c_void_p(start.cuda_event) if start is not None else None
     ep = ctypes.c_void_p(stop.cuda_event) if stop is not None else None
     _check(lib().csa2_set_profile_events(kernel, sp, ep), "csa2_set_profile_events")
+
+
+TOPK_AUTO, TOPK_CLUSTER, TOPK_ROW = 0, 1, 2
+
+
+def set_topk_kernel(which: int):
+    """Kernel of the top-K selections made by later calls in this process:
+    TOPK_AUTO, TOPK_CLUSTER (one thread-block cluster per row) or TOPK_ROW
+    (one CTA per row, rows of at most 131,072 scores)."""
+    _check(lib().csa2_set_topk_kernel(which), "csa2_set_topk_kernel")
 
 
 OP_PREFILL = 4

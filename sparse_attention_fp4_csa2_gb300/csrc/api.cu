@@ -237,7 +237,7 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   r.pool = pool_blocks;
   r.pool_stride = p->candidate_topk_blocks;
   r.out = topk_idx;
-  return cuda_status(launch_topk_cluster(r, stream, launches));
+  return cuda_status(launch_topk(r, stream, launches));
 }
 
 csa2_status run_pool(const float *block_scores, const int32_t *n_vis, int32_t batch, int64_t n_max,
@@ -324,6 +324,12 @@ csa2_status csa2_set_profile_events(csa2_kernel kernel, void *start, void *stop)
   ProfileEvents &pe = profile_events(kernel);
   pe.start = static_cast<cudaEvent_t>(start);
   pe.stop = static_cast<cudaEvent_t>(stop);
+  return CSA2_OK;
+}
+
+csa2_status csa2_set_topk_kernel(int32_t which) {
+  if (which < 0 || which > 2) return CSA2_ERR_INVALID_ARG;
+  set_topk_choice(which);
   return CSA2_OK;
 }
 
@@ -572,7 +578,7 @@ extern "C" csa2_status csa2_prefill_chunk(const csa2_params *params, int32_t bat
     r.pool = nullptr;
     r.pool_stride = 0;
     r.out = topk_idx + q0 * p->index_topk;
-    if (launch_topk_cluster(r, st, &launches) != cudaSuccess) return CSA2_ERR_CUDA;
+    if (launch_topk(r, st, &launches) != cudaSuccess) return CSA2_ERR_CUDA;
     AttnArgs a;
     std::memset(&a, 0, sizeof(a));
     a.q = static_cast<const __nv_bfloat16 *>(q);

@@ -115,6 +115,15 @@ bool topk_cluster_supported(const TopkRows &r);
 // the HSI pool selection.
 cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled = true);
 
+// Single-kernel top-K with one CTA per row, for rows of at most 131,072
+// scores and k <= 2048.
+bool topk_row_supported(const TopkRows &r);
+cudaError_t launch_topk_row(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled = true);
+// The top-K of score rows on the kernel csa2_set_topk_kernel chose (0 auto,
+// 1 cluster, 2 one CTA per row: cudaErrorInvalidValue when a row does not fit).
+void set_topk_choice(int which);
+cudaError_t launch_topk(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled = true);
+
 // Chunked prefill: multi-query indexer over the causally visible entries.
 struct PrefillIdxArgs {
   const float *w;             // [B*T][32] head weights of every chunk token

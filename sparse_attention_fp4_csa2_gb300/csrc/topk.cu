@@ -361,7 +361,7 @@ cudaError_t launch_pool_topk(const TopkRows &r, void *scratch, int num_sms, cuda
   c.row_len = stride;
   c.row_stride = stride;
   c.force_nvis = nullptr;
-  return launch_topk_cluster(c, stream, launches, /*profiled*/ false);
+  return launch_topk(c, stream, launches, /*profiled*/ false);
 }
 
 size_t topk_scratch_bytes(int32_t rows, int64_t row_len, int32_t k) {
