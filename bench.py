@@ -280,6 +280,8 @@ class Workload:
         self.topk = torch.zeros(B, 512, dtype=torch.int32, device=device)
         self.topk_none = torch.full((B, 512), -1, dtype=torch.int32, device=device)   # SWA-only layers
         self.pool = torch.zeros(B, 2048, dtype=torch.int32, device=device)
+        # a Full layer's block scores when its calls are made one by one (end to end)
+        self.bscores = torch.empty(B, (E + 7) // 8, dtype=torch.float32, device=device) if self.hsi else None
         # per layer its output then its log-sum-exp, adjacent: one read-back per layer
         L, n_o = len(cfg.schedule), B * 64 * 512
         self.out_arena = torch.empty(L, n_o + B * 64, device=device)
@@ -350,7 +352,7 @@ class Workload:
         copy = -1
         for i, mode in enumerate(self.cfg.schedule):
             if io:
-                io.wait_in(i)
+                io.wait_in(self.io_first[i])
             li = L[i]
             if mode == "full":
                 copy += 1
@@ -382,9 +384,26 @@ class Workload:
                 on = [k for k in on if k in prof]
                 for k in on:
                     c2.set_profile_events(k, *prof[k])
-            c2.sparse_decode("reuse" if mode == "swa" else mode, self.params, li.q, self.kv[cc], self.n_vis, self.E,
-                             li.swa, li.swa_scale, li.swa_len, self.topk_none if mode == "swa" else self.topk,
-                             self.out[i], self.ws, pool_blocks=self.pool, lse=self.lse[i], **idx_args)
+            if io and mode in ("full", "reindex"):
+                # end to end, the layer's selection and its readout are two
+                # calls, so that the readout's inputs (the bulk of the layer's
+                # copy) may land while the selection runs
+                hsi_full = mode == "full" and self.hsi
+                c2.indexer_score_topk(li.q_idx, li.w, self.k_idx[cc], self.n_vis, self.E, self.params, self.topk,
+                                      self.ws, pool_blocks=self.pool if mode == "reindex" else None,
+                                      block_scores=self.bscores if hsi_full else None)
+                launches += c2.last_launch_count()
+                if hsi_full:
+                    c2.hier_pool_select(self.bscores, self.n_vis, self.E, self.params, self.pool, self.ws)
+                    launches += c2.last_launch_count()
+                io.wait_in(self.io_attn[i])
+                c2.sparse_attn(self.params, li.q, self.kv[cc], self.topk, li.swa, li.swa_scale, li.swa_len,
+                               self.out[i], self.ws, lse=self.lse[i])
+            else:
+                c2.sparse_decode("reuse" if mode == "swa" else mode, self.params, li.q, self.kv[cc], self.n_vis,
+                                 self.E, li.swa, li.swa_scale, li.swa_len,
+                                 self.topk_none if mode == "swa" else self.topk, self.out[i], self.ws,
+                                 pool_blocks=self.pool, lse=self.lse[i], **idx_args)
             for k in on:
                 c2.set_profile_events(k, None, None)
             launches += c2.last_launch_count()
@@ -395,18 +414,24 @@ class Workload:
         return launches
 
     def io_groups(self):
-        """Per layer: the tensors it reads that a caller supplies every step
-        (a Full layer's new entry inputs go with it), and the ones it returns."""
+        """Copy groups in copy order: per layer, the selection's inputs (a
+        Full or Reindex layer: its indexer query and head weights, a Full
+        layer's new entry inputs too), then the readout's (query, SWA rows and
+        scales); per layer the outputs it returns.  Sets which group each
+        layer waits for before it starts and before its readout."""
         ins, outs = [], []
+        self.io_first, self.io_attn = [], []
         copy = -1
         for i, (li, m) in enumerate(zip(self.layers, self.cfg.schedule)):
-            g = [li.q, li.swa, li.swa_scale]
-            if m == "full":
-                copy += 1
-                g = list(self.new_in[copy].values()) + g
+            self.io_first.append(len(ins))
             if m in ("full", "reindex"):
-                g += [li.q_idx, li.w]
-            ins.append(g)
+                g = [li.q_idx, li.w]
+                if m == "full":
+                    copy += 1
+                    g = list(self.new_in[copy].values()) + g
+                ins.append(g)
+            self.io_attn.append(len(ins))
+            ins.append([li.q, li.swa, li.swa_scale])
             outs.append([self.out_arena[i]])
         return ins, outs
 
