@@ -1,4 +1,4 @@
-// Exact top-K of each score row with one CTA per row (three per SM), for
+// Exact top-K of each score row with one CTA per row (two per SM), for
 // calls with many rows of up to 131,072 scores -- the index_topk = 512
 // selection of every chunk token in prefill ("DeepSeek-V4.1-Flash -
 // Architecture", sections 2 and 3) -- where throughput over the rows, not
@@ -14,18 +14,20 @@
 //      plain coalesced loads); two histogram levels (key bits 31..21, then
 //      20..10 inside the threshold bin) give a low threshold t_low with about
 //      twice the sample's share of k above it;
-//   2. filter: the row streams through two 16 KB shared-memory stages
-//      filled by bulk copies one stage ahead; every key >= t_low goes to the
-//      candidate list in index order (per-warp ballots and one scan of the
-//      warp counts per stage give every key its slot: no per-key atomics);
+//   2. filter: the row read once with coalesced loads, eight float4 per
+//      thread in flight; a float compare against the smallest score with a
+//      key >= t_low keeps the candidates, which take slots of a 4,096-entry
+//      list by one shared atomic per warp (the list is in no order);
 //   3. when the list did not overflow and holds every key of the top k (at
 //      least k keys, or every valid key), three radix levels (11, 11 and 10
-//      key bits) over the list find the k-th largest key T and how many keys
-//      equal to T are still needed; one ordered pass writes the keys above T
-//      and the first such ties;
-//   4. otherwise the same levels and the ordered pass run over the whole row
-//      (streamed through the ring each time): exact for any input, only
-//      slower.
+//      key bits) over it find the k-th largest key T and how many keys equal
+//      to T are still needed; the keys above T and the lowest-index ties
+//      (ranked by comparing indices) are gathered and sorted by index
+//      (bitonic) before they are written;
+//   4. otherwise -- the list overflowed, missed part of the top k, or holds
+//      more than 256 ties of T -- the levels (if needed) and an ordered pass
+//      run over the whole row streamed through two shared-memory stages
+//      filled by bulk copies: exact for any input, only slower.
 #include "kernels.cuh"
 
 namespace csa2 {
@@ -41,24 +43,38 @@ constexpr int kRBins = 2048;
 constexpr int kSampleLen = 512;          // sampled scores at the head of every chunk (1/8)
 constexpr int kRowMax = 131072;
 
+constexpr int kRSel = 2048;              // the selection (k <= 2048), sorted by index
+constexpr int kRTies = 256;              // keys equal to the k-th key, ranked by index
+
 struct __align__(128) RowTopkSmem {
-  float ring[kStages][kChunk];
+  float ring[kStages][kChunk];   // the whole-row path's stages
   uint32_t ckey[kRCand];
   int32_t cidx[kRCand];
   uint32_t hist[kRBins];
+  int32_t sel[kRSel];
+  int32_t tidx[kRTies];
   uint64_t full[kStages];
   uint32_t seg[2 * kRW];       // per (half, warp) counts of a stage, then their exclusive prefix
   uint32_t seg_total;
   uint32_t bscan[kRW];
+  uint32_t ccnt, nsel, ntie;
   int thr;
   uint32_t above, total;
 };
 
 constexpr size_t kRowSmem = sizeof(RowTopkSmem) + 128;
-static_assert(3 * (kRowSmem + 1024) <= 233472, "three CTAs must fit on an SM");
+static_assert(2 * (kRowSmem + 1024) <= 233472, "two CTAs must fit on an SM");
 
 __device__ __forceinline__ uint32_t row_key(float v) {
   return (v == -INFINITY || v != v) ? 0u : f32_key(v);
+}
+
+// The smallest score whose key is >= key (key >= 1), so that for any score v
+// (NaN and -inf included) row_key(v) >= key <=> v >= key_floor(key): the
+// filter compares floats and forms keys only for the values it keeps.
+__device__ __forceinline__ float key_floor(uint32_t key) {
+  if (key <= 0x00800000u) return -3.402823466e38f;   // every finite score
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
@@ -75,16 +91,15 @@ __device__ __forceinline__ void hist_agg(uint32_t *h, uint32_t bin) {
 }
 
 // Within-warp exclusive ranks of four flags per lane in (lane, e) order, and
-// the warp's count.
+// the warp's count: the lane counts (0..4) by their three bits, one ballot
+// each.
 __device__ __forceinline__ uint32_t warp_ranks(const bool (&f)[4], uint32_t (&rank)[4]) {
   const uint32_t lt = lanemask_lt();
-  uint32_t m[4], before = 0, tot = 0;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    m[e] = __ballot_sync(0xffffffffu, f[e]);
-    before += __popc(m[e] & lt);
-    tot += __popc(m[e]);
-  }
+  const uint32_t c = (uint32_t)f[0] + (uint32_t)f[1] + (uint32_t)f[2] + (uint32_t)f[3];
+  const uint32_t m0 = __ballot_sync(0xffffffffu, c & 1u), m1 = __ballot_sync(0xffffffffu, c & 2u),
+                 m2 = __ballot_sync(0xffffffffu, c & 4u);
+  const uint32_t before = __popc(m0 & lt) + 2 * __popc(m1 & lt) + 4 * __popc(m2 & lt);
+  const uint32_t tot = __popc(m0) + 2 * __popc(m1) + 4 * __popc(m2);
   uint32_t own = 0;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -243,6 +258,30 @@ __device__ __forceinline__ void stream_cands(RowTopkSmem &S, uint32_t cnt, F &&f
   }
 }
 
+// Sorts sel[0 .. cnt) ascending (bitonic over the next power of two, padded
+// with INT_MAX); cnt <= kRSel.  Ends with the CTA synchronised.
+__device__ void sort_sel(RowTopkSmem &S, uint32_t cnt) {
+  const uint32_t tid = threadIdx.x;
+  uint32_t P = 1;
+  while (P < cnt) P <<= 1;
+  for (uint32_t i = cnt + tid; i < P; i += kRT) S.sel[i] = 0x7fffffff;
+  __syncthreads();
+#pragma unroll 1
+  for (uint32_t size = 2; size <= P; size <<= 1)
+#pragma unroll 1
+    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
+      for (uint32_t t = tid; t < P / 2; t += kRT) {
+        const uint32_t i = 2 * t - (t & (stride - 1)), j = i + stride;   // bit `stride` of i is clear
+        const int32_t a = S.sel[i], b = S.sel[j];
+        if ((a > b) == ((i & size) == 0)) {
+          S.sel[i] = b;
+          S.sel[j] = a;
+        }
+      }
+      __syncthreads();
+    }
+}
+
 __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
   extern __shared__ uint8_t smem_raw[];
   RowTopkSmem &S =
@@ -307,32 +346,48 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
   }
 
   // ------------------------------------------------------------ 2. filter
-  uint32_t g = 0;        // chunks through the ring so far
-  uint32_t ccount = 0;   // candidates (may exceed the list: overflow)
-  stream_row(S, vals, n, g, [&](uint32_t(&keys)[2][4], int64_t base) {
-    uint32_t rk[2][4], cnt[2];
+  // Coalesced loads straight from the row, eight float4 per thread in
+  // flight; the kept keys (a float compare against t_low's smallest score)
+  // take list slots by one shared atomic per warp: the list is in no order.
+  uint32_t g = 0;   // chunks through the ring so far (the whole-row path)
+  if (tid == 0) S.ccnt = 0;
+  __syncthreads();
+  {
+    const float f_low = key_floor(t_low);
+    const int64_t n4 = n / 4;
+    const float4 *v4 = reinterpret_cast<const float4 *>(vals);
+#pragma unroll 1
+    for (int64_t q0 = 0; q0 < n4; q0 += 8 * kRT) {
+      float4 v[8];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      bool f[4];
+      for (int j = 0; j < 8; ++j) {
+        const int64_t q = q0 + tid + (int64_t)j * kRT;
+        v[j] = q < n4 ? __ldcg(v4 + q) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
 #pragma unroll
-      for (int e = 0; e < 4; ++e) f[e] = keys[h][e] >= t_low;
-      cnt[h] = warp_ranks(f, rk[h]);
-    }
-    uint32_t b0, b1, tot;
-    seg_scan(S, cnt[0], cnt[1], b0, b1, tot);
+      for (int j = 0; j < 8; ++j) {
+        const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+        bool f[4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+        for (int e = 0; e < 4; ++e) f[e] = x[e] >= f_low;
+        if (!__any_sync(0xffffffffu, f[0] | f[1] | f[2] | f[3])) continue;
+        uint32_t rk[4];
+        const uint32_t tot = warp_ranks(f, rk);
+        uint32_t base = 0;
+        if ((tid & 31) == 0) base = atomicAdd(&S.ccnt, tot);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        const int64_t i0 = 4 * (q0 + tid + (int64_t)j * kRT);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (keys[h][e] >= t_low) {
-          const uint32_t pos = ccount + (h ? b1 : b0) + rk[h][e];
-          if (pos < kRCand) {
-            S.ckey[pos] = keys[h][e];
-            S.cidx[pos] = (int32_t)(base + 2048 * h + 4 * tid + e);
+        for (int e = 0; e < 4; ++e)
+          if (f[e] && base + rk[e] < (uint32_t)kRCand) {
+            S.ckey[base + rk[e]] = row_key(x[e]);
+            S.cidx[base + rk[e]] = (int32_t)(i0 + e);
           }
-        }
-    ccount += tot;
-  });
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t ccount = S.ccnt;
   // the list holds every key of the top k when it did not overflow and has
   // at least k keys, or every valid key of the row (t_low = 1)
   const bool from_list = ccount <= (uint32_t)kRCand && (ccount >= k || t_low == 1);
@@ -383,6 +438,60 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
 
   int32_t *out = r.out + (int64_t)row * r.k;
   const int32_t *pool = r.pool ? r.pool + (int64_t)row * r.pool_stride : nullptr;
+  auto map = [&](int32_t v) { return pool ? __ldg(pool + v / BLOCK) * BLOCK + (v & (BLOCK - 1)) : v; };
+
+  // From the list: every key above T, and of the keys equal to T the
+  // tie_need lowest indices (ranked here when there are at most kRTies);
+  // the selection is then sorted by index.
+  bool ordered = !from_list;
+  if (from_list) {
+    const int lane = tid & 31;
+    if (tid == 0) {
+      S.nsel = 0;
+      S.ntie = 0;
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (uint32_t i0 = 0; i0 < ccount; i0 += kRT) {
+      const uint32_t i = i0 + tid;
+      const uint32_t key = i < ccount ? S.ckey[i] : 0u;
+      const bool above = key > T, tie = key == T && key != 0u;
+      const uint32_t ma = __ballot_sync(0xffffffffu, above), mt = __ballot_sync(0xffffffffu, tie);
+      uint32_t ba = 0, bt = 0;
+      if (lane == 0) {
+        if (ma) ba = atomicAdd(&S.nsel, (uint32_t)__popc(ma));
+        if (mt) bt = atomicAdd(&S.ntie, (uint32_t)__popc(mt));
+      }
+      ba = __shfl_sync(0xffffffffu, ba, 0);
+      bt = __shfl_sync(0xffffffffu, bt, 0);
+      const uint32_t lt = lanemask_lt();
+      if (above && ba + __popc(ma & lt) < (uint32_t)kRSel) S.sel[ba + __popc(ma & lt)] = S.cidx[i];
+      if (tie && bt + __popc(mt & lt) < (uint32_t)kRTies) S.tidx[bt + __popc(mt & lt)] = S.cidx[i];
+    }
+    __syncthreads();
+    const uint32_t ntie = S.ntie;
+    if (ntie > (uint32_t)kRTies) {
+      ordered = true;   // too many ties to rank here: the ordered pass over the row
+    } else {
+      if (tid < ntie) {
+        const int32_t v = S.tidx[tid];
+        uint32_t rank = 0;
+        for (uint32_t j = 0; j < ntie; ++j) rank += S.tidx[j] < v ? 1u : 0u;
+        if (rank < tie_need) {
+          const uint32_t p = atomicAdd(&S.nsel, 1u);
+          if (p < (uint32_t)kRSel) S.sel[p] = v;
+        }
+      }
+      __syncthreads();
+      const uint32_t cnt = min(S.nsel, k);
+      sort_sel(S, cnt);
+      for (uint32_t i = tid; i < k; i += kRT) out[i] = i < cnt ? map(S.sel[i]) : -1;
+    }
+  }
+  if (!ordered) return;
+
+  // Ordered pass over the row: the keys above T and the first tie_need keys
+  // equal to T, written in index order.
   uint32_t sel_before = 0, tie_before = 0;
   auto emit = [&](uint32_t(&keys)[2][4], int64_t base) {
     bool te[2][4], any_tie = false;
@@ -417,17 +526,12 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
       for (int e = 0; e < 4; ++e)
         if (fl[h][e]) {
           const uint32_t pos = sel_before + (h ? sb1 : sb0) + srk[h][e];
-          const int64_t o = base + 2048 * h + 4 * tid + e;
-          const int32_t v = from_list ? S.cidx[o] : (int32_t)o;
-          if (pos < k) out[pos] = pool ? __ldg(pool + v / BLOCK) * BLOCK + (v & (BLOCK - 1)) : v;
+          if (pos < k) out[pos] = map((int32_t)(base + 2048 * h + 4 * tid + e));
         }
     sel_before += stot;
     tie_before += ttot;
   };
-  if (from_list)
-    stream_cands(S, ccount, emit);
-  else
-    stream_row(S, vals, n, g, emit);
+  stream_row(S, vals, n, g, emit);
   for (uint32_t i = min(sel_before, k) + tid; i < k; i += kRT) out[i] = -1;
 }
 
