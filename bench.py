@@ -43,6 +43,7 @@ SWEEP_FIXED = 32 * 128 * 2 + 32 * 4        # q_idx + w per sequence
 # since its capture has no entry and reports null.
 TRAFFIC = {
     ("indexer_sweep_kernel", "group_decode_32x64k"): 537181184 + 6408192,
+    ("sparse_attn_kernel", "group_decode_32x64k"): 10644480,      # the output stays in L2 during the capture
     # captured at 16 sequences, scaled by the rows read to the 32-sequence launch
     ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411200 + 915968),
 }
