@@ -192,7 +192,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item I = item_of(a, it);
       const int wb = (int)(j & 1);
       if (!mbar_wait(&S.wfull[wb], (uint32_t)((j >> 1) & 1))) { abort_flag(S) = 1; break; }
+      // the head weights of two of this thread's four tokens stay in registers
+      // for the whole item, halving the epilogue's shared-memory reads
+      // (shared-memory bandwidth is what the MMAs run short of); the other
+      // two are read per tile (the warps' register budget holds no more)
       const float *wv = wbuf + wb * kN;
+      float wr[2][HI];
+      {
+        const float4 *w4 = reinterpret_cast<const float4 *>(wv + 4 * half * HI);
+#pragma unroll
+        for (int i = 0; i < HI / 2; ++i) {
+          const float4 ww = w4[i];
+          wr[i >> 3][(4 * i) & (HI - 1)] = ww.x;
+          wr[i >> 3][((4 * i) & (HI - 1)) + 1] = ww.y;
+          wr[i >> 3][((4 * i) & (HI - 1)) + 2] = ww.z;
+          wr[i >> 3][((4 * i) & (HI - 1)) + 3] = ww.w;
+        }
+      }
       int32_t nv[4];
 #pragma unroll
       for (int q = 0; q < 4; ++q) nv[q] = (int32_t)visible(a, I.qg + 4 * half + q);
@@ -214,7 +230,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
           for (int h4 = 0; h4 < HI / 4; ++h4) {
-            const float4 ww = w4[h4];
+            const float4 ww = q < 2 ? make_float4(wr[q & 1][4 * h4], wr[q & 1][4 * h4 + 1], wr[q & 1][4 * h4 + 2],
+                                                  wr[q & 1][4 * h4 + 3])
+                                    : w4[h4];
             s0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f), s0);
             s1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), s1);
             s2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), s2);
