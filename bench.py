@@ -44,6 +44,10 @@ SWEEP_FIXED = 32 * 128 * 2 + 32 * 4        # q_idx + w per sequence
 TRAFFIC = {
     ("indexer_sweep_kernel", "group_decode_32x64k"): 537181184 + 6408192,
     ("sparse_attn_kernel", "group_decode_32x64k"): 10644480,      # the output stays in L2 during the capture
+    # captured on one 1,024-token block of one sequence (--batch 1 --chunk 1024):
+    # the shape of every block launch of the full workload
+    ("prefill_indexer_kernel", "prefill_m2_2x128k+16k"): 50702336 + 214056192,
+    ("topk_row_kernel", "prefill_m2_2x128k+16k"): 272803072 + 4828928,
     # captured at 16 sequences, scaled by the rows read to the 32-sequence launch
     ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411200 + 915968),
 }
