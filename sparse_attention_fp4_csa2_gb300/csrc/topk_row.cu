@@ -22,8 +22,8 @@
 //      least k keys, or every valid key), three radix levels (11, 11 and 10
 //      key bits) over it find the k-th largest key T and how many keys equal
 //      to T are still needed; the keys above T and the lowest-index ties
-//      (ranked by comparing indices) are gathered and sorted by index
-//      (bitonic) before they are written;
+//      (ranked by comparing indices) are gathered and written in index
+//      order through a bitmap of the row (one bit per position);
 //   4. otherwise -- the list overflowed, missed part of the top k, or holds
 //      more than 256 ties of T -- the levels (if needed) and an ordered pass
 //      run over the whole row streamed through two shared-memory stages
@@ -43,7 +43,7 @@ constexpr int kRBins = 2048;
 constexpr int kSampleLen = 512;          // sampled scores at the head of every chunk (1/8)
 constexpr int kRowMax = 131072;
 
-constexpr int kRSel = 2048;              // the selection (k <= 2048), sorted by index
+constexpr int kRSel = 2048;              // the selection (k <= 2048), ordered through a bitmap
 constexpr int kRTies = 256;              // keys equal to the k-th key, ranked by index
 
 struct __align__(128) RowTopkSmem {
@@ -64,6 +64,7 @@ struct __align__(128) RowTopkSmem {
 
 constexpr size_t kRowSmem = sizeof(RowTopkSmem) + 128;
 static_assert(2 * (kRowSmem + 1024) <= 233472, "two CTAs must fit on an SM");
+static_assert(kStages * kChunk * 4 >= kRowMax / 8, "the ordering bitmap fits in the ring");
 
 __device__ __forceinline__ uint32_t row_key(float v) {
   return (v == -INFINITY || v != v) ? 0u : f32_key(v);
@@ -258,28 +259,53 @@ __device__ __forceinline__ void stream_cands(RowTopkSmem &S, uint32_t cnt, F &&f
   }
 }
 
-// Sorts sel[0 .. cnt) ascending (bitonic over the next power of two, padded
-// with INT_MAX); cnt <= kRSel.  Ends with the CTA synchronised.
-__device__ void sort_sel(RowTopkSmem &S, uint32_t cnt) {
-  const uint32_t tid = threadIdx.x;
-  uint32_t P = 1;
-  while (P < cnt) P <<= 1;
-  for (uint32_t i = cnt + tid; i < P; i += kRT) S.sel[i] = 0x7fffffff;
+// Writes the positions sel[0 .. cnt) (distinct, < n <= kRowMax) to out in
+// ascending order through a bitmap of the row held in the ring's space: one
+// bit per position, then each thread emits the set bits of its own run of
+// words at its exclusive prefix of the CTA's counts; out is padded with -1
+// to k.  Ends with the CTA synchronised.
+template <typename M>
+__device__ void write_sorted(RowTopkSmem &S, uint32_t cnt, int64_t n, uint32_t k, int32_t *out, M &&map) {
+  constexpr int kPer = (kRowMax / 32 + kRT - 1) / kRT;   // words per thread (8)
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  uint32_t *bm = reinterpret_cast<uint32_t *>(&S.ring[0][0]);
+  const int nw = (int)((n + 31) / 32);
+  for (int i = tid; i < nw; i += kRT) bm[i] = 0u;
   __syncthreads();
-#pragma unroll 1
-  for (uint32_t size = 2; size <= P; size <<= 1)
-#pragma unroll 1
-    for (uint32_t stride = size >> 1; stride > 0; stride >>= 1) {
-      for (uint32_t t = tid; t < P / 2; t += kRT) {
-        const uint32_t i = 2 * t - (t & (stride - 1)), j = i + stride;   // bit `stride` of i is clear
-        const int32_t a = S.sel[i], b = S.sel[j];
-        if ((a > b) == ((i & size) == 0)) {
-          S.sel[i] = b;
-          S.sel[j] = a;
-        }
-      }
-      __syncthreads();
+  for (uint32_t i = tid; i < cnt; i += kRT) {
+    const int32_t v = S.sel[i];
+    atomicOr(&bm[v >> 5], 1u << (v & 31));
+  }
+  __syncthreads();
+  const int w0 = tid * kPer;
+  uint32_t word[kPer], loc = 0;
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    word[j] = w0 + j < nw ? bm[w0 + j] : 0u;
+    loc += __popc(word[j]);
+  }
+  uint32_t incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += x;
+  }
+  if (lane == 31) S.bscan[w] = incl;
+  __syncthreads();
+  uint32_t pos = incl - loc;
+  for (int i = 0; i < w; ++i) pos += S.bscan[i];
+#pragma unroll
+  for (int j = 0; j < kPer; ++j) {
+    uint32_t b = word[j];
+    while (b) {
+      const int bit = __ffs(b) - 1;
+      b &= b - 1;
+      if (pos < k) out[pos] = map((int32_t)(32 * (w0 + j) + bit));
+      ++pos;
     }
+  }
+  for (uint32_t i = min(cnt, k) + tid; i < k; i += kRT) out[i] = -1;
+  __syncthreads();
 }
 
 __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
@@ -483,9 +509,7 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
         }
       }
       __syncthreads();
-      const uint32_t cnt = min(S.nsel, k);
-      sort_sel(S, cnt);
-      for (uint32_t i = tid; i < k; i += kRT) out[i] = i < cnt ? map(S.sel[i]) : -1;
+      write_sorted(S, min(S.nsel, k), n, k, out, map);
     }
   }
   if (!ordered) return;
