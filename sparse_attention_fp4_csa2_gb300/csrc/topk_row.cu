@@ -42,6 +42,8 @@ constexpr int kRCand = 4096;             // candidate list
 constexpr int kRBins = 2048;
 constexpr int kSampleLen = 512;          // sampled scores at the head of every chunk (1/8)
 constexpr int kRowMax = 131072;
+constexpr int kH = kChunk / (4 * kRT);   // float4 per thread per stage (index order: h, warp, lane)
+static_assert(kH * kRW == 32, "a stage's (h, warp) segments are scanned by one warp");
 
 constexpr int kRSel = 2048;              // the selection (k <= 2048), ordered through a bitmap
 constexpr int kRTies = 256;              // keys equal to the k-th key, ranked by index
@@ -54,7 +56,7 @@ struct __align__(128) RowTopkSmem {
   int32_t sel[kRSel];
   int32_t tidx[kRTies];
   uint64_t full[kStages];
-  uint32_t seg[2 * kRW];       // per (half, warp) counts of a stage, then their exclusive prefix
+  uint32_t seg[kH * kRW];      // per (h, warp) counts of a stage, then their exclusive prefix
   uint32_t seg_total;
   uint32_t bscan[kRW];
   uint32_t ccnt, nsel, ntie;
@@ -110,15 +112,14 @@ __device__ __forceinline__ uint32_t warp_ranks(const bool (&f)[4], uint32_t (&ra
   return tot;
 }
 
-// Exclusive prefix of the (half, warp) segment counts in (half, warp) order
-// -- the index order of a stage -- and their total.  Two CTA barriers.
-__device__ __forceinline__ void seg_scan(RowTopkSmem &S, uint32_t c0, uint32_t c1, uint32_t &b0, uint32_t &b1,
+// Exclusive prefix of the (h, warp) segment counts in (h, warp) order -- the
+// index order of a stage -- and their total.  Two CTA barriers.
+__device__ __forceinline__ void seg_scan(RowTopkSmem &S, const uint32_t (&c)[kH], uint32_t (&b)[kH],
                                          uint32_t &total) {
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  if (lane == 0) {
-    S.seg[w] = c0;
-    S.seg[kRW + w] = c1;
-  }
+  if (lane == 0)
+#pragma unroll
+    for (int h = 0; h < kH; ++h) S.seg[h * kRW + w] = c[h];
   __syncthreads();
   if (w == 0) {
     const uint32_t v = S.seg[lane];
@@ -132,8 +133,8 @@ __device__ __forceinline__ void seg_scan(RowTopkSmem &S, uint32_t c0, uint32_t c
     if (lane == 31) S.seg_total = incl;
   }
   __syncthreads();
-  b0 = S.seg[w];
-  b1 = S.seg[kRW + w];
+#pragma unroll
+  for (int h = 0; h < kH; ++h) b[h] = S.seg[h * kRW + w];
   total = S.seg_total;
 }
 
@@ -199,7 +200,7 @@ __device__ __forceinline__ uint32_t level_bin(uint32_t key, int level, uint32_t 
 }
 
 // Streams chunks [0, nch) of the row through the ring: f(keys, base) per
-// chunk, keys[h][e] the key at base + 2048 h + 4 tid + e (0 past n).  `g` is
+// chunk, keys[h][e] the key at base + 4 (kRT h + tid) + e (0 past n).  `g` is
 // the running count of chunks through the ring (the stage and barrier phase
 // of every chunk); thread 0 refills a stage after the CTA barrier that ends
 // its chunk.
@@ -220,10 +221,10 @@ __device__ __forceinline__ void stream_row(RowTopkSmem &S, const float *vals, in
     const int s = (int)(g % kStages);
     (void)mbar_wait(&S.full[s], (g / kStages) & 1u);
     const int64_t base = (int64_t)c * kChunk;
-    uint32_t keys[2][4];
+    uint32_t keys[kH][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int o = 2048 * h + 4 * tid;
+    for (int h = 0; h < kH; ++h) {
+      const int o = 4 * (kRT * h + tid);
       const float4 v = *reinterpret_cast<const float4 *>(&S.ring[s][o]);
       const bool in = base + o < n;   // n % 4 == 0: a float4 is wholly in or out
       keys[h][0] = in ? row_key(v.x) : 0u;
@@ -243,10 +244,10 @@ __device__ __forceinline__ void stream_cands(RowTopkSmem &S, uint32_t cnt, F &&f
   const int tid = threadIdx.x;
 #pragma unroll 1
   for (uint32_t base = 0; base < cnt; base += kChunk) {
-    uint32_t keys[2][4];
+    uint32_t keys[kH][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t o = base + 2048 * h + 4 * tid;
+    for (int h = 0; h < kH; ++h) {
+      const uint32_t o = base + 4 * (kRT * h + tid);
       const uint4 k4 = o < cnt ? *reinterpret_cast<const uint4 *>(&S.ckey[o]) : make_uint4(0, 0, 0, 0);
       // entries past cnt inside the last float4 hold stale keys: mask them
       keys[h][0] = o + 0 < cnt ? k4.x : 0u;
@@ -426,9 +427,9 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
     uint32_t need = k, prefix = 0;
 #pragma unroll 1
     for (int L = 0; L < 3; ++L) {
-      auto hist = [&](uint32_t(&keys)[2][4], int64_t) {
+      auto hist = [&](uint32_t(&keys)[kH][4], int64_t) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < kH; ++h)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const uint32_t bin = level_bin(keys[h][e], L, prefix);
@@ -517,40 +518,40 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
   // Ordered pass over the row: the keys above T and the first tie_need keys
   // equal to T, written in index order.
   uint32_t sel_before = 0, tie_before = 0;
-  auto emit = [&](uint32_t(&keys)[2][4], int64_t base) {
-    bool te[2][4], any_tie = false;
+  auto emit = [&](uint32_t(&keys)[kH][4], int64_t base) {
+    bool te[kH][4], any_tie = false;
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < kH; ++h)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         te[h][e] = keys[h][e] == T && keys[h][e] != 0u;
         any_tie |= te[h][e];
       }
-    uint32_t trk[2][4] = {}, tb0 = 0, tb1 = 0, ttot = 0;
+    uint32_t trk[kH][4] = {}, tb[kH] = {}, ttot = 0;
     if (__syncthreads_or(any_tie)) {
-      uint32_t tc[2];
+      uint32_t tc[kH];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) tc[h] = warp_ranks(te[h], trk[h]);
-      seg_scan(S, tc[0], tc[1], tb0, tb1, ttot);
+      for (int h = 0; h < kH; ++h) tc[h] = warp_ranks(te[h], trk[h]);
+      seg_scan(S, tc, tb, ttot);
     }
-    bool fl[2][4];
-    uint32_t srk[2][4], sc[2];
+    bool fl[kH][4];
+    uint32_t srk[kH][4], sc[kH];
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
+    for (int h = 0; h < kH; ++h) {
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        fl[h][e] = keys[h][e] > T || (te[h][e] && tie_before + (h ? tb1 : tb0) + trk[h][e] < tie_need);
+        fl[h][e] = keys[h][e] > T || (te[h][e] && tie_before + tb[h] + trk[h][e] < tie_need);
       sc[h] = warp_ranks(fl[h], srk[h]);
     }
-    uint32_t sb0, sb1, stot;
-    seg_scan(S, sc[0], sc[1], sb0, sb1, stot);
+    uint32_t sb[kH], stot;
+    seg_scan(S, sc, sb, stot);
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
+    for (int h = 0; h < kH; ++h)
 #pragma unroll
       for (int e = 0; e < 4; ++e)
         if (fl[h][e]) {
-          const uint32_t pos = sel_before + (h ? sb1 : sb0) + srk[h][e];
-          if (pos < k) out[pos] = map((int32_t)(base + 2048 * h + 4 * tid + e));
+          const uint32_t pos = sel_before + sb[h] + srk[h][e];
+          if (pos < k) out[pos] = map((int32_t)(base + 4 * (kRT * h + tid) + e));
         }
     sel_before += stot;
     tie_before += ttot;
