@@ -309,7 +309,7 @@ __device__ void write_sorted(RowTopkSmem &S, uint32_t cnt, int64_t n, uint32_t k
   __syncthreads();
 }
 
-__global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
+__global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
   extern __shared__ uint8_t smem_raw[];
   RowTopkSmem &S =
       *reinterpret_cast<RowTopkSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -375,14 +375,21 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
   // ------------------------------------------------------------ 2. filter
   // Coalesced loads straight from the row, eight float4 per thread in
   // flight; the kept keys (a float compare against t_low's smallest score)
-  // take list slots by one shared atomic per warp: the list is in no order.
+  // go to the warp's own segment of a list in the ring's space (the warp
+  // keeps its count in a register: no shared atomics), and the segments are
+  // then packed into the candidate list (in no particular order).
   uint32_t g = 0;   // chunks through the ring so far (the whole-row path)
-  if (tid == 0) S.ccnt = 0;
-  __syncthreads();
+  constexpr int kSeg = kRCand / kRW;   // entries per warp segment
+  static_assert(2 * kRCand * 4 <= kStages * kChunk * 4, "the warp segments fit in the ring");
+  uint32_t *seg_key = reinterpret_cast<uint32_t *>(&S.ring[0][0]);
+  int32_t *seg_idx = reinterpret_cast<int32_t *>(seg_key + kRCand);
+  uint32_t ccount;
   {
+    const int lane = tid & 31, w = tid >> 5;
     const float f_low = key_floor(t_low);
     const int64_t n4 = n / 4;
     const float4 *v4 = reinterpret_cast<const float4 *>(vals);
+    uint32_t wcnt = 0;   // this warp's candidates (the same in every lane)
 #pragma unroll 1
     for (int64_t q0 = 0; q0 < n4; q0 += 8 * kRT) {
       float4 v[8];
@@ -400,21 +407,34 @@ __global__ void __launch_bounds__(kRT, 1) topk_row_kernel(const TopkRows r) {
         if (!__any_sync(0xffffffffu, f[0] | f[1] | f[2] | f[3])) continue;
         uint32_t rk[4];
         const uint32_t tot = warp_ranks(f, rk);
-        uint32_t base = 0;
-        if ((tid & 31) == 0) base = atomicAdd(&S.ccnt, tot);
-        base = __shfl_sync(0xffffffffu, base, 0);
         const int64_t i0 = 4 * (q0 + tid + (int64_t)j * kRT);
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (f[e] && base + rk[e] < (uint32_t)kRCand) {
-            S.ckey[base + rk[e]] = row_key(x[e]);
-            S.cidx[base + rk[e]] = (int32_t)(i0 + e);
+          if (f[e] && wcnt + rk[e] < (uint32_t)kSeg) {
+            seg_key[w * kSeg + wcnt + rk[e]] = row_key(x[e]);
+            seg_idx[w * kSeg + wcnt + rk[e]] = (int32_t)(i0 + e);
           }
+        wcnt += tot;
       }
     }
+    if (lane == 0) S.seg[w] = wcnt;
+    __syncthreads();
+    uint32_t base = 0, total = 0;
+    bool over = false;
+    for (int i = 0; i < kRW; ++i) {
+      const uint32_t c = S.seg[i];
+      base += i < w ? c : 0u;
+      total += c;
+      over |= c > (uint32_t)kSeg;
+    }
+    ccount = over ? (uint32_t)kRCand + 1u : total;   // a full segment counts as an overflow
+    if (!over)
+      for (uint32_t i = lane; i < wcnt; i += 32) {
+        S.ckey[base + i] = seg_key[w * kSeg + i];
+        S.cidx[base + i] = seg_idx[w * kSeg + i];
+      }
   }
   __syncthreads();
-  const uint32_t ccount = S.ccnt;
   // the list holds every key of the top k when it did not overflow and has
   // at least k keys, or every valid key of the row (t_low = 1)
   const bool from_list = ccount <= (uint32_t)kRCand && (ccount >= k || t_low == 1);
