@@ -86,11 +86,15 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
   return m;
 }
 
-// Histogram add aggregated over the warp's equal bins (kRBins: none); every
-// lane of the warp calls it.
+// Histogram add (kRBins: none) for bins that crowd: the lanes sharing lane
+// 0's bin add as one atomic, the others one each.  (Cheaper than grouping
+// every distinct bin: __match_any_sync costs several microseconds over a
+// row's sample.)  Every lane of the warp calls it.
 __device__ __forceinline__ void hist_agg(uint32_t *h, uint32_t bin) {
-  const uint32_t peers = __match_any_sync(0xffffffffu, bin);
-  if (bin < kRBins && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+  const uint32_t b0 = __shfl_sync(0xffffffffu, bin, 0);
+  const uint32_t same = __ballot_sync(0xffffffffu, bin == b0);
+  if ((threadIdx.x & 31) == 0 && b0 < kRBins) atomicAdd(&h[b0], (uint32_t)__popc(same));
+  if (bin != b0 && bin < kRBins) atomicAdd(&h[bin], 1u);
 }
 
 // Within-warp exclusive ranks of four flags per lane in (lane, e) order, and
