@@ -118,6 +118,8 @@ def parse():
     ap.add_argument("--project-ik", action="store_true",
                     help="a Full layer writes its new indexer key as the projection of its main-KV entry "
                          "(csa2_kv_quant_write_ik; decode workloads)")
+    ap.add_argument("--topk-kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="top-K kernel (csa2_set_topk_kernel): 0 automatic, 1 a cluster per row, 2 a CTA per row")
     return ap.parse_args()
 
 
@@ -275,8 +277,11 @@ class Workload:
         self.project = PROJECT_IK
         self.w_ik = [synth.normal((128, 512), seed + 101 * c + 13, 0, device, std=512 ** -0.5)
                      for c in range(self.copies)] if PROJECT_IK else None
-        if self.fp4:
-            self.PROFILED = ((0, "indexer_sweep_fp4_kernel"), (3, "topk_cluster_kernel"), (1, "sparse_attn_kernel"))
+        c2.set_topk_kernel(TOPK_KERNEL)
+        # the Full layer's top-K: B rows of E scores
+        tk = topk_kernel_name(B, E, torch.cuda.get_device_properties(device).multi_processor_count)
+        self.PROFILED = ((0, "indexer_sweep_fp4_kernel" if self.fp4 else "indexer_sweep_kernel"), (3, tk),
+                         (1, "sparse_attn_kernel"))
         self.layers = [synth.layer_inputs(s, B, device=device) for s in cfg.layer_seeds]
         self.new_pos = torch.full((B,), (E - 1) * m + (m - 1), dtype=torch.int64, device=device)
         self.new_slot = torch.arange(B, dtype=torch.int64, device=device) * E + (E - 1)
@@ -322,9 +327,9 @@ class Workload:
         if launch_ms.get(sweep) and n_full:
             out.append(roof_entry(sweep, wl, "hbm", B * (K_BYTES[self.fp4] * E + SWEEP_FIXED),
                                   launch_ms[sweep], n_full, peaks_))
-        if launch_ms.get("topk_cluster_kernel") and n_full:
-            out.append(roof_entry("topk_cluster_kernel", wl, "hbm", B * (4 * E + 4 * 512),
-                                  launch_ms["topk_cluster_kernel"], n_full, peaks_))
+        topk = self.PROFILED[1][1]
+        if launch_ms.get(topk) and n_full:
+            out.append(roof_entry(topk, wl, "hbm", B * (4 * E + 4 * 512), launch_ms[topk], n_full, peaks_))
         if launch_ms.get("sparse_attn_kernel"):
             out.append(roof_entry("sparse_attn_kernel", wl, "hbm", B * ATTN_BYTES,
                                   launch_ms["sparse_attn_kernel"], n_attn, peaks_))
@@ -488,6 +493,9 @@ class PrefillWorkload:
         self.lse = self.out_arena[n_o:n_o + n_l].view(B, T, 64)
         self.topk = self.out_arena[n_o + n_l:].view(torch.int32).view(B, T, 512)
         self.ws = c2.workspace(c2.OP_PREFILL, B, self.E, self.params, device=device)
+        c2.set_topk_kernel(TOPK_KERNEL)
+        tk = topk_kernel_name(1024, self.E, torch.cuda.get_device_properties(device).multi_processor_count)
+        self.PROFILED = ((2, "prefill_indexer_kernel"), (3, tk), (1, "sparse_attn_kernel"))
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
@@ -536,9 +544,9 @@ class PrefillWorkload:
         if launch_ms.get("prefill_indexer_kernel"):
             out.append(roof_entry("prefill_indexer_kernel", wl, "tensor", vis * 32 * 128 * 2,
                                   launch_ms["prefill_indexer_kernel"], n_blk, peaks_))
-        if launch_ms.get("topk_row_kernel"):
-            out.append(roof_entry("topk_row_kernel", wl, "hbm", 4 * vis + 1024 * 512 * 4,
-                                  launch_ms["topk_row_kernel"], n_blk, peaks_))
+        topk = self.PROFILED[1][1]
+        if launch_ms.get(topk):
+            out.append(roof_entry(topk, wl, "hbm", 4 * vis + 1024 * 512 * 4, launch_ms[topk], n_blk, peaks_))
         if launch_ms.get("sparse_attn_kernel"):
             out.append(roof_entry("sparse_attn_kernel", wl, "hbm", 1024 * ATTN_BYTES,
                                   launch_ms["sparse_attn_kernel"], n_blk, peaks_))
@@ -560,6 +568,15 @@ LONG_CONFIG = "decoder20_4x1m"           # its 1M-context workload, timed beside
 ATTN_KERNEL = 0       # csa2_params.attn_kernel of the workloads (--attn-kernel)
 INDEXER_FP4 = False   # csa2_params.indexer_fp4 of the decode workloads (--indexer-fp4)
 PROJECT_IK = False    # Full layers project their new indexer key (--project-ik)
+TOPK_KERNEL = 0       # csa2_set_topk_kernel (--topk-kernel)
+
+
+def topk_kernel_name(rows, row_len, sms):
+    """The top-K kernel a call of `rows` rows of `row_len` scores runs on
+    (the library's automatic rule, or the forced choice)."""
+    if TOPK_KERNEL == 2 or (TOPK_KERNEL == 0 and rows >= 2 * sms and row_len <= 131072):
+        return "topk_row_kernel"
+    return "topk_cluster_kernel"
 
 
 def measure(args, cfg, dev, rank, world, local_rank, steps):
@@ -725,10 +742,11 @@ def measure(args, cfg, dev, rank, world, local_rank, steps):
 
 
 def run_ours(args, rank, world, local_rank):
-    global ATTN_KERNEL, INDEXER_FP4, PROJECT_IK
+    global ATTN_KERNEL, INDEXER_FP4, PROJECT_IK, TOPK_KERNEL
     ATTN_KERNEL = args.attn_kernel
     INDEXER_FP4 = args.indexer_fp4
     PROJECT_IK = args.project_ik
+    TOPK_KERNEL = args.topk_kernel
     import torch
 
     import synth

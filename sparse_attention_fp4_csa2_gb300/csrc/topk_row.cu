@@ -11,9 +11,10 @@
 //
 // No cluster barriers, no global scratch:
 //   1. sample: the first 512 scores of every 4096 (an eighth of the row,
-//      plain coalesced loads); two histogram levels (key bits 31..21, then
-//      20..10 inside the threshold bin) give a low threshold t_low with about
-//      twice the sample's share of k above it;
+//      plain coalesced loads); a histogram of key bits 31..21 gives a low
+//      threshold t_low with about twice the sample's share of k above it --
+//      refined by a second level (bits 20..10 inside the threshold bin) when
+//      that bin would bring more candidates than the list should hold;
 //   2. filter: the row read once with coalesced loads, eight float4 per
 //      thread in flight; a float compare against the smallest score with a
 //      key >= t_low keeps the candidates, which take slots of a 4,096-entry
@@ -61,7 +62,7 @@ struct __align__(128) RowTopkSmem {
   uint32_t bscan[kRW];
   uint32_t ccnt, nsel, ntie;
   int thr;
-  uint32_t above, total;
+  uint32_t above, total, in_thr;
 };
 
 constexpr size_t kRowSmem = sizeof(RowTopkSmem) + 128;
@@ -175,6 +176,7 @@ __device__ void row_threshold(RowTopkSmem &S, uint32_t need, int bins) {
     S.thr = -1;
     S.above = total;
     S.total = total;
+    S.in_thr = 0;
   }
   __syncthreads();
   if (total > need) {
@@ -184,6 +186,7 @@ __device__ void row_threshold(RowTopkSmem &S, uint32_t need, int bins) {
       if (b >= 0 && before < need && before + c[j] >= need) {
         S.thr = b;
         S.above = before;
+        S.in_thr = c[j];
       }
       before += c[j];
     }
@@ -369,7 +372,11 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
   uint32_t t_low = 1;                   // 1: every valid key
   sample(0, 0);
   row_threshold(S, need_s, kRBins);
-  if (S.thr >= 0) {
+  // the second level only when the first level's bin would bring too many
+  // candidates (the sample is an eighth of the row)
+  if (S.thr >= 0 && 8 * (S.above + S.in_thr) <= (uint32_t)(kRCand * 5 / 8)) {
+    t_low = (uint32_t)S.thr << 21;
+  } else if (S.thr >= 0) {
     const uint32_t b0 = (uint32_t)S.thr, above0 = S.above;
     sample(1, b0);
     row_threshold(S, need_s - above0, kRBins);
@@ -378,15 +385,15 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
 
   // ------------------------------------------------------------ 2. filter
   // Coalesced loads straight from the row, eight float4 per thread in
-  // flight; the kept keys (a float compare against t_low's smallest score)
-  // go to the warp's own segment of a list in the ring's space (the warp
-  // keeps its count in a register: no shared atomics), and the segments are
-  // then packed into the candidate list (in no particular order).
+  // flight; the kept positions (a float compare against t_low's smallest
+  // score) go to the warp's own segment of a list in the ring's space (the
+  // warp keeps its count in a register: no shared atomics), and the
+  // segments are then packed, with their keys read again, into the
+  // candidate list (in no particular order).
   uint32_t g = 0;   // chunks through the ring so far (the whole-row path)
   constexpr int kSeg = kRCand / kRW;   // entries per warp segment
-  static_assert(2 * kRCand * 4 <= kStages * kChunk * 4, "the warp segments fit in the ring");
-  uint32_t *seg_key = reinterpret_cast<uint32_t *>(&S.ring[0][0]);
-  int32_t *seg_idx = reinterpret_cast<int32_t *>(seg_key + kRCand);
+  static_assert(kRCand * 4 <= kStages * kChunk * 4, "the warp segments fit in the ring");
+  int32_t *seg_idx = reinterpret_cast<int32_t *>(&S.ring[0][0]);
   uint32_t ccount;
   {
     const int lane = tid & 31, w = tid >> 5;
@@ -402,24 +409,32 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
         const int64_t q = q0 + tid + (int64_t)j * kRT;
         v[j] = q < n4 ? __ldcg(v4 + q) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
       }
+      // this thread's 32 flags as one mask, one warp scan of the counts,
+      // then a slot per set bit (the keys are read again when packed)
+      uint32_t mask = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
-        bool f[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) f[e] = x[e] >= f_low;
-        if (!__any_sync(0xffffffffu, f[0] | f[1] | f[2] | f[3])) continue;
-        uint32_t rk[4];
-        const uint32_t tot = warp_ranks(f, rk);
-        const int64_t i0 = 4 * (q0 + tid + (int64_t)j * kRT);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (f[e] && wcnt + rk[e] < (uint32_t)kSeg) {
-            seg_key[w * kSeg + wcnt + rk[e]] = row_key(x[e]);
-            seg_idx[w * kSeg + wcnt + rk[e]] = (int32_t)(i0 + e);
-          }
-        wcnt += tot;
+        mask |= (v[j].x >= f_low ? 1u : 0u) << (4 * j);
+        mask |= (v[j].y >= f_low ? 1u : 0u) << (4 * j + 1);
+        mask |= (v[j].z >= f_low ? 1u : 0u) << (4 * j + 2);
+        mask |= (v[j].w >= f_low ? 1u : 0u) << (4 * j + 3);
       }
+      const uint32_t c = __popc(mask);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      uint32_t pos = wcnt + incl - c;
+      while (mask) {
+        const int bit = __ffs(mask) - 1;
+        mask &= mask - 1;
+        if (pos < (uint32_t)kSeg)
+          seg_idx[w * kSeg + pos] = (int32_t)(4 * (q0 + tid + (int64_t)(bit >> 2) * kRT) + (bit & 3));
+        ++pos;
+      }
+      wcnt += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) S.seg[w] = wcnt;
     __syncthreads();
@@ -434,8 +449,9 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
     ccount = over ? (uint32_t)kRCand + 1u : total;   // a full segment counts as an overflow
     if (!over)
       for (uint32_t i = lane; i < wcnt; i += 32) {
-        S.ckey[base + i] = seg_key[w * kSeg + i];
-        S.cidx[base + i] = seg_idx[w * kSeg + i];
+        const int32_t idx = seg_idx[w * kSeg + i];
+        S.ckey[base + i] = row_key(__ldcg(vals + idx));
+        S.cidx[base + i] = idx;
       }
   }
   __syncthreads();
