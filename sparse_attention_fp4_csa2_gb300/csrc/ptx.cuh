@@ -514,4 +514,12 @@ __device__ __forceinline__ uint32_t f32_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// The smallest float whose f32_key is >= key (key >= 1): for every v (NaN and
+// -inf included, which never pass) f32_key(v) >= key <=> v >= f32_key_floor(key),
+// so a threshold on keys is one float compare.
+__device__ __forceinline__ float f32_key_floor(uint32_t key) {
+  if (key <= 0x00800000u) return -3.402823466e38f;   // every finite value
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 }  // namespace csa2

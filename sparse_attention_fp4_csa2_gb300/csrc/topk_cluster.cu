@@ -565,6 +565,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
   // and prefix-summed across the warp at once; warps are in index order, and
   // a CTA prefix sum of the warp totals places them.
   uint32_t n_cand = 0;
+  const float f_low = f32_key_floor(t_low);   // keys >= t_low <=> values >= f_low
   for (int64_t base = lo; base < hi; base += kRound) {
     float4 v[kVec];
     if (one_round) {
@@ -576,8 +577,7 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
     uint32_t pk[2] = {0u, 0u};
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
-      const uint32_t c = (score_key(v[j].x) >= t_low) + (score_key(v[j].y) >= t_low) +
-                         (score_key(v[j].z) >= t_low) + (score_key(v[j].w) >= t_low);
+      const uint32_t c = (v[j].x >= f_low) + (v[j].y >= f_low) + (v[j].z >= f_low) + (v[j].w >= f_low);
       pk[j >> 2] |= c << (8 * (j & 3));
     }
     uint32_t inc[2] = {pk[0], pk[1]};
@@ -607,10 +607,9 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
       const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const uint32_t key = score_key(x[e]);
-        if (key >= t_low) {
+        if (x[e] >= f_low) {
           if (pos < kCand) {
-            S.ckey[pos] = key;
+            S.ckey[pos] = score_key(x[e]);
             S.cidx[pos] = i0 + e;
           }
           ++pos;

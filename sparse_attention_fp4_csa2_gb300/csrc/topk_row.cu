@@ -73,13 +73,6 @@ __device__ __forceinline__ uint32_t row_key(float v) {
   return (v == -INFINITY || v != v) ? 0u : f32_key(v);
 }
 
-// The smallest score whose key is >= key (key >= 1), so that for any score v
-// (NaN and -inf included) row_key(v) >= key <=> v >= key_floor(key): the
-// filter compares floats and forms keys only for the values it keeps.
-__device__ __forceinline__ float key_floor(uint32_t key) {
-  if (key <= 0x00800000u) return -3.402823466e38f;   // every finite score
-  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
 
 __device__ __forceinline__ uint32_t lanemask_lt() {
   uint32_t m;
@@ -397,7 +390,7 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
   uint32_t ccount;
   {
     const int lane = tid & 31, w = tid >> 5;
-    const float f_low = key_floor(t_low);
+    const float f_low = f32_key_floor(t_low);   // the filter compares floats
     const int64_t n4 = n / 4;
     const float4 *v4 = reinterpret_cast<const float4 *>(vals);
     uint32_t wcnt = 0;   // this warp's candidates (the same in every lane)
