@@ -17,8 +17,11 @@
 //      that bin would bring more candidates than the list should hold;
 //   2. filter: the row read once with coalesced loads, eight float4 per
 //      thread in flight; a float compare against the smallest score with a
-//      key >= t_low keeps the candidates, which take slots of a 4,096-entry
-//      list by one shared atomic per warp (the list is in no order);
+//      key >= t_low keeps the candidates (32 flags per thread as one mask,
+//      one warp scan of the counts), whose positions go to the warp's own
+//      segment of a list (its count kept in a register: no atomics); the
+//      segments are then packed, keys read again, into one 4,096-entry list
+//      in no particular order;
 //   3. when the list did not overflow and holds every key of the top k (at
 //      least k keys, or every valid key), three radix levels (11, 11 and 10
 //      key bits) over it find the k-th largest key T and how many keys equal
@@ -60,7 +63,7 @@ struct __align__(128) RowTopkSmem {
   uint32_t seg[kH * kRW];      // per (h, warp) counts of a stage, then their exclusive prefix
   uint32_t seg_total;
   uint32_t bscan[kRW];
-  uint32_t ccnt, nsel, ntie;
+  uint32_t nsel, ntie;
   int thr;
   uint32_t above, total, in_thr;
 };
