@@ -41,6 +41,19 @@ def test_defaults_and_sizes(c2):
     assert c2.lib().csa2_status_string(3) == b"workspace too small"
 
 
+def test_topk_kernel_choice(c2):
+    """csa2_set_topk_kernel takes 0 (automatic), 1 (a cluster per row) or 2
+    (a CTA per row) and rejects anything else; the choice is host state."""
+    L = c2.lib()
+    for v in (1, 2, 0):
+        assert L.csa2_set_topk_kernel(v) == 0
+    for v in (-1, 3, 100):
+        assert L.csa2_set_topk_kernel(v) == c2.lib().csa2_set_topk_kernel(v) != 0
+    with pytest.raises(c2.Csa2Error):
+        c2.set_topk_kernel(7)
+    c2.set_topk_kernel(c2.TOPK_AUTO)
+
+
 def test_workspace_sizes(c2):
     p = c2.Params.make()
     for op in range(4):
