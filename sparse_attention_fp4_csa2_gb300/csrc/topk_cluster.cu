@@ -94,10 +94,21 @@ __device__ __forceinline__ uint32_t level_digit(uint32_t key, int level) {
 }
 
 // Histogram add of the warp's 32 bins (kBins: none), aggregated over equal
-// bins -- for keys that crowd into a few bins (the top 11 key bits).
+// bins -- for keys that crowd into a few bins (the top 11 key bits of the
+// gathered candidates).
 __device__ __forceinline__ void hist_add(uint32_t *h, uint32_t bin, int lane) {
   const uint32_t peers = __match_any_sync(0xffffffffu, bin);
   if (bin < kBins && lane == __ffs(peers) - 1) atomicAdd(&h[bin], (uint32_t)__popc(peers));
+}
+
+// The lanes sharing lane 0's bin add as one atomic, the others one each --
+// for the sample's top bits, spread over many bins, where grouping every
+// distinct bin costs more than it saves.
+__device__ __forceinline__ void hist_add_lead(uint32_t *h, uint32_t bin, int lane) {
+  const uint32_t b0 = __shfl_sync(0xffffffffu, bin, 0);
+  const uint32_t same = __ballot_sync(0xffffffffu, bin == b0);
+  if (lane == 0 && b0 < kBins) atomicAdd(&h[b0], (uint32_t)__popc(same));
+  if (bin != b0 && bin < kBins) atomicAdd(&h[bin], 1u);
 }
 
 // The same without aggregation -- for the finer levels, where a warp's bins
@@ -233,7 +244,7 @@ __device__ __forceinline__ void sample_hist(TopkClusterSmem &S, const float *val
                            : lvl == 0 ? (key >> 21)
                            : (key >> 21) == b0 ? ((key >> 10) & 2047u) : (uint32_t)kBins;
       if (lvl == 0)
-        hist_add(S.hist, bin, lane);
+        hist_add_lead(S.hist, bin, lane);
       else
         hist_add_plain(S.hist, bin);
     }
