@@ -203,11 +203,16 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
     load_bf16x16(z + (e * 2 + 1) * D + c0, z1);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
-      // explicit IEEE double ops: no contraction into fused multiply-adds
+      // explicit IEEE double ops: no contraction into fused multiply-adds.
+      // The larger logit's exponent is exp(0) = 1 exactly, so only the other
+      // one is evaluated, and its weight 1 / den is the correctly rounded
+      // reciprocal (the same values as two exps and two divisions).
       const double zm = fmax((double)z0[i], (double)z1[i]);
-      const double ea = exp(__dsub_rn((double)z0[i], zm)), eb = exp(__dsub_rn((double)z1[i], zm));
-      const double den = __dadd_rn(ea, eb);
-      const double wa = __ddiv_rn(ea, den), wb = __ddiv_rn(eb, den);
+      const bool first = (double)z0[i] >= (double)z1[i];
+      const double eo = exp(__dsub_rn(first ? (double)z1[i] : (double)z0[i], zm));
+      const double den = __dadd_rn(1.0, eo);
+      const double w_one = __drcp_rn(den), w_other = __ddiv_rn(eo, den);
+      const double wa = first ? w_one : w_other, wb = first ? w_other : w_one;
       const double num = __dadd_rn(__dmul_rn(wa, (double)x0[i]), __dmul_rn(wb, (double)x1[i]));
       x[i] = __double2float_rn(num);
     }
