@@ -547,6 +547,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   __syncwarp();
   if (a.C > 1) cluster_arrive();
+  // the previous kernel in the stream is complete past here (programmatic
+  // launch: everything above touches only this CTA's shared memory)
+  pdl_enter();
 
   // The first block's row of this thread: row tid / 2 for the workers, and
   // in a single block row 128 + (tid - 288) / 2 for warps 9 and 10
@@ -1073,19 +1076,7 @@ cudaError_t launch_sparse_attn(AttnArgs a, void *scratch, cudaStream_t stream, i
   if (err != cudaSuccess) return err;
   const ProfileEvents &pe = profile_events(CSA2_KERNEL_SPARSE_ATTN);
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)a.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  err = cudaLaunchKernelEx(&cfg, kern, tm_q, a);
+  err = launch_pdl(kern, dim3((unsigned)grid), dim3(kThreads), kSmemBytes, stream, (unsigned)a.C, tm_q, a);
   if (err != cudaSuccess) return err;
   ++*launches;
   if (pe.stop && (err = record_profile_event(pe.stop, stream)) != cudaSuccess) return err;

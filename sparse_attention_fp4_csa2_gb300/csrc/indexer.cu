@@ -136,6 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_q);
   }
+  // the inputs' producer is complete past here (programmatic launch)
+  pdl_wait();
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, 64);
     tmem_relinquish();
@@ -297,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&S.empty[s]);
         mma_commit(&S.accfull[acc]);
       }
+      pdl_release();   // the last tile's MMAs are issued: the next kernel's CTAs may be dispatched
       // every MMA has completed before TMEM is released
       mma_commit(&S.mma_done);
       mbar_wait(&S.mma_done, 0);
@@ -354,16 +357,16 @@ cudaError_t launch_indexer_sweep(const CUtensorMap &tm_k, const CUtensorMap &tm_
     err = cudaFuncSetAttribute(indexer_sweep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    indexer_sweep_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
+    err = launch_pdl(indexer_sweep_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, stream, 0u, tm_k, tm_q, a);
   } else {
     err = cudaFuncSetAttribute(indexer_sweep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    indexer_sweep_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
+    err = launch_pdl(indexer_sweep_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, stream, 0u, tm_k, tm_q, a);
   }
+  if (err != cudaSuccess) return err;
   ++*launches;
-  err = cudaGetLastError();
-  if (err == cudaSuccess && pe.stop) err = record_profile_event(pe.stop, stream);
+  if (pe.stop) err = record_profile_event(pe.stop, stream);
   return err;
 }
 

@@ -148,6 +148,7 @@ __device__ __forceinline__ void load_bf16x4(const __nv_bfloat16 *p, float (&x)[4
 __global__ void __launch_bounds__(256) indexer_k_quant_kernel(const __nv_bfloat16 *__restrict__ k, int64_t n,
                                                               const int64_t *__restrict__ slot,
                                                               uint8_t *__restrict__ planes, int64_t rows) {
+  pdl_wait();   // the inputs' producer is complete past here (programmatic launch)
   const int lane = threadIdx.x & 31;
   const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= n) return;   // warp-uniform
@@ -169,6 +170,7 @@ __global__ void __launch_bounds__(256) indexer_k_quant_kernel(const __nv_bfloat1
 __global__ void __launch_bounds__(256) indexer_q_fp4_kernel(const __nv_bfloat16 *__restrict__ q,
                                                             const float *__restrict__ w, int64_t rows,
                                                             uint8_t *__restrict__ out, float *__restrict__ wq) {
+  pdl_wait();   // the inputs' producer is complete past here (programmatic launch)
   const int lane = threadIdx.x & 31;
   const int64_t i = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (i >= rows) return;
@@ -230,6 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_q);
   }
+  // the inputs' producer is complete past here (programmatic launch)
+  pdl_wait();
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
@@ -364,6 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&S.tile_empty[st]);
         mma_commit(&S.accfull[acc]);
       }
+      pdl_release();   // the last tile's MMAs are issued: the next kernel's CTAs may be dispatched
       mma_commit(&S.mma_done);
       mbar_wait(&S.mma_done, 0);
     }
@@ -494,18 +499,16 @@ cudaError_t launch_indexer_k_quant(const void *k, int64_t n, const int64_t *slot
                                    cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   const int warps = 8;
-  indexer_k_quant_kernel<<<(unsigned)((n + warps - 1) / warps), warps * 32, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(k), n, slot, k_fp4, rows);
-  return cudaGetLastError();
+  return launch_pdl(indexer_k_quant_kernel, dim3((unsigned)((n + warps - 1) / warps)), dim3(warps * 32), 0, stream,
+                    0u, static_cast<const __nv_bfloat16 *>(k), n, slot, k_fp4, rows);
 }
 
 cudaError_t launch_indexer_q_fp4(const void *q, const float *w, int64_t rows, void *q_e5m2, float *wq,
                                  cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   const int warps = 8;
-  indexer_q_fp4_kernel<<<(unsigned)((rows + warps - 1) / warps), warps * 32, 0, stream>>>(
-      static_cast<const __nv_bfloat16 *>(q), w, rows, static_cast<uint8_t *>(q_e5m2), wq);
-  return cudaGetLastError();
+  return launch_pdl(indexer_q_fp4_kernel, dim3((unsigned)((rows + warps - 1) / warps)), dim3(warps * 32), 0,
+                    stream, 0u, static_cast<const __nv_bfloat16 *>(q), w, rows, static_cast<uint8_t *>(q_e5m2), wq);
 }
 
 cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
@@ -520,16 +523,18 @@ cudaError_t launch_indexer_sweep_fp4(const CUtensorMap &tm_k, const CUtensorMap 
     err = cudaFuncSetAttribute(indexer_sweep_fp4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    indexer_sweep_fp4_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
+    err = launch_pdl(indexer_sweep_fp4_kernel<true>, dim3(grid), dim3(kThreads), kSmemBytes, stream, 0u, tm_k, tm_q,
+                     a);
   } else {
     err = cudaFuncSetAttribute(indexer_sweep_fp4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)kSmemBytes);
     if (err != cudaSuccess) return err;
-    indexer_sweep_fp4_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
+    err = launch_pdl(indexer_sweep_fp4_kernel<false>, dim3(grid), dim3(kThreads), kSmemBytes, stream, 0u, tm_k, tm_q,
+                     a);
   }
+  if (err != cudaSuccess) return err;
   ++*launches;
-  err = cudaGetLastError();
-  if (err == cudaSuccess && pe.stop) err = record_profile_event(pe.stop, stream);
+  if (pe.stop) err = record_profile_event(pe.stop, stream);
   return err;
 }
 

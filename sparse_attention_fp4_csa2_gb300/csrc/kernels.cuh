@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <utility>
 
 #include "ptx.cuh"
 
@@ -64,6 +65,34 @@ void set_last_launch_count(int32_t n);
 // Records `ev` on `stream`; inside a stream capture it becomes an event-record
 // node of the graph, so every replay records it.
 cudaError_t record_profile_event(cudaEvent_t ev, cudaStream_t stream);
+
+// Launches `kern` with programmatic stream serialisation (the kernel enters
+// through pdl_enter / pdl_wait before touching global memory) and, when
+// cluster_x > 0, thread-block clusters of cluster_x CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              unsigned cluster_x, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // 2-D bf16 tensor map over rows of `inner` elements, box {64, box_rows}, 128B swizzle.
 bool make_tmap_bf16(CUtensorMap *m, const void *ptr, int64_t inner, int64_t rows, uint32_t box_rows);

@@ -145,6 +145,7 @@ __global__ void __launch_bounds__(256) kv_quant_write_kernel(const __nv_bfloat16
                                                              const int64_t *__restrict__ slot,
                                                              uint8_t *__restrict__ kv, int64_t kv_rows,
                                                              const RopeFreqs freqs, const IkOut ik) {
+  pdl_wait();   // the inputs' producer is complete past here (programmatic launch)
   const int lane = threadIdx.x & 31;
   // one entry per warp; when projecting, one entry per block of 4 warps:
   // warp 0 writes the entry, then each warp projects 32 rows of W_ik
@@ -280,15 +281,13 @@ cudaError_t launch_kv_quant_write(const void *latent, const void *z, int m, int6
     cudaError_t err = cudaFuncSetAttribute(kv_quant_write_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            smem);
     if (err != cudaSuccess) return err;
-    kv_quant_write_kernel<true><<<(unsigned)n_entries, (DI / 32) * 32, smem, stream>>>(
-        static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
-        kv, kv_rows, freqs, ik);
-  } else {
-    kv_quant_write_kernel<false><<<(unsigned)blocks, warps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries, pos, slot,
-        kv, kv_rows, freqs, ik);
+    return launch_pdl(kv_quant_write_kernel<true>, dim3((unsigned)n_entries), dim3((DI / 32) * 32), smem, stream, 0u,
+                      static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries,
+                      pos, slot, kv, kv_rows, freqs, ik);
   }
-  return cudaGetLastError();
+  return launch_pdl(kv_quant_write_kernel<false>, dim3((unsigned)blocks), dim3(warps * 32), 0, stream, 0u,
+                    static_cast<const __nv_bfloat16 *>(latent), static_cast<const __nv_bfloat16 *>(z), m, n_entries,
+                    pos, slot, kv, kv_rows, freqs, ik);
 }
 
 }  // namespace csa2

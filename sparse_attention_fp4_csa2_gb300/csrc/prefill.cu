@@ -102,6 +102,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_q);
   }
+  // the inputs' producer is complete past here (programmatic launch)
+  pdl_wait();
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, 2 * kN);
     tmem_relinquish();
@@ -179,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&S.qempty);
         if (stop) { abort_flag(S) = 1; break; }
       }
+      pdl_release();   // the last item's MMAs are issued: the next kernel's CTAs may be dispatched
       mma_commit(&S.mma_done);
       mbar_wait(&S.mma_done, 0);
     }
@@ -269,10 +272,10 @@ cudaError_t launch_prefill_indexer(const CUtensorMap &tm_k, const CUtensorMap &t
   const int grid = (int)(n_items < num_sms ? n_items : num_sms);
   const ProfileEvents &pe = profile_events(CSA2_KERNEL_PREFILL_INDEXER);
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-  prefill_indexer_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tm_k, tm_q, a);
+  err = launch_pdl(prefill_indexer_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, 0u, tm_k, tm_q, a);
+  if (err != cudaSuccess) return err;
   ++*launches;
-  err = cudaGetLastError();
-  if (err == cudaSuccess && pe.stop) err = record_profile_event(pe.stop, stream);
+  if (pe.stop) err = record_profile_event(pe.stop, stream);
   return err;
 }
 

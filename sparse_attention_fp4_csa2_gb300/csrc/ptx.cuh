@@ -28,6 +28,30 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream
+// serialisation (launch_pdl): its CTAs may be dispatched while the kernel
+// before it in the stream is still running.  pdl_wait (griddepcontrol.wait)
+// blocks the thread until every grid this launch depends on has completed and
+// its memory is visible; it returns at once when there is none.  Each kernel
+// calls it before its first global-memory access and before it allocates
+// tensor memory, so a CTA dispatched early holds only shared memory and
+// registers while it waits, and no two kernels past their waits run at once.
+// pdl_release (griddepcontrol.launch_dependents) lets the next kernel's CTAs
+// be dispatched once every CTA of this grid has issued it or exited (the
+// first thread of a CTA to issue it counts for the CTA).  The readout
+// releases on entry: the next kernel's CTAs cannot share an SM with it, so
+// they take each SM it leaves.  The other kernels release late -- the sweeps
+// once their last MMAs are issued, a top-K once its row is read (the cluster
+// kernel's leader before it selects alone) -- since CTAs that wait beside a
+// running kernel's CTAs for its whole length slowed the steps.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_release();
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");

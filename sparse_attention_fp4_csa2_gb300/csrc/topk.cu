@@ -60,6 +60,7 @@ __device__ __forceinline__ void load_keys(const TopkRows &r, const float *row, i
 
 __global__ void __launch_bounds__(kHistThreads) topk_hist_kernel(const TopkRows r, TopkScratch s) {
   __shared__ uint32_t hist[TOPK_BINS];
+  pdl_wait();   // the inputs' producer is complete past here (programmatic launch)
   const int row = blockIdx.y;
   for (int i = threadIdx.x; i < TOPK_BINS; i += kHistThreads) hist[i] = 0;
   __syncthreads();
@@ -131,6 +132,7 @@ __global__ void __launch_bounds__(kHistThreads) topk_select_kernel(const TopkRow
   __shared__ uint32_t scan[kHistThreads / 32];
   __shared__ int T_sh;
   __shared__ uint32_t above_sh;
+  pdl_wait();   // the histograms are complete past here (programmatic launch)
   const int row = blockIdx.y;
   find_threshold(s.hist + (int64_t)row * TOPK_BINS, r.k, &T_sh, &above_sh, scan);
   const int T = T_sh;
@@ -190,6 +192,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(const TopkRows
   __shared__ int digit_sh;
   __shared__ uint32_t above_sh;
   __shared__ int last_sh;
+  pdl_wait();   // the selection counts are complete past here (programmatic launch)
 
   const int row = blockIdx.x;
   const uint32_t *cnt = s.counters + (int64_t)row * 4;
@@ -331,6 +334,7 @@ __global__ void __launch_bounds__(kFinThreads) topk_finish_kernel(const TopkRows
 // Rows of block scores with the forced block set to +inf, padded with -inf
 // to `stride` (a multiple of 4) values: the input of the cluster top-K.
 __global__ void __launch_bounds__(256) pool_force_copy_kernel(const TopkRows r, float *dst, int64_t stride) {
+  pdl_wait();   // the block scores' producer is complete past here (programmatic launch)
   const int row = blockIdx.y;
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= stride) return;
@@ -351,10 +355,9 @@ cudaError_t launch_pool_topk(const TopkRows &r, void *scratch, int num_sms, cuda
   float *copy = static_cast<float *>(scratch);
   if (stride > 0) {
     dim3 grid((unsigned)((stride + 255) / 256), (unsigned)r.rows);
-    pool_force_copy_kernel<<<grid, 256, 0, stream>>>(r, copy, stride);
-    ++*launches;
-    cudaError_t err = cudaGetLastError();
+    cudaError_t err = launch_pdl(pool_force_copy_kernel, grid, dim3(256), 0, stream, 0u, r, copy, stride);
     if (err != cudaSuccess) return err;
+    ++*launches;
   }
   TopkRows c = r;
   c.vals = copy;
@@ -395,8 +398,10 @@ cudaError_t launch_topk(const TopkRows &r, const TopkScratch &s, int num_sms, cu
   const int64_t chunks = (r.row_len + kChunk - 1) / kChunk;
   if (chunks > 0) {
     dim3 grid((unsigned)chunks, (unsigned)r.rows);
-    topk_hist_kernel<<<grid, kHistThreads, 0, stream>>>(r, s);
-    topk_select_kernel<<<grid, kHistThreads, 0, stream>>>(r, s);
+    err = launch_pdl(topk_hist_kernel, grid, dim3(kHistThreads), 0, stream, 0u, r, s);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(topk_select_kernel, grid, dim3(kHistThreads), 0, stream, 0u, r, s);
+    if (err != cudaSuccess) return err;
     *launches += 2;
   }
   int P = 1;
@@ -404,9 +409,10 @@ cudaError_t launch_topk(const TopkRows &r, const TopkScratch &s, int num_sms, cu
   const size_t smem = (size_t)kCandSmem * 8 + (size_t)P * 4;
   err = cudaFuncSetAttribute(topk_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  topk_finish_kernel<<<r.rows, kFinThreads, smem, stream>>>(r, s);
+  err = launch_pdl(topk_finish_kernel, dim3((unsigned)r.rows), dim3(kFinThreads), smem, stream, 0u, r, s);
+  if (err != cudaSuccess) return err;
   ++*launches;
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace csa2

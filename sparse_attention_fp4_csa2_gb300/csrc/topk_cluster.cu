@@ -528,16 +528,6 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
   // a slice of one round stays in registers from here: the sample and the
   // filter read it there
   const bool one_round = hi - lo <= kRound;
-  float4 vr[kVec];
-  if (one_round) {
-    load_round(vals, lo, hi, vr);
-  } else if (tid == 0) {
-    // a longer slice is read three times (two sample levels, the filter):
-    // bring all of it into L2 now, one round (32 KB) per bulk prefetch
-    for (int64_t b = lo; b < hi; b += kRound)
-      prefetch_l2_bulk(vals + b, (uint32_t)(4 * (hi - b < kRound ? hi - b : kRound)));
-  }
-
   for (int i = tid; i < kBins; i += kThreads) {
     S.hist[i] = 0;
     S.tot[0][i] = 0;
@@ -553,6 +543,17 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
     S.n_sel = 0;
     S.n_tie = 0;
     S.g_used = 0;
+  }
+  // the scores' producer is complete past here (programmatic launch)
+  pdl_wait();
+  float4 vr[kVec];
+  if (one_round) {
+    load_round(vals, lo, hi, vr);
+  } else if (tid == 0) {
+    // a longer slice is read three times (two sample levels, the filter):
+    // bring all of it into L2 now, one round (32 KB) per bulk prefetch
+    for (int64_t b = lo; b < hi; b += kRound)
+      prefetch_l2_bulk(vals + b, (uint32_t)(4 * (hi - b < kRound ? hi - b : kRound)));
   }
   cluster_sync();   // every CTA's totals are cleared before anyone pushes
 
@@ -656,7 +657,10 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
   if (!overflow && total_cand >= (uint32_t)r.k && total_cand <= (uint32_t)kGather) {
     // every candidate is in the leader, which selects alone; the other CTAs
     // are done (nothing reads their memory any more)
-    if (crank == 0) leader_select(S, r, row, nctas);
+    if (crank == 0) {
+      pdl_release();   // the next kernel's CTAs may take the SMs the others leave
+      leader_select(S, r, row, nctas);
+    }
     return;
   }
 
@@ -697,22 +701,11 @@ cudaError_t launch_topk_cluster(const TopkRows &r, cudaStream_t stream, int *lau
   const int64_t fill = 3 * (int64_t)sms / r.rows;   // three CTAs fit on an SM
   if (c > fill) c = fill;
   if (c < 1) c = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)c, (unsigned)r.rows, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)c;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   static const ProfileEvents kNone;
   const ProfileEvents &pe = profiled ? profile_events(CSA2_KERNEL_TOPK) : kNone;
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-  err = cudaLaunchKernelEx(&cfg, topk_cluster_kernel, r);
+  err = launch_pdl(topk_cluster_kernel, dim3((unsigned)c, (unsigned)r.rows), dim3(kThreads), smem, stream,
+                   (unsigned)c, r);
   if (err != cudaSuccess) return err;
   ++*launches;
   if (pe.stop) err = record_profile_event(pe.stop, stream);

@@ -322,14 +322,16 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
   const int64_t n = r.row_len;
   const uint32_t k = (uint32_t)r.k;
 
+  if (tid < kStages) mbar_init(&S.full[tid], 1);
+  for (int i = tid; i < kRBins; i += kRT) S.hist[i] = 0;
+  fence_barrier_init();
+  // the scores' producer is complete past here (programmatic launch)
+  pdl_wait();
   // the whole row heads for L2 at once (the filter reads it again after the
   // sample levels): one bulk prefetch per chunk
   if (tid == 0)
     for (int64_t c = 0; c * kChunk < n; ++c)
       prefetch_l2_bulk(vals + c * kChunk, (uint32_t)(4 * min((int64_t)kChunk, n - c * kChunk)));
-  if (tid < kStages) mbar_init(&S.full[tid], 1);
-  for (int i = tid; i < kRBins; i += kRT) S.hist[i] = 0;
-  fence_barrier_init();
   __syncthreads();
 
   // ------------------------------------------------------------ 1. sample
@@ -454,6 +456,8 @@ __global__ void __launch_bounds__(kRT, 2) topk_row_kernel(const TopkRows r) {
   // the list holds every key of the top k when it did not overflow and has
   // at least k keys, or every valid key of the row (t_low = 1)
   const bool from_list = ccount <= (uint32_t)kRCand && (ccount >= k || t_low == 1);
+
+  pdl_release();   // the row is read: the next kernel's CTAs may be dispatched
 
   // --------------------------------------------------------- 3./4. select
   // T: the k-th largest key; keys above T are taken, and of the keys equal
@@ -611,8 +615,7 @@ cudaError_t launch_topk_row(const TopkRows &r, cudaStream_t stream, int *launche
   static const ProfileEvents kNone;
   const ProfileEvents &pe = profiled ? profile_events(CSA2_KERNEL_TOPK) : kNone;
   if (pe.start && (err = record_profile_event(pe.start, stream)) != cudaSuccess) return err;
-  topk_row_kernel<<<(unsigned)r.rows, kRT, kRowSmem, stream>>>(r);
-  err = cudaGetLastError();
+  err = launch_pdl(topk_row_kernel, dim3((unsigned)r.rows), dim3(kRT), kRowSmem, stream, 0u, r);
   if (err != cudaSuccess) return err;
   ++*launches;
   if (pe.stop) err = record_profile_event(pe.stop, stream);
