@@ -195,7 +195,14 @@ csa2_status csa2_indexer_k_quant(const void *k, int64_t n, const int64_t *slot, 
  *     per block of 8 positions the max (or sum) of its visible scores, -inf
  *     for blocks with no visible position -- the HSI block scores.
  *   ws / ws_bytes: scratch of at least csa2_workspace_bytes(...) bytes,
- *     256-byte aligned; contents need no initialisation.
+ *     256-byte aligned.  Its contents never change a result.  The bf16 sweep
+ *     counts each row's scores by key range at the start of the workspace
+ *     for the top-K, which then needs no sample of the row, and the top-K
+ *     leaves those counts zero; a workspace that starts zeroed (or was last
+ *     used by this entry point with the same batch and n_max) gives the
+ *     first call that benefit too, any other contents only make that call's
+ *     selection take a slower path.  csa2_sparse_decode keeps the same counts
+ *     in its own workspace, in a place its other steps leave untouched.
  */
 csa2_status csa2_indexer_score_topk(const void *q_idx, const float *w, const void *k_idx,
                                     int32_t batch, int64_t cap, const int32_t *n_vis,

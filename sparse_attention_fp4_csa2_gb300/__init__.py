@@ -133,11 +133,13 @@ def workspace_bytes(op: int, batch: int, n_max: int, params: Params) -> int:
 
 
 def workspace(op: int, batch: int, n_max: int, params: Params, device=None) -> torch.Tensor:
-    """A caller-owned scratch buffer of the size the operation needs."""
+    """A caller-owned scratch buffer of the size the operation needs, zeroed
+    (the indexer keeps per-row counts in it between its kernels and leaves
+    them zero: a zeroed buffer lets the first call use them too)."""
     n = workspace_bytes(op, batch, n_max, params)
     if n == 0:
         raise Csa2Error("invalid workspace request")
-    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
 
 
 def get_device_status(stream=None) -> int:

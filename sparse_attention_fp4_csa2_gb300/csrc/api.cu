@@ -117,17 +117,24 @@ bool params_ok(const csa2_params *p) {
 }
 
 // ------------------------------------------------------------ workspace
+// The rows' score histograms, handed from the sweep to the top-K: at the
+// start of the indexer's workspace, in the same place for Full and Reindex
+// calls, and kept out of the pool selection's and the readout's scratch in a
+// decode call (the top-K leaves them zero for the next call).
+size_t hist_ws(int32_t batch) { return (size_t)round_up((int64_t)batch * TOPK_HIST_BINS * 4, 256); }
+
 struct IndexerLayout {
   int64_t row_len;       // scores per row
-  size_t scores_off, q8_off, wq_off, end;
+  size_t hist_off, scores_off, q8_off, wq_off, end;
 };
 
 IndexerLayout indexer_layout(int32_t batch, int64_t n_max, const csa2_params *p, bool pool) {
   IndexerLayout L;
   const bool fp4 = p->indexer_fp4 != 0;
   L.row_len = pool ? (int64_t)p->candidate_topk_blocks * BLOCK : round_up(n_max, fp4 ? FP4_SWEEP_TILE : SWEEP_TILE);
-  L.scores_off = 0;
-  L.q8_off = (size_t)round_up((int64_t)batch * L.row_len * 4, 256);
+  L.hist_off = 0;
+  L.scores_off = hist_ws(batch);
+  L.q8_off = L.scores_off + (size_t)round_up((int64_t)batch * L.row_len * 4, 256);
   // MXFP4 indexer: the queries' E5M2 rows and the head weights with their
   // row exponents folded in; the cluster top-K needs no scratch beyond the scores
   L.wq_off = L.q8_off + (fp4 ? (size_t)round_up((int64_t)batch * HI * DI, 256) : 0);
@@ -153,10 +160,11 @@ size_t attn_ws(int32_t batch, const csa2_params *p) {
 size_t decode_ws(int32_t batch, int64_t n_max, const csa2_params *p) {
   const int64_t nblk = (n_max + BLOCK - 1) / BLOCK;
   size_t bs = (size_t)round_up((int64_t)batch * nblk * 4, 256);
-  size_t a = indexer_ws(batch, n_max, p), b = pool_ws(batch, n_max, p), c = attn_ws(batch, p);
+  const size_t h = hist_ws(batch);
+  size_t a = indexer_ws(batch, n_max, p) - h, b = pool_ws(batch, n_max, p), c = attn_ws(batch, p);
   size_t m = a > b ? a : b;
   m = m > c ? m : c;
-  return bs + m;
+  return bs + h + m;
 }
 
 constexpr int64_t kPrefillBlock = 1024;   // query tokens per indexer / top-K / attention block
@@ -220,11 +228,6 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   a.block_reduce = p->block_reduce;
   a.k_scales = fp4 ? static_cast<const uint8_t *>(k_idx) + (int64_t)batch * cap * (DI / 2) : nullptr;
   a.k_rows = (int64_t)batch * cap;
-  const int sms = num_sms();
-  cudaError_t e = fp4 ? launch_indexer_sweep_fp4(tm_k, tm_q, a, sms, stream, launches)
-                      : launch_indexer_sweep(tm_k, tm_q, a, sms, stream, launches);
-  if (e != cudaSuccess) return CSA2_ERR_CUDA;
-
   TopkRows r;
   r.vals = scores;
   r.row_len = L.row_len;
@@ -237,6 +240,16 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   r.pool = pool_blocks;
   r.pool_stride = p->candidate_topk_blocks;
   r.out = topk_idx;
+  // the bf16 sweep counts the rows' keys for the cluster top-K, which then
+  // needs no sample of the scores (and clears the counts)
+  if (!fp4 && topk_cluster_supported(r) && topk_runs_cluster(r)) {
+    r.hist = reinterpret_cast<uint32_t *>(wsb + L.hist_off);
+    a.hist = r.hist;
+  }
+  const int sms = num_sms();
+  cudaError_t e = fp4 ? launch_indexer_sweep_fp4(tm_k, tm_q, a, sms, stream, launches)
+                      : launch_indexer_sweep(tm_k, tm_q, a, sms, stream, launches);
+  if (e != cudaSuccess) return CSA2_ERR_CUDA;
   return cuda_status(launch_topk(r, stream, launches));
 }
 
@@ -479,21 +492,23 @@ csa2_status csa2_sparse_decode(csa2_mode mode, const csa2_params *params, int32_
   const int64_t nblk = (n_max + BLOCK - 1) / BLOCK;
   const size_t bs_bytes = (size_t)round_up((int64_t)batch * nblk * 4, 256);
   float *bscores = reinterpret_cast<float *>(wsb);
-  uint8_t *rest = wsb + bs_bytes;
+  uint8_t *rest = wsb + bs_bytes;   // the indexer's workspace, its histograms first
   const size_t rest_bytes = ws_bytes - bs_bytes;
+  uint8_t *after_hist = rest + hist_ws(batch);   // the pool selection's and the readout's scratch
+  const size_t after_bytes = rest_bytes - hist_ws(batch);
   int launches = 0;
   csa2_status s = CSA2_OK;
   if (mode == CSA2_MODE_FULL) {
     s = run_indexer(q_idx, w, k_idx, batch, cap, n_vis, n_max, nullptr, params, topk_idx,
                     params->hsi ? bscores : nullptr, rest, rest_bytes, st, &launches);
     if (s == CSA2_OK && params->hsi)
-      s = run_pool(bscores, n_vis, batch, n_max, params, pool_blocks, rest, rest_bytes, st, &launches);
+      s = run_pool(bscores, n_vis, batch, n_max, params, pool_blocks, after_hist, after_bytes, st, &launches);
   } else if (mode == CSA2_MODE_REINDEX) {
     s = run_indexer(q_idx, w, k_idx, batch, cap, n_vis, n_max, pool_blocks, params, topk_idx, nullptr, rest,
                     rest_bytes, st, &launches);
   }
   if (s == CSA2_OK)
-    s = run_attn(params, batch, q, kv, cap, topk_idx, swa, swa_scale, swa_len, out, lse, rest, rest_bytes, st,
+    s = run_attn(params, batch, q, kv, cap, topk_idx, swa, swa_scale, swa_len, out, lse, after_hist, after_bytes, st,
                  &launches);
   if (s == CSA2_OK) g_last_launches = launches;
   return s;

@@ -41,6 +41,8 @@ struct __align__(8) SweepSmem {
   uint64_t accfull[2];
   uint64_t accempty[2];
   uint64_t mma_done;
+  uint64_t hseg[2];    // histogram slot: the four epilogue warps are done adding to it
+  uint64_t hfree[2];   // histogram slot: flushed and cleared
   uint32_t tmem_base;
   uint32_t abort;
 };
@@ -49,7 +51,10 @@ __device__ __forceinline__ volatile uint32_t &abort_flag(SweepSmem &S) {
   return *reinterpret_cast<volatile uint32_t *>(&S.abort);
 }
 
-constexpr size_t kSmemBytes = 1024 /*align slack*/ + (size_t)kStages * kTileBytes + 2 * kQBytes + sizeof(SweepSmem);
+constexpr size_t kHistOff = (sizeof(SweepSmem) + 15) / 16 * 16;   // after the control block
+constexpr size_t kSmemBytes =
+    1024 /*align slack*/ + (size_t)kStages * kTileBytes + 2 * kQBytes + kHistOff + 2 * TOPK_HIST_BINS * 2;
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 
 __device__ __forceinline__ int32_t clamp_nvis(const int32_t *n_vis, int b, int64_t n_max) {
   int32_t v = __ldg(n_vis + b);
@@ -63,19 +68,22 @@ __device__ __forceinline__ int32_t clamp_nvis(const int32_t *n_vis, int b, int64
 // Row r of tile t of sequence b: score = sum_h w_h ReLU(dot_h) ("DeepSeek-
 // V4.1-Flash - Architecture", section 2), -inf where the position is not
 // visible; the Full sweep also writes the max (or sum) over each block of 8
-// ("DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression", 2.3.4).
+// ("DeepSeek-v4.1 Flash: Pushing the Limits of KV Cache Compression", 2.3.4),
+// and counts the score's key in the row's histogram when one is kept.
 // Called by all 32 lanes of a warp (the block reduction shuffles).
 template <bool kPool>
 __device__ __forceinline__ void sweep_store_row(const SweepArgs &a, int b, int t, int r, int lane, int32_t nv,
-                                                const float (&wv)[HI], const uint32_t (&v)[32]) {
+                                                const float (&wv)[HI], const uint32_t (&v)[32], uint32_t *hs) {
   float sc = 0.0f;
 #pragma unroll
   for (int h = 0; h < HI; ++h) sc = fmaf(wv[h], fmaxf(__uint_as_float(v[h]), 0.0f), sc);
   float *srow = a.scores + (int64_t)b * a.row_len;
+  float stored;
   if (!kPool) {
     const int64_t pos = (int64_t)t * SWEEP_TILE + r;
     const bool valid = pos < nv;
-    srow[pos] = valid ? sc : -INFINITY;
+    stored = valid ? sc : -INFINITY;
+    srow[pos] = stored;
     if (a.block_scores) {
       float bv;
       if (a.block_reduce == 0) {
@@ -99,8 +107,50 @@ __device__ __forceinline__ void sweep_store_row(const SweepArgs &a, int b, int t
     const int32_t blk = __ldg(a.pool + (int64_t)b * a.pool_nb + slot / BLOCK);
     const int64_t pos = (int64_t)blk * BLOCK + (r & (BLOCK - 1));
     const bool valid = blk >= 0 && pos < nv;
-    srow[slot] = valid ? sc : -INFINITY;
+    stored = valid ? sc : -INFINITY;
+    srow[slot] = stored;
   }
+  if (hs) {
+    // the row's histogram for its top-K, in this CTA's shared memory: 16-bit
+    // counts, two bins to a word
+    const uint32_t key = topk_score_key(stored);
+    if (key) {
+      const uint32_t bin = key >> (32 - TOPK_HIST_BITS);
+      atomicAdd(hs + (bin >> 1), (bin & 1u) ? 0x10000u : 1u);
+    }
+  }
+}
+
+// The shared-memory histogram of the sweep: two slots of TOPK_HIST_BINS
+// 16-bit counts, used by segments of a CTA's tiles (a segment: the tiles of
+// one row, at most kSegTiles of them, so that no count passes 65,535).
+constexpr int kSegTiles = 256;
+constexpr int kHistWords = TOPK_HIST_BINS / 2;   // per slot
+
+// End of histogram segment `seg` (slot seg & 1) for row `row`, by each of
+// the four epilogue warps (quadrant `quad`): once all four are done adding
+// (hseg), each adds its quarter of the slot into the row's global histogram
+// and clears it, then marks it free (hfree) for segment seg + 2.
+__device__ __forceinline__ void hist_segment_end(SweepSmem &S, uint32_t *hist_s, uint32_t *g, int seg, int quad,
+                                                 int lane) {
+  const int p = seg & 1;
+  const uint32_t use = (uint32_t)(seg >> 1) & 1u;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&S.hseg[p]);
+  mbar_wait(&S.hseg[p], use);
+  uint32_t *hs = hist_s + p * kHistWords;
+  constexpr int kQuarter = kHistWords / 4;
+#pragma unroll 4
+  for (int i = quad * kQuarter + lane; i < (quad + 1) * kQuarter; i += 32) {
+    const uint32_t c = hs[i];
+    if (c) {
+      hs[i] = 0u;
+      if (c & 0xFFFFu) atomicAdd(g + 2 * i, c & 0xFFFFu);
+      if (c >> 16) atomicAdd(g + 2 * i + 1, c >> 16);
+    }
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&S.hfree[p]);
 }
 
 template <bool kPool>
@@ -112,6 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *kbuf = base;                                  // kStages x 32 KB, 1024-aligned
   uint8_t *qbuf = base + (size_t)kStages * kTileBytes;   // 2 x 8 KB
   SweepSmem &S = *reinterpret_cast<SweepSmem *>(qbuf + 2 * kQBytes);
+  // the rows' histogram slots (two, by segment parity) when the top-K takes one
+  uint32_t *hist_s = reinterpret_cast<uint32_t *>(qbuf + 2 * kQBytes + kHistOff);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t total = (int64_t)a.batch * a.tiles_per_seq;
@@ -131,11 +183,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&S.accempty[i], 4 * 32);
     }
     mbar_init(&S.mma_done, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.hseg[i], 4);
+      mbar_init(&S.hfree[i], 4);
+    }
     abort_flag(S) = 0;
     fence_barrier_init();
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_q);
   }
+  if (a.hist)
+    for (int i = threadIdx.x; i < 2 * kHistWords; i += kThreads) hist_s[i] = 0u;
   // the inputs' producer is complete past here (programmatic launch)
   pdl_wait();
   if (warp == 1) {
@@ -311,10 +369,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     int prev_b = -1;
     int32_t nv = 0;
     float wv[HI];
+    int seg = -1, seg_left = 0;   // histogram segment: its parity picks the slot
     for (int64_t it = it0; it < it1; ++it) {
       if (abort_flag(S)) break;
       const int b = (int)(it / a.tiles_per_seq);
       const int t = (int)(it % a.tiles_per_seq);
+      if (a.hist && (b != prev_b || seg_left == 0)) {
+        if (seg >= 0)
+          hist_segment_end(S, hist_s, a.hist + (int64_t)prev_b * TOPK_HIST_BINS, seg, quad, lane);
+        ++seg;
+        seg_left = kSegTiles;
+        // the slot's previous segment is flushed before this one adds to it
+        if (seg >= 2) mbar_wait(&S.hfree[seg & 1], (uint32_t)((seg >> 1) - 1) & 1u);
+      }
+      --seg_left;
       if (b != prev_b) {
 #pragma unroll
         for (int h = 0; h < HI; ++h) wv[h] = __ldg(a.w + (int64_t)b * HI + h);
@@ -331,8 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&S.accempty[acc]);
-      sweep_store_row<kPool>(a, b, t, r, lane, nv, wv, v);
+      sweep_store_row<kPool>(a, b, t, r, lane, nv, wv, v, a.hist ? hist_s + (seg & 1) * kHistWords : nullptr);
     }
+    if (seg >= 0) hist_segment_end(S, hist_s, a.hist + (int64_t)prev_b * TOPK_HIST_BINS, seg, quad, lane);
   }
 
   tc_fence_before();

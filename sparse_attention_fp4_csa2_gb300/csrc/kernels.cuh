@@ -27,6 +27,12 @@ constexpr int FP4_SWEEP_TILE = 256;   // keys per tile of the MXFP4 sweep
 // Radix select: 11-bit first digit.
 constexpr int TOPK_BINS = 2048;
 constexpr int TOPK_MAX_K = 8192;
+// Score histogram of each row, handed from an indexer sweep to the cluster
+// top-K of the same call: the row's valid scores counted by the top
+// TOPK_HIST_BITS bits of their keys (topk_score_key).  The sweep adds to it,
+// the top-K reads it and leaves it zero for the next call.
+constexpr int TOPK_HIST_BITS = 12;
+constexpr int TOPK_HIST_BINS = 1 << TOPK_HIST_BITS;
 
 // Per-row scratch of a top-K selection (kept in the caller's workspace).
 struct TopkScratch {
@@ -52,6 +58,9 @@ struct TopkRows {
   const int32_t *pool;
   int32_t pool_stride;
   int32_t *out;             // [rows][k] ascending, -1 padded
+  // [rows][TOPK_HIST_BINS] histogram of the rows from the sweep that wrote
+  // them, or NULL; the cluster top-K starts from it and clears it
+  uint32_t *hist = nullptr;
 };
 
 // Benchmark timing hook (csa2_set_profile_events): events recorded around a kernel.
@@ -120,6 +129,7 @@ struct SweepArgs {
   int32_t block_reduce;       // 0 max, 1 sum
   const uint8_t *k_scales;    // MXFP4 sweep: the scale plane [k_rows][4]
   int64_t k_rows;             // MXFP4 sweep: rows of the planes (batch * cap)
+  uint32_t *hist = nullptr;   // [B][TOPK_HIST_BINS] (zero on entry) or NULL: every score's key counted
 };
 
 cudaError_t launch_indexer_sweep(const CUtensorMap &tm_k, const CUtensorMap &tm_q, const SweepArgs &a,
@@ -152,6 +162,9 @@ cudaError_t launch_topk_row(const TopkRows &r, cudaStream_t stream, int *launche
 // 1 cluster, 2 one CTA per row: cudaErrorInvalidValue when a row does not fit).
 void set_topk_choice(int which);
 cudaError_t launch_topk(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled = true);
+// True when launch_topk(r) runs the cluster kernel (the one that takes a
+// sweep's histogram).
+bool topk_runs_cluster(const TopkRows &r);
 
 // Chunked prefill: multi-query indexer over the causally visible entries.
 struct PrefillIdxArgs {

@@ -546,4 +546,10 @@ __device__ __forceinline__ float f32_key_floor(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
+// A score's top-K key: f32_key, and 0 for a slot that is never selected
+// (-inf marks an invalid position; NaN is treated the same).
+__device__ __forceinline__ uint32_t topk_score_key(float v) {
+  return (v == -INFINITY || v != v) ? 0u : f32_key(v);
+}
+
 }  // namespace csa2

@@ -67,12 +67,14 @@ struct __align__(16) TopkClusterSmem {
   uint32_t warp_cnt[kThreads / 32];
   int thr;
   uint32_t above, total, in_thr;
+  int cross;                           // the sweep's histogram: the thread holding the threshold bin
+  uint32_t cross_before;               // and the keys in the bins above its group
 };
 
 static_assert(3 * (sizeof(TopkClusterSmem) + 1024 + 16) <= 232448, "three CTAs must fit on an SM");
 
 __device__ __forceinline__ uint32_t score_key(float v) {
-  return (v == -INFINITY || v != v) ? 0u : f32_key(v);
+  return topk_score_key(v);
 }
 
 __device__ __forceinline__ void red_add_remote(uint32_t addr, uint32_t v) {
@@ -276,6 +278,57 @@ __device__ __forceinline__ uint32_t block_excl_scan(TopkClusterSmem &S, uint32_t
   __syncthreads();   // S.scan may be reused
   *total = tot;
   return before + incl - v;
+}
+
+// Threshold of the row's histogram from the sweep (h: TOPK_HIST_BINS counts)
+// for `need` keys: S.thr = the bin where the count from the top reaches
+// need, or -1 when the row holds no more than need valid keys; S.above = the
+// keys in the bins above it, S.in_thr = the keys in it.  Thread t sums the
+// t-th group of TOPK_HIST_BINS / 256 bins from the top; the warp of the group
+// that holds the crossing reads that group again, a bin per lane.  Ends
+// synchronised.
+__device__ void hist_threshold(TopkClusterSmem &S, const uint32_t *h, uint32_t need) {
+  constexpr int kPer = TOPK_HIST_BINS / kThreads;
+  static_assert(kPer % 4 == 0 && kPer <= 32, "whole uint4 groups, at most one bin per lane in the second read");
+  const int tid = threadIdx.x, lane = tid & 31;
+  const uint4 *g = reinterpret_cast<const uint4 *>(h + TOPK_HIST_BINS - kPer * (tid + 1));
+  uint32_t loc = 0;
+#pragma unroll
+  for (int j = 0; j < kPer / 4; ++j) {
+    const uint4 x = __ldcg(g + j);
+    loc += x.x + x.y + x.z + x.w;
+  }
+  uint32_t total;
+  const uint32_t before = block_excl_scan(S, loc, &total);
+  if (tid == 0) {
+    S.thr = -1;
+    S.above = total;
+    S.in_thr = 0;
+    S.total = total;
+  }
+  if (total > need && before < need && before + loc >= need) {
+    S.cross = tid;
+    S.cross_before = before;
+  }
+  __syncthreads();
+  if (total > need && (tid >> 5) == (S.cross >> 5)) {
+    const int t = S.cross;
+    const int bin = TOPK_HIST_BINS - 1 - kPer * t - lane;   // lane 0 the group's top bin
+    const uint32_t c = lane < kPer ? __ldcg(h + bin) : 0u;
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    const uint32_t above = S.cross_before + incl - c;
+    if (lane < kPer && above < need && above + c >= need) {
+      S.thr = bin;
+      S.above = above;
+      S.in_thr = c;
+    }
+  }
+  __syncthreads();
 }
 
 // Calls f(key, index) for the CTA's candidate list; uniform trip count.
@@ -515,7 +568,7 @@ __device__ __forceinline__ void select_together(TopkClusterSmem &S, const TopkRo
     for (int i = (int)min(all, (uint32_t)r.k) + tid; i < r.k; i += kThreads) out[i] = -1;
 }
 
-__global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r) {
+__global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkRows r) {
   extern __shared__ uint8_t smem_raw[];
   TopkClusterSmem &S = *reinterpret_cast<TopkClusterSmem *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~uintptr_t(15));
@@ -544,6 +597,9 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
     S.n_tie = 0;
     S.g_used = 0;
   }
+  // every CTA's totals and counters are cleared before anyone adds to them
+  // remotely: a cluster barrier, awaited before the first remote add
+  cluster_arrive();
   // the scores' producer is complete past here (programmatic launch)
   pdl_wait();
   float4 vr[kVec];
@@ -555,20 +611,35 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
     for (int64_t b = lo; b < hi; b += kRound)
       prefetch_l2_bulk(vals + b, (uint32_t)(4 * (hi - b < kRound ? hi - b : kRound)));
   }
-  cluster_sync();   // every CTA's totals are cleared before anyone pushes
 
-  // 1. sample: load 0 of every warp of every round, 1/8 of the values
-  // about twice the sample's share of k above the low threshold, located to
-  // 22 key bits: the level-0 bin, then the level-1 bin inside it
-  const uint32_t need_s = (uint32_t)(2 * r.k / kSampleEvery) + 16;
-  sample_hist(S, vals, lo, hi, one_round, vr[0], 0, 0u, nctas);
-  local_threshold(S, 0, need_s, kBins);
+  // 1. the low threshold t_low: every key >= t_low is a candidate.  From the
+  // sweep's histogram of the row when it has one and the keys down to the
+  // bin where the count reaches k fit the leader's list (exact counts: no
+  // sampling); otherwise from a sample of load 0 of every warp of every
+  // round, 1/8 of the values, about twice the sample's share of k above it,
+  // located to 22 key bits: the level-0 bin, then the level-1 bin inside it
   uint32_t t_low = 1u;
-  if (S.thr >= 0) {
-    const uint32_t b0 = (uint32_t)S.thr, above0 = S.above;
-    sample_hist(S, vals, lo, hi, one_round, vr[0], 1, b0, nctas);
-    local_threshold(S, 1, need_s - above0, kBins);
-    t_low = S.thr < 0 ? (b0 << 21) : ((b0 << 21) | ((uint32_t)S.thr << 10));
+  bool sample = true;
+  if (r.hist) {
+    hist_threshold(S, r.hist + (int64_t)row * TOPK_HIST_BINS, (uint32_t)r.k);
+    if (S.thr < 0) {
+      sample = false;   // every valid key
+    } else if (S.above + S.in_thr <= (uint32_t)kGather) {
+      sample = false;
+      t_low = max((uint32_t)S.thr << (32 - TOPK_HIST_BITS), 1u);
+    }
+  }
+  cluster_wait();
+  if (sample) {
+    const uint32_t need_s = (uint32_t)(2 * r.k / kSampleEvery) + 16;
+    sample_hist(S, vals, lo, hi, one_round, vr[0], 0, 0u, nctas);
+    local_threshold(S, 0, need_s, kBins);
+    if (S.thr >= 0) {
+      const uint32_t b0 = (uint32_t)S.thr, above0 = S.above;
+      sample_hist(S, vals, lo, hi, one_round, vr[0], 1, b0, nctas);
+      local_threshold(S, 1, need_s - above0, kBins);
+      t_low = S.thr < 0 ? (b0 << 21) : ((b0 << 21) | ((uint32_t)S.thr << 10));
+    }
   }
 
   // 2. filter into the candidate list, in index order.  Within a warp the
@@ -648,6 +719,13 @@ __global__ void __launch_bounds__(kThreads) topk_cluster_kernel(const TopkRows r
     dsmem_st_u32(dsmem_addr(&S.cand_base[crank], (uint32_t)tid), gb);
   }
   cluster_sync();
+  if (r.hist) {
+    // every CTA has read the row's histogram: clear it for the next call,
+    // a slice per CTA
+    uint32_t *h = r.hist + (int64_t)row * TOPK_HIST_BINS;
+    for (uint32_t i = crank * TOPK_HIST_BINS / nctas + tid; i < (crank + 1) * TOPK_HIST_BINS / nctas; i += kThreads)
+      h[i] = 0u;
+  }
   uint32_t total_cand = 0;
   bool overflow = false;
   for (uint32_t c = 0; c < nctas; ++c) {

@@ -73,7 +73,7 @@ static_assert(2 * (kRowSmem + 1024) <= 233472, "two CTAs must fit on an SM");
 static_assert(kStages * kChunk * 4 >= kRowMax / 8, "the ordering bitmap fits in the ring");
 
 __device__ __forceinline__ uint32_t row_key(float v) {
-  return (v == -INFINITY || v != v) ? 0u : f32_key(v);
+  return topk_score_key(v);
 }
 
 
@@ -629,8 +629,8 @@ int g_topk_choice = 0;
 
 void set_topk_choice(int which) { g_topk_choice = which; }
 
-cudaError_t launch_topk(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled) {
-  if (g_topk_choice == 2) return launch_topk_row(r, stream, launches, profiled);   // strict: no fallback
+bool topk_runs_cluster(const TopkRows &r) {
+  if (g_topk_choice == 2) return false;   // strict: no fallback
   // automatic: one CTA per row once the rows fill every SM twice (the cluster
   // kernel then runs a single CTA per row too, with a longer chain per row);
   // fewer rows go to a cluster per row, which spreads each row over SMs
@@ -642,9 +642,14 @@ cudaError_t launch_topk(const TopkRows &r, cudaStream_t stream, int *launches, b
                                                     cudaSuccess)
         sms = 1 << 20;
     }
-    if (r.rows >= 2 * sms) return launch_topk_row(r, stream, launches, profiled);
+    if (r.rows >= 2 * sms) return false;
   }
-  return launch_topk_cluster(r, stream, launches, profiled);
+  return true;
+}
+
+cudaError_t launch_topk(const TopkRows &r, cudaStream_t stream, int *launches, bool profiled) {
+  if (topk_runs_cluster(r)) return launch_topk_cluster(r, stream, launches, profiled);
+  return launch_topk_row(r, stream, launches, profiled);
 }
 
 }  // namespace csa2
