@@ -241,7 +241,9 @@ csa2_status run_indexer(const void *q_idx, const float *w, const void *k_idx, in
   r.pool_stride = p->candidate_topk_blocks;
   r.out = topk_idx;
   // the bf16 sweep counts the rows' keys for the cluster top-K, which then
-  // needs no sample of the scores (and clears the counts)
+  // needs no sample of the scores (and clears the counts).  The MXFP4 sweep
+  // does not: its epilogue shares issue slots with the code conversion, and
+  // counting there cost it more than the top-K saved.
   if (!fp4 && topk_cluster_supported(r) && topk_runs_cluster(r)) {
     r.hist = reinterpret_cast<uint32_t *>(wsb + L.hist_off);
     a.hist = r.hist;

@@ -53,7 +53,8 @@ __device__ __forceinline__ volatile uint32_t &abort_flag(SweepSmem &S) {
 
 constexpr size_t kHistOff = (sizeof(SweepSmem) + 15) / 16 * 16;   // after the control block
 constexpr size_t kSmemBytes =
-    1024 /*align slack*/ + (size_t)kStages * kTileBytes + 2 * kQBytes + kHistOff + 2 * TOPK_HIST_BINS * 2;
+    1024 /*align slack*/ + (size_t)kStages * kTileBytes + 2 * kQBytes + kHistOff + 2 * kHistWords * 4;
+constexpr int kSegTiles = 256;   // 128 keys a tile: a segment's counts stay below 2^16
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 
 __device__ __forceinline__ int32_t clamp_nvis(const int32_t *n_vis, int b, int64_t n_max) {
@@ -110,47 +111,7 @@ __device__ __forceinline__ void sweep_store_row(const SweepArgs &a, int b, int t
     stored = valid ? sc : -INFINITY;
     srow[slot] = stored;
   }
-  if (hs) {
-    // the row's histogram for its top-K, in this CTA's shared memory: 16-bit
-    // counts, two bins to a word
-    const uint32_t key = topk_score_key(stored);
-    if (key) {
-      const uint32_t bin = key >> (32 - TOPK_HIST_BITS);
-      atomicAdd(hs + (bin >> 1), (bin & 1u) ? 0x10000u : 1u);
-    }
-  }
-}
-
-// The shared-memory histogram of the sweep: two slots of TOPK_HIST_BINS
-// 16-bit counts, used by segments of a CTA's tiles (a segment: the tiles of
-// one row, at most kSegTiles of them, so that no count passes 65,535).
-constexpr int kSegTiles = 256;
-constexpr int kHistWords = TOPK_HIST_BINS / 2;   // per slot
-
-// End of histogram segment `seg` (slot seg & 1) for row `row`, by each of
-// the four epilogue warps (quadrant `quad`): once all four are done adding
-// (hseg), each adds its quarter of the slot into the row's global histogram
-// and clears it, then marks it free (hfree) for segment seg + 2.
-__device__ __forceinline__ void hist_segment_end(SweepSmem &S, uint32_t *hist_s, uint32_t *g, int seg, int quad,
-                                                 int lane) {
-  const int p = seg & 1;
-  const uint32_t use = (uint32_t)(seg >> 1) & 1u;
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&S.hseg[p]);
-  mbar_wait(&S.hseg[p], use);
-  uint32_t *hs = hist_s + p * kHistWords;
-  constexpr int kQuarter = kHistWords / 4;
-#pragma unroll 4
-  for (int i = quad * kQuarter + lane; i < (quad + 1) * kQuarter; i += 32) {
-    const uint32_t c = hs[i];
-    if (c) {
-      hs[i] = 0u;
-      if (c & 0xFFFFu) atomicAdd(g + 2 * i, c & 0xFFFFu);
-      if (c >> 16) atomicAdd(g + 2 * i + 1, c >> 16);
-    }
-  }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&S.hfree[p]);
+  if (hs) hist_count(hs, stored);
 }
 
 template <bool kPool>
@@ -184,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&S.mma_done, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&S.hseg[i], 4);
+      mbar_init(&S.hseg[i], 4);   // the four epilogue warps
       mbar_init(&S.hfree[i], 4);
     }
     abort_flag(S) = 0;
@@ -193,7 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_q);
   }
   if (a.hist)
-    for (int i = threadIdx.x; i < 2 * kHistWords; i += kThreads) hist_s[i] = 0u;
+    for (int i = threadIdx.x; i < 2 * kHistWords; i += kThreads) hist_s[i] = 0u;   // both slots
   // the inputs' producer is complete past here (programmatic launch)
   pdl_wait();
   if (warp == 1) {
@@ -369,20 +330,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int prev_b = -1;
     int32_t nv = 0;
     float wv[HI];
-    int seg = -1, seg_left = 0;   // histogram segment: its parity picks the slot
+    HistSegments hseg(S.hseg, S.hfree, hist_s, a.hist, kSegTiles, quad, lane);
     for (int64_t it = it0; it < it1; ++it) {
       if (abort_flag(S)) break;
       const int b = (int)(it / a.tiles_per_seq);
       const int t = (int)(it % a.tiles_per_seq);
-      if (a.hist && (b != prev_b || seg_left == 0)) {
-        if (seg >= 0)
-          hist_segment_end(S, hist_s, a.hist + (int64_t)prev_b * TOPK_HIST_BINS, seg, quad, lane);
-        ++seg;
-        seg_left = kSegTiles;
-        // the slot's previous segment is flushed before this one adds to it
-        if (seg >= 2) mbar_wait(&S.hfree[seg & 1], (uint32_t)((seg >> 1) - 1) & 1u);
-      }
-      --seg_left;
+      hseg.tile(b);
       if (b != prev_b) {
 #pragma unroll
         for (int h = 0; h < HI; ++h) wv[h] = __ldg(a.w + (int64_t)b * HI + h);
@@ -399,9 +352,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&S.accempty[acc]);
-      sweep_store_row<kPool>(a, b, t, r, lane, nv, wv, v, a.hist ? hist_s + (seg & 1) * kHistWords : nullptr);
+      sweep_store_row<kPool>(a, b, t, r, lane, nv, wv, v, hseg.slot());
     }
-    if (seg >= 0) hist_segment_end(S, hist_s, a.hist + (int64_t)prev_b * TOPK_HIST_BINS, seg, quad, lane);
+    hseg.finish();
   }
 
   tc_fence_before();
