@@ -67,6 +67,7 @@ struct __align__(16) TopkClusterSmem {
   uint32_t warp_cnt[kThreads / 32];
   int thr;
   uint32_t above, total, in_thr;
+  uint32_t up;                         // leader: candidates above the histogram's threshold bin
   int cross;                           // the sweep's histogram: the thread holding the threshold bin
   uint32_t cross_before;               // and the keys in the bins above its group
 };
@@ -397,7 +398,7 @@ __device__ uint32_t run_levels(TopkClusterSmem &S, const TopkRows &r, const floa
 // one list, three radix levels over local histograms (11, 11 and 10 key
 // bits) locate the full key T of the k-th largest, and the keys above T plus
 // the lowest-index keys equal to T are written ascending (list order).
-__device__ void leader_select(TopkClusterSmem &S, const TopkRows &r, int row, uint32_t nctas) {
+__device__ void leader_select(TopkClusterSmem &S, const TopkRows &r, int row, uint32_t nctas, int hb) {
   const uint32_t tid = threadIdx.x;
   uint32_t n = 0;
 #pragma unroll 1
@@ -412,21 +413,50 @@ __device__ void leader_select(TopkClusterSmem &S, const TopkRows &r, int row, ui
   }
   __syncthreads();
   uint32_t need = (uint32_t)r.k, prefix = 0;   // k <= n: checked by the caller
+  // hb >= 0: every candidate's top TOPK_HIST_BITS key bits are >= hb (the
+  // sweep's threshold bin): the keys above that bin, counted here, are all
+  // taken, and two levels on the remaining bits rank the keys in it.  Otherwise (or if
+  // the count says the bin cannot hold the k-th key) three levels of 11, 11
+  // and 10 bits over the whole list.
+  bool hm = false;
+  if (hb >= 0) {
+    if (tid == 0) S.up = 0u;
+    __syncthreads();
 #pragma unroll 1
-  for (int L = 0; L < 3; ++L) {
-    const int sh = L == 0 ? 21 : L == 1 ? 10 : 0, width = L == 2 ? 10 : 11;
+    for (uint32_t b0 = 0; b0 < n; b0 += kThreads) {
+      const uint32_t i = b0 + tid;
+      const bool up = i < n && (S.ckey[i] >> (32 - TOPK_HIST_BITS)) > (uint32_t)hb;
+      const uint32_t c = __popc(__ballot_sync(0xffffffffu, up));
+      if ((tid & 31) == 0 && c) atomicAdd(&S.up, c);
+    }
+    __syncthreads();
+    const uint32_t up = S.up;
+    if (up < need) {
+      hm = true;
+      need -= up;
+      prefix = (uint32_t)hb;
+    }
+  }
+  const int levels = hm ? 2 : 3;
+#pragma unroll 1
+  for (int L = 0; L < levels; ++L) {
+    // below the histogram's bits: a level on the upper half, one on the lower
+    constexpr int kRest = 32 - TOPK_HIST_BITS, kLow = kRest / 2;
+    static_assert(kRest - kLow <= 11 && kLow >= 8, "level widths within the bins, per-thread groups whole");
+    const int sh = hm ? (L == 0 ? kLow : 0) : (L == 0 ? 21 : L == 1 ? 10 : 0);
+    const int width = hm ? (L == 0 ? kRest - kLow : kLow) : (L == 2 ? 10 : 11);
     const uint32_t nb = 1u << width;
     for (int b = tid; b < kBins; b += kThreads) S.hist[b] = 0;
     __syncthreads();
-    // level 0: warp-aggregated adds (the candidates crowd into a few top
-    // bins); below it the bins are mostly distinct
+    // the top 11 bits: warp-aggregated adds (the candidates crowd into a few
+    // bins); below them the bins are mostly distinct
 #pragma unroll 1
     for (uint32_t b0 = 0; b0 < n; b0 += kThreads) {
       const uint32_t i = b0 + tid;
       const uint32_t key = i < n ? S.ckey[i] : 0u;
-      const bool m = i < n && (L == 0 || (key >> (sh + width)) == prefix);
+      const bool m = i < n && ((L == 0 && !hm) || (key >> (sh + width)) == prefix);
       const uint32_t bin = m ? ((key >> sh) & (nb - 1)) : (uint32_t)kBins;
-      if (L == 0)
+      if (L == 0 && !hm)
         hist_add(S.hist, bin, tid & 31);
       else
         hist_add_plain(S.hist, bin);
@@ -620,12 +650,14 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkRow
   // located to 22 key bits: the level-0 bin, then the level-1 bin inside it
   uint32_t t_low = 1u;
   bool sample = true;
+  int hbin = -1;   // the histogram's threshold bin when t_low comes from it
   if (r.hist) {
     hist_threshold(S, r.hist + (int64_t)row * TOPK_HIST_BINS, (uint32_t)r.k);
     if (S.thr < 0) {
       sample = false;   // every valid key
     } else if (S.above + S.in_thr <= (uint32_t)kGather) {
       sample = false;
+      hbin = S.thr;
       t_low = max((uint32_t)S.thr << (32 - TOPK_HIST_BITS), 1u);
     }
   }
@@ -737,7 +769,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cluster_kernel(const TopkRow
     // are done (nothing reads their memory any more)
     if (crank == 0) {
       pdl_release();   // the next kernel's CTAs may take the SMs the others leave
-      leader_select(S, r, row, nctas);
+      leader_select(S, r, row, nctas, hbin);
     }
     return;
   }
