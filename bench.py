@@ -42,14 +42,15 @@ SWEEP_FIXED = 32 * 128 * 2 + 32 * 4        # q_idx + w per sequence
 # stands on that workload (stored, not measured by this run); a kernel changed
 # since its capture has no entry and reports null.
 TRAFFIC = {
-    ("indexer_sweep_kernel", "group_decode_32x64k"): 537181184 + 6408192,
+    ("indexer_sweep_kernel", "group_decode_32x64k"): 537262848 + 6632192,
     ("sparse_attn_kernel", "group_decode_32x64k"): 10644480,      # the output stays in L2 during the capture
     # captured on one 1,024-token block of one sequence (--batch 1 --chunk 1024):
     # the shape of every block launch of the full workload
-    ("prefill_indexer_kernel", "prefill_m2_2x128k+16k"): 50702336 + 214056192,
-    ("topk_row_kernel", "prefill_m2_2x128k+16k"): 272803072 + 4828928,
+    ("prefill_indexer_kernel", "prefill_m2_2x128k+16k"): 49437696 + 211717632,
+    ("topk_row_kernel", "prefill_m2_2x128k+16k"): 273513472 + 4727296,
     # captured at 16 sequences, scaled by the rows read to the 32-sequence launch
-    ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411200 + 915968),
+    ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411712 + 1119232),
+    ("topk_cluster_kernel", "group_decode_32x64k"): 8978432,   # the scores and the sweep's histograms
 }
 REINDEX_BYTES = 16384 * 256 + 18560         # per (seq, layer)
 K_BYTES = {False: 256, True: 68}            # indexer-K bytes per position: bf16, MXFP4 (codes + scales)
