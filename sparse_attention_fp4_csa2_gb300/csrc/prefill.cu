@@ -228,19 +228,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v[32];
           tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * kN + qq * HI), v);
           tmem_ld_wait();
-          // four independent partial sums of w_h * ReLU(q_h . k)
+          // four independent partial sums of w_h * ReLU(q_h . k), two per
+          // packed fp32 FMA (heads h, h + 1 of every four in one, h + 2, h + 3
+          // in the other; each lane as fmaf)
           const float4 *w4 = reinterpret_cast<const float4 *>(wv + qq * HI);
-          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+          uint64_t s01 = 0ull, s23 = 0ull;
 #pragma unroll
           for (int h4 = 0; h4 < HI / 4; ++h4) {
             const float4 ww = q < 2 ? make_float4(wr[q & 1][4 * h4], wr[q & 1][4 * h4 + 1], wr[q & 1][4 * h4 + 2],
                                                   wr[q & 1][4 * h4 + 3])
                                     : w4[h4];
-            s0 = fmaf(ww.x, fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f), s0);
-            s1 = fmaf(ww.y, fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f), s1);
-            s2 = fmaf(ww.z, fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f), s2);
-            s3 = fmaf(ww.w, fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f), s3);
+            s01 = f32x2_fma(f32x2_pack(ww.x, ww.y),
+                            f32x2_pack(fmaxf(__uint_as_float(v[4 * h4 + 0]), 0.0f),
+                                       fmaxf(__uint_as_float(v[4 * h4 + 1]), 0.0f)),
+                            s01);
+            s23 = f32x2_fma(f32x2_pack(ww.z, ww.w),
+                            f32x2_pack(fmaxf(__uint_as_float(v[4 * h4 + 2]), 0.0f),
+                                       fmaxf(__uint_as_float(v[4 * h4 + 3]), 0.0f)),
+                            s23);
           }
+          float s0, s1, s2, s3;
+          f32x2_unpack(s01, s0, s1);
+          f32x2_unpack(s23, s2, s3);
           const float sc = (s0 + s1) + (s2 + s3);
           srow[(int64_t)q * a.row_len + pos] = pos < nv[q] ? sc : -INFINITY;
         }

@@ -546,6 +546,22 @@ __device__ __forceinline__ float f32_key_floor(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
+// Two fp32 lanes at once (the packed fp32 pipe): d = a * b + c per lane,
+// each lane rounded as fmaf.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // A score's top-K key: f32_key, and 0 for a slot that is never selected
 // (-inf marks an invalid position; NaN is treated the same).
 __device__ __forceinline__ uint32_t topk_score_key(float v) {
