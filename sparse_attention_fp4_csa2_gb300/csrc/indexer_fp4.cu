@@ -443,12 +443,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&S.accempty[acc]);
-      float s0 = 0.0f, s1 = 0.0f;
+      // sum_h w_h ReLU(.) for the two keys, as two partial sums each (even
+      // and odd heads) on the packed fp32 pipe
+      uint64_t p0 = 0ull, p1 = 0ull;
 #pragma unroll
-      for (int h = 0; h < HI; ++h) {
-        s0 = fmaf(wv[h], fmaxf(__uint_as_float(v0[h]), 0.0f), s0);
-        s1 = fmaf(wv[h], fmaxf(__uint_as_float(v1[h]), 0.0f), s1);
+      for (int h = 0; h < HI; h += 2) {
+        const uint64_t w2 = f32x2_pack(wv[h], wv[h + 1]);
+        p0 = f32x2_fma(w2, f32x2_pack(fmaxf(__uint_as_float(v0[h]), 0.0f), fmaxf(__uint_as_float(v0[h + 1]), 0.0f)),
+                       p0);
+        p1 = f32x2_fma(w2, f32x2_pack(fmaxf(__uint_as_float(v1[h]), 0.0f), fmaxf(__uint_as_float(v1[h + 1]), 0.0f)),
+                       p1);
       }
+      float e0, o0, e1, o1;
+      f32x2_unpack(p0, e0, o0);
+      f32x2_unpack(p1, e1, o1);
+      const float s0 = e0 + o0, s1 = e1 + o1;
       float *srow = a.scores + (int64_t)b * a.row_len;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
