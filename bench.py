@@ -46,10 +46,10 @@ TRAFFIC = {
     ("sparse_attn_kernel", "group_decode_32x64k"): 10644480,      # the output stays in L2 during the capture
     # captured on one 1,024-token block of one sequence (--batch 1 --chunk 1024):
     # the shape of every block launch of the full workload
-    ("prefill_indexer_kernel", "prefill_m2_2x128k+16k"): 49437696 + 211717632,
-    ("topk_row_kernel", "prefill_m2_2x128k+16k"): 273513472 + 4727296,
+    ("prefill_indexer_kernel", "prefill_m2_2x128k+16k"): 50376448 + 213900544,
+    ("topk_row_kernel", "prefill_m2_2x128k+16k"): 273602560 + 4833792,
     # captured at 16 sequences, scaled by the rows read to the 32-sequence launch
-    ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411712 + 1119232),
+    ("indexer_sweep_fp4_kernel", "group_decode_32x64k"): 2 * (71411200 + 1121024),
     ("topk_cluster_kernel", "group_decode_32x64k"): 8978432,   # the scores and the sweep's histograms
 }
 REINDEX_BYTES = 16384 * 256 + 18560         # per (seq, layer)
