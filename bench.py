@@ -298,6 +298,16 @@ class Workload:
         self.out = self.out_arena[:, :n_o].view(L, B, 64, 512)
         self.lse = self.out_arena[:, n_o:].view(L, B, 64)
         self.ws = c2.workspace(c2.OP_DECODE, B, E, self.params, device=device)
+        # the split Full / Reindex layers' indexer calls get a workspace of
+        # their own: it carries the rows' histograms from one call to the
+        # next, which the pool selection's and the readout's scratch would
+        # overwrite
+        self.ws_idx = c2.workspace(c2.OP_INDEXER, B, E, self.params, device=device)
+        # a Full layer's new main-KV entry may be written on a second stream
+        # while the layer's selection runs (only the readout reads it)
+        self.side = torch.cuda.Stream(device=device)
+        self.ev_fork = [torch.cuda.Event() for _ in range(self.copies)]
+        self.ev_join = [torch.cuda.Event() for _ in range(self.copies)]
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
 
@@ -353,13 +363,17 @@ class Workload:
         layer's) are bracketed by those events; with io (a HostIO), every
         layer's inputs arrive from pinned host memory on a copy stream and its
         outputs go back on another while later layers compute.  A Full layer
-        first writes its cache copy's new entry; a SWA-only layer attends to
+        writes its cache copy's new entry (without io, on a second stream
+        while its selection runs, unless the write also projects the new
+        indexer key, which the selection reads); a SWA-only layer attends to
         its window alone (no selected entries)."""
+        import torch
         c2, L, m = self.c2, self.layers, self.m
         launches = 0
         if io:
             io.start()
         copy = -1
+        forked = False   # the new entry's write runs on the side stream
         for i, mode in enumerate(self.cfg.schedule):
             if io:
                 io.wait_in(self.io_first[i])
@@ -375,9 +389,20 @@ class Workload:
                                          indexer_fp4=self.fp4)
                     launches += c2.last_launch_count()
                 else:
-                    c2.kv_quant_write(new["latent"], new.get("z"), m, self.new_pos, self.new_slot,
-                                      self.kv[copy].view(-1, 288))
-                    launches += c2.last_launch_count()
+                    if FORK_KV_WRITE and not io:
+                        main = torch.cuda.current_stream()
+                        self.ev_fork[copy].record(main)
+                        self.side.wait_event(self.ev_fork[copy])
+                        with torch.cuda.stream(self.side):
+                            c2.kv_quant_write(new["latent"], new.get("z"), m, self.new_pos, self.new_slot,
+                                              self.kv[copy].view(-1, 288))
+                            launches += c2.last_launch_count()
+                        self.ev_join[copy].record(self.side)
+                        forked = True
+                    else:
+                        c2.kv_quant_write(new["latent"], new.get("z"), m, self.new_pos, self.new_slot,
+                                          self.kv[copy].view(-1, 288))
+                        launches += c2.last_launch_count()
                     if self.fp4:
                         c2.indexer_k_quant(new["k"], self.new_slot, self.k_idx[copy])
                         launches += c2.last_launch_count()
@@ -394,19 +419,24 @@ class Workload:
                 on = [k for k in on if k in prof]
                 for k in on:
                     c2.set_profile_events(k, *prof[k])
-            if io and mode in ("full", "reindex"):
-                # end to end, the layer's selection and its readout are two
-                # calls, so that the readout's inputs (the bulk of the layer's
-                # copy) may land while the selection runs
+            if (io or forked) and mode in ("full", "reindex"):
+                # the layer's selection and its readout as two calls: the
+                # readout waits for the new entry's write (a Full layer) and,
+                # end to end, for its inputs (the bulk of the layer's copy),
+                # which land while the selection runs
                 hsi_full = mode == "full" and self.hsi
                 c2.indexer_score_topk(li.q_idx, li.w, self.k_idx[cc], self.n_vis, self.E, self.params, self.topk,
-                                      self.ws, pool_blocks=self.pool if mode == "reindex" else None,
+                                      self.ws_idx, pool_blocks=self.pool if mode == "reindex" else None,
                                       block_scores=self.bscores if hsi_full else None)
                 launches += c2.last_launch_count()
                 if hsi_full:
                     c2.hier_pool_select(self.bscores, self.n_vis, self.E, self.params, self.pool, self.ws)
                     launches += c2.last_launch_count()
-                io.wait_in(self.io_attn[i])
+                if forked:
+                    torch.cuda.current_stream().wait_event(self.ev_join[copy])
+                    forked = False
+                if io:
+                    io.wait_in(self.io_attn[i])
                 c2.sparse_attn(self.params, li.q, self.kv[cc], self.topk, li.swa, li.swa_scale, li.swa_len,
                                self.out[i], self.ws, lse=self.lse[i])
             else:
@@ -570,6 +600,10 @@ ATTN_KERNEL = 0       # csa2_params.attn_kernel of the workloads (--attn-kernel)
 INDEXER_FP4 = False   # csa2_params.indexer_fp4 of the decode workloads (--indexer-fp4)
 PROJECT_IK = False    # Full layers project their new indexer key (--project-ik)
 TOPK_KERNEL = 0       # csa2_set_topk_kernel (--topk-kernel)
+# a Full layer's main-KV write on a second stream, overlapping its selection
+# (device-resident steps; with host copies in flight it cost the end-to-end
+# step more than it saved there)
+FORK_KV_WRITE = True
 
 
 def topk_kernel_name(rows, row_len, sms):
