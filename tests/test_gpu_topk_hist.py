@@ -127,3 +127,27 @@ def test_hist_tied_threshold_bin(c2, orc, n_top, n_tie):
         s = orc.index_scores(q_idx[i], w[i], k[i, :int(nv[i])])
         assert np.array_equal(sel[i], orc.topk(s, K))
     assert _counts_zero(ws, B)
+
+
+def test_hist_random_shapes_one_workspace(c2, orc):
+    """Seeded random batches, lengths, visible counts and k on one workspace
+    sized for the largest (a call's layout follows its own batch, so a call
+    may start from another call's scores): every selection exact, the
+    call's counts zero after it."""
+    g = np.random.default_rng(2024)
+    Bmax, capmax = 6, 40000
+    pmax = c2.Params.make(index_topk=2048, candidate_topk_blocks=2048)
+    ws = c2.workspace(c2.OP_INDEXER, Bmax, capmax, pmax)
+    for trial in range(8):
+        B = int(g.integers(1, Bmax + 1))
+        cap = int(g.integers(1, capmax // 4) * 4)
+        K = int(g.choice([16, 100, 512, 2048]))
+        n_vis = [int(g.integers(0, cap + 1)) for _ in range(B)]
+        n_vis[0] = cap
+        q_idx, w, k, nv = _case(300 + trial, B, cap, n_vis)
+        p = c2.Params.make(index_topk=K)
+        sel = _select(c2, p, q_idx, w, k, nv, cap, ws)
+        for i in range(B):
+            s = orc.index_scores(q_idx[i], w[i], k[i, :n_vis[i]])
+            check_topk(sel[i], orc.topk(s, K), s, n_valid=n_vis[i])
+        assert _counts_zero(ws, B)
