@@ -1,25 +1,32 @@
 // Exact top-K of each indexer score row in one kernel: one thread-block
 // cluster per row, radix select across the cluster through distributed
-// shared memory, no global scratch.  Used for the index_topk = 512 selection
-// of the Full and Reindex layers and of every chunk token in prefill
-// ("DeepSeek-V4.1-Flash - Architecture", sections 2 and 3).
+// shared memory, no global scratch (beyond reading, and clearing, the row
+// histograms an indexer sweep may hand over).  Used for the index_topk = 512
+// selection of the Full and Reindex layers, the HSI pool's top-2048 blocks,
+// and prefill blocks of few rows ("DeepSeek-V4.1-Flash - Architecture",
+// sections 2 and 3).
 //
 // Scores become order-preserving 32-bit keys (-inf marks an invalid slot).
 // The CTAs of the cluster split the row into contiguous slices; in a round
 // each warp covers 1024 consecutive values with 8 coalesced float4 loads in
 // flight per thread (a slice of one round stays in registers throughout).
-//   1. sample: the first of every warp's 8 loads (1/8 of the values); a low
-//      threshold t_low with about twice the sample's share of k above it,
-//      located to 22 key bits by two histogram levels (the top 11 bits, then
-//      the next 11 inside the threshold bin);
+//   1. the low threshold t_low (every key >= t_low is a candidate): with the
+//      sweep's histogram of the row (the valid keys counted by their top 12
+//      bits), the exact bin where the count from the top reaches k, when the
+//      keys down to that bin fit the leader's list; otherwise from a sample,
+//      the first of every warp's 8 loads (1/8 of the values), about twice
+//      the sample's share of k above it, located to 22 key bits by two
+//      histogram levels (the top 11 bits, then the next 11 inside the bin);
 //   2. filter: every key >= t_low goes to the CTA's candidate list in shared
 //      memory, in index order (warp and CTA prefix sums of per-thread counts
 //      give every thread its output slots: no per-key atomics), and then to a
 //      block of the leader's (rank 0) list reserved by a remote atomic add;
 //   3. when every list fits its slot and together they hold >= k keys, the
-//      leader alone finds the exact top k in the gathered list (three radix
-//      levels over local histograms, ties on the full key toward the lower
-//      index) and writes them in list order, which is index order;
+//      leader alone finds the exact top k in the gathered list (after a
+//      histogram threshold: the keys above the bin are counted and taken, two
+//      radix levels rank those in it; else three levels over the list; ties
+//      on the full key toward the lower index) and writes them in list
+//      order, which is index order;
 //   4. otherwise the cluster selects together: exact radix select -- 11, 11
 //      and 10 key bits -- on the candidate lists when together they hold >= k
 //      keys and none overflowed, else on the whole slices; a level stops early
@@ -28,6 +35,8 @@
 //      index order, after a cluster prefix of the per-CTA tie counts); each
 //      CTA sorts the indices it selected and writes them at its cluster prefix
 //      offset (slices are in index order); the last CTA pads with -1.
+// Any t_low gives the exact result: the candidates are all keys >= t_low, so
+// at least k of them hold the top k, and fewer (or an overflow) go to step 4.
 // Selected positions are mapped through the HSI pool for Reindex rows.
 // Histograms are exchanged by pushing each CTA's non-zero bins into every
 // CTA's cluster total with remote atomic adds; all waiting is at cluster
