@@ -19,8 +19,10 @@
 //
 // Persistent, warp-specialised CTA (one per SM): warp 0 issues TMA loads of
 // the K tiles into a ring of shared-memory stages, warp 1 issues the MMAs into
-// two TMEM accumulators, warps 2-5 drain the accumulators.  Every CTA owns a
-// contiguous run of (sequence, tile) work items.
+// two TMEM accumulators, warps 2-5 drain the accumulators (and, when the
+// cluster top-K follows, count every score's key in the row's histogram; see
+// HistSegments).  Every CTA owns a contiguous run of (sequence, tile) work
+// items.
 #include "pipeline.cuh"
 
 namespace csa2 {
